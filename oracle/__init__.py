@@ -1,0 +1,145 @@
+"""Oracle: a plain fp64 CPU reference for the fused row-wise RMSNorm.
+
+TEST INFRASTRUCTURE, NOT PRODUCT CODE.  Only the test suite, the smoke check
+and the benchmark's CPU-baseline / reference legs may import this package.
+It shares no code with the CUDA library and never imports it.
+
+The arithmetic lives in ``rmsnorm_oracle.c`` (plain C, binary64, built with
+``-O2 -ffp-contract=off`` and no fast-math).  This module only compiles that
+file with gcc, loads it with ctypes and passes numpy buffers to it.  Rows are
+independent, so ``threads > 1`` splits the row range into contiguous blocks and
+runs one C call per block on a thread pool (ctypes releases the GIL for the
+call); the per-row arithmetic is unchanged by that split.
+
+What it computes follows the RMSNorm definition of "Building a GPU compiler
+from scratch: from PyTorch to CUDA via multi-level IR (Emmy)" (running example
+and section "Tensor IR"); the C file lists the readings taken where the pages
+are silent.
+
+Data convention: bf16 tensors are numpy ``uint16`` arrays of raw bf16 bits;
+fp32 tensors are numpy ``float32`` arrays.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "rmsnorm_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle_rmsnorm.so")
+
+DTYPES = {"f32": 0, "bf16": 1}
+_NP_TYPE = {"f32": np.float32, "bf16": np.uint16}
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the C oracle into ``oracle/_build`` with gcc and return its path."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    stale = (not os.path.exists(_LIB_PATH)
+             or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
+    if force or stale:
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-ffp-contract=off", "-fno-fast-math", "-std=c11",
+               "-Wall", "-Wextra", "-shared", "-fPIC", _SRC, "-o", tmp, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            vp, i64 = ctypes.c_void_p, ctypes.c_int64
+            lib.oracle_rmsnorm_rows.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64,
+                                                ctypes.c_float, ctypes.c_int]
+            lib.oracle_rmsnorm_rows.restype = ctypes.c_int
+            lib.oracle_bf16_from_double.argtypes = [vp, vp, i64]
+            lib.oracle_bf16_from_double.restype = None
+            lib.oracle_double_from_bf16.argtypes = [vp, vp, i64]
+            lib.oracle_double_from_bf16.restype = None
+            _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+def _check(a, name, dtype, shape):
+    if a is None:
+        return None
+    a = np.ascontiguousarray(a)
+    if a.dtype != _NP_TYPE[dtype]:
+        raise TypeError(f"{name}: expected {_NP_TYPE[dtype].__name__} for dtype {dtype}, got {a.dtype}")
+    if a.shape != shape:
+        raise ValueError(f"{name}: expected shape {shape}, got {a.shape}")
+    return a
+
+
+def rmsnorm(x, w=None, residual=None, eps: float = 1e-6, dtype: str = "bf16",
+            want_exact: bool = False, threads: int = 1):
+    """Reference RMSNorm of every row of ``x`` ([rows, hidden]).
+
+    Returns ``(y, residual_out, y_exact)``: ``y`` in the I/O type,
+    ``residual_out`` (= the rounded ``x + residual``) or None, and the fp64
+    value of ``y`` before its final rounding, or None unless ``want_exact``.
+    """
+    if dtype not in DTYPES:
+        raise ValueError(f"unknown dtype {dtype!r}")
+    x = np.ascontiguousarray(x)
+    if x.ndim != 2:
+        raise ValueError("x must be 2-D [rows, hidden]")
+    rows, hidden = x.shape
+    x = _check(x, "x", dtype, (rows, hidden))
+    residual = _check(residual, "residual", dtype, (rows, hidden))
+    w = _check(w, "w", dtype, (hidden,))
+
+    y = np.empty((rows, hidden), dtype=_NP_TYPE[dtype])
+    res_out = None if residual is None else np.empty((rows, hidden), dtype=_NP_TYPE[dtype])
+    y64 = np.empty((rows, hidden), dtype=np.float64) if want_exact else None
+    if rows == 0 or hidden == 0:
+        return y, res_out, y64
+
+    lib = _load()
+    args = (_ptr(x), _ptr(residual), _ptr(w), _ptr(y), _ptr(y64), _ptr(res_out))
+
+    def run(lo, hi):
+        rc = lib.oracle_rmsnorm_rows(*args, lo, hi, hidden, float(eps), DTYPES[dtype])
+        if rc != 0:
+            raise ValueError("oracle rejected its arguments")
+
+    threads = max(1, min(int(threads), rows))
+    if threads == 1:
+        run(0, rows)
+    else:
+        bounds = np.linspace(0, rows, threads + 1).astype(np.int64)
+        with ThreadPoolExecutor(max_workers=threads) as ex:
+            list(ex.map(lambda i: run(int(bounds[i]), int(bounds[i + 1])), range(threads)))
+    return y, res_out, y64
+
+
+def bf16_from_double(v) -> np.ndarray:
+    """Round fp64 values to bf16 bits (round to nearest, ties to even)."""
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    out = np.empty(v.shape, dtype=np.uint16)
+    _load().oracle_bf16_from_double(_ptr(v), _ptr(out), v.size)
+    return out
+
+
+def double_from_bf16(bits) -> np.ndarray:
+    """Decode bf16 bits to fp64 values."""
+    bits = np.ascontiguousarray(bits, dtype=np.uint16)
+    out = np.empty(bits.shape, dtype=np.float64)
+    _load().oracle_double_from_bf16(_ptr(bits), _ptr(out), bits.size)
+    return out

@@ -1,0 +1,178 @@
+/*
+ * rmsnorm_oracle.c -- plain fp64 CPU reference for the fused row-wise RMSNorm.
+ *
+ * TEST INFRASTRUCTURE, NOT PRODUCT CODE.  Only the test suite, the smoke check
+ * and the benchmark's CPU-baseline / reference legs load this file.  It shares
+ * no code, header, table or helper with the CUDA library, and it does not
+ * include anything from it.
+ *
+ * What it computes, for each row of a row-major [rows, hidden] tensor:
+ *
+ *   h_i   = x_i                               (no residual)
+ *   h_i   = RN_T(x_i + residual_i)            (fused residual add; h is stored
+ *                                               as residual_out, and the norm
+ *                                               is taken of this rounded h)
+ *   S     = sum_i h_i^2                        (fp64, index order)
+ *   r     = 1 / sqrt(S / hidden + eps)
+ *   y_i   = RN_T(h_i * r * w_i)                (w_i dropped with no weight)
+ *
+ * Sources:
+ *  - "Building a GPU compiler from scratch: from PyTorch to CUDA via
+ *    multi-level IR (Emmy)", opening description of the running example: the
+ *    mean of the squares of the row, plus epsilon, inverse square root, and a
+ *    scale of every element by that value and by its learned weight.
+ *  - Same page, section "Tensor IR": the step list square, sum, division by
+ *    the count, addition of epsilon, rsqrt, two multiplications.  The loop
+ *    below takes exactly those steps in that order.
+ *  - The fused residual add, the optional weight and the bf16/fp32 I/O are
+ *    not described on the pages; the reading taken is: h is the sum rounded
+ *    once to the I/O type, and the norm is taken of that rounded h.
+ *  - eps arrives as a float; its exact float value is used.
+ *
+ * Arithmetic: every step in IEEE binary64 with round-to-nearest-even, no
+ * fused multiply-add (built with -ffp-contract=off) and no fast-math.  The
+ * only rounding to the I/O type is the final one per output (and the one that
+ * defines h with a residual).
+ *
+ * bf16 is the upper 16 bits of an IEEE binary32 value: 1 sign bit, 8 exponent
+ * bits, 7 fraction bits.  It is decoded by placing the 16 bits on top of 16
+ * zero bits.  Rounding a double to bf16 is done from that definition: round
+ * the magnitude to 8 significant bits (a fixed quantum of 2^-133 below the
+ * smallest normal 2^-126), ties to even, and overflow to infinity beyond the
+ * largest finite value 255 * 2^120.
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+#include <string.h>
+
+enum { ORACLE_F32 = 0, ORACLE_BF16 = 1 };
+
+static double bf16_to_double(uint16_t bits)
+{
+    uint32_t u = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+static uint16_t double_to_bf16(double v)
+{
+    uint16_t sign = signbit(v) ? 0x8000u : 0u;
+    if (isnan(v))
+        return (uint16_t)(sign | 0x7FC0u);
+    double a = fabs(v);
+    if (isinf(a))
+        return (uint16_t)(sign | 0x7F80u);
+    if (a == 0.0)
+        return sign;
+    int e;
+    frexp(a, &e);            /* a lies in [2^(e-1), 2^e)                  */
+    int q = e - 8;           /* 8 significant bits: quantum 2^(e-1-7)      */
+    if (q < -133)
+        q = -133;            /* subnormal range: fixed quantum 2^-133      */
+    double n = nearbyint(ldexp(a, -q));  /* exact scaling, ties to even    */
+    double r = ldexp(n, q);
+    if (r > ldexp(255.0, 120))           /* above the largest finite bf16  */
+        return (uint16_t)(sign | 0x7F80u);
+    float f = (float)r;                  /* exact: r has <= 8 bits         */
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return (uint16_t)(sign | (uint16_t)(u >> 16));
+}
+
+static double load_elem(const void *p, int64_t i, int dtype)
+{
+    if (dtype == ORACLE_BF16)
+        return bf16_to_double(((const uint16_t *)p)[i]);
+    return (double)((const float *)p)[i];
+}
+
+/* Round v to the I/O type and store it. */
+static void store_elem(void *p, int64_t i, int dtype, double v)
+{
+    if (dtype == ORACLE_BF16)
+        ((uint16_t *)p)[i] = double_to_bf16(v);
+    else
+        ((float *)p)[i] = (float)v;   /* C conversion: round to nearest even */
+}
+
+/* The value the I/O type holds for v (v rounded once to the type). */
+static double round_to_type(double v, int dtype)
+{
+    if (dtype == ORACLE_BF16)
+        return bf16_to_double(double_to_bf16(v));
+    return (double)(float)v;
+}
+
+/* h_i: the row element that is normalised. */
+static double row_input(const void *x, const void *residual, int64_t i, int dtype)
+{
+    double xi = load_elem(x, i, dtype);
+    if (residual == NULL)
+        return xi;
+    return round_to_type(xi + load_elem(residual, i, dtype), dtype);
+}
+
+/*
+ * Rows [row_begin, row_end) of the op.
+ *   x, residual, w : inputs in the I/O type (residual and w may be NULL)
+ *   y              : output in the I/O type
+ *   y_exact        : optional fp64 copy of y before the final rounding
+ *   residual_out   : h in the I/O type; required iff residual is given
+ * Returns 0, or -1 on an invalid argument.
+ */
+int oracle_rmsnorm_rows(const void *x, const void *residual, const void *w,
+                        void *y, double *y_exact, void *residual_out,
+                        int64_t row_begin, int64_t row_end, int64_t hidden,
+                        float eps, int dtype)
+{
+    if (x == NULL || y == NULL || hidden <= 0 || row_begin < 0 || row_end < row_begin)
+        return -1;
+    if (dtype != ORACLE_F32 && dtype != ORACLE_BF16)
+        return -1;
+    if ((residual == NULL) != (residual_out == NULL))
+        return -1;
+
+    const double e = (double)eps;
+    for (int64_t row = row_begin; row < row_end; ++row) {
+        const int64_t base = row * hidden;
+
+        /* square and sum */
+        double sum_sq = 0.0;
+        for (int64_t i = 0; i < hidden; ++i) {
+            double h = row_input(x, residual, base + i, dtype);
+            sum_sq += h * h;
+        }
+        /* divide by the count, add epsilon, inverse square root */
+        double mean_sq = sum_sq / (double)hidden;
+        double inv_rms = 1.0 / sqrt(mean_sq + e);
+
+        /* two multiplications, then one rounding to the I/O type */
+        for (int64_t i = 0; i < hidden; ++i) {
+            double h = row_input(x, residual, base + i, dtype);
+            double v = h * inv_rms;
+            if (w != NULL)
+                v = v * load_elem(w, i, dtype);
+            if (y_exact != NULL)
+                y_exact[base + i] = v;
+            store_elem(y, base + i, dtype, v);
+            if (residual_out != NULL)
+                store_elem(residual_out, base + i, dtype, h);
+        }
+    }
+    return 0;
+}
+
+/* Elementwise conversions, exposed so that tests can pin them on their own. */
+void oracle_bf16_from_double(const double *v, uint16_t *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = double_to_bf16(v[i]);
+}
+
+void oracle_double_from_bf16(const uint16_t *bits, double *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = bf16_to_double(bits[i]);
+}

@@ -1,0 +1,146 @@
+"""Seeded synthetic inputs for the fused RMSNorm, shared by the tests and the benchmark.
+
+This module holds no arithmetic of the method: it only draws random tensors
+and rounds them once to the I/O type.  Both the CUDA path and the CPU oracle
+receive the identical bits from here.
+
+The shapes stand in for the models the pages run: width 576 (SmolLM2-135M) and
+2048 (Llama-3.2-1B) from the model-as-a-kernel card ("Measured"), and the
+per-head qk-norm over 128-element heads (Qwen3 style) from "CuTeDSL at
+Perplexity", section "QK Norm".  Distributions are written N(mean, std).
+
+Recipe: each tensor is drawn in fp32 from its own ``torch.Generator`` on the
+requested device, seeded ``seed`` (x), ``seed+1`` (residual), ``seed+2`` (w) and
+``seed+3`` (outlier mask), scaled and shifted as listed, then rounded once to
+the I/O type.  Outliers: an independent Bernoulli(p) mask multiplies the
+selected entries of x by ``outlier_scale`` before the rounding.  The random
+stream differs between CPU and CUDA generators, so a given (seed, device)
+pair names one input set; parity checks always hand the same tensors to both
+sides.
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Optional
+
+import torch
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    dtype: str                 # "bf16" | "f32" (I/O type of every tensor)
+    rows: int
+    hidden: int
+    eps: float
+    x_std: float
+    res_std: Optional[float]   # None: no fused residual add
+    w_std: Optional[float]     # None: no weight (w ~ 1 + N(0, w_std) otherwise)
+    outlier_frac: float = 0.0
+    outlier_scale: float = 1.0
+    note: str = ""
+
+    @property
+    def has_res(self) -> bool:
+        return self.res_std is not None
+
+    @property
+    def has_w(self) -> bool:
+        return self.w_std is not None
+
+    @property
+    def elem_bytes(self) -> int:
+        return 2 if self.dtype == "bf16" else 4
+
+    def algorithmic_bytes(self, rows: Optional[int] = None) -> int:
+        """Bytes one pass must move: read x (+ residual), write y (+ residual_out), read w once."""
+        r = self.rows if rows is None else rows
+        per_row = self.hidden * self.elem_bytes * (2 + (2 if self.has_res else 0))
+        return r * per_row + (self.hidden * self.elem_bytes if self.has_w else 0)
+
+    def with_rows(self, rows: int) -> "Workload":
+        return dataclasses.replace(self, rows=rows, name=f"{self.name}@rows={rows}")
+
+
+WORKLOADS = {
+    w.name: w
+    for w in [
+        Workload("f32_64x256", "f32", 64, 256, 1e-6, 1.0, None, 0.1,
+                 note="small case the oracle finishes at once"),
+        Workload("bf16_4096x576", "bf16", 4096, 576, 1e-5, 1.0, None, 0.05,
+                 note="SmolLM2-135M width, warp-per-row"),
+        Workload("bf16_res_16384x2048", "bf16", 16384, 2048, 1e-5, 0.5, 1.0, 0.05,
+                 note="Llama-3.2-1B width, fused residual add"),
+        Workload("bf16_qk_262144x128", "bf16", 262144, 128, 1e-6, 2.0, None, 0.1,
+                 note="per-head qk-norm, 8192 tokens x 32 heads, shared weight"),
+        Workload("bf16_decode_1x4096", "bf16", 1, 4096, 1e-6, 2.0, None, 0.1, note="decode latency"),
+        Workload("bf16_decode_8x4096", "bf16", 8, 4096, 1e-6, 2.0, None, 0.1, note="decode latency"),
+        Workload("bf16_decode_64x4096", "bf16", 64, 4096, 1e-6, 2.0, None, 0.1, note="decode latency"),
+        Workload("bf16_res_65536x8192_w", "bf16", 65536, 8192, 1e-6, 1.0, 1.0, 0.1,
+                 outlier_frac=1e-3, outlier_scale=100.0,
+                 note="bandwidth-roofline case with outliers, weight"),
+        Workload("bf16_res_65536x8192_nw", "bf16", 65536, 8192, 1e-6, 1.0, 1.0, None,
+                 outlier_frac=1e-3, outlier_scale=100.0,
+                 note="bandwidth-roofline case with outliers, no weight"),
+    ]
+}
+
+TORCH_DTYPE = {"bf16": torch.bfloat16, "f32": torch.float32}
+
+
+def _gen(device, seed):
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    return g
+
+
+def make_inputs(wl: Workload, seed: int = 0, device="cpu", rows: Optional[int] = None):
+    """Draw (x, residual, w) for ``wl`` as tensors of the I/O type on ``device``.
+
+    ``residual`` and ``w`` are None when the workload has none.  ``rows``
+    overrides the row count (same distributions).
+    """
+    device = torch.device(device)
+    r = wl.rows if rows is None else int(rows)
+    h = wl.hidden
+    dt = TORCH_DTYPE[wl.dtype]
+    x = torch.randn((r, h), generator=_gen(device, seed), device=device, dtype=torch.float32)
+    x.mul_(wl.x_std)
+    if wl.outlier_frac > 0.0:
+        u = torch.rand((r, h), generator=_gen(device, seed + 3), device=device, dtype=torch.float32)
+        x = torch.where(u < wl.outlier_frac, x * wl.outlier_scale, x)
+        del u
+    x = x.to(dt)
+    residual = None
+    if wl.has_res:
+        residual = torch.randn((r, h), generator=_gen(device, seed + 1), device=device,
+                               dtype=torch.float32).mul_(wl.res_std).to(dt)
+    w = None
+    if wl.has_w:
+        w = (torch.randn((h,), generator=_gen(device, seed + 2), device=device,
+                         dtype=torch.float32).mul_(wl.w_std).add_(1.0)).to(dt)
+    return x, residual, w
+
+
+def random_rows(dtype: str, rows: int, hidden: int, seed: int, device="cpu", std: float = 1.0):
+    """Plain N(0, std) rows in the I/O type (edge-case and sweep tests)."""
+    t = torch.randn((rows, hidden), generator=_gen(torch.device(device), seed),
+                    device=device, dtype=torch.float32).mul_(std)
+    return t.to(TORCH_DTYPE[dtype])
+
+
+def to_numpy_bits(t: Optional[torch.Tensor]):
+    """Host numpy view of a tensor in the oracle's convention (bf16 -> uint16 bits)."""
+    if t is None:
+        return None
+    t = t.detach().to("cpu").contiguous()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view("uint16")
+    return t.numpy()
+
+
+def from_numpy_bits(a, dtype: str) -> torch.Tensor:
+    """Inverse of ``to_numpy_bits`` (CPU tensor)."""
+    if dtype == "bf16":
+        return torch.from_numpy(a.view("int16").copy()).view(torch.bfloat16)
+    return torch.from_numpy(a.copy())

@@ -1,0 +1,18 @@
+"""Test configuration: the ``gpu`` marker and import paths.
+
+``-m "not gpu"`` runs the oracle pins, the host-side logic and the library
+load/export checks on a machine without a GPU; ``-m gpu`` runs the parity
+tests of the CUDA path against the oracle on a GB300.
+"""
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+TESTS = os.path.dirname(os.path.abspath(__file__))
+for p in (ROOT, TESTS):
+    if p not in sys.path:
+        sys.path.insert(0, p)
+
+
+def pytest_configure(config):
+    config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a) and the built library")

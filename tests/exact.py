@@ -1,0 +1,134 @@
+"""Exact rational arithmetic used to pin the oracle (brute force on tiny rows).
+
+Nothing here shares code with the oracle or the CUDA library.  Floating-point
+formats are decoded from their IEEE definitions into ``fractions.Fraction``,
+and a result of the form ``sign * sqrt(q)`` with ``q`` rational is rounded to
+the nearest representable value (ties to even) by comparing ``q`` with exact
+squares of the candidate values and of the midpoints between them.  No
+floating-point operation takes part in a decision.
+"""
+from __future__ import annotations
+
+from fractions import Fraction
+
+# (exponent bits, fraction bits) of the formats the path uses.
+FORMATS = {"bf16": (8, 7), "f32": (8, 23)}
+
+
+def _fmt(fmt):
+    e_bits, f_bits = FORMATS[fmt]
+    bias = (1 << (e_bits - 1)) - 1
+    inf_ord = ((1 << e_bits) - 1) << f_bits        # ordinal of +inf
+    return e_bits, f_bits, bias, inf_ord
+
+
+def decode(bits: int, fmt: str):
+    """Exact value of a finite encoding as a Fraction (None for inf/NaN)."""
+    e_bits, f_bits, bias, _ = _fmt(fmt)
+    sign = -1 if (bits >> (e_bits + f_bits)) & 1 else 1
+    e = (bits >> f_bits) & ((1 << e_bits) - 1)
+    f = bits & ((1 << f_bits) - 1)
+    if e == (1 << e_bits) - 1:
+        return None
+    if e == 0:
+        mag = Fraction(f, 1 << f_bits) * Fraction(2) ** (1 - bias)
+    else:
+        mag = (1 + Fraction(f, 1 << f_bits)) * Fraction(2) ** (e - bias)
+    return sign * mag
+
+
+def _ord_value(k: int, fmt: str) -> Fraction:
+    """Value of positive ordinal k; the +inf ordinal stands for 2^(emax+1)."""
+    e_bits, f_bits, bias, inf_ord = _fmt(fmt)
+    if k == inf_ord:
+        return Fraction(2) ** (bias + 1)
+    return decode(k, fmt)
+
+
+def round_sqrt(sign: int, q: Fraction, fmt: str) -> int:
+    """Bits of the correctly rounded (nearest, ties to even) value sign*sqrt(q), q >= 0."""
+    e_bits, f_bits, bias, inf_ord = _fmt(fmt)
+    sign_bit = (1 << (e_bits + f_bits)) if sign < 0 else 0
+    if q == 0:
+        return sign_bit
+    # largest ordinal k with value(k)^2 <= q (k may be the inf ordinal's predecessor)
+    lo, hi = 0, inf_ord
+    if _ord_value(inf_ord, fmt) ** 2 <= q:
+        return sign_bit | inf_ord
+    while hi - lo > 1:
+        mid = (lo + hi) // 2
+        if _ord_value(mid, fmt) ** 2 <= q:
+            lo = mid
+        else:
+            hi = mid
+    a, b = _ord_value(lo, fmt), _ord_value(hi, fmt)
+    m2 = ((a + b) / 2) ** 2
+    if q < m2:
+        k = lo
+    elif q > m2:
+        k = hi
+    else:
+        k = lo if lo % 2 == 0 else hi
+    return sign_bit | k
+
+
+def round_value(v: Fraction, fmt: str) -> int:
+    """Bits of the correctly rounded value of a rational v."""
+    return round_sqrt(-1 if v < 0 else 1, v * v, fmt)
+
+
+def midpoint_distance(sign_q: Fraction, fmt: str) -> Fraction:
+    """Relative distance |q - m^2| / m^2 from q to the nearest rounding midpoint squared."""
+    q = sign_q
+    e_bits, f_bits, bias, inf_ord = _fmt(fmt)
+    lo, hi = 0, inf_ord
+    while hi - lo > 1:
+        mid = (lo + hi) // 2
+        if _ord_value(mid, fmt) ** 2 <= q:
+            lo = mid
+        else:
+            hi = mid
+    best = None
+    for k in (lo - 1, lo, hi):
+        if k < 0 or k + 1 > inf_ord:
+            continue
+        m2 = ((_ord_value(k, fmt) + _ord_value(k + 1, fmt)) / 2) ** 2
+        d = abs(q - m2) / m2
+        best = d if best is None else min(best, d)
+    return best
+
+
+def rmsnorm_row_exact(x, w, residual, eps_bits_value: Fraction, fmt: str):
+    """Exact RMSNorm of one row given as lists of encodings (ints).
+
+    Returns (y_bits, residual_out_bits or None, q_list, signs) where y_i =
+    sign_i * sqrt(q_i) exactly, before rounding.
+    """
+    n = len(x)
+    xs = [decode(b, fmt) for b in x]
+    if residual is not None:
+        rs = [decode(b, fmt) for b in residual]
+        h_bits = [round_value(a + b, fmt) for a, b in zip(xs, rs)]
+        hs = [decode(b, fmt) for b in h_bits]
+    else:
+        h_bits = None
+        hs = xs
+    ws = [decode(b, fmt) for b in w] if w is not None else [Fraction(1)] * n
+    s = sum(h * h for h in hs)
+    denom = s / n + eps_bits_value
+    qs, signs, y_bits = [], [], []
+    sign_mask = 1 << (sum(FORMATS[fmt]))
+    for i in range(n):
+        p = hs[i] * ws[i]
+        q = p * p / denom
+        if p != 0:
+            sg = -1 if p < 0 else 1
+        else:
+            # IEEE sign of a zero product: XOR of the operand signs (r > 0)
+            hb = (h_bits[i] if h_bits is not None else x[i]) & sign_mask
+            wb = (w[i] & sign_mask) if w is not None else 0
+            sg = -1 if (hb != 0) != (wb != 0) else 1
+        qs.append(q)
+        signs.append(sg)
+        y_bits.append(round_sqrt(sg, q, fmt))
+    return y_bits, h_bits, qs, signs

@@ -1,0 +1,109 @@
+"""Deliberately broken RMSNorm variants, used to show that the pins catch the
+plausible mistakes an oracle could make (a dropped term, a wrong index, the
+wrong rounding, eps in the wrong place ...).
+
+``reference(...)`` is an independent numpy fp64 restatement of the definition
+("Building a GPU compiler from scratch ... (Emmy)", running example and
+section "Tensor IR").  With ``mistake=None`` it must pass every pin; with any
+named mistake at least one pin must fail.  Test code only.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+# significant bits, smallest quantum exponent, largest finite value
+_FMT = {"bf16": (8, -133, 255.0 * 2.0 ** 120), "f32": (24, -149, (2.0 ** 24 - 1) * 2.0 ** 104)}
+
+MISTAKES = [
+    "eps_on_sum", "eps_outside_sqrt", "divide_by_h_minus_1", "no_sqrt", "sqrt_not_inverse",
+    "weight_reversed", "no_weight", "unrounded_residual", "global_mean", "trunc_rounding",
+    "ties_away", "abs_output", "residual_out_is_x", "sum_of_abs", "stats_from_x",
+    "eps_as_double", "round_via_f32",
+]
+
+
+def _round(v, dt, mode="rne"):
+    """Round fp64 values to the format (value as fp64) with the given tie rule."""
+    p, qmin, vmax = _FMT[dt]
+    a = np.abs(v)
+    with np.errstate(invalid="ignore", over="ignore"):
+        _, e = np.frexp(a)
+        q = np.maximum(e - p, qmin)
+        s = np.ldexp(a, -q)
+        if mode == "rne":
+            n = np.rint(s)
+        elif mode == "trunc":
+            n = np.floor(s)
+        else:  # ties away from zero
+            n = np.floor(s + 0.5)
+        r = np.ldexp(n, q)
+        r = np.where(np.isinf(a), np.inf, r)
+        r = np.where(r > vmax, np.inf, r)
+        r = np.copysign(r, v)
+        r = np.where(np.isnan(v), np.nan, r)
+    return r
+
+
+def _decode(a, dt):
+    if dt == "bf16":
+        return (np.asarray(a, dtype=np.uint32) << 16).view(np.float32).astype(np.float64)
+    return np.asarray(a, dtype=np.float32).astype(np.float64)
+
+
+def _encode(v, dt):
+    f = v.astype(np.float32)   # exact: v already holds a value of the format
+    if dt == "bf16":
+        return (f.view(np.uint32) >> 16).astype(np.uint16)
+    return f
+
+
+def reference(x, w, residual, eps, dt, mistake=None):
+    mode = {"trunc_rounding": "trunc", "ties_away": "away"}.get(mistake, "rne")
+    xv = _decode(x, dt)
+    e = float(eps) if mistake == "eps_as_double" else float(np.float32(eps))
+    if residual is not None:
+        s = xv + _decode(residual, dt)
+        h_store = _round(s, dt, mode)
+        h = s if mistake == "unrounded_residual" else h_store
+        if mistake == "residual_out_is_x":
+            h_store = xv
+    else:
+        h = xv
+        h_store = None
+    stats = xv if mistake == "stats_from_x" else h
+    n = h.shape[1]
+    with np.errstate(invalid="ignore", divide="ignore", over="ignore"):
+        sq = np.abs(stats) if mistake == "sum_of_abs" else stats * stats
+        if mistake == "global_mean":
+            total = sq.sum() / sq.size * n
+            ssum = np.full((h.shape[0], 1), total)
+        else:
+            ssum = sq.sum(axis=1, keepdims=True)
+        denom = n - 1 if (mistake == "divide_by_h_minus_1" and n > 1) else n
+        if mistake == "eps_on_sum":
+            inner = ssum + e
+            mean_e = inner / denom
+        else:
+            mean_e = ssum / denom + e
+        if mistake == "eps_outside_sqrt":
+            r = 1.0 / (np.sqrt(ssum / denom) + e)
+        elif mistake == "no_sqrt":
+            r = 1.0 / mean_e
+        elif mistake == "sqrt_not_inverse":
+            r = np.sqrt(mean_e)
+        else:
+            r = 1.0 / np.sqrt(mean_e)
+        y = h * r
+        if w is not None and mistake != "no_weight":
+            wv = _decode(w, dt)
+            if mistake == "weight_reversed":
+                wv = wv[::-1]
+            y = y * wv
+        if mistake == "abs_output":
+            y = np.abs(y)
+    if mistake == "round_via_f32":
+        y = y.astype(np.float32).astype(np.float64)
+    yr = _round(y, dt, mode)
+    out_y = _encode(yr, dt)
+    out_h = None if h_store is None else _encode(h_store, dt)
+    return out_y, out_h, y

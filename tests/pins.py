@@ -1,0 +1,374 @@
+"""Pins for an RMSNorm reference implementation: facts fixed by the definition
+and by mathematics, not by any implementation.
+
+Each ``pin_*`` takes ``impl(x, w, residual, eps, dtype) -> (y, residual_out, y_exact)``
+with numpy arrays in the oracle's convention (bf16 as uint16 bits, fp32 as
+float32) and returns a list of failure messages (empty when the pin holds).
+The same pins run against the oracle (all must hold) and against deliberately
+broken variants of it (each must be caught by at least one pin).
+
+Where the definition comes from: "Building a GPU compiler from scratch: from
+PyTorch to CUDA via multi-level IR (Emmy)" -- running example and section
+"Tensor IR".  Expected values are derived with exact rational arithmetic
+(``tests/exact.py``) or are closed forms / invariants of that definition.
+"""
+from __future__ import annotations
+
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+
+import exact
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "closed_forms.txt")
+SIGN_MASK = {"bf16": 0x8000, "f32": 0x80000000}
+
+
+# ---------------------------------------------------------------- helpers
+
+def bits_of(a, dtype):
+    a = np.ascontiguousarray(a)
+    return a.astype(np.uint16) if dtype == "bf16" else a.view(np.uint32)
+
+
+def encode_exact(v: Fraction, dtype):
+    """Encoding of an exactly representable rational (raises if not exact)."""
+    b = exact.round_value(v, dtype)
+    if exact.decode(b, dtype) != v:
+        raise ValueError(f"{v} is not representable in {dtype}")
+    if v == 0:
+        b = 0
+    return b
+
+
+def to_array(bits_list, dtype):
+    if dtype == "bf16":
+        return np.array(bits_list, dtype=np.uint16)
+    return np.array(bits_list, dtype=np.uint32).view(np.float32)
+
+
+def f32_exact(eps) -> Fraction:
+    return Fraction(float(np.float32(eps)))
+
+
+def _expand(tokens):
+    out = []
+    for t in tokens:
+        if "*" in t:
+            v, n = t.split("*")
+            out.extend([v] * int(n))
+        else:
+            out.append(t)
+    return out
+
+
+def parse_golden(path=GOLDEN):
+    cases, cur = [], None
+    for raw in open(path):
+        line = raw.strip()
+        if not line or line.startswith("#"):
+            continue
+        key, *rest = line.split()
+        if key == "case":
+            cur = {"name": rest[0]}
+            cases.append(cur)
+            continue
+        if key == "dtype":
+            cur["dtype"] = rest[0]
+        elif key == "eps":
+            cur["eps"] = Fraction(rest[0])
+        elif key in ("x", "w", "residual", "y2", "resout"):
+            cur[key] = None if rest == ["-"] else [Fraction(t) for t in _expand(rest)]
+        elif key == "sign":
+            cur["sign"] = [-1 if t == "-" else 1 for t in _expand(rest)]
+        else:
+            raise ValueError(f"unknown key {key!r} in {path}")
+    return cases
+
+
+def random_bits(rng, dtype, n, lo_exp=-6, hi_exp=6):
+    """Random finite encodings: random sign and fraction, exponent in a range
+    that keeps squares and sums far from overflow and underflow."""
+    if dtype == "bf16":
+        e_bits, f_bits, bias = 8, 7, 127
+    else:
+        e_bits, f_bits, bias = 8, 23, 127
+    sign = rng.integers(0, 2, n)
+    e = rng.integers(lo_exp + bias, hi_exp + bias + 1, n)
+    f = rng.integers(0, 1 << f_bits, n)
+    bits = (sign << (e_bits + f_bits)) | (e << f_bits) | f
+    return [int(b) for b in bits]
+
+
+# ---------------------------------------------------------------- pins
+
+def pin_golden(impl):
+    """Hand-derived closed-form cases stored in tests/golden/closed_forms.txt."""
+    fails = []
+    for c in parse_golden():
+        dt = c["dtype"]
+        n = len(c["x"])
+        x = to_array([encode_exact(v, dt) for v in c["x"]], dt).reshape(1, n)
+        w = None if c["w"] is None else to_array([encode_exact(v, dt) for v in c["w"]], dt)
+        res = None if c["residual"] is None else to_array(
+            [encode_exact(v, dt) for v in c["residual"]], dt).reshape(1, n)
+        eps = float(c["eps"])
+        y, rout, _ = impl(x, w, res, eps, dt)
+        want = [exact.round_sqrt(s, q, dt) for s, q in zip(c["sign"], c["y2"])]
+        got = [int(b) for b in bits_of(y, dt).reshape(-1)]
+        if got != want:
+            fails.append(f"golden {c['name']}: y bits {got[:8]} != {want[:8]}")
+        if c.get("resout") is not None:
+            want_r = [encode_exact(v, dt) for v in c["resout"]]
+            got_r = [int(b) for b in bits_of(rout, dt).reshape(-1)] if rout is not None else None
+            if got_r != want_r:
+                fails.append(f"golden {c['name']}: residual_out {got_r} != {want_r}")
+    return fails
+
+
+def pin_bruteforce(impl, n_cases=60, seed=1234):
+    """Random tiny rows (hidden 1..8, three rows each), every option combination,
+    checked bit for bit against the exactly rounded rational answer."""
+    rng = np.random.default_rng(seed)
+    fails = []
+    eps_choices = [0.0, 1e-6, 1e-5, 0.25, 3.0]
+    for k in range(n_cases):
+        dt = ("bf16", "f32")[k % 2]
+        has_w = bool((k // 2) % 2)
+        has_res = bool((k // 4) % 2)
+        hidden = int(rng.integers(1, 9))
+        rows = 3
+        eps = eps_choices[k % len(eps_choices)]
+        xb = [random_bits(rng, dt, hidden) for _ in range(rows)]
+        rb = [random_bits(rng, dt, hidden) for _ in range(rows)] if has_res else None
+        wb = random_bits(rng, dt, hidden, -2, 2) if has_w else None
+        x = to_array(sum(xb, []), dt).reshape(rows, hidden)
+        res = to_array(sum(rb, []), dt).reshape(rows, hidden) if has_res else None
+        w = to_array(wb, dt) if has_w else None
+        y, rout, _ = impl(x, w, res, eps, dt)
+        yb = bits_of(y, dt).reshape(rows, hidden)
+        for r in range(rows):
+            want, want_h, qs, signs = exact.rmsnorm_row_exact(
+                xb[r], wb, rb[r] if has_res else None, f32_exact(eps), dt)
+            for i in range(hidden):
+                if int(yb[r, i]) != want[i]:
+                    d = exact.midpoint_distance(qs[i], dt)
+                    if d is None or d > Fraction(1, 2 ** 44):
+                        fails.append(f"bruteforce case {k} ({dt}, w={has_w}, res={has_res}, "
+                                     f"H={hidden}, eps={eps}) row {r} elem {i}: "
+                                     f"{int(yb[r, i]):#x} != {want[i]:#x}")
+            if has_res:
+                got_h = [int(b) for b in bits_of(rout, dt).reshape(rows, hidden)[r]]
+                if got_h != want_h:
+                    fails.append(f"bruteforce case {k}: residual_out row {r} {got_h} != {want_h}")
+    return fails
+
+
+def pin_constant_row(impl):
+    """x_i = c for every i: y_i = c / sqrt(c^2 + eps) * w_i (closed form)."""
+    fails = []
+    rng = np.random.default_rng(7)
+    for dt in ("bf16", "f32"):
+        for hidden in (1, 7, 576, 4096):
+            for c in (Fraction(3, 4), Fraction(-5, 2), Fraction(1, 64)):
+                for eps in (0.0, 1e-5, 0.5):
+                    cb = encode_exact(c, dt)
+                    x = to_array([cb] * hidden, dt).reshape(1, hidden)
+                    wb = random_bits(rng, dt, hidden, -1, 1)
+                    w = to_array(wb, dt)
+                    y, _, _ = impl(x, w, None, eps, dt)
+                    e = f32_exact(eps)
+                    got = bits_of(y, dt).reshape(-1)
+                    for i in (0, hidden // 2, hidden - 1):
+                        wi = exact.decode(wb[i], dt)
+                        p = c * wi
+                        q = p * p / (c * c + e)
+                        want = exact.round_sqrt(-1 if p < 0 else 1, q, dt)
+                        if int(got[i]) != want:
+                            fails.append(f"constant row {dt} H={hidden} c={c} eps={eps} i={i}: "
+                                         f"{int(got[i]):#x} != {want:#x}")
+    return fails
+
+
+def pin_scale_invariance(impl):
+    """With eps = 0, y(a*x) = sign(a) * y(x) for a power of two a (bit-exact in
+    the I/O type, since the scaled inputs are exact); also y(-x) = -y(x)."""
+    fails = []
+    rng = np.random.default_rng(11)
+    for dt in ("bf16", "f32"):
+        for hidden in (5, 64, 1000):
+            xb = random_bits(rng, dt, 4 * hidden, -3, 3)
+            x = to_array(xb, dt).reshape(4, hidden)
+            w = to_array(random_bits(rng, dt, hidden, -1, 1), dt)
+            y0, _, y0e = impl(x, w, None, 0.0, dt)
+            for a in (2.0 ** 5, 2.0 ** -7, -1.0, -(2.0 ** 3)):
+                if dt == "bf16":
+                    xf = np.array(xb, dtype=np.uint32) << 16
+                    xs = (xf.view(np.float32) * np.float32(a)).view(np.uint32) >> 16
+                    xa = xs.astype(np.uint16).reshape(4, hidden)
+                else:
+                    xa = (x * np.float32(a)).astype(np.float32)
+                ya, _, _ = impl(xa, w, None, 0.0, dt)
+                b0 = bits_of(y0, dt).astype(np.uint64)
+                ba = bits_of(ya, dt).astype(np.uint64)
+                if a < 0:
+                    b0 = b0 ^ SIGN_MASK[dt]
+                if not np.array_equal(b0, ba):
+                    fails.append(f"scale invariance {dt} H={hidden} a={a}: "
+                                 f"{int((b0 != ba).sum())} elements differ")
+    return fails
+
+
+def pin_unit_rms(impl):
+    """With no weight and eps = 0, the fp64 result has mean(y^2) = 1."""
+    fails = []
+    rng = np.random.default_rng(5)
+    for dt in ("bf16", "f32"):
+        for hidden in (3, 128, 2048):
+            x = to_array(random_bits(rng, dt, 5 * hidden, -4, 4), dt).reshape(5, hidden)
+            _, _, ye = impl(x, None, None, 0.0, dt)
+            if ye is None:
+                fails.append("unit rms: no fp64 result")
+                continue
+            m = (ye * ye).mean(axis=1)
+            if not np.all(np.abs(m - 1.0) < 1e-12):
+                fails.append(f"unit rms {dt} H={hidden}: mean(y^2) = {m}")
+    return fails
+
+
+def pin_special_values(impl):
+    """NaN, infinity and zero rows follow IEEE arithmetic of the definition."""
+    fails = []
+    for dt in ("bf16", "f32"):
+        one = encode_exact(Fraction(1), dt)
+        two = encode_exact(Fraction(2), dt)
+        nan = 0x7FC0 if dt == "bf16" else 0x7FC00000
+        inf = 0x7F80 if dt == "bf16" else 0x7F800000
+        x = to_array([one, two, nan, one,    # NaN row -> all NaN
+                      one, inf, two, 0,      # inf row -> inf*0 = NaN at inf, 0 elsewhere
+                      0, 0, 0, 0], dt).reshape(3, 4)  # zero row, eps > 0 -> zeros
+        y, _, _ = impl(x, None, None, 1e-5, dt)
+        yv = (np.array(bits_of(y, dt), dtype=np.uint32) << 16).view(np.float32) if dt == "bf16" \
+            else np.asarray(y, dtype=np.float32)
+        yv = yv.reshape(3, 4)
+        if not np.all(np.isnan(yv[0])):
+            fails.append(f"special {dt}: NaN row gave {yv[0]}")
+        if not (np.isnan(yv[1, 1]) and np.all(yv[1, [0, 2, 3]] == 0)):
+            fails.append(f"special {dt}: inf row gave {yv[1]}")
+        if not np.all(yv[2] == 0):
+            fails.append(f"special {dt}: zero row gave {yv[2]}")
+        # eps = 0 on a zero row: 0 * (1 / sqrt(0)) = 0 * inf = NaN
+        y0, _, _ = impl(to_array([0, 0], dt).reshape(1, 2), None, None, 0.0, dt)
+        y0v = (np.array(bits_of(y0, dt), dtype=np.uint32) << 16).view(np.float32) if dt == "bf16" \
+            else np.asarray(y0, dtype=np.float32)
+        if not np.all(np.isnan(y0v)):
+            fails.append(f"special {dt}: zero row with eps=0 gave {y0v}")
+    return fails
+
+
+def pin_single_element(impl):
+    """hidden = 1: y = x * w / sqrt(x^2 + eps)."""
+    fails = []
+    rng = np.random.default_rng(3)
+    for dt in ("bf16", "f32"):
+        xb = random_bits(rng, dt, 16, -3, 3)
+        wb = random_bits(rng, dt, 1, -1, 1)
+        x = to_array(xb, dt).reshape(16, 1)
+        w = to_array(wb, dt)
+        for eps in (0.0, 1e-6, 2.0):
+            y, _, _ = impl(x, w, None, eps, dt)
+            got = bits_of(y, dt).reshape(-1)
+            e = f32_exact(eps)
+            wv = exact.decode(wb[0], dt)
+            for i, b in enumerate(xb):
+                xv = exact.decode(b, dt)
+                p = xv * wv
+                want = exact.round_sqrt(-1 if p < 0 else 1, p * p / (xv * xv + e), dt)
+                if int(got[i]) != want:
+                    fails.append(f"single element {dt} eps={eps}: {int(got[i]):#x} != {want:#x}")
+    return fails
+
+
+def pin_row_independence(impl):
+    """Each row is normalised on its own: a batch equals its rows run one by one."""
+    fails = []
+    rng = np.random.default_rng(9)
+    for dt in ("bf16", "f32"):
+        x = to_array(random_bits(rng, dt, 6 * 33, -5, 5), dt).reshape(6, 33)
+        r = to_array(random_bits(rng, dt, 6 * 33, -5, 5), dt).reshape(6, 33)
+        w = to_array(random_bits(rng, dt, 33, -1, 1), dt)
+        yb, hb, _ = impl(x, w, r, 1e-6, dt)
+        for i in range(6):
+            yi, hi, _ = impl(x[i:i + 1], w, r[i:i + 1], 1e-6, dt)
+            if not (np.array_equal(bits_of(yi, dt), bits_of(yb[i:i + 1], dt))
+                    and np.array_equal(bits_of(hi, dt), bits_of(hb[i:i + 1], dt))):
+                fails.append(f"row independence {dt}: row {i} differs")
+    return fails
+
+
+def pin_eps_dominated(impl):
+    """Rows far below eps: y_i ~ c * w_i / sqrt(eps), which depends on the exact
+    float32 value of eps (the value the caller passes); every element is checked."""
+    fails = []
+    rng = np.random.default_rng(21)
+    for dt in ("bf16", "f32"):
+        hidden = 4096
+        c = Fraction(1, 2 ** 20)
+        x = to_array([encode_exact(c, dt)] * hidden, dt).reshape(1, hidden)
+        wb = random_bits(rng, dt, hidden, -1, 1)
+        w = to_array(wb, dt)
+        for eps in (1e-6, 1e-5):
+            y, _, _ = impl(x, w, None, eps, dt)
+            got = bits_of(y, dt).reshape(-1)
+            e = f32_exact(eps)
+            bad = 0
+            for i in range(hidden):
+                p = c * exact.decode(wb[i], dt)
+                want = exact.round_sqrt(-1 if p < 0 else 1, p * p / (c * c + e), dt)
+                bad += int(got[i]) != want
+            if bad:
+                fails.append(f"eps-dominated {dt} eps={eps}: {bad} of {hidden} elements differ")
+    return fails
+
+
+def pin_near_ties(impl, trials=400_000, seed=77):
+    """bf16 outputs whose exact value lies within 2^-20 (relative) of a rounding
+    midpoint, found by a seeded search over random two-element rows; each is
+    checked against the exactly rounded answer.  A result rounded twice (to
+    fp32 first, then to bf16) fails here."""
+    rng = np.random.default_rng(seed)
+    dt = "bf16"
+    xb = np.array(random_bits(rng, dt, 2 * trials, -4, 4), dtype=np.uint32).reshape(trials, 2)
+    wb = np.array(random_bits(rng, dt, 2, -1, 1), dtype=np.uint32)
+    xv = (xb << 16).view(np.float32).astype(np.float64)
+    wv = (wb << 16).view(np.float32).astype(np.float64)
+    y = xv * wv / np.sqrt((xv * xv).mean(axis=1, keepdims=True))
+    a = np.abs(y)
+    _, e = np.frexp(a)
+    scaled = np.ldexp(a, -(e - 8))            # 8 significant bits before the point
+    frac = scaled - np.floor(scaled)
+    near = np.abs(frac - 0.5) < 2.0 ** -12    # within 2^-20 relative of a midpoint
+    rows_idx = np.unique(np.nonzero(near)[0])[:64]
+    fails = []
+    if len(rows_idx) < 8:
+        return [f"near ties: search found only {len(rows_idx)} rows"]
+    x = xb[rows_idx].astype(np.uint16)
+    w = wb.astype(np.uint16)
+    yo, _, _ = impl(x, w, None, 0.0, dt)
+    got = bits_of(yo, dt)
+    for k, r in enumerate(rows_idx):
+        want, _, qs, _ = exact.rmsnorm_row_exact([int(b) for b in xb[r]], [int(b) for b in wb],
+                                                 None, Fraction(0), dt)
+        for i in range(2):
+            if int(got[k, i]) != want[i]:
+                d = exact.midpoint_distance(qs[i], dt)
+                if d is None or d > Fraction(1, 2 ** 44):
+                    fails.append(f"near ties row {r} elem {i}: {int(got[k, i]):#x} != {want[i]:#x}")
+    return fails
+
+
+ALL_PINS = [pin_golden, pin_bruteforce, pin_constant_row, pin_scale_invariance,
+            pin_unit_rms, pin_special_values, pin_single_element, pin_row_independence,
+            pin_eps_dominated, pin_near_ties]

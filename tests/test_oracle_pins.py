@@ -1,0 +1,84 @@
+"""The oracle pinned to facts other than itself (CPU only).
+
+Every pin in ``pins.py`` must hold for the oracle; every planted mistake in
+``mutants.py`` must be caught by at least one pin; and an independent numpy
+restatement of the definition must agree with the oracle bit for bit on
+seeded inputs shaped like the workloads.
+"""
+import numpy as np
+import pytest
+
+import mutants
+import oracle
+import pins
+from row_reduction_norm_gb300 import workloads as W
+
+
+def oracle_impl(x, w, residual, eps, dtype):
+    return oracle.rmsnorm(x, w=w, residual=residual, eps=eps, dtype=dtype, want_exact=True)
+
+
+@pytest.mark.parametrize("pin", pins.ALL_PINS, ids=lambda p: p.__name__)
+def test_oracle_pin(pin):
+    assert pin(oracle_impl) == []
+
+
+def test_oracle_bruteforce_many():
+    assert pins.pin_bruteforce(oracle_impl, n_cases=600, seed=99) == []
+
+
+def test_numpy_restatement_passes_pins():
+    impl = lambda x, w, r, e, d: mutants.reference(x, w, r, e, d)
+    for pin in pins.ALL_PINS:
+        assert pin(impl) == [], pin.__name__
+
+
+@pytest.mark.parametrize("mistake", mutants.MISTAKES)
+def test_pins_catch_planted_mistake(mistake):
+    impl = lambda x, w, r, e, d: mutants.reference(x, w, r, e, d, mistake=mistake)
+    caught = []
+    for pin in pins.ALL_PINS:
+        try:
+            fails = pin(impl)
+        except Exception as ex:  # a crash also counts as caught
+            fails = [repr(ex)]
+        if fails:
+            caught.append(pin.__name__)
+            break   # one catching pin is enough; the pins are ordered cheapest first
+    assert caught, f"no pin catches the planted mistake {mistake!r}"
+
+
+@pytest.mark.parametrize("name", ["f32_64x256", "bf16_4096x576", "bf16_res_16384x2048",
+                                  "bf16_res_65536x8192_nw"])
+def test_oracle_matches_numpy_restatement(name):
+    wl = W.WORKLOADS[name]
+    rows = min(wl.rows, 256)
+    x, r, w = W.make_inputs(wl, seed=3, rows=rows)
+    xn, rn, wn = W.to_numpy_bits(x), W.to_numpy_bits(r), W.to_numpy_bits(w)
+    y, h, _ = oracle.rmsnorm(xn, w=wn, residual=rn, eps=wl.eps, dtype=wl.dtype)
+    y2, h2, _ = mutants.reference(xn, wn, rn, wl.eps, wl.dtype)
+    assert np.array_equal(pins.bits_of(y, wl.dtype), pins.bits_of(y2, wl.dtype))
+    if rn is not None:
+        assert np.array_equal(pins.bits_of(h, wl.dtype), pins.bits_of(h2, wl.dtype))
+
+
+def test_oracle_threads_match_single_thread():
+    wl = W.WORKLOADS["bf16_res_16384x2048"]
+    x, r, w = W.make_inputs(wl, seed=5, rows=300)
+    xn, rn, wn = W.to_numpy_bits(x), W.to_numpy_bits(r), W.to_numpy_bits(w)
+    a = oracle.rmsnorm(xn, w=wn, residual=rn, eps=wl.eps, dtype="bf16", threads=1)
+    b = oracle.rmsnorm(xn, w=wn, residual=rn, eps=wl.eps, dtype="bf16", threads=7)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_bf16_conversion_definition():
+    # every bf16 encoding decodes to the value of its fp32 extension and rounds back to itself
+    bits = np.arange(0, 1 << 16, dtype=np.uint32).astype(np.uint16)
+    vals = oracle.double_from_bf16(bits)
+    with np.errstate(invalid="ignore"):
+        ref = (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    same = (vals == ref) | (np.isnan(vals) & np.isnan(ref))
+    assert same.all()
+    finite = ~np.isnan(vals)
+    back = oracle.bf16_from_double(vals[finite])
+    assert np.array_equal(back, bits[finite])
