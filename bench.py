@@ -1,0 +1,604 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused row-wise RMSNorm on GB300 (one JSON line on stdout).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+A step is one pass of the whole op (load, optional residual add, sum of
+squares, scale, weighted store) over one batch of the workload: one launch of
+the library through its C ABI.  The headline workload is bf16 4096 x 576 with
+a weight (SmolLM2-135M width).  The metric is achieved HBM bandwidth over the
+op's algorithmic bytes (read x [+ residual], write y [+ residual_out], read w
+once per launch), with rows/s beside it.
+
+Timing: inputs are resident on the device before the timed region; launches
+are recorded in CUDA graphs and rotate through enough distinct buffer sets
+that their footprint is at least 4x the L2 size, so each launch reads from
+HBM; CUDA events on the launching stream bracket exactly K steps, with a
+barrier and a device synchronise on both sides; nvidia-smi samples clocks
+during the timed region.  ``e2e`` repeats the measurement with the inputs
+copied from pinned host memory and the outputs read back every step.  The
+CPU baseline is the fp64 oracle on the host cores over a bounded sample.
+
+Under torchrun each rank runs its own replica on its own GPU (the op has no
+exchange between rows, so there is no collective on the data path); the
+value is the work of all ranks over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+HEADLINE = "bf16_4096x576"
+METRIC = "RMSNorm achieved HBM GB/s and % of GB300 peak; rows/s per config"
+PER_CONFIG = ["f32_64x256", "bf16_res_16384x2048", "bf16_qk_262144x128", "bf16_decode_1x4096",
+              "bf16_decode_8x4096", "bf16_decode_64x4096", "bf16_res_65536x8192_w",
+              "bf16_res_65536x8192_nw"]
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description="fused RMSNorm benchmark")
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200000)
+    ap.add_argument("--warmup", type=int, default=2000)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=HEADLINE)
+    ap.add_argument("--no-per-config", action="store_true", help="skip the per-config table")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="CPU work for the oracle baseline (0 disables it)")
+    ap.add_argument("--e2e-steps", type=int, default=0, help="steps of the e2e region (0: auto)")
+    ap.add_argument("--ncu-case", default=None,
+                    help="profiling mode: launch this workload --launches times and exit")
+    ap.add_argument("--launches", type=int, default=3)
+    return ap.parse_args(argv)
+
+
+# ------------------------------------------------------------------ helpers
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "row_reduction_norm_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload):
+    """DRAM bytes per launch from the committed ncu summary of this workload,
+    if it was taken on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", f"rmsnorm_{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m_hash = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", text)
+    m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
+    if not (m_hash and m_bytes) or m_hash.group(1) != kernel_source_hash():
+        return None
+    return int(m_bytes.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi samples (host receive time attached) while the GPU works."""
+
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={','.join(self.FIELDS)}", "--format=csv,noheader,nounits",
+               "-lms", "100"]
+        if self.gpu_id is not None:
+            cmd += ["-i", str(self.gpu_id)]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != len(self.FIELDS):
+                continue
+            self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0, t1):
+        def num(s):
+            try:
+                return float(s)
+            except ValueError:
+                return None
+        window = [p for t, p in self.samples if t0 <= t <= t1]
+        source = "timed region"
+        if not window:
+            window = [p for _, p in self.samples]
+            source = "whole run (timed region shorter than the sampling period)"
+        if not window:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "nvidia-smi unavailable"}
+        sm = [num(p[0]) for p in window if num(p[0]) is not None]
+        mx = [num(p[1]) for p in window if num(p[1]) is not None]
+        pw = [num(p[2]) for p in window if num(p[2]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for p in window:
+            for name, v in zip(names, p[4:8]):
+                if v.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None, "reasons": sorted(reasons),
+                "samples": len(window), "source": source}
+
+
+def gpu_id_for(local_rank):
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(local_rank).uuid)
+        return u if u.startswith("GPU-") else f"GPU-{u}"
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        if vis:
+            return vis.split(",")[local_rank]
+        return local_rank
+
+
+# ------------------------------------------------------------ device side
+
+class Launcher:
+    """Buffer sets of one workload and a C-ABI launch over set i % n_sets."""
+
+    def __init__(self, wl, device, stream, min_footprint, seed=0):
+        import torch
+        from row_reduction_norm_gb300 import _native as N
+        from row_reduction_norm_gb300 import api, workloads as W
+        self.N = N
+        self.wl = wl
+        self.stream = stream
+        per_set = wl.rows * wl.hidden * wl.elem_bytes * (4 if wl.has_res else 2)
+        self.n_sets = max(1, math.ceil(min_footprint / max(per_set, 1)))
+        self.sets = []
+        w = None
+        for s in range(self.n_sets):
+            x, r, w_s = W.make_inputs(wl, seed=seed + 16 * s, device=device)
+            if w is None:
+                w = w_s
+            y = torch.empty_like(x)
+            h = torch.empty_like(x) if r is not None else None
+            self.sets.append((x, r, y, h))
+        self.w = w
+        self.code = api.dtype_code(self.sets[0][0].dtype)
+        self.ptrs = [(x.data_ptr(), None if r is None else r.data_ptr(), y.data_ptr(),
+                      None if h is None else h.data_ptr()) for x, r, y, h in self.sets]
+        self.w_ptr = None if w is None else w.data_ptr()
+        self.footprint = per_set * self.n_sets
+        x0, r0, y0, h0 = self.sets[0]
+        self.plan = api.plan_for(x0, w=w, residual=r0, out=y0, residual_out=h0)
+
+    def launch(self, i):
+        x, r, y, h = self.ptrs[i % self.n_sets]
+        self.N.rmsnorm_fwd(x, r, self.w_ptr, y, h, self.wl.rows, self.wl.hidden, self.wl.eps, self.code,
+                           self.stream.cuda_stream)
+
+    def graph(self, start, count):
+        import torch
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=self.stream):
+            for i in range(start, start + count):
+                self.launch(i)
+        return g
+
+
+def time_launches(L, steps, warmup, barrier=None, sampler_window=None, graph_len=1024):
+    """Exactly `steps` launches between two events on L.stream; returns ms."""
+    import torch
+    with torch.cuda.stream(L.stream):
+        L.launch(0)   # fills the library's per-device caches outside any capture
+    L.stream.synchronize()
+    G = max(1, min(steps, graph_len))
+    G = max(1, (G // L.n_sets) * L.n_sets) if G >= L.n_sets else G
+    g_main = L.graph(0, G)
+    rem = steps % G
+    g_rem = L.graph(0, rem) if rem else None
+    with torch.cuda.stream(L.stream):
+        for _ in range(max(1, math.ceil(warmup / G))):
+            g_main.replay()
+    L.stream.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    if barrier:
+        barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    with torch.cuda.stream(L.stream):
+        ev0.record(L.stream)
+        for _ in range(steps // G):
+            g_main.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        ev1.record(L.stream)
+    L.stream.synchronize()
+    torch.cuda.synchronize()
+    t1 = time.time()
+    if barrier:
+        barrier()
+    if sampler_window is not None:
+        sampler_window.extend([t0, t1])
+    return ev0.elapsed_time(ev1)
+
+
+def time_e2e(L, steps):
+    """Per step: pinned host -> device copies of the inputs, the launch, and the
+    device -> pinned host read of the outputs, all in one stream; returns
+    (ms, h2d bytes per step, d2h bytes per step)."""
+    import torch
+    x, r, y, h = L.sets[0]
+    hx = x.cpu().pin_memory()
+    hr = None if r is None else r.cpu().pin_memory()
+    hw = None if L.w is None else L.w.cpu().pin_memory()
+    hy = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+    hh = None if h is None else torch.empty(h.shape, dtype=h.dtype).pin_memory()
+    h2d = hx.numel() * hx.element_size() + (0 if hr is None else hr.numel() * hr.element_size()) + \
+        (0 if hw is None else hw.numel() * hw.element_size())
+    d2h = hy.numel() * hy.element_size() + (0 if hh is None else hh.numel() * hh.element_size())
+
+    def one(i):
+        xd, rd, yd, hd = L.sets[i % L.n_sets]
+        xd.copy_(hx, non_blocking=True)
+        if rd is not None:
+            rd.copy_(hr, non_blocking=True)
+        if hw is not None:
+            L.w.copy_(hw, non_blocking=True)
+        L.launch(i)
+        hy.copy_(yd, non_blocking=True)
+        if hh is not None:
+            hh.copy_(hd, non_blocking=True)
+
+    with torch.cuda.stream(L.stream):
+        for i in range(3):
+            one(i)
+    L.stream.synchronize()
+    G = max(1, min(steps, 64))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=L.stream):
+        for i in range(G):
+            one(i)
+    rem = steps % G
+    g2 = None
+    if rem:
+        g2 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g2, stream=L.stream):
+            for i in range(rem):
+                one(i)
+    with torch.cuda.stream(L.stream):
+        g.replay()
+    L.stream.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(L.stream):
+        ev0.record(L.stream)
+        for _ in range(steps // G):
+            g.replay()
+        if g2 is not None:
+            g2.replay()
+        ev1.record(L.stream)
+    L.stream.synchronize()
+    return ev0.elapsed_time(ev1), h2d, d2h
+
+
+def single_launch_latency_us(L, reps=200):
+    import torch
+    ts = []
+    for i in range(reps):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(L.stream):
+            e0.record(L.stream)
+            L.launch(i)
+            e1.record(L.stream)
+        e1.synchronize()
+        ts.append(e0.elapsed_time(e1) * 1e3)
+    return statistics.median(ts)
+
+
+def plan_summary(p):
+    d = p.as_dict()
+    return {"kernel": d["kernel_name"], "regime": d["regime_name"], "threads_per_row": d["threads_per_row"],
+            "chunks_per_thread": d["chunks_per_thread"], "vec_elems": d["vec_elems"],
+            "block": d["block_threads"], "grid": d["grid"]}
+
+
+# ------------------------------------------------------------ CPU oracle
+
+def oracle_rate(wl, seconds, threads, host_inputs=None):
+    """The oracle, as it stands, over whole batches of the workload (or row
+    blocks of it) until `seconds` of work; returns a dict."""
+    import oracle
+    from row_reduction_norm_gb300 import workloads as W
+    if host_inputs is None:
+        x, r, w = W.make_inputs(wl, seed=0, device="cpu")
+        host_inputs = (W.to_numpy_bits(x), W.to_numpy_bits(r), W.to_numpy_bits(w))
+    xn, rn, wn = host_inputs
+    rows_done = 0
+    t0 = time.perf_counter()
+    passes = 0
+    while True:
+        oracle.rmsnorm(xn, w=wn, residual=rn, eps=wl.eps, dtype=wl.dtype, threads=threads)
+        rows_done += xn.shape[0]
+        passes += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    per_launch_bytes = wl.algorithmic_bytes(rows=xn.shape[0])
+    return {"value": per_launch_bytes * passes / dt / 1e9, "unit": "GB/s", "cores": threads,
+            "kind": "oracle", "rows_per_s": rows_done / dt,
+            "sample": f"{passes} full passes over the {xn.shape[0]}x{wl.hidden} {wl.dtype} batch "
+                      f"({dt:.1f} s, fp64 C oracle, {threads} threads over row blocks)"}
+
+
+# ------------------------------------------------------------------ arms
+
+def run_ours(args):
+    import torch
+    rank, world, local = dist_env()
+    from row_reduction_norm_gb300 import build as B
+    B.build()
+    from row_reduction_norm_gb300 import workloads as W
+
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    peak, peak_src = load_peaks()
+    props = torch.cuda.get_device_properties(device)
+    l2 = int(getattr(props, "L2_cache_size", 0) or 128 * 2 ** 20)
+    min_footprint = 4 * l2
+    stream = torch.cuda.Stream(device)
+    wl = W.WORKLOADS[args.workload]
+
+    if args.ncu_case:
+        L = Launcher(W.WORKLOADS[args.ncu_case], device, stream, 0)
+        with torch.cuda.stream(stream):
+            for i in range(args.launches):
+                L.launch(i)
+        stream.synchronize()
+        print(json.dumps({"ncu_case": args.ncu_case, "launches": args.launches,
+                          "plan": plan_summary(L.plan)}))
+        return
+
+    L = Launcher(wl, device, stream, min_footprint)
+    sampler = ClockSampler(gpu_id_for(local)) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    window = []
+    ms = time_launches(L, args.steps, args.warmup, barrier=barrier, sampler_window=window)
+    if sampler:
+        time.sleep(0.15)
+        sampler.stop()
+    ms_t = torch.tensor([ms], dtype=torch.float64, device=device)
+    if dist is not None:
+        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
+    ms_max = float(ms_t.item())
+    launch_bytes = wl.algorithmic_bytes()
+    per_launch_s = ms / 1e3 / args.steps
+    achieved = launch_bytes / per_launch_s / 1e9
+    value = world * launch_bytes * args.steps / (ms_max / 1e3) / 1e9
+    rows_per_s = world * wl.rows * args.steps / (ms_max / 1e3)
+
+    e2e_steps = args.e2e_steps or max(64, min(args.steps, 4096))
+    e_ms, h2d, d2h = time_e2e(L, e2e_steps)
+    e_t = torch.tensor([e_ms], dtype=torch.float64, device=device)
+    if dist is not None:
+        dist.all_reduce(e_t, op=dist.ReduceOp.MAX)
+    e2e_value = world * launch_bytes * e2e_steps / (float(e_t.item()) / 1e3) / 1e9
+
+    per_config = []
+    if not args.no_per_config:
+        del L
+        torch.cuda.empty_cache()
+        for name in PER_CONFIG:
+            cw = W.WORKLOADS[name]
+            CL = Launcher(cw, device, stream, min_footprint)
+            # calibrate: about 0.3 s of launches
+            cal = time_launches(CL, 64, 8)
+            k = int(max(64, min(200000, 0.3 / max(cal / 1e3 / 64, 1e-9))))
+            cms = time_launches(CL, k, max(3, k // 20), barrier=barrier)
+            t_launch = cms / 1e3 / k
+            b = cw.algorithmic_bytes()
+            entry = {"workload": name, "rows": cw.rows, "hidden": cw.hidden, "dtype": cw.dtype,
+                     "residual": cw.has_res, "weight": cw.has_w, "bytes_per_launch": b,
+                     "us_per_launch": round(t_launch * 1e6, 3),
+                     "gbs": round(b / t_launch / 1e9, 1), "frac_of_peak": round(b / t_launch / 1e9 / peak, 4),
+                     "rows_per_s": round(cw.rows / t_launch, 1), "steps": k,
+                     "buffer_sets": CL.n_sets, "plan": plan_summary(CL.plan)}
+            if cw.rows <= 64:
+                entry["single_launch_latency_us"] = round(single_launch_latency_us(CL), 2)
+            per_config.append(entry)
+            del CL
+            torch.cuda.empty_cache()
+        L = Launcher(wl, device, stream, 0)
+
+    cpu = None
+    if rank == 0 and world == 1 and args.cpu_seconds > 0:
+        x0, r0, _, _ = L.sets[0]
+        host = (W.to_numpy_bits(x0), W.to_numpy_bits(r0), W.to_numpy_bits(L.w))
+        cpu = oracle_rate(wl, args.cpu_seconds, os.cpu_count() or 1, host)
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+    clocks = sampler.summary(window[0], window[1]) if sampler and window else None
+    traffic = profiled_traffic(args.workload)
+    out = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_max / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": wl.dtype,
+        "data": "synthetic",
+        "rows_per_s": round(rows_per_s, 1),
+        "frac_of_peak": round(achieved / peak, 4),
+        "config": {
+            "workload": wl.name, "rows": wl.rows, "hidden": wl.hidden, "eps": wl.eps,
+            "residual": wl.has_res, "weight": wl.has_w, "bytes_per_step": launch_bytes,
+            "l2": f"inputs larger than L2 in aggregate: launches rotate over {L_sets(args, wl, min_footprint)} "
+                  f"buffer sets (>= 4x the {l2 // 2**20} MiB L2)",
+            "timing": "CUDA graphs of C-ABI launches, CUDA events on the launching stream",
+            "plan": plan_summary(L.plan),
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        },
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
+                     else "fallback 6.8 TB/s", "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": traffic,
+                     "kernel": f"rms_{plan_summary(L.plan)['kernel']}_kernel",
+                     "algorithmic_bytes_per_launch": launch_bytes},
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "what": "pinned host -> device inputs (x, w), C-ABI launch, device -> pinned host y, "
+                        "every step"},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+        "per_config": per_config,
+    }
+    print(json.dumps(out))
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def L_sets(args, wl, min_footprint):
+    per_set = wl.rows * wl.hidden * wl.elem_bytes * (4 if wl.has_res else 2)
+    return max(1, math.ceil(min_footprint / max(per_set, 1)))
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    from row_reduction_norm_gb300 import workloads as W
+    wl = W.WORKLOADS[args.workload]
+    threads = os.cpu_count() or 1
+    x, r, w = W.make_inputs(wl, seed=0, device="cpu")
+    xn, rn, wn = W.to_numpy_bits(x), W.to_numpy_bits(r), W.to_numpy_bits(w)
+    # size each step so that warmup + steps take about a minute of host time
+    t0 = time.perf_counter()
+    oracle.rmsnorm(xn, w=wn, residual=rn, eps=wl.eps, dtype=wl.dtype, threads=threads)
+    t_full = max(time.perf_counter() - t0, 1e-6)
+    budget = 60.0 / max(1, args.steps + args.warmup)
+    rows_per_step = int(max(1, min(wl.rows, wl.rows * budget / t_full)))
+
+    def step(i):
+        lo = (i * rows_per_step) % wl.rows
+        hi = min(wl.rows, lo + rows_per_step)
+        oracle.rmsnorm(xn[lo:hi], w=wn, residual=None if rn is None else rn[lo:hi], eps=wl.eps,
+                       dtype=wl.dtype, threads=threads)
+        return hi - lo
+
+    for i in range(args.warmup):
+        step(i)
+    rows_done = 0
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        rows_done += step(i)
+    dt = time.perf_counter() - t0
+    row_bytes = wl.algorithmic_bytes(rows=1) - (wl.hidden * wl.elem_bytes if wl.has_w else 0)
+    wbytes = wl.hidden * wl.elem_bytes if wl.has_w else 0
+    value = (rows_done * row_bytes + args.steps * wbytes) / dt / 1e9
+    sample = (f"{rows_per_step} of {wl.rows} rows per step ({rows_per_step * wl.hidden} elements), "
+              f"fp64 C oracle, {threads} threads over row blocks")
+    out = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
+        "rows_per_s": round(rows_done / dt, 1),
+        "config": {"workload": wl.name, "rows": wl.rows, "hidden": wl.hidden, "eps": wl.eps,
+                   "residual": wl.has_res, "weight": wl.has_w, "rows_per_step": rows_per_step,
+                   "l2": "host run: no GPU L2 involved"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(out))
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,168 @@
+/*
+ * rmsnorm.h -- C ABI of the GB300 (sm_103a) fused row-wise RMSNorm library.
+ *
+ * The operation (one row at a time, rows of a row-major [rows, hidden] tensor):
+ *
+ *   h_i          = x_i,   or  h_i = RN_T(x_i + residual_i) with a residual
+ *   residual_out = h                                   (only with a residual)
+ *   y_i          = RN_T( h_i * rsqrt(mean_j(h_j^2) + eps) * w_i )
+ *                  (w_i dropped when no weight is given)
+ *
+ * Definition: "Building a GPU compiler from scratch: from PyTorch to CUDA via
+ * multi-level IR (Emmy)" -- the running example (mean of the squares of the
+ * row, plus epsilon, inverse square root, times each element and its learned
+ * weight) and section "Tensor IR" (square, sum, division by the count, plus
+ * epsilon, rsqrt, two multiplications).  The weight / no-weight and per-dtype
+ * specialisation follows "CuTeDSL at Perplexity", section on the large
+ * configuration space.  RN_T is round-to-nearest-even to the I/O type T.
+ * The residual add is not described on the pages; the reading taken is that
+ * residual_out is the sum rounded once to T and the norm is taken of it.
+ *
+ * Arithmetic: inputs are widened to fp32; the sum of squares is formed in
+ * fp32 in a fixed order that depends only on (hidden, dtype, alignment), so
+ * every call gives bit-identical results for a row, whatever the row count,
+ * grid or stream ("batch invariant").  Accuracy: y is within 1 ulp of the
+ * correctly rounded result for bf16 and within 2e-6 relative for fp32;
+ * residual_out is the correctly rounded sum (bit-exact).
+ *
+ * Conventions common to every entry point:
+ *  - All tensor pointers are DEVICE pointers owned by the caller, on the
+ *    caller's current CUDA device; the library allocates and frees nothing.
+ *  - Every tensor shares one I/O type (dtype).  x, residual, y and
+ *    residual_out are contiguous row-major [rows, hidden]; w is [hidden].
+ *  - Calls are asynchronous on `stream` (0 = the legacy default stream) and
+ *    never synchronise.  Errors detected before the launch return a status
+ *    and launch nothing.
+ *  - Aliasing: an input may be the very same buffer as an output (y == x,
+ *    residual_out == residual, ...): each thread reads its elements before it
+ *    writes them.  y and residual_out must not overlap each other, w must not
+ *    overlap an output, and partial overlaps are undefined.
+ *  - Alignment: when every pointer is 16-byte aligned and hidden * sizeof(T)
+ *    is a multiple of 16, rows move with 128-bit loads and stores; otherwise a
+ *    scalar path runs (same results up to the stated tolerance).
+ *  - Thread safety: entry points may be called from several host threads.
+ *    The only library state is a per-device cache of the SM count and of
+ *    kernel occupancy.
+ */
+#ifndef ROW_REDUCTION_NORM_GB300_RMSNORM_H
+#define ROW_REDUCTION_NORM_GB300_RMSNORM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *rmsnorm_stream_t;
+
+/* I/O types (the `dtype` argument). */
+enum { RMSNORM_F32 = 0, RMSNORM_BF16 = 1 };
+
+/* Status codes. */
+enum {
+    RMSNORM_OK = 0,
+    RMSNORM_EINVAL = -1,        /* null x or y, rows < 0, hidden <= 0, unknown dtype,
+                                   eps negative or not finite, residual given without
+                                   residual_out or the reverse, bad plan            */
+    RMSNORM_EUNSUPPORTED = -2,  /* hidden above rmsnorm_max_hidden()               */
+    RMSNORM_ECUDA = -3          /* the CUDA runtime reported an error (launch,
+                                   device query)                                    */
+};
+
+/* Kernel families (rmsnorm_plan_t.kernel). */
+enum {
+    RMSNORM_KERNEL_REG = 0,   /* row held in registers, 128-bit I/O, one pass     */
+    RMSNORM_KERNEL_LOOP = 1   /* row streamed twice (second read from L2): any
+                                 alignment, and rows too long for registers       */
+};
+
+/* Regimes (rmsnorm_plan_t.regime), a summary of how rows map to threads. */
+enum {
+    RMSNORM_REGIME_WARP = 0,        /* 4..32 lanes of one warp per row               */
+    RMSNORM_REGIME_CTA = 1,         /* several warps per row, shared-memory combine  */
+    RMSNORM_REGIME_PERSISTENT = 2,  /* grid capped at the resident capacity; blocks
+                                       stride over the rows                          */
+    RMSNORM_REGIME_LOOPED = 3       /* RMSNORM_KERNEL_LOOP                           */
+};
+
+/*
+ * A launch plan.  The per-row schedule (kernel, threads_per_row,
+ * chunks_per_thread, vec_elems, block_threads) depends only on hidden, dtype
+ * and the alignment of the pointers; rows only sizes the grid.
+ */
+typedef struct {
+    int32_t kernel;             /* RMSNORM_KERNEL_*                                   */
+    int32_t regime;             /* RMSNORM_REGIME_*                                   */
+    int32_t threads_per_row;    /* REG: 4..512 (power of two); LOOP: block_threads   */
+    int32_t chunks_per_thread;  /* REG: upper bound of vector chunks per thread; LOOP:
+                                   0                                                  */
+    int32_t vec_elems;          /* elements per load: 16 / sizeof(T), or 1 (scalar)  */
+    int32_t block_threads;      /* threads per block                                  */
+    int32_t rows_per_block;     /* rows one block handles per loop iteration          */
+    int32_t persistent;         /* 1 if grid < row blocks (blocks stride over rows)   */
+    int64_t grid;               /* blocks launched (0 when rows == 0)                 */
+} rmsnorm_plan_t;
+
+/*
+ * Fused RMSNorm forward (the op above).
+ *   x            [rows, hidden]  input
+ *   residual     [rows, hidden]  optional (NULL): added to x before the norm
+ *   w            [hidden]        optional (NULL): per-element weight
+ *   y            [rows, hidden]  output
+ *   residual_out [rows, hidden]  required iff residual is given: receives h
+ *   rows >= 0 (0 is a successful no-op), 1 <= hidden <= rmsnorm_max_hidden(dtype)
+ *   eps          finite, >= 0; used as the float value passed
+ *   dtype        RMSNORM_F32 or RMSNORM_BF16
+ * Returns RMSNORM_OK or a negative status (see above).
+ */
+int rmsnorm_fwd(const void *x, const void *residual, const void *w, void *y,
+                void *residual_out, int64_t rows, int64_t hidden, float eps,
+                int dtype, rmsnorm_stream_t stream);
+
+/*
+ * Pure host planning (no CUDA call): the plan rmsnorm_fwd would use on a
+ * device with `sm_count` SMs where the chosen kernel keeps `blocks_per_sm`
+ * blocks resident.  vec_ok: 1 if every pointer is 16-byte aligned and
+ * hidden * sizeof(T) is a multiple of 16.  Returns a status.
+ */
+int rmsnorm_plan(int64_t rows, int64_t hidden, int dtype, int vec_ok, int sm_count,
+                 int blocks_per_sm, rmsnorm_plan_t *plan);
+
+/*
+ * The plan rmsnorm_fwd would use for these pointers on the current device
+ * (queries the SM count and the kernel's occupancy once per device).
+ */
+int rmsnorm_plan_for(const void *x, const void *residual, const void *w, const void *y,
+                     const void *residual_out, int64_t rows, int64_t hidden, int dtype,
+                     rmsnorm_plan_t *plan);
+
+/*
+ * rmsnorm_fwd with a caller-chosen plan (tests and schedule sweeps).  The plan
+ * is validated against the shape and the pointers: a REG plan must cover the
+ * row (threads_per_row * chunks_per_thread * vec_elems >= hidden, with
+ * chunks_per_thread <= the compiled bound), block_threads and rows_per_block
+ * must match threads_per_row, a vector plan needs aligned pointers, and
+ * grid >= 1.  Returns RMSNORM_EINVAL for a plan that does not fit.
+ */
+int rmsnorm_fwd_plan(const void *x, const void *residual, const void *w, void *y,
+                     void *residual_out, int64_t rows, int64_t hidden, float eps,
+                     int dtype, const rmsnorm_plan_t *plan, rmsnorm_stream_t stream);
+
+/* Largest supported hidden size for a dtype (0 for an unknown dtype). */
+int64_t rmsnorm_max_hidden(int dtype);
+
+/* Largest chunks_per_thread a REG plan may use. */
+int rmsnorm_reg_max_chunks(void);
+
+/* Static text for a status code. */
+const char *rmsnorm_strerror(int status);
+
+/* Static text describing the build (target architecture, version). */
+const char *rmsnorm_build_info(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ROW_REDUCTION_NORM_GB300_RMSNORM_H */

@@ -1,0 +1,171 @@
+"""ctypes binding of the C ABI in ``include/rmsnorm.h`` (argument marshalling only).
+
+The functions keep the C names and argument order; pointers are plain
+integers (device addresses), streams are ``cudaStream_t`` values as integers.
+A non-zero status raises ``RmsNormError``.  Nothing here computes any part of
+the op: every step runs in the CUDA kernels of ``librmsnorm_gb300.so``, and a
+missing library is an error, never a fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "librmsnorm_gb300.so")
+
+RMSNORM_F32 = 0
+RMSNORM_BF16 = 1
+
+RMSNORM_OK = 0
+RMSNORM_EINVAL = -1
+RMSNORM_EUNSUPPORTED = -2
+RMSNORM_ECUDA = -3
+
+RMSNORM_KERNEL_REG = 0
+RMSNORM_KERNEL_LOOP = 1
+
+RMSNORM_REGIME_WARP = 0
+RMSNORM_REGIME_CTA = 1
+RMSNORM_REGIME_PERSISTENT = 2
+RMSNORM_REGIME_LOOPED = 3
+
+REGIME_NAMES = {0: "warp", 1: "cta", 2: "persistent", 3: "looped"}
+KERNEL_NAMES = {0: "reg", 1: "loop"}
+
+# Every symbol the header declares (checked by the CPU tests).
+EXPORTED = ["rmsnorm_fwd", "rmsnorm_plan", "rmsnorm_plan_for", "rmsnorm_fwd_plan",
+            "rmsnorm_max_hidden", "rmsnorm_reg_max_chunks", "rmsnorm_strerror",
+            "rmsnorm_build_info"]
+
+
+class RmsNormError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {rmsnorm_strerror(status)} (status {status})")
+
+
+class Plan(ctypes.Structure):
+    """Mirror of ``rmsnorm_plan_t``."""
+    _fields_ = [
+        ("kernel", ctypes.c_int32),
+        ("regime", ctypes.c_int32),
+        ("threads_per_row", ctypes.c_int32),
+        ("chunks_per_thread", ctypes.c_int32),
+        ("vec_elems", ctypes.c_int32),
+        ("block_threads", ctypes.c_int32),
+        ("rows_per_block", ctypes.c_int32),
+        ("persistent", ctypes.c_int32),
+        ("grid", ctypes.c_int64),
+    ]
+
+    def as_dict(self):
+        d = {k: getattr(self, k) for k, _ in self._fields_}
+        d["kernel_name"] = KERNEL_NAMES.get(self.kernel, "?")
+        d["regime_name"] = REGIME_NAMES.get(self.regime, "?")
+        return d
+
+    def copy(self):
+        p = Plan()
+        ctypes.pointer(p)[0] = self
+        return p
+
+    def __repr__(self):
+        return f"Plan({self.as_dict()})"
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return LIB_PATH
+
+
+def load():
+    """Load the CUDA library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with `python -m row_reduction_norm_gb300.build` "
+                "(there is no CPU fallback)")
+        lib = ctypes.CDLL(LIB_PATH)
+        vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        fwd_args = [vp, vp, vp, vp, vp, i64, i64, ctypes.c_float, i32]
+        lib.rmsnorm_fwd.argtypes = fwd_args + [vp]
+        lib.rmsnorm_fwd.restype = i32
+        lib.rmsnorm_fwd_plan.argtypes = fwd_args + [ctypes.POINTER(Plan), vp]
+        lib.rmsnorm_fwd_plan.restype = i32
+        lib.rmsnorm_plan.argtypes = [i64, i64, i32, i32, i32, i32, ctypes.POINTER(Plan)]
+        lib.rmsnorm_plan.restype = i32
+        lib.rmsnorm_plan_for.argtypes = [vp, vp, vp, vp, vp, i64, i64, i32, ctypes.POINTER(Plan)]
+        lib.rmsnorm_plan_for.restype = i32
+        lib.rmsnorm_max_hidden.argtypes = [i32]
+        lib.rmsnorm_max_hidden.restype = i64
+        lib.rmsnorm_reg_max_chunks.argtypes = []
+        lib.rmsnorm_reg_max_chunks.restype = i32
+        lib.rmsnorm_strerror.argtypes = [i32]
+        lib.rmsnorm_strerror.restype = ctypes.c_char_p
+        lib.rmsnorm_build_info.argtypes = []
+        lib.rmsnorm_build_info.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def _check(status: int, where: str):
+    if status != RMSNORM_OK:
+        raise RmsNormError(status, where)
+
+
+def rmsnorm_fwd(x, residual, w, y, residual_out, rows, hidden, eps, dtype, stream=0):
+    _check(load().rmsnorm_fwd(x, residual, w, y, residual_out, rows, hidden, eps, dtype, stream),
+           "rmsnorm_fwd")
+
+
+def rmsnorm_fwd_status(x, residual, w, y, residual_out, rows, hidden, eps, dtype, stream=0) -> int:
+    """rmsnorm_fwd returning the raw status instead of raising."""
+    return load().rmsnorm_fwd(x, residual, w, y, residual_out, rows, hidden, eps, dtype, stream)
+
+
+def rmsnorm_fwd_plan(x, residual, w, y, residual_out, rows, hidden, eps, dtype, plan: Plan, stream=0):
+    _check(load().rmsnorm_fwd_plan(x, residual, w, y, residual_out, rows, hidden, eps, dtype,
+                                   ctypes.byref(plan), stream), "rmsnorm_fwd_plan")
+
+
+def rmsnorm_fwd_plan_status(x, residual, w, y, residual_out, rows, hidden, eps, dtype, plan, stream=0):
+    return load().rmsnorm_fwd_plan(x, residual, w, y, residual_out, rows, hidden, eps, dtype,
+                                   ctypes.byref(plan) if plan is not None else None, stream)
+
+
+def rmsnorm_plan(rows, hidden, dtype, vec_ok, sm_count, blocks_per_sm) -> Plan:
+    p = Plan()
+    _check(load().rmsnorm_plan(rows, hidden, dtype, int(vec_ok), sm_count, blocks_per_sm,
+                               ctypes.byref(p)), "rmsnorm_plan")
+    return p
+
+
+def rmsnorm_plan_for(x, residual, w, y, residual_out, rows, hidden, dtype) -> Plan:
+    p = Plan()
+    _check(load().rmsnorm_plan_for(x, residual, w, y, residual_out, rows, hidden, dtype,
+                                   ctypes.byref(p)), "rmsnorm_plan_for")
+    return p
+
+
+def rmsnorm_max_hidden(dtype) -> int:
+    return int(load().rmsnorm_max_hidden(dtype))
+
+
+def rmsnorm_reg_max_chunks() -> int:
+    return int(load().rmsnorm_reg_max_chunks())
+
+
+def rmsnorm_strerror(status) -> str:
+    return load().rmsnorm_strerror(int(status)).decode()
+
+
+def rmsnorm_build_info() -> str:
+    return load().rmsnorm_build_info().decode()

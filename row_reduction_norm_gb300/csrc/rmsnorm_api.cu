@@ -1,0 +1,372 @@
+// rmsnorm_api.cu -- the C ABI declared in include/rmsnorm.h: argument checks,
+// host-side planning (which kernel, how many threads per row, grid size) and
+// the launch.  No allocation, no synchronisation, the caller's stream.
+//
+// Planning follows the host-side decisions of "CuTeDSL at Perplexity":
+// sections on the large configuration space (compile-time specialisation on
+// dtype, weight / no weight and hidden size -- a branch that does not exist
+// beats one that is always or never taken), on prefill vs decode (threads per
+// block chosen from the token count, hidden size and SM count) and "Blackwell
+// support" (the SM count is read from the device, not hard-coded).  The
+// per-row schedule depends on hidden, dtype and alignment only; the row count
+// only sizes the grid, so a row's result is the same in every batch.
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "kernel_table.h"
+#include "rmsnorm.h"
+#include "rmsnorm_kernels.cuh"
+
+namespace {
+
+constexpr int64_t kMaxHidden = 65536;
+constexpr int kMaxDevices = 64;
+// Largest per-thread chain of squares the two-pass kernel may form (keeps the
+// fp32 error bound of the sum the same as the register kernel's).
+constexpr int64_t kLoopMaxTermsPerThread = 64;
+// Dynamic shared memory of a register-kernel block with a weight: the weight
+// row, at most kRegMaxGT * kRegMaxCH chunks of 16 bytes.
+constexpr int kRegMaxWeightSmem = rrn::kRegMaxGT * rrn::kRegMaxCH * 16;
+
+int elem_size(int dtype) { return dtype == RMSNORM_BF16 ? 2 : 4; }
+int vec_elems_of(int dtype) { return 16 / elem_size(dtype); }
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int64_t next_pow2(int64_t v) {
+    int64_t p = 1;
+    while (p < v) p <<= 1;
+    return p;
+}
+
+bool aligned16(const void *p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned_to(const void *p, int a) {
+    return p == nullptr || (reinterpret_cast<uintptr_t>(p) % (uintptr_t)a) == 0;
+}
+
+int check_args(const void *x, const void *residual, const void *y, const void *residual_out,
+               int64_t rows, int64_t hidden, float eps, int dtype) {
+    if (dtype != RMSNORM_F32 && dtype != RMSNORM_BF16) return RMSNORM_EINVAL;
+    if (x == nullptr || y == nullptr) return RMSNORM_EINVAL;
+    if ((residual == nullptr) != (residual_out == nullptr)) return RMSNORM_EINVAL;
+    if (rows < 0 || hidden <= 0) return RMSNORM_EINVAL;
+    if (!std::isfinite(eps) || eps < 0.f) return RMSNORM_EINVAL;
+    if (hidden > kMaxHidden) return RMSNORM_EUNSUPPORTED;
+    if (rows > INT64_MAX / (hidden * elem_size(dtype))) return RMSNORM_EINVAL;
+    return RMSNORM_OK;
+}
+
+// Element alignment is required on every path (a misaligned element access
+// would fault); 16-byte alignment selects the vector path.
+bool elem_aligned(const void *x, const void *r, const void *w, const void *y, const void *ro, int dtype) {
+    const int a = elem_size(dtype);
+    return aligned_to(x, a) && aligned_to(r, a) && aligned_to(w, a) && aligned_to(y, a) && aligned_to(ro, a);
+}
+
+int vec_ok_of(const void *x, const void *r, const void *w, const void *y, const void *ro,
+              int64_t hidden, int dtype) {
+    return aligned16(x) && aligned16(r) && aligned16(w) && aligned16(y) && aligned16(ro) &&
+           (hidden * elem_size(dtype)) % 16 == 0;
+}
+
+// The per-row schedule: everything but the grid.
+void schedule(int64_t hidden, int dtype, int vec_ok, rmsnorm_plan_t *p) {
+    std::memset(p, 0, sizeof(*p));
+    const int V = vec_elems_of(dtype);
+    if (vec_ok) {
+        const int64_t nch = hidden / V;
+        // aim at up to 8 chunks (128 bytes) per thread, at least 4 lanes per row
+        int64_t gt = next_pow2(ceil_div(nch, rrn::kRegMaxCH));
+        if (gt < 4) gt = 4;
+        if (gt <= rrn::kRegMaxGT) {
+            int64_t need = ceil_div(nch, gt);
+            int ch = 1;
+            while (ch < need) ch <<= 1;
+            p->kernel = RMSNORM_KERNEL_REG;
+            p->threads_per_row = (int32_t)gt;
+            p->chunks_per_thread = ch;
+            p->vec_elems = V;
+            p->block_threads = rrn::reg_block_threads((int)gt);
+            p->rows_per_block = p->block_threads / (int32_t)gt;
+            p->regime = gt <= 32 ? RMSNORM_REGIME_WARP : RMSNORM_REGIME_CTA;
+            return;
+        }
+    }
+    p->kernel = RMSNORM_KERNEL_LOOP;
+    p->vec_elems = vec_ok ? V : 1;
+    const int64_t units = hidden / p->vec_elems;
+    int block = rrn::kLoopBlocks[2];
+    for (int b : rrn::kLoopBlocks) {
+        if (ceil_div(units, b) * p->vec_elems <= kLoopMaxTermsPerThread) {
+            block = b;
+            break;
+        }
+    }
+    p->block_threads = block;
+    p->threads_per_row = block;
+    p->chunks_per_thread = 0;
+    p->rows_per_block = 1;
+    p->regime = RMSNORM_REGIME_LOOPED;
+}
+
+void size_grid(int64_t rows, int sm_count, int blocks_per_sm, rmsnorm_plan_t *p) {
+    const int64_t row_blocks = ceil_div(rows, p->rows_per_block);
+    int64_t cap = (int64_t)(sm_count > 0 ? sm_count : 1) * (blocks_per_sm > 0 ? blocks_per_sm : 1);
+    if (cap > INT_MAX) cap = INT_MAX;
+    p->persistent = row_blocks > cap;
+    p->grid = row_blocks > cap ? cap : row_blocks;
+    if (p->persistent && p->kernel == RMSNORM_KERNEL_REG) p->regime = RMSNORM_REGIME_PERSISTENT;
+}
+
+size_t dyn_smem_of(const rmsnorm_plan_t *p, int64_t hidden, int dtype, bool has_w) {
+    if (p->kernel != RMSNORM_KERNEL_REG || !has_w) return 0;
+    return (size_t)(hidden / vec_elems_of(dtype)) * 16;
+}
+
+const void *kernel_of(const rmsnorm_plan_t *p, int dtype, bool res, bool w) {
+    if (p->kernel == RMSNORM_KERNEL_REG) {
+        return dtype == RMSNORM_BF16 ? rrn::reg_kernel_bf16(p->threads_per_row, p->chunks_per_thread, res, w)
+                                     : rrn::reg_kernel_f32(p->threads_per_row, p->chunks_per_thread, res, w);
+    }
+    const bool vec = p->vec_elems != 1;
+    return dtype == RMSNORM_BF16 ? rrn::loop_kernel_bf16(p->block_threads, vec, res, w)
+                                 : rrn::loop_kernel_f32(p->block_threads, vec, res, w);
+}
+
+// Checks a plan against the shape and pointers (caller-made plans included).
+int validate_plan(const rmsnorm_plan_t *p, int64_t rows, int64_t hidden, int dtype, int vec_ok) {
+    if (p == nullptr) return RMSNORM_EINVAL;
+    const int V = vec_elems_of(dtype);
+    if (rows > 0 && (p->grid < 1 || p->grid > INT_MAX)) return RMSNORM_EINVAL;
+    if (p->kernel == RMSNORM_KERNEL_REG) {
+        const int gt = p->threads_per_row, ch = p->chunks_per_thread;
+        if (!vec_ok || p->vec_elems != V) return RMSNORM_EINVAL;
+        if (gt < 4 || gt > rrn::kRegMaxGT || (gt & (gt - 1)) != 0) return RMSNORM_EINVAL;
+        if (ch < 1 || ch > rrn::kRegMaxCH || (ch & (ch - 1)) != 0) return RMSNORM_EINVAL;
+        if ((int64_t)gt * ch * V < hidden) return RMSNORM_EINVAL;
+        if (p->block_threads != rrn::reg_block_threads(gt)) return RMSNORM_EINVAL;
+        if (p->rows_per_block != p->block_threads / gt) return RMSNORM_EINVAL;
+        return RMSNORM_OK;
+    }
+    if (p->kernel == RMSNORM_KERNEL_LOOP) {
+        if (p->vec_elems != 1 && !(p->vec_elems == V && vec_ok)) return RMSNORM_EINVAL;
+        bool known = false;
+        for (int b : rrn::kLoopBlocks) known = known || (b == p->block_threads);
+        if (!known) return RMSNORM_EINVAL;
+        if (p->rows_per_block != 1) return RMSNORM_EINVAL;
+        if (ceil_div(hidden / p->vec_elems, p->block_threads) * p->vec_elems > kLoopMaxTermsPerThread)
+            return RMSNORM_EINVAL;
+        return RMSNORM_OK;
+    }
+    return RMSNORM_EINVAL;
+}
+
+// ------------------------------------------------------------ device caches
+
+std::mutex g_mu;
+int g_sm_count[kMaxDevices];
+
+struct OccEntry {
+    int dev;
+    const void *fn;
+    size_t smem;
+    int blocks;
+};
+constexpr int kOccSlots = 512;
+OccEntry g_occ[kOccSlots];
+int g_occ_used = 0;
+
+struct AttrEntry {
+    int dev;
+    const void *fn;
+};
+AttrEntry g_attr[kOccSlots];
+int g_attr_used = 0;
+
+int sm_count_of(int dev, int *out) {
+    if (dev < 0 || dev >= kMaxDevices) return RMSNORM_ECUDA;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (g_sm_count[dev] > 0) {
+            *out = g_sm_count[dev];
+            return RMSNORM_OK;
+        }
+    }
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+        return RMSNORM_ECUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_sm_count[dev] = n;
+    *out = n;
+    return RMSNORM_OK;
+}
+
+// Opt a kernel in to the largest dynamic shared memory it may be given.
+int ensure_smem_attr(int dev, const void *fn) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (int i = 0; i < g_attr_used; ++i)
+        if (g_attr[i].dev == dev && g_attr[i].fn == fn) return RMSNORM_OK;
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kRegMaxWeightSmem) != cudaSuccess)
+        return RMSNORM_ECUDA;
+    if (g_attr_used < kOccSlots) g_attr[g_attr_used++] = AttrEntry{dev, fn};
+    return RMSNORM_OK;
+}
+
+int blocks_per_sm_of(int dev, const void *fn, int block, size_t smem, int *out) {
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        for (int i = 0; i < g_occ_used; ++i) {
+            if (g_occ[i].dev == dev && g_occ[i].fn == fn && g_occ[i].smem == smem) {
+                *out = g_occ[i].blocks;
+                return RMSNORM_OK;
+            }
+        }
+    }
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, block, smem) != cudaSuccess || n <= 0)
+        return RMSNORM_ECUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_occ_used < kOccSlots) g_occ[g_occ_used++] = OccEntry{dev, fn, smem, n};
+    *out = n;
+    return RMSNORM_OK;
+}
+
+// Full device-side planning for concrete pointers.
+int plan_for_device(const void *x, const void *residual, const void *w, const void *y,
+                    const void *residual_out, int64_t rows, int64_t hidden, int dtype,
+                    rmsnorm_plan_t *plan, int *dev_out) {
+    const int vec_ok = vec_ok_of(x, residual, w, y, residual_out, hidden, dtype);
+    schedule(hidden, dtype, vec_ok, plan);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return RMSNORM_ECUDA;
+    int sms = 0;
+    int st = sm_count_of(dev, &sms);
+    if (st != RMSNORM_OK) return st;
+    const bool res = residual != nullptr, hw = w != nullptr;
+    const void *fn = kernel_of(plan, dtype, res, hw);
+    if (fn == nullptr) return RMSNORM_EINVAL;
+    const size_t smem = dyn_smem_of(plan, hidden, dtype, hw);
+    if (smem > 0 && (st = ensure_smem_attr(dev, fn)) != RMSNORM_OK) return st;
+    int bps = 0;
+    if ((st = blocks_per_sm_of(dev, fn, plan->block_threads, smem, &bps)) != RMSNORM_OK) return st;
+    size_grid(rows, sms, bps, plan);
+    if (dev_out) *dev_out = dev;
+    return RMSNORM_OK;
+}
+
+int launch(const rrn::Params &prm, const rmsnorm_plan_t *plan, int dtype, int dev,
+           rmsnorm_stream_t stream) {
+    const bool res = prm.res != nullptr, hw = prm.w != nullptr;
+    const void *fn = kernel_of(plan, dtype, res, hw);
+    if (fn == nullptr) return RMSNORM_EINVAL;
+    const size_t smem = dyn_smem_of(plan, prm.row_elems, dtype, hw);
+    if (smem > 0) {
+        int st = ensure_smem_attr(dev, fn);
+        if (st != RMSNORM_OK) return st;
+    }
+    rrn::Params args = prm;
+    void *argv[] = {&args};
+    cudaError_t e = cudaLaunchKernel(fn, dim3((unsigned)plan->grid), dim3((unsigned)plan->block_threads),
+                                     argv, smem, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();   // clear the non-sticky launch error
+        return RMSNORM_ECUDA;
+    }
+    return RMSNORM_OK;
+}
+
+rrn::Params make_params(const void *x, const void *residual, const void *w, void *y, void *residual_out,
+                        int64_t rows, int64_t hidden, float eps, int vec_elems) {
+    rrn::Params prm;
+    prm.x = x;
+    prm.res = residual;
+    prm.w = w;
+    prm.y = y;
+    prm.res_out = residual_out;
+    prm.rows = rows;
+    prm.row_elems = hidden;
+    prm.units = (int32_t)(hidden / vec_elems);
+    prm.hidden_f = (float)hidden;
+    prm.eps = eps;
+    return prm;
+}
+
+}  // namespace
+
+extern "C" {
+
+int rmsnorm_plan(int64_t rows, int64_t hidden, int dtype, int vec_ok, int sm_count, int blocks_per_sm,
+                 rmsnorm_plan_t *plan) {
+    if (plan == nullptr || dtype < RMSNORM_F32 || dtype > RMSNORM_BF16 || rows < 0 || hidden <= 0)
+        return RMSNORM_EINVAL;
+    if (hidden > kMaxHidden) return RMSNORM_EUNSUPPORTED;
+    if (vec_ok && (hidden * elem_size(dtype)) % 16 != 0) return RMSNORM_EINVAL;
+    schedule(hidden, dtype, vec_ok ? 1 : 0, plan);
+    size_grid(rows, sm_count, blocks_per_sm, plan);
+    return RMSNORM_OK;
+}
+
+int rmsnorm_plan_for(const void *x, const void *residual, const void *w, const void *y,
+                     const void *residual_out, int64_t rows, int64_t hidden, int dtype,
+                     rmsnorm_plan_t *plan) {
+    if (plan == nullptr) return RMSNORM_EINVAL;
+    int st = check_args(x, residual, y, residual_out, rows, hidden, 0.f, dtype);
+    if (st != RMSNORM_OK) return st;
+    if (!elem_aligned(x, residual, w, y, residual_out, dtype)) return RMSNORM_EINVAL;
+    return plan_for_device(x, residual, w, y, residual_out, rows, hidden, dtype, plan, nullptr);
+}
+
+int rmsnorm_fwd(const void *x, const void *residual, const void *w, void *y, void *residual_out,
+                int64_t rows, int64_t hidden, float eps, int dtype, rmsnorm_stream_t stream) {
+    int st = check_args(x, residual, y, residual_out, rows, hidden, eps, dtype);
+    if (st != RMSNORM_OK) return st;
+    if (!elem_aligned(x, residual, w, y, residual_out, dtype)) return RMSNORM_EINVAL;
+    if (rows == 0) return RMSNORM_OK;
+    rmsnorm_plan_t plan;
+    int dev = 0;
+    st = plan_for_device(x, residual, w, y, residual_out, rows, hidden, dtype, &plan, &dev);
+    if (st != RMSNORM_OK) return st;
+    return launch(make_params(x, residual, w, y, residual_out, rows, hidden, eps, plan.vec_elems), &plan,
+                  dtype, dev, stream);
+}
+
+int rmsnorm_fwd_plan(const void *x, const void *residual, const void *w, void *y, void *residual_out,
+                     int64_t rows, int64_t hidden, float eps, int dtype, const rmsnorm_plan_t *plan,
+                     rmsnorm_stream_t stream) {
+    int st = check_args(x, residual, y, residual_out, rows, hidden, eps, dtype);
+    if (st != RMSNORM_OK) return st;
+    if (!elem_aligned(x, residual, w, y, residual_out, dtype)) return RMSNORM_EINVAL;
+    const int vec_ok = vec_ok_of(x, residual, w, y, residual_out, hidden, dtype);
+    if ((st = validate_plan(plan, rows, hidden, dtype, vec_ok)) != RMSNORM_OK) return st;
+    if (rows == 0) return RMSNORM_OK;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return RMSNORM_ECUDA;
+    return launch(make_params(x, residual, w, y, residual_out, rows, hidden, eps, plan->vec_elems), plan,
+                  dtype, dev, stream);
+}
+
+int64_t rmsnorm_max_hidden(int dtype) {
+    return (dtype == RMSNORM_F32 || dtype == RMSNORM_BF16) ? kMaxHidden : 0;
+}
+
+int rmsnorm_reg_max_chunks(void) { return rrn::kRegMaxCH; }
+
+const char *rmsnorm_strerror(int status) {
+    switch (status) {
+        case RMSNORM_OK: return "ok";
+        case RMSNORM_EINVAL: return "invalid argument";
+        case RMSNORM_EUNSUPPORTED: return "hidden size above the supported maximum";
+        case RMSNORM_ECUDA: return "CUDA runtime error";
+        default: return "unknown status";
+    }
+}
+
+const char *rmsnorm_build_info(void) {
+    return "row_reduction_norm_gb300 fused RMSNorm 0.1; target sm_103a; kernels: register (warp/CTA/"
+           "persistent), two-pass";
+}
+
+}  // extern "C"

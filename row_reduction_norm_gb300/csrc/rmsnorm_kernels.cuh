@@ -1,0 +1,476 @@
+// rmsnorm_kernels.cuh -- sm_103a kernels of the fused row-wise RMSNorm.
+//
+// The op, per row: h = x (or RN_T(x + residual), stored as residual_out),
+// y = RN_T(h * rsqrt(mean(h^2) + eps) * w).  Definition: "Building a GPU
+// compiler from scratch: from PyTorch to CUDA via multi-level IR (Emmy)",
+// running example and section "Tensor IR" (square, sum, division by the count,
+// plus epsilon, rsqrt, two multiplications); section "Loop IR" fuses all of it
+// into one kernel whose statistic never leaves the chip, which is what both
+// kernel families below do.
+//
+// This path is a row reduction bound by HBM bandwidth (about 1 flop per byte),
+// not a contraction, so it uses no tensor cores.  What matters on GB300 is
+// bytes in flight per SM, coalesced 128-bit accesses and a grid sized to the
+// SM count:
+//
+//  * rms_reg_kernel  -- the row lives in registers.  threads_per_row (GT)
+//    threads cooperate on a row, each owning up to CH 16-byte chunks
+//    (chunk index c*GT + t), so a warp's loads of one chunk slot cover 32
+//    consecutive 16-byte pieces.  GT <= 32 is the warp / sub-warp regime
+//    ("CuTeDSL at Perplexity", section "QK Norm": a half warp of 16 lanes x 8
+//    bf16 covers a 128-element head, reduced with xor butterflies); GT > 32
+//    adds a shared-memory combine across the row's warps (the "256 workers
+//    per row" schedule of the Emmy page, section "Tile IR").  Blocks stride
+//    over row groups, so a grid capped at the resident capacity is the
+//    persistent regime, and w (the same for every row) is staged once per
+//    block in shared memory.
+//  * rms_loop_kernel -- one block per row, the row streamed twice: the first
+//    pass forms h (and writes residual_out) and the sum of squares, the second
+//    re-reads h (an L2 hit: the rows in flight are far smaller than L2) and
+//    writes y.  It serves rows whose pointers are not 16-byte aligned
+//    (scalar accesses) and rows too long to hold in registers.
+//
+// Reduction order is fixed by (hidden, dtype, alignment) alone: per-thread
+// accumulators in a set order, a fixed tree over them, xor butterflies, then
+// a fixed tree over warps.  No atomics.  A row's result therefore does not
+// depend on the row count or grid, and repeated runs are bit-identical
+// (the determinism requirement of the model-as-a-kernel card).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace rrn {
+
+// Kernel arguments (passed by value).
+struct Params {
+    const void *x;
+    const void *res;     // nullable
+    const void *w;       // nullable
+    void *y;
+    void *res_out;       // nullable
+    int64_t rows;
+    int64_t row_elems;   // hidden
+    int32_t units;       // loads per row: hidden / vec_elems
+    float hidden_f;      // hidden as float (exact for hidden <= 2^24)
+    float eps;
+};
+
+struct BF16 {
+    using storage = uint16_t;
+    static constexpr int kVec = 8;   // elements per 16-byte chunk
+};
+struct F32 {
+    using storage = float;
+    static constexpr int kVec = 4;
+};
+
+struct __align__(16) Chunk {
+    uint32_t u[4];
+};
+
+// ------------------------------------------------------------------ memory
+// x and residual are read once: keep them out of L1 and mark their L2 lines
+// first to go.  w is read-only and reused by every row: the read-only path.
+// Plain (not .nc) loads for x/residual keep in-place calls (y == x) safe.
+
+__device__ __forceinline__ Chunk ld_stream16(const void *p) {
+    Chunk c;
+    asm volatile("ld.global.cs.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(c.u[0]), "=r"(c.u[1]), "=r"(c.u[2]), "=r"(c.u[3])
+                 : "l"(p));
+    return c;
+}
+
+// First read of a row that will be read again from L2 (two-pass kernel).
+__device__ __forceinline__ Chunk ld_keep_l2_16(const void *p) {
+    Chunk c;
+    asm volatile("ld.global.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(c.u[0]), "=r"(c.u[1]), "=r"(c.u[2]), "=r"(c.u[3])
+                 : "l"(p));
+    return c;
+}
+
+__device__ __forceinline__ Chunk ld_readonly16(const void *p) {
+    Chunk c;
+    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(c.u[0]), "=r"(c.u[1]), "=r"(c.u[2]), "=r"(c.u[3])
+                 : "l"(p));
+    return c;
+}
+
+__device__ __forceinline__ void st16(void *p, const Chunk &c) {
+    asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};"
+                 :
+                 : "l"(p), "r"(c.u[0]), "r"(c.u[1]), "r"(c.u[2]), "r"(c.u[3])
+                 : "memory");
+}
+
+// ------------------------------------------------------------- conversions
+// bf16 is the upper half of an fp32 encoding: widening is a 16-bit shift.
+// Narrowing rounds to nearest even with the CUDA intrinsic.
+
+__device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);   // .x = lo (lower address)
+    return *reinterpret_cast<uint32_t *>(&b);
+}
+
+__device__ __forceinline__ void unpack(const Chunk &c, float (&f)[8], BF16) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        f[2 * k] = bf16_lo(c.u[k]);
+        f[2 * k + 1] = bf16_hi(c.u[k]);
+    }
+}
+__device__ __forceinline__ void unpack(const Chunk &c, float (&f)[4], F32) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) f[k] = __uint_as_float(c.u[k]);
+}
+__device__ __forceinline__ Chunk pack(const float (&f)[8], BF16) {
+    Chunk c;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) c.u[k] = pack_bf16x2(f[2 * k], f[2 * k + 1]);
+    return c;
+}
+__device__ __forceinline__ Chunk pack(const float (&f)[4], F32) {
+    Chunk c;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) c.u[k] = __float_as_uint(f[k]);
+    return c;
+}
+
+// RN_T(a + b) for the residual add: one fp32 add, then one rounding to T.
+// For bf16 the fp32 sum of two bf16 values rounded to bf16 equals the
+// correctly rounded sum (fp32 carries more than 2*8+2 significant bits).
+__device__ __forceinline__ float add_round(float a, float b, BF16) {
+    return __bfloat162float(__float2bfloat16_rn(__fadd_rn(a, b)));
+}
+__device__ __forceinline__ float add_round(float a, float b, F32) { return __fadd_rn(a, b); }
+
+// ----------------------------------------------------------------- helpers
+
+__host__ __device__ constexpr int reg_block_threads(int gt) { return gt >= 256 ? gt : 256; }
+
+template <int LANES>
+__device__ __forceinline__ float butterfly_sum(float v) {
+    // xor butterfly inside aligned groups of LANES lanes; a + b == b + a, so
+    // every lane of a group ends with the same bits.
+#pragma unroll
+    for (int off = LANES / 2; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    return v;
+}
+
+template <int N>
+__device__ __forceinline__ float tree_sum(float (&v)[N]) {
+#pragma unroll
+    for (int s = N / 2; s > 0; s >>= 1) {
+#pragma unroll
+        for (int i = 0; i < s; ++i) v[i] += v[i + s];
+    }
+    return v[0];
+}
+
+// ------------------------------------------------------- register kernel
+
+template <typename T, int GT, int CH, bool RES, bool W>
+__global__ void __launch_bounds__(reg_block_threads(GT))
+rms_reg_kernel(const Params p) {
+    constexpr int V = T::kVec;
+    constexpr int BLOCK = reg_block_threads(GT);
+    constexpr int RPB = BLOCK / GT;               // rows per block iteration
+    constexpr int LANES = GT < 32 ? GT : 32;      // butterfly width
+    constexpr int WPR = GT > 32 ? GT / 32 : 1;    // warps per row
+    static_assert((GT & (GT - 1)) == 0 && GT >= 4 && GT <= 1024, "GT: power of two in [4, 1024]");
+    __shared__ float red[2][RPB][WPR];
+
+    const int tid = threadIdx.x;
+    const int slot = tid / GT;
+    const int t = tid % GT;
+    const int nch = p.units;
+    const int64_t row_bytes = p.row_elems * (int64_t)sizeof(typename T::storage);
+
+    // w is the same for every row: staged once per block in shared memory
+    // (dynamic, units * 16 bytes) and read from there in every epilogue.
+    extern __shared__ Chunk w_smem[];
+    if constexpr (W) {
+        for (int i = tid; i < nch; i += BLOCK)
+            w_smem[i] = ld_readonly16(static_cast<const char *>(p.w) + (int64_t)i * 16);
+        __syncthreads();
+    }
+
+    int parity = 0;
+    for (int64_t rb = blockIdx.x; rb * RPB < p.rows; rb += gridDim.x) {
+        const int64_t row = rb * RPB + slot;
+        const bool row_ok = row < p.rows;
+        const int64_t off = row * row_bytes;
+
+        // A1: load the row's chunks (zeros where a slot is past the row end)
+        Chunk hc[CH];
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+            const int u = c * GT + t;
+            if (row_ok && u < nch)
+                hc[c] = ld_stream16(static_cast<const char *>(p.x) + off + (int64_t)u * 16);
+            else
+                hc[c] = Chunk{{0u, 0u, 0u, 0u}};
+        }
+        // A2: h = RN_T(x + residual), written out as residual_out
+        if constexpr (RES) {
+            Chunk rc[CH];
+#pragma unroll
+            for (int c = 0; c < CH; ++c) {
+                const int u = c * GT + t;
+                if (row_ok && u < nch)
+                    rc[c] = ld_stream16(static_cast<const char *>(p.res) + off + (int64_t)u * 16);
+                else
+                    rc[c] = Chunk{{0u, 0u, 0u, 0u}};
+            }
+#pragma unroll
+            for (int c = 0; c < CH; ++c) {
+                const int u = c * GT + t;
+                float a[V], b[V];
+                unpack(hc[c], a, T{});
+                unpack(rc[c], b, T{});
+#pragma unroll
+                for (int e = 0; e < V; ++e) a[e] = add_round(a[e], b[e], T{});
+                hc[c] = pack(a, T{});
+                if (row_ok && u < nch)
+                    st16(static_cast<char *>(p.res_out) + off + (int64_t)u * 16, hc[c]);
+            }
+        }
+        // A3: squares into V accumulators, chunk order; zero slots add +0 exactly
+        float acc[V];
+#pragma unroll
+        for (int e = 0; e < V; ++e) acc[e] = 0.f;
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+            float a[V];
+            unpack(hc[c], a, T{});
+#pragma unroll
+            for (int e = 0; e < V; ++e) acc[e] = fmaf(a[e], a[e], acc[e]);
+        }
+        float sum = tree_sum(acc);
+        // A4: butterfly across the row's lanes of this warp
+        sum = butterfly_sum<LANES>(sum);
+        // A5: fixed-order combine across the row's warps
+        if constexpr (WPR > 1) {
+            if ((tid & 31) == 0) red[parity][slot][t / 32] = sum;
+            __syncthreads();
+            float v[WPR];
+#pragma unroll
+            for (int i = 0; i < WPR; ++i) v[i] = red[parity][slot][i];
+            sum = tree_sum(v);
+            parity ^= 1;   // the next iteration writes the other buffer
+        }
+        // A6: the row's scale
+        const float r = rsqrtf(sum / p.hidden_f + p.eps);
+        // A7: y = RN_T(h * r * w)
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+            const int u = c * GT + t;
+            if (row_ok && u < nch) {
+                float a[V];
+                unpack(hc[c], a, T{});
+                if constexpr (W) {
+                    float wv[V];
+                    unpack(w_smem[u], wv, T{});
+#pragma unroll
+                    for (int e = 0; e < V; ++e) a[e] = (a[e] * r) * wv[e];
+                } else {
+#pragma unroll
+                    for (int e = 0; e < V; ++e) a[e] = a[e] * r;
+                }
+                st16(static_cast<char *>(p.y) + off + (int64_t)u * 16, pack(a, T{}));
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------- two-pass kernel
+// Units are VE elements: VE == T::kVec (one 16-byte chunk) or 1 (a scalar).
+// Raw units stay packed in registers until they are used.
+
+template <typename T, int VE>
+struct UnitIO;
+
+template <typename T>
+struct UnitIO<T, T::kVec> {
+    static constexpr int VE = T::kVec;
+    using Raw = Chunk;
+    __device__ static Raw zero() { return Chunk{{0u, 0u, 0u, 0u}}; }
+    __device__ static Raw load_first(const void *base, int64_t u) {
+        return ld_keep_l2_16(static_cast<const char *>(base) + u * 16);
+    }
+    __device__ static Raw load_last(const void *base, int64_t u) {
+        return ld_stream16(static_cast<const char *>(base) + u * 16);
+    }
+    __device__ static Raw load_w(const void *base, int64_t u) {
+        return ld_readonly16(static_cast<const char *>(base) + u * 16);
+    }
+    __device__ static void widen(const Raw &r, float (&f)[VE]) { unpack(r, f, T{}); }
+    __device__ static void store(void *base, int64_t u, const float (&f)[VE]) {
+        st16(static_cast<char *>(base) + u * 16, pack(f, T{}));
+    }
+};
+
+// Scalar units: the raw value is the element's bit pattern in 32 bits.
+__device__ __forceinline__ uint32_t ld_bits(const void *p, int64_t i, BF16, int hint) {
+    unsigned short v;
+    const void *a = static_cast<const uint16_t *>(p) + i;
+    if (hint == 0)
+        asm volatile("ld.global.L1::no_allocate.u16 %0, [%1];" : "=h"(v) : "l"(a));
+    else if (hint == 1)
+        asm volatile("ld.global.cs.u16 %0, [%1];" : "=h"(v) : "l"(a));
+    else
+        asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(a));
+    return (uint32_t)v;
+}
+__device__ __forceinline__ uint32_t ld_bits(const void *p, int64_t i, F32, int hint) {
+    uint32_t v;
+    const void *a = static_cast<const float *>(p) + i;
+    if (hint == 0)
+        asm volatile("ld.global.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(a));
+    else if (hint == 1)
+        asm volatile("ld.global.cs.u32 %0, [%1];" : "=r"(v) : "l"(a));
+    else
+        asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(a));
+    return v;
+}
+__device__ __forceinline__ float widen_bits(uint32_t b, BF16) { return __uint_as_float(b << 16); }
+__device__ __forceinline__ float widen_bits(uint32_t b, F32) { return __uint_as_float(b); }
+__device__ __forceinline__ void st_scalar(void *p, int64_t i, float v, BF16) {
+    __nv_bfloat16 b = __float2bfloat16_rn(v);
+    unsigned short s = *reinterpret_cast<unsigned short *>(&b);
+    asm volatile("st.global.u16 [%0], %1;" : : "l"(static_cast<uint16_t *>(p) + i), "h"(s) : "memory");
+}
+__device__ __forceinline__ void st_scalar(void *p, int64_t i, float v, F32) {
+    asm volatile("st.global.f32 [%0], %1;" : : "l"(static_cast<float *>(p) + i), "f"(v) : "memory");
+}
+
+template <typename T>
+struct UnitIO<T, 1> {
+    static constexpr int VE = 1;
+    using Raw = uint32_t;
+    __device__ static Raw zero() { return 0u; }
+    __device__ static Raw load_first(const void *base, int64_t u) { return ld_bits(base, u, T{}, 0); }
+    __device__ static Raw load_last(const void *base, int64_t u) { return ld_bits(base, u, T{}, 1); }
+    __device__ static Raw load_w(const void *base, int64_t u) { return ld_bits(base, u, T{}, 2); }
+    __device__ static void widen(const Raw &r, float (&f)[1]) { f[0] = widen_bits(r, T{}); }
+    __device__ static void store(void *base, int64_t u, const float (&f)[1]) {
+        st_scalar(base, u, f[0], T{});
+    }
+};
+
+template <typename T, int VE, int BLOCK, bool RES, bool W>
+__global__ void __launch_bounds__(BLOCK, 1)
+rms_loop_kernel(const Params p) {
+    using IO = UnitIO<T, VE>;
+    using Raw = typename IO::Raw;
+    constexpr int NACC = 8;                          // per-thread accumulators
+    constexpr int U = VE == 1 ? NACC : 2;            // units in flight per step
+    constexpr int NW = BLOCK / 32;
+    static_assert(BLOCK % 32 == 0 && (NW & (NW - 1)) == 0, "BLOCK: power-of-two warps");
+    static_assert((U * VE) % NACC == 0 || NACC % (U * VE) == 0, "accumulator cycle");
+    __shared__ float red[2][NW];
+
+    const int tid = threadIdx.x;
+    const int64_t nunits = p.units;
+    const int64_t row_bytes = p.row_elems * (int64_t)sizeof(typename T::storage);
+    int parity = 0;
+
+    for (int64_t row = blockIdx.x; row < p.rows; row += gridDim.x) {
+        const int64_t off = row * row_bytes;
+        const void *xr = static_cast<const char *>(p.x) + off;
+        const void *rr = RES ? static_cast<const char *>(p.res) + off : nullptr;
+        void *hr = RES ? static_cast<char *>(p.res_out) + off : nullptr;
+        void *yr = static_cast<char *>(p.y) + off;
+
+        // pass 1: h (and residual_out), sum of squares.  Element e of the
+        // j-th unit of a step feeds accumulator (j * VE + e) % NACC.
+        float acc[NACC];
+#pragma unroll
+        for (int i = 0; i < NACC; ++i) acc[i] = 0.f;
+        for (int64_t base = tid; base < nunits; base += (int64_t)BLOCK * U) {
+            Raw xa[U];
+            Raw rb[RES ? U : 1];
+#pragma unroll
+            for (int j = 0; j < U; ++j) {
+                const int64_t u = base + (int64_t)j * BLOCK;
+                xa[j] = u < nunits ? IO::load_first(xr, u) : IO::zero();
+            }
+            if constexpr (RES) {
+#pragma unroll
+                for (int j = 0; j < U; ++j) {
+                    const int64_t u = base + (int64_t)j * BLOCK;
+                    rb[j] = u < nunits ? IO::load_first(rr, u) : IO::zero();
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < U; ++j) {
+                const int64_t u = base + (int64_t)j * BLOCK;
+                float a[VE];
+                IO::widen(xa[j], a);
+                if constexpr (RES) {
+                    float b[VE];
+                    IO::widen(rb[j], b);
+#pragma unroll
+                    for (int e = 0; e < VE; ++e) a[e] = add_round(a[e], b[e], T{});
+                    if (u < nunits) IO::store(hr, u, a);
+                }
+#pragma unroll
+                for (int e = 0; e < VE; ++e) {
+                    const int k = (j * VE + e) % NACC;
+                    acc[k] = fmaf(a[e], a[e], acc[k]);
+                }
+            }
+        }
+        float sum = tree_sum(acc);
+        sum = butterfly_sum<32>(sum);
+        if constexpr (NW > 1) {
+            if ((tid & 31) == 0) red[parity][tid / 32] = sum;
+            __syncthreads();
+            float v[NW];
+#pragma unroll
+            for (int i = 0; i < NW; ++i) v[i] = red[parity][i];
+            sum = tree_sum(v);
+            parity ^= 1;
+        }
+        const float r = rsqrtf(sum / p.hidden_f + p.eps);
+
+        // pass 2: re-read h (x, or residual_out written above by this same
+        // thread) and write y
+        const void *src = RES ? static_cast<const void *>(hr) : xr;
+        for (int64_t base = tid; base < nunits; base += (int64_t)BLOCK * U) {
+            Raw ha[U];
+            Raw wa[W ? U : 1];
+#pragma unroll
+            for (int j = 0; j < U; ++j) {
+                const int64_t u = base + (int64_t)j * BLOCK;
+                ha[j] = u < nunits ? IO::load_last(src, u) : IO::zero();
+                if constexpr (W) wa[j] = u < nunits ? IO::load_w(p.w, u) : IO::zero();
+            }
+#pragma unroll
+            for (int j = 0; j < U; ++j) {
+                const int64_t u = base + (int64_t)j * BLOCK;
+                float a[VE];
+                IO::widen(ha[j], a);
+                if constexpr (W) {
+                    float wv[VE];
+                    IO::widen(wa[j], wv);
+#pragma unroll
+                    for (int e = 0; e < VE; ++e) a[e] = (a[e] * r) * wv[e];
+                } else {
+#pragma unroll
+                    for (int e = 0; e < VE; ++e) a[e] = a[e] * r;
+                }
+                if (u < nunits) IO::store(yr, u, a);
+            }
+        }
+    }
+}
+
+}  // namespace rrn

@@ -1,0 +1,146 @@
+"""The C ABI without a GPU: the library loads, exports what the header
+declares, plans correctly, and rejects bad arguments before any CUDA call."""
+import ctypes
+import re
+
+import pytest
+
+import row_reduction_norm_gb300 as R
+from row_reduction_norm_gb300 import _native as N
+from row_reduction_norm_gb300 import build as B
+
+HEADER = B.os.path.join(B.INCLUDE, "rmsnorm.h")
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(rmsnorm_\w+)\s*\(", text)))
+
+
+def test_library_builds_and_loads():
+    B.build()
+    lib = N.load()
+    assert "sm_103a" in R.rmsnorm_build_info()
+    assert lib is N.load()
+
+
+def test_every_declared_symbol_is_exported():
+    lib = ctypes.CDLL(N.library_path())
+    declared = header_functions()
+    assert declared == sorted(N.EXPORTED)
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_strerror_and_limits():
+    assert R.rmsnorm_strerror(0) == "ok"
+    assert "invalid" in R.rmsnorm_strerror(-1)
+    assert R.rmsnorm_max_hidden(N.RMSNORM_BF16) == 65536
+    assert R.rmsnorm_max_hidden(N.RMSNORM_F32) == 65536
+    assert R.rmsnorm_max_hidden(7) == 0
+    assert R.rmsnorm_reg_max_chunks() == 8
+
+
+def _status(*args):
+    return N.rmsnorm_fwd_status(*args)
+
+
+def test_invalid_arguments_rejected_without_cuda():
+    P = 1 << 20   # a fake, aligned address: never dereferenced, checks fail first
+    assert _status(None, None, None, P, None, 4, 64, 1e-6, 1, 0) == N.RMSNORM_EINVAL
+    assert _status(P, None, None, None, None, 4, 64, 1e-6, 1, 0) == N.RMSNORM_EINVAL
+    assert _status(P, None, None, P, None, -1, 64, 1e-6, 1, 0) == N.RMSNORM_EINVAL
+    assert _status(P, None, None, P, None, 4, 0, 1e-6, 1, 0) == N.RMSNORM_EINVAL
+    assert _status(P, None, None, P, None, 4, 64, 1e-6, 5, 0) == N.RMSNORM_EINVAL
+    assert _status(P, None, None, P, None, 4, 64, -1e-6, 1, 0) == N.RMSNORM_EINVAL
+    assert _status(P, None, None, P, None, 4, 64, float("inf"), 1, 0) == N.RMSNORM_EINVAL
+    assert _status(P, P, None, P, None, 4, 64, 1e-6, 1, 0) == N.RMSNORM_EINVAL
+    assert _status(P, None, None, P, P, 4, 64, 1e-6, 1, 0) == N.RMSNORM_EINVAL
+    assert _status(P, None, None, P, None, 4, 65537, 1e-6, 1, 0) == N.RMSNORM_EUNSUPPORTED
+    assert _status(P + 1, None, None, P, None, 4, 64, 1e-6, 1, 0) == N.RMSNORM_EINVAL   # odd address
+    assert _status(P, None, P + 2, P, None, 4, 64, 1e-6, 0, 0) == N.RMSNORM_EINVAL     # f32 needs 4
+    assert _status(P, None, None, P, None, 1 << 62, 64, 1e-6, 1, 0) == N.RMSNORM_EINVAL  # overflow
+    # rows == 0 is a successful no-op (no CUDA call)
+    assert _status(P, None, None, P, None, 0, 64, 1e-6, 1, 0) == N.RMSNORM_OK
+
+
+HIDDENS = [1, 2, 7, 8, 16, 31, 33, 64, 127, 128, 256, 576, 1000, 1024, 1025, 2048, 3072, 4096,
+           5120, 7168, 8192, 12288, 16384, 32768, 65536]
+
+
+@pytest.mark.parametrize("dtype", [N.RMSNORM_BF16, N.RMSNORM_F32])
+@pytest.mark.parametrize("hidden", HIDDENS)
+def test_plan_properties(dtype, hidden):
+    V = 8 if dtype == N.RMSNORM_BF16 else 4
+    esz = 2 if dtype == N.RMSNORM_BF16 else 4
+    for vec_ok in (True, False):
+        if vec_ok and (hidden * esz) % 16:
+            with pytest.raises(N.RmsNormError):
+                R.rmsnorm_plan(10, hidden, dtype, True, 152, 2)
+            continue
+        plans = [R.rmsnorm_plan(rows, hidden, dtype, vec_ok, 152, 2) for rows in (1, 7, 1000, 10 ** 6)]
+        sched = {(p.kernel, p.threads_per_row, p.chunks_per_thread, p.vec_elems, p.block_threads,
+                  p.rows_per_block) for p in plans}
+        assert len(sched) == 1, "the per-row schedule must not depend on the row count"
+        for rows, p in zip((1, 7, 1000, 10 ** 6), plans):
+            row_blocks = -(-rows // p.rows_per_block)
+            assert 1 <= p.grid <= min(row_blocks, 152 * 2)
+            assert p.persistent == (row_blocks > 152 * 2)
+            if p.kernel == N.RMSNORM_KERNEL_REG:
+                assert vec_ok and p.vec_elems == V
+                gt, ch = p.threads_per_row, p.chunks_per_thread
+                assert gt * ch * V >= hidden and gt & (gt - 1) == 0 and 4 <= gt <= 512
+                assert ch in (1, 2, 4, 8)
+                assert p.block_threads == max(gt, 256) and p.rows_per_block == p.block_threads // gt
+                want = (N.RMSNORM_REGIME_PERSISTENT if p.persistent else
+                        N.RMSNORM_REGIME_WARP if gt <= 32 else N.RMSNORM_REGIME_CTA)
+                assert p.regime == want
+            else:
+                assert p.kernel == N.RMSNORM_KERNEL_LOOP and p.regime == N.RMSNORM_REGIME_LOOPED
+                assert p.vec_elems == (V if vec_ok else 1)
+                units = hidden // p.vec_elems
+                assert -(-units // p.block_threads) * p.vec_elems <= 64
+        if not vec_ok:
+            assert plans[0].kernel == N.RMSNORM_KERNEL_LOOP
+
+
+def test_qk_norm_is_warp_regime_and_large_rows_cta():
+    qk = R.rmsnorm_plan(1024, 128, N.RMSNORM_BF16, True, 152, 4)
+    assert qk.regime == N.RMSNORM_REGIME_WARP and qk.threads_per_row <= 32
+    big = R.rmsnorm_plan(100, 8192, N.RMSNORM_BF16, True, 152, 4)
+    assert big.regime == N.RMSNORM_REGIME_CTA and big.threads_per_row > 32
+
+
+def test_plan_rejects_bad_input():
+    with pytest.raises(N.RmsNormError):
+        R.rmsnorm_plan(-1, 128, 1, True, 152, 1)
+    with pytest.raises(N.RmsNormError) as e:
+        R.rmsnorm_plan(1, 1 << 20, 1, True, 152, 1)
+    assert e.value.status == N.RMSNORM_EUNSUPPORTED
+
+
+def test_fwd_plan_validation_without_cuda():
+    P = 1 << 20
+    p = R.rmsnorm_plan(4, 64, N.RMSNORM_BF16, True, 152, 1)
+    q = p.copy()
+    q.threads_per_row = 3
+    assert N.rmsnorm_fwd_plan_status(P, None, None, P, None, 4, 64, 1e-6, 1, q, 0) == N.RMSNORM_EINVAL
+    q = p.copy()
+    q.chunks_per_thread = 16
+    assert N.rmsnorm_fwd_plan_status(P, None, None, P, None, 4, 64, 1e-6, 1, q, 0) == N.RMSNORM_EINVAL
+    q = p.copy()
+    q.grid = 0
+    assert N.rmsnorm_fwd_plan_status(P, None, None, P, None, 4, 64, 1e-6, 1, q, 0) == N.RMSNORM_EINVAL
+    # a vector plan on a misaligned pointer
+    assert N.rmsnorm_fwd_plan_status(P + 2, None, None, P, None, 4, 64, 1e-6, 1, p, 0) == N.RMSNORM_EINVAL
+    assert N.rmsnorm_fwd_plan_status(P, None, None, P, None, 4, 64, 1e-6, 1, None, 0) == N.RMSNORM_EINVAL
+    # rows == 0 with a valid plan: no-op
+    assert N.rmsnorm_fwd_plan_status(P, None, None, P, None, 0, 64, 1e-6, 1, p, 0) == N.RMSNORM_OK
+
+
+def test_torch_api_refuses_cpu_tensors():
+    import torch
+    x = torch.zeros(4, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        R.rms_norm(x)
