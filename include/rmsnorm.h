@@ -101,6 +101,11 @@ typedef struct {
     int32_t block_threads;      /* threads per block                                  */
     int32_t rows_per_block;     /* rows one block handles per loop iteration          */
     int32_t persistent;         /* 1 if grid < row blocks (blocks stride over rows)   */
+    int32_t pdl;                /* 1: launch with programmatic stream serialisation
+                                   (the kernel may start while the previous kernel on
+                                   the stream drains; it reads no input before that
+                                   kernel has completed).  Planning sets 1.          */
+    int32_t reserved;           /* 0                                                  */
     int64_t grid;               /* blocks launched (0 when rows == 0)                 */
 } rmsnorm_plan_t;
 
@@ -111,7 +116,8 @@ typedef struct {
  *   w            [hidden]        optional (NULL): per-element weight
  *   y            [rows, hidden]  output
  *   residual_out [rows, hidden]  required iff residual is given: receives h
- *   rows >= 0 (0 is a successful no-op), 1 <= hidden <= rmsnorm_max_hidden(dtype)
+ *   rows >= 0 (0 is a successful no-op that reads no pointer, which may then
+ *   be NULL), 1 <= hidden <= rmsnorm_max_hidden(dtype)
  *   eps          finite, >= 0; used as the float value passed
  *   dtype        RMSNORM_F32 or RMSNORM_BF16
  * Returns RMSNORM_OK or a negative status (see above).

@@ -57,6 +57,8 @@ class Plan(ctypes.Structure):
         ("block_threads", ctypes.c_int32),
         ("rows_per_block", ctypes.c_int32),
         ("persistent", ctypes.c_int32),
+        ("pdl", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
         ("grid", ctypes.c_int64),
     ]
 

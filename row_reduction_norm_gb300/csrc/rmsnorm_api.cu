@@ -20,9 +20,17 @@
 #include "rmsnorm.h"
 #include "rmsnorm_kernels.cuh"
 
+static_assert(sizeof(rmsnorm_plan_t) == 48, "rmsnorm_plan_t layout is part of the ABI");
+
 namespace {
 
 constexpr int64_t kMaxHidden = 65536;
+constexpr int64_t kRegTargetCH = 4;
+// Row-group blocks beyond this many waves of resident blocks switch the grid
+// to the persistent form (blocks stride over row groups).  Measured on GB300,
+// one block per row group beats a grid capped at one wave for every workload
+// up to 65536 x 8192, so the cap only engages for very large row counts.
+constexpr int64_t kPersistentWaves = 4096;
 constexpr int kMaxDevices = 64;
 // Largest per-thread chain of squares the two-pass kernel may form (keeps the
 // fp32 error bound of the sum the same as the register kernel's).
@@ -50,12 +58,13 @@ bool aligned_to(const void *p, int a) {
 int check_args(const void *x, const void *residual, const void *y, const void *residual_out,
                int64_t rows, int64_t hidden, float eps, int dtype) {
     if (dtype != RMSNORM_F32 && dtype != RMSNORM_BF16) return RMSNORM_EINVAL;
-    if (x == nullptr || y == nullptr) return RMSNORM_EINVAL;
-    if ((residual == nullptr) != (residual_out == nullptr)) return RMSNORM_EINVAL;
     if (rows < 0 || hidden <= 0) return RMSNORM_EINVAL;
     if (!std::isfinite(eps) || eps < 0.f) return RMSNORM_EINVAL;
     if (hidden > kMaxHidden) return RMSNORM_EUNSUPPORTED;
     if (rows > INT64_MAX / (hidden * elem_size(dtype))) return RMSNORM_EINVAL;
+    if (rows == 0) return RMSNORM_OK;   // nothing is accessed: pointers may be NULL
+    if (x == nullptr || y == nullptr) return RMSNORM_EINVAL;
+    if ((residual == nullptr) != (residual_out == nullptr)) return RMSNORM_EINVAL;
     return RMSNORM_OK;
 }
 
@@ -78,9 +87,14 @@ void schedule(int64_t hidden, int dtype, int vec_ok, rmsnorm_plan_t *p) {
     const int V = vec_elems_of(dtype);
     if (vec_ok) {
         const int64_t nch = hidden / V;
-        // aim at up to 8 chunks (128 bytes) per thread, at least 4 lanes per row
-        int64_t gt = next_pow2(ceil_div(nch, rrn::kRegMaxCH));
+        // Aim at 4 chunks (64 bytes of each input) per thread with at least 4
+        // lanes per row: measured on GB300, this keeps every row-group block
+        // resident in one wave at the occupancy the registers allow and beats
+        // 8 chunks per thread.  Rows longer than 512 threads x 4 chunks take
+        // up to 8 chunks per thread.
+        int64_t gt = next_pow2(ceil_div(nch, kRegTargetCH));
         if (gt < 4) gt = 4;
+        if (gt > rrn::kRegMaxGT && ceil_div(nch, rrn::kRegMaxGT) <= rrn::kRegMaxCH) gt = rrn::kRegMaxGT;
         if (gt <= rrn::kRegMaxGT) {
             int64_t need = ceil_div(nch, gt);
             int ch = 1;
@@ -114,10 +128,12 @@ void schedule(int64_t hidden, int dtype, int vec_ok, rmsnorm_plan_t *p) {
 
 void size_grid(int64_t rows, int sm_count, int blocks_per_sm, rmsnorm_plan_t *p) {
     const int64_t row_blocks = ceil_div(rows, p->rows_per_block);
-    int64_t cap = (int64_t)(sm_count > 0 ? sm_count : 1) * (blocks_per_sm > 0 ? blocks_per_sm : 1);
+    int64_t cap = (int64_t)(sm_count > 0 ? sm_count : 1) * (blocks_per_sm > 0 ? blocks_per_sm : 1) *
+                  kPersistentWaves;
     if (cap > INT_MAX) cap = INT_MAX;
     p->persistent = row_blocks > cap;
     p->grid = row_blocks > cap ? cap : row_blocks;
+    p->pdl = 1;
     if (p->persistent && p->kernel == RMSNORM_KERNEL_REG) p->regime = RMSNORM_REGIME_PERSISTENT;
 }
 
@@ -141,6 +157,7 @@ int validate_plan(const rmsnorm_plan_t *p, int64_t rows, int64_t hidden, int dty
     if (p == nullptr) return RMSNORM_EINVAL;
     const int V = vec_elems_of(dtype);
     if (rows > 0 && (p->grid < 1 || p->grid > INT_MAX)) return RMSNORM_EINVAL;
+    if (p->pdl != 0 && p->pdl != 1) return RMSNORM_EINVAL;
     if (p->kernel == RMSNORM_KERNEL_REG) {
         const int gt = p->threads_per_row, ch = p->chunks_per_thread;
         if (!vec_ok || p->vec_elems != V) return RMSNORM_EINVAL;
@@ -269,8 +286,17 @@ int launch(const rrn::Params &prm, const rmsnorm_plan_t *plan, int dtype, int de
     }
     rrn::Params args = prm;
     void *argv[] = {&args};
-    cudaError_t e = cudaLaunchKernel(fn, dim3((unsigned)plan->grid), dim3((unsigned)plan->block_threads),
-                                     argv, smem, reinterpret_cast<cudaStream_t>(stream));
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)plan->grid);
+    cfg.blockDim = dim3((unsigned)plan->block_threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+    cfg.attrs = attr;
+    cfg.numAttrs = plan->pdl ? 1 : 0;
+    cudaError_t e = cudaLaunchKernelExC(&cfg, fn, argv);
     if (e != cudaSuccess) {
         (void)cudaGetLastError();   // clear the non-sticky launch error
         return RMSNORM_ECUDA;

@@ -107,6 +107,16 @@ __device__ __forceinline__ void st16(void *p, const Chunk &c) {
                  : "memory");
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialisation may start while the kernel before it drains.  It must not
+// read its inputs before griddepcontrol.wait returns (the grids it depends on
+// have completed and their writes are visible); without that launch
+// attribute the wait returns at once.  Signalling launch_dependents at entry
+// lets the next kernel's blocks be placed as soon as every block of this one
+// is resident.
+__device__ __forceinline__ void pdl_wait_for_inputs() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_allow_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
+
 // ------------------------------------------------------------- conversions
 // bf16 is the upper half of an fp32 encoding: widening is a 16-bit shift.
 // Narrowing rounds to nearest even with the CUDA intrinsic.
@@ -193,14 +203,15 @@ rms_reg_kernel(const Params p) {
     const int nch = p.units;
     const int64_t row_bytes = p.row_elems * (int64_t)sizeof(typename T::storage);
 
+    pdl_wait_for_inputs();
+    pdl_allow_dependents();
+
     // w is the same for every row: staged once per block in shared memory
-    // (dynamic, units * 16 bytes) and read from there in every epilogue.
+    // (dynamic, units * 16 bytes) and read from there in every epilogue.  The
+    // staging happens after the first row's loads are issued, so the two
+    // memory round trips overlap.
     extern __shared__ Chunk w_smem[];
-    if constexpr (W) {
-        for (int i = tid; i < nch; i += BLOCK)
-            w_smem[i] = ld_readonly16(static_cast<const char *>(p.w) + (int64_t)i * 16);
-        __syncthreads();
-    }
+    bool w_staged = false;
 
     int parity = 0;
     for (int64_t rb = blockIdx.x; rb * RPB < p.rows; rb += gridDim.x) {
@@ -218,9 +229,8 @@ rms_reg_kernel(const Params p) {
             else
                 hc[c] = Chunk{{0u, 0u, 0u, 0u}};
         }
-        // A2: h = RN_T(x + residual), written out as residual_out
+        Chunk rc[RES ? CH : 1];
         if constexpr (RES) {
-            Chunk rc[CH];
 #pragma unroll
             for (int c = 0; c < CH; ++c) {
                 const int u = c * GT + t;
@@ -229,6 +239,17 @@ rms_reg_kernel(const Params p) {
                 else
                     rc[c] = Chunk{{0u, 0u, 0u, 0u}};
             }
+        }
+        if constexpr (W) {
+            if (!w_staged) {   // first iteration of the block (uniform across it)
+                for (int i = tid; i < nch; i += BLOCK)
+                    w_smem[i] = ld_readonly16(static_cast<const char *>(p.w) + (int64_t)i * 16);
+                __syncthreads();
+                w_staged = true;
+            }
+        }
+        // A2: h = RN_T(x + residual), written out as residual_out
+        if constexpr (RES) {
 #pragma unroll
             for (int c = 0; c < CH; ++c) {
                 const int u = c * GT + t;
@@ -381,6 +402,8 @@ rms_loop_kernel(const Params p) {
     const int64_t nunits = p.units;
     const int64_t row_bytes = p.row_elems * (int64_t)sizeof(typename T::storage);
     int parity = 0;
+    pdl_wait_for_inputs();
+    pdl_allow_dependents();
 
     for (int64_t row = blockIdx.x; row < p.rows; row += gridDim.x) {
         const int64_t off = row * row_bytes;

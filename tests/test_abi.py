@@ -33,6 +33,11 @@ def test_every_declared_symbol_is_exported():
         assert hasattr(lib, name), name
 
 
+def test_plan_struct_layout():
+    assert ctypes.sizeof(N.Plan) == 48
+    assert N.Plan.grid.offset == 40
+
+
 def test_strerror_and_limits():
     assert R.rmsnorm_strerror(0) == "ok"
     assert "invalid" in R.rmsnorm_strerror(-1)
@@ -61,8 +66,10 @@ def test_invalid_arguments_rejected_without_cuda():
     assert _status(P + 1, None, None, P, None, 4, 64, 1e-6, 1, 0) == N.RMSNORM_EINVAL   # odd address
     assert _status(P, None, P + 2, P, None, 4, 64, 1e-6, 0, 0) == N.RMSNORM_EINVAL     # f32 needs 4
     assert _status(P, None, None, P, None, 1 << 62, 64, 1e-6, 1, 0) == N.RMSNORM_EINVAL  # overflow
-    # rows == 0 is a successful no-op (no CUDA call)
+    # rows == 0 is a successful no-op (no CUDA call, no pointer read: NULL is fine)
     assert _status(P, None, None, P, None, 0, 64, 1e-6, 1, 0) == N.RMSNORM_OK
+    assert _status(None, None, None, None, None, 0, 64, 1e-6, 1, 0) == N.RMSNORM_OK
+    assert _status(None, None, None, None, None, 0, 64, -1.0, 1, 0) == N.RMSNORM_EINVAL
 
 
 HIDDENS = [1, 2, 7, 8, 16, 31, 33, 64, 127, 128, 256, 576, 1000, 1024, 1025, 2048, 3072, 4096,
@@ -80,13 +87,19 @@ def test_plan_properties(dtype, hidden):
                 R.rmsnorm_plan(10, hidden, dtype, True, 152, 2)
             continue
         plans = [R.rmsnorm_plan(rows, hidden, dtype, vec_ok, 152, 2) for rows in (1, 7, 1000, 10 ** 6)]
+        huge = R.rmsnorm_plan(10 ** 12, hidden, dtype, vec_ok, 152, 2)
+        assert huge.persistent == 1 and huge.grid == 152 * 2 * 4096
+        if huge.kernel == N.RMSNORM_KERNEL_REG:
+            assert huge.regime == N.RMSNORM_REGIME_PERSISTENT
         sched = {(p.kernel, p.threads_per_row, p.chunks_per_thread, p.vec_elems, p.block_threads,
                   p.rows_per_block) for p in plans}
         assert len(sched) == 1, "the per-row schedule must not depend on the row count"
+        cap = 152 * 2 * 4096
         for rows, p in zip((1, 7, 1000, 10 ** 6), plans):
             row_blocks = -(-rows // p.rows_per_block)
-            assert 1 <= p.grid <= min(row_blocks, 152 * 2)
-            assert p.persistent == (row_blocks > 152 * 2)
+            assert 1 <= p.grid <= min(row_blocks, cap)
+            assert p.persistent == (row_blocks > cap)
+            assert p.pdl == 1
             if p.kernel == N.RMSNORM_KERNEL_REG:
                 assert vec_ok and p.vec_elems == V
                 gt, ch = p.threads_per_row, p.chunks_per_thread

@@ -125,11 +125,12 @@ def all_plans(rows, hidden, dtype_code, vec_ok, sm_count=152):
             p.rows_per_block = 1
             plans.append(p)
     out = []
-    for p in plans:
+    for k, p in enumerate(plans):
         row_blocks = -(-rows // p.rows_per_block)
         for grid in sorted({row_blocks, max(1, min(row_blocks, 3))}):
             q = p.copy()
             q.grid = grid
+            q.pdl = (k + grid) % 2   # both launch modes across the set
             out.append(q)
     return out
 
