@@ -61,6 +61,12 @@ def parse_args(argv=None):
     ap.add_argument("--ncu-case", default=None,
                     help="profiling mode: launch this workload --launches times and exit")
     ap.add_argument("--launches", type=int, default=3)
+    ap.add_argument("--rows", type=int, default=0, help="profiling mode: override the row count")
+    ap.add_argument("--hidden", type=int, default=0, help="profiling mode: override the hidden size")
+    ap.add_argument("--grid", type=int, default=0,
+                    help="profiling mode: force this grid (blocks stride over row groups)")
+    ap.add_argument("--misalign", action="store_true",
+                    help="profiling mode: offset every tensor by one element (scalar path)")
     return ap.parse_args(argv)
 
 
@@ -95,18 +101,42 @@ def kernel_source_hash():
 
 
 def profiled_traffic(workload):
-    """DRAM bytes per launch from the committed ncu summary of this workload,
-    if it was taken on the current kernel sources (else None)."""
-    path = os.path.join(ROOT, "profiles", f"rmsnorm_{workload}.md")
+    """DRAM bytes per launch from the committed ncu summary of this workload
+    (profiles/ncu_*.md with a matching ``profile_workload:`` line), if it was
+    taken on the current kernel sources; else None."""
+    pdir = os.path.join(ROOT, "profiles")
     try:
-        text = open(path).read()
+        names = sorted(os.listdir(pdir))
     except OSError:
         return None
-    m_hash = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", text)
-    m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
-    if not (m_hash and m_bytes) or m_hash.group(1) != kernel_source_hash():
-        return None
-    return int(m_bytes.group(1))
+    for name in names:
+        if not (name.startswith("ncu_") and name.endswith(".md")):
+            continue
+        text = open(os.path.join(pdir, name)).read()
+        m_wl = re.search(r"profile_workload:\s*(\S+)\s*$", text, re.M)
+        if not m_wl or m_wl.group(1) != workload:
+            continue
+        m_hash = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", text)
+        m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
+        if m_hash and m_bytes and m_hash.group(1) == kernel_source_hash():
+            return int(m_bytes.group(1))
+    return None
+
+
+def aggregate(world, bytes_per_step, rows_per_step, steps, ms_max):
+    """Whole-job throughput: the work of all ranks over the slowest rank's time."""
+    secs = ms_max / 1e3
+    return world * bytes_per_step * steps / secs / 1e9, world * rows_per_step * steps / secs
+
+
+def reduce_max(value, dist, device):
+    """Max over ranks of a float (identity without a process group)."""
+    if dist is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
 
 
 class ClockSampler:
@@ -414,13 +444,7 @@ def run_ours(args):
     wl = W.WORKLOADS[args.workload]
 
     if args.ncu_case:
-        L = Launcher(W.WORKLOADS[args.ncu_case], device, stream, 0)
-        with torch.cuda.stream(stream):
-            for i in range(args.launches):
-                L.launch(i)
-        stream.synchronize()
-        print(json.dumps({"ncu_case": args.ncu_case, "launches": args.launches,
-                          "plan": plan_summary(L.plan)}))
+        run_profile_case(args, device, stream)
         return
 
     L = Launcher(wl, device, stream, min_footprint)
@@ -433,22 +457,15 @@ def run_ours(args):
     if sampler:
         time.sleep(0.15)
         sampler.stop()
-    ms_t = torch.tensor([ms], dtype=torch.float64, device=device)
-    if dist is not None:
-        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
-    ms_max = float(ms_t.item())
+    ms_max = reduce_max(ms, dist, device)
     launch_bytes = wl.algorithmic_bytes()
     per_launch_s = ms / 1e3 / args.steps
     achieved = launch_bytes / per_launch_s / 1e9
-    value = world * launch_bytes * args.steps / (ms_max / 1e3) / 1e9
-    rows_per_s = world * wl.rows * args.steps / (ms_max / 1e3)
+    value, rows_per_s = aggregate(world, launch_bytes, wl.rows, args.steps, ms_max)
 
     e2e_steps = args.e2e_steps or max(64, min(args.steps, 4096))
     e_ms, h2d, d2h = time_e2e(L, e2e_steps)
-    e_t = torch.tensor([e_ms], dtype=torch.float64, device=device)
-    if dist is not None:
-        dist.all_reduce(e_t, op=dist.ReduceOp.MAX)
-    e2e_value = world * launch_bytes * e2e_steps / (float(e_t.item()) / 1e3) / 1e9
+    e2e_value, _ = aggregate(world, launch_bytes, wl.rows, e2e_steps, reduce_max(e_ms, dist, device))
 
     per_config = []
     if not args.no_per_config:
@@ -530,6 +547,42 @@ def run_ours(args):
     print(json.dumps(out))
     if dist is not None:
         dist.destroy_process_group()
+
+
+def run_profile_case(args, device, stream):
+    """A few launches of one workload, for ncu (no timing)."""
+    import dataclasses
+    import torch
+    from row_reduction_norm_gb300 import _native as N
+    from row_reduction_norm_gb300 import api, workloads as W
+    wl = W.WORKLOADS[args.ncu_case]
+    if args.rows or args.hidden:
+        wl = dataclasses.replace(wl, rows=args.rows or wl.rows, hidden=args.hidden or wl.hidden)
+    x, r, w = W.make_inputs(wl, seed=0, device=device)
+    off = 1 if args.misalign else 0
+
+    def shifted(t):
+        if t is None or not off:
+            return t
+        buf = torch.empty(t.numel() + off, dtype=t.dtype, device=t.device)
+        v = buf[off:].view(t.shape)
+        v.copy_(t)
+        return v
+
+    x, r, w = shifted(x), shifted(r), shifted(w)
+    y = shifted(torch.empty_like(x))
+    h = None if r is None else shifted(torch.empty_like(x))
+    plan = api.plan_for(x, w=w, residual=r, out=y, residual_out=h)
+    if args.grid:
+        plan.grid = args.grid
+        plan.persistent = 1
+    with torch.cuda.stream(stream):
+        for _ in range(args.launches):
+            api.rms_norm(x, w=w, residual=r, eps=wl.eps, out=y, residual_out=h, stream=stream, plan=plan)
+    stream.synchronize()
+    print(json.dumps({"ncu_case": wl.name, "rows": wl.rows, "hidden": wl.hidden,
+                      "launches": args.launches, "bytes_per_launch": wl.algorithmic_bytes(),
+                      "plan": plan_summary(plan)}))
 
 
 def L_sets(args, wl, min_footprint):

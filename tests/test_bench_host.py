@@ -1,0 +1,96 @@
+"""Host-side logic of bench.py on CPU: aggregation over ranks (world size 2
+over gloo), clock-record parsing, and the reference arm's JSON line."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    ms = [12.5, 20.0][rank]
+    m = bench.reduce_max(ms, dist, "cpu")
+    value, rows = bench.aggregate(world, 1000, 10, 4, m)
+    q.put((rank, m, value, rows))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_gloo_world2():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    got = sorted(q.get(timeout=10) for _ in range(2))
+    for rank, m, value, rows in got:
+        assert m == 20.0                                   # slowest rank's time
+        assert value == pytest.approx(2 * 1000 * 4 / 0.020 / 1e9)
+        assert rows == pytest.approx(2 * 10 * 4 / 0.020)
+
+
+def test_aggregate_single_rank():
+    v, r = bench.aggregate(1, 9438336, 4096, 1000, 3.0)
+    assert v == pytest.approx(9438336 * 1000 / 3e-3 / 1e9)
+    assert r == pytest.approx(4096 * 1000 / 3e-3)
+    assert bench.reduce_max(3.5, None, "cpu") == 3.5
+
+
+def test_clock_summary_flags_slowdown():
+    s = bench.ClockSampler(None)
+    s.samples = [(1.0, ["2070", "2070", "500", "0x0", "Not Active", "Not Active", "Not Active", "Not Active"]),
+                 (2.0, ["1900", "2070", "900", "0x4", "Not Active", "Not Active", "Not Active", "Active"]),
+                 (3.0, ["2000", "2070", "800", "0x0", "Active", "Not Active", "Not Active", "Not Active"]),
+                 (9.0, ["300", "2070", "90", "0x0", "Not Active", "Not Active", "Not Active", "Not Active"])]
+    c = s.summary(0.5, 3.5)
+    assert c["samples"] == 3 and c["sm_mhz"] == 2000 and c["sm_max_mhz"] == 2070
+    assert c["reasons"] == ["hw_slowdown", "sw_power_cap"]
+    c2 = s.summary(100.0, 101.0)   # nothing in the window: falls back to the whole run
+    assert c2["samples"] == 4
+
+
+def test_reference_arm_json_line():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "5", "--warmup", "3"], capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+              "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert k in line, k
+    assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["value"] > 0
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+    assert line["config"]["workload"] == "bf16_4096x576"
+
+
+def test_reference_arm_other_ranks_exit_quietly():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "5", "--warmup", "3"], capture_output=True, text=True, timeout=300, env=env)
+    assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_warmup_floor():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "5", "--warmup", "2"], capture_output=True, text=True, timeout=120)
+    assert r.returncode != 0
