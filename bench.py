@@ -259,6 +259,12 @@ class Launcher:
         self.N.rmsnorm_fwd(x, r, self.w_ptr, y, h, self.wl.rows, self.wl.hidden, self.wl.eps, self.code,
                            self.stream.cuda_stream)
 
+    def launch_with(self, i, slot, w_ptr):
+        """Launch on buffer set `slot` with the given weight pointer."""
+        x, r, y, h = self.ptrs[slot]
+        self.N.rmsnorm_fwd(x, r, w_ptr, y, h, self.wl.rows, self.wl.hidden, self.wl.eps, self.code,
+                           self.stream.cuda_stream)
+
     def graph(self, start, count):
         import torch
         g = torch.cuda.CUDAGraph()
@@ -306,10 +312,14 @@ def time_launches(L, steps, warmup, barrier=None, sampler_window=None, graph_len
     return ev0.elapsed_time(ev1)
 
 
-def time_e2e(L, steps):
-    """Per step: pinned host -> device copies of the inputs, the launch, and the
-    device -> pinned host read of the outputs, all in one stream; returns
-    (ms, h2d bytes per step, d2h bytes per step)."""
+def time_e2e(L, steps, pipelined=True):
+    """End-to-end steps through the public call: every step copies its inputs
+    (x, residual, w) from pinned host memory to the device, launches, and reads
+    y (and residual_out) back into pinned host memory.  Pipelined: uploads,
+    launches and read-backs run on three streams with per-buffer events, so
+    step i's read-back overlaps step i+1's upload and launch (device buffer
+    slots are reused only after their previous read-back finished).  Returns
+    (ms for `steps` steps, h2d bytes per step, d2h bytes per step)."""
     import torch
     x, r, y, h = L.sets[0]
     hx = x.cpu().pin_memory()
@@ -320,50 +330,108 @@ def time_e2e(L, steps):
     h2d = hx.numel() * hx.element_size() + (0 if hr is None else hr.numel() * hr.element_size()) + \
         (0 if hw is None else hw.numel() * hw.element_size())
     d2h = hy.numel() * hy.element_size() + (0 if hh is None else hh.numel() * hh.element_size())
+    nbuf = min(L.n_sets, 4) if pipelined else 1
+    s_k = L.stream
+    s_up = torch.cuda.Stream(s_k.device) if nbuf > 1 else s_k
+    s_dn = torch.cuda.Stream(s_k.device) if nbuf > 1 else s_k
+    # one device weight copy per slot, so an upload never races a running launch
+    w_slots = [None if L.w is None else torch.empty_like(L.w) for _ in range(nbuf)]
 
-    def one(i):
-        xd, rd, yd, hd = L.sets[i % L.n_sets]
-        xd.copy_(hx, non_blocking=True)
-        if rd is not None:
-            rd.copy_(hr, non_blocking=True)
-        if hw is not None:
-            L.w.copy_(hw, non_blocking=True)
-        L.launch(i)
-        hy.copy_(yd, non_blocking=True)
-        if hh is not None:
-            hh.copy_(hd, non_blocking=True)
+    def step(i, ev):
+        slot = i % nbuf
+        xd, rd, yd, hd = L.sets[slot]
+        wd = w_slots[slot]
+        up, kd, dn = ev[i]
+        with torch.cuda.stream(s_up):
+            if i >= nbuf:
+                s_up.wait_event(ev[i - nbuf][1])    # the launch that read this slot is done
+            xd.copy_(hx, non_blocking=True)
+            if rd is not None:
+                rd.copy_(hr, non_blocking=True)
+            if wd is not None:
+                wd.copy_(hw, non_blocking=True)
+            up.record(s_up)
+        with torch.cuda.stream(s_k):
+            s_k.wait_event(up)
+            if i >= nbuf:
+                s_k.wait_event(ev[i - nbuf][2])     # the read-back of this slot is done
+            L.launch_with(i, slot, None if wd is None else wd.data_ptr())
+            kd.record(s_k)
+        with torch.cuda.stream(s_dn):
+            s_dn.wait_event(kd)
+            hy.copy_(yd, non_blocking=True)
+            if hh is not None:
+                hh.copy_(hd, non_blocking=True)
+            dn.record(s_dn)
 
-    with torch.cuda.stream(L.stream):
-        for i in range(3):
-            one(i)
-    L.stream.synchronize()
+    def capture(count):
+        ev = [(torch.cuda.Event(), torch.cuda.Event(), torch.cuda.Event()) for _ in range(count)]
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s_k):
+            s_up.wait_stream(s_k)
+            s_dn.wait_stream(s_k)
+            for i in range(count):
+                step(i, ev)
+            s_k.wait_stream(s_up)
+            s_k.wait_stream(s_dn)
+        return g
+
+    # eager warm-up of the three-stream schedule, then capture
+    ev = [(torch.cuda.Event(), torch.cuda.Event(), torch.cuda.Event()) for _ in range(3)]
+    s_up.wait_stream(s_k)
+    s_dn.wait_stream(s_k)
+    for i in range(3):
+        step(i, ev)
+    s_k.wait_stream(s_up)
+    s_k.wait_stream(s_dn)
+    torch.cuda.synchronize()
     G = max(1, min(steps, 64))
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=L.stream):
-        for i in range(G):
-            one(i)
+    g = capture(G)
     rem = steps % G
-    g2 = None
-    if rem:
-        g2 = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g2, stream=L.stream):
-            for i in range(rem):
-                one(i)
-    with torch.cuda.stream(L.stream):
+    g2 = capture(rem) if rem else None
+    with torch.cuda.stream(s_k):
         g.replay()
-    L.stream.synchronize()
+    torch.cuda.synchronize()
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    with torch.cuda.stream(L.stream):
-        ev0.record(L.stream)
+    with torch.cuda.stream(s_k):
+        ev0.record(s_k)
         for _ in range(steps // G):
             g.replay()
         if g2 is not None:
             g2.replay()
-        ev1.record(L.stream)
-    L.stream.synchronize()
+        ev1.record(s_k)
+    torch.cuda.synchronize()
     return ev0.elapsed_time(ev1), h2d, d2h
+
+
+def copy_floor_us(L, steps=8192):
+    """Mean time of a plain device copy (torch ``copy_``, y <- x) moving the
+    same read + write bytes as one launch of the workload (no residual or
+    weight traffic), in the same setting: CUDA graphs of dependent launches
+    over the same rotating buffer sets.  It bounds what any kernel of this
+    size achieves launch after launch on this device."""
+    import torch
+    G = max(1, min(steps, 1024))
+    G = max(1, (G // L.n_sets) * L.n_sets) if G >= L.n_sets else G
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=L.stream):
+        for i in range(G):
+            x, _, y, _ = L.sets[i % L.n_sets]
+            y.copy_(x)
+    with torch.cuda.stream(L.stream):
+        g.replay()
+    L.stream.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    reps = max(1, steps // G)
+    with torch.cuda.stream(L.stream):
+        e0.record(L.stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(L.stream)
+    L.stream.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / (reps * G)
 
 
 def single_launch_latency_us(L, reps=200):
@@ -466,7 +534,10 @@ def run_ours(args):
     e2e_steps = args.e2e_steps or max(64, min(args.steps, 4096))
     e_ms, h2d, d2h = time_e2e(L, e2e_steps)
     e2e_value, _ = aggregate(world, launch_bytes, wl.rows, e2e_steps, reduce_max(e_ms, dist, device))
+    s_ms, _, _ = time_e2e(L, e2e_steps, pipelined=False)
+    e2e_serial, _ = aggregate(world, launch_bytes, wl.rows, e2e_steps, reduce_max(s_ms, dist, device))
 
+    floor_us = copy_floor_us(L)
     per_config = []
     if not args.no_per_config:
         del L
@@ -537,8 +608,14 @@ def run_ours(args):
                      "algorithmic_bytes_per_launch": launch_bytes},
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                "what": "pinned host -> device inputs (x, w), C-ABI launch, device -> pinned host y, "
-                        "every step"},
+                "serial_value": round(e2e_serial, 2),
+                "what": "every step: pinned host -> device copy of its inputs (x, w), the C-ABI launch, "
+                        "device -> pinned host copy of y; uploads, launches and read-backs pipelined on "
+                        "three streams over 4 device buffer slots (serial_value: one stream, no overlap)"},
+        "launch_floor": {"copy_us": round(floor_us, 3), "kernel_us": round(per_launch_s * 1e6, 3),
+                         "kernel_vs_copy": round(floor_us / (per_launch_s * 1e6), 3),
+                         "what": "torch copy_ of the same x -> y bytes, same graphs and buffer rotation: "
+                                 "the per-launch floor of a dependent chain of this size"},
         "gpu_launches": args.steps,
         "clocks": clocks,
         "cpu_baseline": cpu,
