@@ -274,6 +274,43 @@ class Launcher:
         return g
 
 
+class QKLauncher(Launcher):
+    """Buffer sets of a fused Q+K workload, normalised in place (the usual use on
+    a packed projection), with the same launch interface as Launcher."""
+
+    def __init__(self, wl, device, stream, min_footprint, seed=0):  # noqa: super().__init__ not used
+        import torch
+        from row_reduction_norm_gb300 import _native as N
+        from row_reduction_norm_gb300 import api, workloads as W
+        self.N = N
+        self.wl = wl
+        self.stream = stream
+        per_set = wl.tokens * wl.width * wl.elem_bytes
+        self.n_sets = max(1, math.ceil(min_footprint / max(per_set, 1)))
+        self.sets = []
+        qw = kw = None
+        for s in range(self.n_sets):
+            qkv, q_w, k_w = W.make_qk_inputs(wl, seed=seed + 16 * s, device=device)
+            if qw is None:
+                qw, kw = q_w, k_w
+            self.sets.append((qkv, None, qkv, None))
+        self.w, self.k_w = qw, kw
+        self.code = api.dtype_code(self.sets[0][0].dtype)
+        self.ptrs = [(x.data_ptr(), None, x.data_ptr(), None) for x, _, _, _ in self.sets]
+        self.w_ptr = None if qw is None else qw.data_ptr()
+        self.kw_ptr = None if kw is None else kw.data_ptr()
+        self.footprint = per_set * self.n_sets
+        self.plan = api.qk_plan_for(self.sets[0][0], wl.q_heads, wl.k_heads, wl.head_dim, qw, kw)
+        self.stride = self.sets[0][0].stride(0)
+
+    def launch(self, i):
+        x, _, y, _ = self.ptrs[i % self.n_sets]
+        wl = self.wl
+        self.N.rmsnorm_qk_fwd(x, y, wl.tokens, self.stride, self.stride, wl.q_heads, wl.k_heads, wl.head_dim,
+                              self.w_ptr, self.kw_ptr, wl.weight_bias, wl.eps, self.code, None,
+                              self.stream.cuda_stream)
+
+
 def time_launches(L, steps, warmup, barrier=None, sampler_window=None, graph_len=1024):
     """Exactly `steps` launches between two events on L.stream; returns ms."""
     import torch
@@ -542,22 +579,29 @@ def run_ours(args):
     if not args.no_per_config:
         del L
         torch.cuda.empty_cache()
-        for name in PER_CONFIG:
-            cw = W.WORKLOADS[name]
-            CL = Launcher(cw, device, stream, min_footprint)
+        for name in PER_CONFIG + list(W.QK_WORKLOADS):
+            qk = name in W.QK_WORKLOADS
+            cw = W.QK_WORKLOADS[name] if qk else W.WORKLOADS[name]
+            CL = (QKLauncher if qk else Launcher)(cw, device, stream, min_footprint)
             # calibrate: about 0.3 s of launches
             cal = time_launches(CL, 64, 8)
             k = int(max(64, min(200000, 0.3 / max(cal / 1e3 / 64, 1e-9))))
             cms = time_launches(CL, k, max(3, k // 20), barrier=barrier)
             t_launch = cms / 1e3 / k
             b = cw.algorithmic_bytes()
-            entry = {"workload": name, "rows": cw.rows, "hidden": cw.hidden, "dtype": cw.dtype,
-                     "residual": cw.has_res, "weight": cw.has_w, "bytes_per_launch": b,
-                     "us_per_launch": round(t_launch * 1e6, 3),
+            rows = cw.tokens * (cw.q_heads + cw.k_heads) if qk else cw.rows
+            entry = {"workload": name, "rows": rows, "hidden": cw.head_dim if qk else cw.hidden,
+                     "dtype": cw.dtype, "bytes_per_launch": b, "us_per_launch": round(t_launch * 1e6, 3),
                      "gbs": round(b / t_launch / 1e9, 1), "frac_of_peak": round(b / t_launch / 1e9 / peak, 4),
-                     "rows_per_s": round(cw.rows / t_launch, 1), "steps": k,
+                     "rows_per_s": round(rows / t_launch, 1), "steps": k,
                      "buffer_sets": CL.n_sets, "plan": plan_summary(CL.plan)}
-            if cw.rows <= 64:
+            if qk:
+                entry.update({"op": "fused q+k head norm, in place", "tokens": cw.tokens,
+                              "q_heads": cw.q_heads, "k_heads": cw.k_heads, "v_heads": cw.v_heads,
+                              "weight_bias": cw.weight_bias})
+            else:
+                entry.update({"residual": cw.has_res, "weight": cw.has_w})
+            if rows <= 64 or (qk and cw.tokens <= 64):
                 entry["single_launch_latency_us"] = round(single_launch_latency_us(CL), 2)
             per_config.append(entry)
             del CL

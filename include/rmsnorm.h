@@ -94,7 +94,8 @@ enum {
 typedef struct {
     int32_t kernel;             /* RMSNORM_KERNEL_*                                   */
     int32_t regime;             /* RMSNORM_REGIME_*                                   */
-    int32_t threads_per_row;    /* REG: 4..512 (power of two); LOOP: block_threads   */
+    int32_t threads_per_row;    /* REG: 4..512 (4..32 for head rows), power of two;
+                                   LOOP: block_threads                                */
     int32_t chunks_per_thread;  /* REG: upper bound of vector chunks per thread; LOOP:
                                    0                                                  */
     int32_t vec_elems;          /* elements per load: 16 / sizeof(T), or 1 (scalar)  */
@@ -154,6 +155,57 @@ int rmsnorm_plan_for(const void *x, const void *residual, const void *w, const v
 int rmsnorm_fwd_plan(const void *x, const void *residual, const void *w, void *y,
                      void *residual_out, int64_t rows, int64_t hidden, float eps,
                      int dtype, const rmsnorm_plan_t *plan, rmsnorm_stream_t stream);
+
+/*
+ * rmsnorm_fwd with a weight bias and an optional plan:
+ *   y_i = RN_T( h_i * rsqrt(mean(h^2) + eps) * (w_i + weight_bias) )
+ * The constant added to every weight element is the "weight bias" knob of
+ * "CuTeDSL at Perplexity" (configuration-space section; WEIGHT_BIAS in
+ * section "QK Norm"), read as an offset of the weight: weight_bias = 1 gives
+ * the (1 + w) form.  weight_bias = 0 is exactly rmsnorm_fwd.  A non-zero
+ * weight_bias requires w; it must be finite.  plan may be NULL (the library's
+ * plan) or a plan as for rmsnorm_fwd_plan.  Other arguments, layout and
+ * status codes as rmsnorm_fwd.
+ */
+int rmsnorm_fwd_ex(const void *x, const void *residual, const void *w, void *y,
+                   void *residual_out, int64_t rows, int64_t hidden, float eps,
+                   float weight_bias, int dtype, const rmsnorm_plan_t *plan,
+                   rmsnorm_stream_t stream);
+
+/*
+ * Fused query + key per-head RMSNorm in one launch ("CuTeDSL at Perplexity",
+ * section "QK Norm": per-head norm over 64..256 elements, the kernel picks
+ * the query or key weight per head; the model-as-a-kernel card lists the
+ * Qwen3-style qk RMSNorm).  Every head is one row of head_dim elements,
+ * normalised on its own with the op of rmsnorm_fwd_ex (no residual).
+ *
+ * Layout (element offsets; token rows of a packed projection such as
+ * [tokens, (q_heads + k_heads + v_heads) * head_dim]):
+ *   query head j of token t:  t * x_token_stride + j * head_dim
+ *   key head j of token t:    t * x_token_stride + (q_heads + j) * head_dim
+ * y uses the same layout with y_token_stride.  Elements of a token row past
+ * (q_heads + k_heads) * head_dim (the value heads) are neither read nor
+ * written.  y == x (same stride) normalises in place.
+ *   q_w, k_w    [head_dim] weights of the query and key heads: both or neither
+ *   weight_bias as rmsnorm_fwd_ex (requires weights when non-zero)
+ *   tokens >= 0 (0: no-op); q_heads, k_heads >= 0 with q_heads + k_heads >= 1;
+ *   1 <= head_dim <= rmsnorm_max_hidden(dtype);
+ *   x_token_stride, y_token_stride >= (q_heads + k_heads) * head_dim
+ *   plan        NULL (the library's plan) or a caller plan (validated)
+ * Returns RMSNORM_OK or a negative status (RMSNORM_EINVAL also for strides
+ * shorter than the heads, or y == x with different strides).
+ */
+int rmsnorm_qk_fwd(const void *x, void *y, int64_t tokens, int64_t x_token_stride,
+                   int64_t y_token_stride, int32_t q_heads, int32_t k_heads,
+                   int64_t head_dim, const void *q_w, const void *k_w, float weight_bias,
+                   float eps, int dtype, const rmsnorm_plan_t *plan,
+                   rmsnorm_stream_t stream);
+
+/* The plan rmsnorm_qk_fwd would use for these arguments on the current device. */
+int rmsnorm_qk_plan_for(const void *x, const void *y, int64_t tokens, int64_t x_token_stride,
+                        int64_t y_token_stride, int32_t q_heads, int32_t k_heads,
+                        int64_t head_dim, const void *q_w, const void *k_w, int dtype,
+                        rmsnorm_plan_t *plan);
 
 /* Largest supported hidden size for a dtype (0 for an unknown dtype). */
 int64_t rmsnorm_max_hidden(int dtype);

@@ -62,7 +62,7 @@ def _load():
             lib = ctypes.CDLL(build())
             vp, i64 = ctypes.c_void_p, ctypes.c_int64
             lib.oracle_rmsnorm_rows.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64,
-                                                ctypes.c_float, ctypes.c_int]
+                                                ctypes.c_float, ctypes.c_float, ctypes.c_int]
             lib.oracle_rmsnorm_rows.restype = ctypes.c_int
             lib.oracle_bf16_from_double.argtypes = [vp, vp, i64]
             lib.oracle_bf16_from_double.restype = None
@@ -88,12 +88,13 @@ def _check(a, name, dtype, shape):
 
 
 def rmsnorm(x, w=None, residual=None, eps: float = 1e-6, dtype: str = "bf16",
-            want_exact: bool = False, threads: int = 1):
+            want_exact: bool = False, threads: int = 1, weight_bias: float = 0.0):
     """Reference RMSNorm of every row of ``x`` ([rows, hidden]).
 
     Returns ``(y, residual_out, y_exact)``: ``y`` in the I/O type,
     ``residual_out`` (= the rounded ``x + residual``) or None, and the fp64
     value of ``y`` before its final rounding, or None unless ``want_exact``.
+    ``weight_bias`` is added to every weight element (float value).
     """
     if dtype not in DTYPES:
         raise ValueError(f"unknown dtype {dtype!r}")
@@ -115,7 +116,7 @@ def rmsnorm(x, w=None, residual=None, eps: float = 1e-6, dtype: str = "bf16",
     args = (_ptr(x), _ptr(residual), _ptr(w), _ptr(y), _ptr(y64), _ptr(res_out))
 
     def run(lo, hi):
-        rc = lib.oracle_rmsnorm_rows(*args, lo, hi, hidden, float(eps), DTYPES[dtype])
+        rc = lib.oracle_rmsnorm_rows(*args, lo, hi, hidden, float(eps), float(weight_bias), DTYPES[dtype])
         if rc != 0:
             raise ValueError("oracle rejected its arguments")
 
@@ -127,6 +128,29 @@ def rmsnorm(x, w=None, residual=None, eps: float = 1e-6, dtype: str = "bf16",
         with ThreadPoolExecutor(max_workers=threads) as ex:
             list(ex.map(lambda i: run(int(bounds[i]), int(bounds[i + 1])), range(threads)))
     return y, res_out, y64
+
+
+def rmsnorm_qk(x, q_heads: int, k_heads: int, head_dim: int, q_w=None, k_w=None, eps: float = 1e-6,
+               dtype: str = "bf16", weight_bias: float = 0.0, threads: int = 1):
+    """Reference per-head RMSNorm of the query and key heads of packed token rows.
+
+    ``x`` is [tokens, stride] with stride >= (q_heads + k_heads) * head_dim:
+    query head j of a token occupies columns [j*head_dim, (j+1)*head_dim),
+    key head j the columns after the query heads.  Each head is one row of
+    the op above, with ``q_w`` for query heads and ``k_w`` for key heads
+    ("CuTeDSL at Perplexity", section "QK Norm").  Returns ``(q_y, k_y)`` of
+    shapes [tokens, q_heads, head_dim] and [tokens, k_heads, head_dim]; the
+    columns past the key heads are not part of the op.
+    """
+    x = np.ascontiguousarray(x)
+    tokens = x.shape[0]
+    q_cols = q_heads * head_dim
+    k_cols = k_heads * head_dim
+    q_rows = x[:, :q_cols].reshape(tokens * q_heads, head_dim)
+    k_rows = x[:, q_cols:q_cols + k_cols].reshape(tokens * k_heads, head_dim)
+    qy = rmsnorm(q_rows, w=q_w, eps=eps, dtype=dtype, threads=threads, weight_bias=weight_bias)[0]
+    ky = rmsnorm(k_rows, w=k_w, eps=eps, dtype=dtype, threads=threads, weight_bias=weight_bias)[0]
+    return qy.reshape(tokens, q_heads, head_dim), ky.reshape(tokens, k_heads, head_dim)
 
 
 def bf16_from_double(v) -> np.ndarray:

@@ -15,6 +15,7 @@
  *   S     = sum_i h_i^2                        (fp64, index order)
  *   r     = 1 / sqrt(S / hidden + eps)
  *   y_i   = RN_T(h_i * r * w_i)                (w_i dropped with no weight)
+ *   y_i   = RN_T(h_i * r * (w_i + b))          (weight bias b, when non-zero)
  *
  * Sources:
  *  - "Building a GPU compiler from scratch: from PyTorch to CUDA via
@@ -28,6 +29,9 @@
  *    not described on the pages; the reading taken is: h is the sum rounded
  *    once to the I/O type, and the norm is taken of that rounded h.
  *  - eps arrives as a float; its exact float value is used.
+ *  - The weight bias is the "weight bias" knob of "CuTeDSL at Perplexity"
+ *    (configuration-space section, WEIGHT_BIAS in section "QK Norm"), read as
+ *    a constant added to every weight element (1 gives the (1 + w) form).
  *
  * Arithmetic: every step in IEEE binary64 with round-to-nearest-even, no
  * fused multiply-add (built with -ffp-contract=off) and no fast-math.  The
@@ -120,12 +124,14 @@ static double row_input(const void *x, const void *residual, int64_t i, int dtyp
  *   y              : output in the I/O type
  *   y_exact        : optional fp64 copy of y before the final rounding
  *   residual_out   : h in the I/O type; required iff residual is given
+ *   weight_bias    : added to every weight element (0: the weight itself);
+ *                    must be 0 without a weight
  * Returns 0, or -1 on an invalid argument.
  */
 int oracle_rmsnorm_rows(const void *x, const void *residual, const void *w,
                         void *y, double *y_exact, void *residual_out,
                         int64_t row_begin, int64_t row_end, int64_t hidden,
-                        float eps, int dtype)
+                        float eps, float weight_bias, int dtype)
 {
     if (x == NULL || y == NULL || hidden <= 0 || row_begin < 0 || row_end < row_begin)
         return -1;
@@ -133,8 +139,11 @@ int oracle_rmsnorm_rows(const void *x, const void *residual, const void *w,
         return -1;
     if ((residual == NULL) != (residual_out == NULL))
         return -1;
+    if (w == NULL && weight_bias != 0.0f)
+        return -1;
 
     const double e = (double)eps;
+    const double b = (double)weight_bias;
     for (int64_t row = row_begin; row < row_end; ++row) {
         const int64_t base = row * hidden;
 
@@ -153,7 +162,7 @@ int oracle_rmsnorm_rows(const void *x, const void *residual, const void *w,
             double h = row_input(x, residual, base + i, dtype);
             double v = h * inv_rms;
             if (w != NULL)
-                v = v * load_elem(w, i, dtype);
+                v = v * (load_elem(w, i, dtype) + b);
             if (y_exact != NULL)
                 y_exact[base + i] = v;
             store_elem(y, base + i, dtype, v);

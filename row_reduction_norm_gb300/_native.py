@@ -35,9 +35,9 @@ REGIME_NAMES = {0: "warp", 1: "cta", 2: "persistent", 3: "looped"}
 KERNEL_NAMES = {0: "reg", 1: "loop"}
 
 # Every symbol the header declares (checked by the CPU tests).
-EXPORTED = ["rmsnorm_fwd", "rmsnorm_plan", "rmsnorm_plan_for", "rmsnorm_fwd_plan",
-            "rmsnorm_max_hidden", "rmsnorm_reg_max_chunks", "rmsnorm_strerror",
-            "rmsnorm_build_info"]
+EXPORTED = ["rmsnorm_fwd", "rmsnorm_plan", "rmsnorm_plan_for", "rmsnorm_fwd_plan", "rmsnorm_fwd_ex",
+            "rmsnorm_qk_fwd", "rmsnorm_qk_plan_for", "rmsnorm_max_hidden", "rmsnorm_reg_max_chunks",
+            "rmsnorm_strerror", "rmsnorm_build_info"]
 
 
 class RmsNormError(RuntimeError):
@@ -102,6 +102,15 @@ def load():
         lib.rmsnorm_fwd.restype = i32
         lib.rmsnorm_fwd_plan.argtypes = fwd_args + [ctypes.POINTER(Plan), vp]
         lib.rmsnorm_fwd_plan.restype = i32
+        lib.rmsnorm_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i64, i64, ctypes.c_float, ctypes.c_float, i32,
+                                       ctypes.POINTER(Plan), vp]
+        lib.rmsnorm_fwd_ex.restype = i32
+        lib.rmsnorm_qk_fwd.argtypes = [vp, vp, i64, i64, i64, ctypes.c_int32, ctypes.c_int32, i64, vp, vp,
+                                       ctypes.c_float, ctypes.c_float, i32, ctypes.POINTER(Plan), vp]
+        lib.rmsnorm_qk_fwd.restype = i32
+        lib.rmsnorm_qk_plan_for.argtypes = [vp, vp, i64, i64, i64, ctypes.c_int32, ctypes.c_int32, i64, vp, vp,
+                                            i32, ctypes.POINTER(Plan)]
+        lib.rmsnorm_qk_plan_for.restype = i32
         lib.rmsnorm_plan.argtypes = [i64, i64, i32, i32, i32, i32, ctypes.POINTER(Plan)]
         lib.rmsnorm_plan.restype = i32
         lib.rmsnorm_plan_for.argtypes = [vp, vp, vp, vp, vp, i64, i64, i32, ctypes.POINTER(Plan)]
@@ -141,6 +150,42 @@ def rmsnorm_fwd_plan(x, residual, w, y, residual_out, rows, hidden, eps, dtype, 
 def rmsnorm_fwd_plan_status(x, residual, w, y, residual_out, rows, hidden, eps, dtype, plan, stream=0):
     return load().rmsnorm_fwd_plan(x, residual, w, y, residual_out, rows, hidden, eps, dtype,
                                    ctypes.byref(plan) if plan is not None else None, stream)
+
+
+def _plan_ref(plan):
+    return None if plan is None else ctypes.byref(plan)
+
+
+def rmsnorm_fwd_ex(x, residual, w, y, residual_out, rows, hidden, eps, weight_bias, dtype, plan=None,
+                   stream=0):
+    _check(load().rmsnorm_fwd_ex(x, residual, w, y, residual_out, rows, hidden, eps, weight_bias, dtype,
+                                 _plan_ref(plan), stream), "rmsnorm_fwd_ex")
+
+
+def rmsnorm_fwd_ex_status(x, residual, w, y, residual_out, rows, hidden, eps, weight_bias, dtype, plan=None,
+                          stream=0) -> int:
+    return load().rmsnorm_fwd_ex(x, residual, w, y, residual_out, rows, hidden, eps, weight_bias, dtype,
+                                 _plan_ref(plan), stream)
+
+
+def rmsnorm_qk_fwd(x, y, tokens, x_token_stride, y_token_stride, q_heads, k_heads, head_dim, q_w, k_w,
+                   weight_bias, eps, dtype, plan=None, stream=0):
+    _check(rmsnorm_qk_fwd_status(x, y, tokens, x_token_stride, y_token_stride, q_heads, k_heads, head_dim,
+                                 q_w, k_w, weight_bias, eps, dtype, plan, stream), "rmsnorm_qk_fwd")
+
+
+def rmsnorm_qk_fwd_status(x, y, tokens, x_token_stride, y_token_stride, q_heads, k_heads, head_dim, q_w, k_w,
+                          weight_bias, eps, dtype, plan=None, stream=0) -> int:
+    return load().rmsnorm_qk_fwd(x, y, tokens, x_token_stride, y_token_stride, q_heads, k_heads, head_dim,
+                                 q_w, k_w, weight_bias, eps, dtype, _plan_ref(plan), stream)
+
+
+def rmsnorm_qk_plan_for(x, y, tokens, x_token_stride, y_token_stride, q_heads, k_heads, head_dim, q_w, k_w,
+                        dtype) -> Plan:
+    p = Plan()
+    _check(load().rmsnorm_qk_plan_for(x, y, tokens, x_token_stride, y_token_stride, q_heads, k_heads,
+                                      head_dim, q_w, k_w, dtype, ctypes.byref(p)), "rmsnorm_qk_plan_for")
+    return p
 
 
 def rmsnorm_plan(rows, hidden, dtype, vec_ok, sm_count, blocks_per_sm) -> Plan:

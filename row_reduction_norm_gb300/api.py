@@ -43,12 +43,13 @@ def _check_tensor(t, name, x):
 def rms_norm(x: torch.Tensor, w: Optional[torch.Tensor] = None, residual: Optional[torch.Tensor] = None,
              eps: float = 1e-6, out: Optional[torch.Tensor] = None,
              residual_out: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None,
-             plan: Optional[N.Plan] = None):
-    """y = x * rsqrt(mean(x^2) + eps) * w over the last dimension.
+             plan: Optional[N.Plan] = None, weight_bias: float = 0.0):
+    """y = x * rsqrt(mean(x^2) + eps) * (w + weight_bias) over the last dimension.
 
     With ``residual``: h = x + residual (rounded to the I/O type) is written to
     ``residual_out`` and normalised; returns ``(y, residual_out)``.  Without:
     returns ``y``.  ``plan`` forces a launch plan (see ``rmsnorm_fwd_plan``).
+    ``weight_bias`` = 1 gives the (1 + w) weight form.
     """
     if x.dim() < 1:
         raise ValueError("x must have at least one dimension")
@@ -69,12 +70,69 @@ def rms_norm(x: torch.Tensor, w: Optional[torch.Tensor] = None, residual: Option
     with torch.cuda.device(x.device):
         s = stream if stream is not None else torch.cuda.current_stream(x.device)
         args = (_ptr(x), _ptr(residual), _ptr(w), _ptr(y), _ptr(residual_out), rows, hidden,
-                float(eps), code)
-        if plan is None:
-            N.rmsnorm_fwd(*args, s.cuda_stream)
+                float(eps))
+        if weight_bias:
+            N.rmsnorm_fwd_ex(*args, float(weight_bias), code, plan, s.cuda_stream)
+        elif plan is None:
+            N.rmsnorm_fwd(*args, code, s.cuda_stream)
         else:
-            N.rmsnorm_fwd_plan(*args, plan, s.cuda_stream)
+            N.rmsnorm_fwd_plan(*args, code, plan, s.cuda_stream)
     return (y, residual_out) if residual is not None else y
+
+
+def _token_view(t: torch.Tensor, name: str):
+    """(tokens, token_stride) of a [tokens, width] tensor with a contiguous last dimension."""
+    if t.dim() != 2:
+        raise ValueError(f"{name} must be a 2-D [tokens, width] tensor")
+    if t.stride(1) != 1 and t.shape[1] > 1:
+        raise ValueError(f"{name}: the last dimension must be contiguous")
+    return t.shape[0], t.stride(0), t
+
+
+def qk_norm(qkv: torch.Tensor, q_heads: int, k_heads: int, head_dim: int, q_w: Optional[torch.Tensor] = None,
+            k_w: Optional[torch.Tensor] = None, eps: float = 1e-6, weight_bias: float = 0.0,
+            out: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None,
+            plan: Optional[N.Plan] = None) -> torch.Tensor:
+    """Per-head RMSNorm of the query and key heads of packed token rows in one launch.
+
+    ``qkv`` is [tokens, width] (last dimension contiguous, token rows evenly
+    strided, e.g. a view of a fused projection) holding q_heads query heads, then
+    k_heads key heads of head_dim elements, then anything else (value heads),
+    which is left alone.  Query heads take ``q_w``, key heads ``k_w``.  The
+    result goes to ``out`` (same layout; pass ``out=qkv`` to normalise in
+    place) or to a new tensor whose other columns are copied from ``qkv``.
+    """
+    _check_tensor(qkv, "qkv", qkv)
+    code = dtype_code(qkv.dtype)
+    tokens, xs, rows = _token_view(qkv, "qkv")
+    if out is None:
+        out = qkv.clone()
+    if out.shape != qkv.shape:
+        raise ValueError("out must have the shape of qkv")
+    _, ys, _ = _token_view(out, "out")
+    for name, t in (("q_w", q_w), ("k_w", k_w)):
+        if t is not None:
+            _check_tensor(t, name, qkv)
+            if tuple(t.shape) != (head_dim,):
+                raise ValueError(f"{name} must have shape ({head_dim},)")
+    if out.device != qkv.device or out.dtype != qkv.dtype:
+        raise ValueError("out must match qkv's device and dtype")
+    with torch.cuda.device(qkv.device):
+        s = stream if stream is not None else torch.cuda.current_stream(qkv.device)
+        N.rmsnorm_qk_fwd(_ptr(qkv), _ptr(out), tokens, xs, ys, int(q_heads), int(k_heads), int(head_dim),
+                         _ptr(q_w), _ptr(k_w), float(weight_bias), float(eps), code, plan, s.cuda_stream)
+    return out
+
+
+def qk_plan_for(qkv: torch.Tensor, q_heads: int, k_heads: int, head_dim: int, q_w=None, k_w=None,
+                out=None) -> N.Plan:
+    """The plan ``qk_norm`` would launch for these tensors."""
+    tokens, xs, _ = _token_view(qkv, "qkv")
+    y = qkv if out is None else out
+    _, ys, _ = _token_view(y, "out")
+    with torch.cuda.device(qkv.device):
+        return N.rmsnorm_qk_plan_for(_ptr(qkv), _ptr(y), tokens, xs, ys, int(q_heads), int(k_heads),
+                                     int(head_dim), _ptr(q_w), _ptr(k_w), dtype_code(qkv.dtype))
 
 
 def plan_for(x: torch.Tensor, w=None, residual=None, out=None, residual_out=None) -> N.Plan:

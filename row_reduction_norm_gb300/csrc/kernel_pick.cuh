@@ -1,0 +1,74 @@
+// kernel_pick.cuh -- maps runtime (threads per row, chunks, weight mode) to
+// compiled instantiations (internal; included by the instantiation files).
+#pragma once
+
+#include "rmsnorm_kernels.cuh"
+
+namespace rrn {
+namespace pick {
+
+template <typename T, int GT, int CH, bool RES, bool HEADS>
+const void *reg_wm(int wm) {
+    switch (wm) {
+        case kNoWeight: return reinterpret_cast<const void *>(&rms_reg_kernel<T, GT, CH, RES, kNoWeight, HEADS>);
+        case kWeight: return reinterpret_cast<const void *>(&rms_reg_kernel<T, GT, CH, RES, kWeight, HEADS>);
+        case kWeightBias: return reinterpret_cast<const void *>(&rms_reg_kernel<T, GT, CH, RES, kWeightBias, HEADS>);
+        default: return nullptr;
+    }
+}
+
+template <typename T, int GT, bool RES, bool HEADS>
+const void *reg_ch(int ch, int wm) {
+    switch (ch) {
+        case 1: return reg_wm<T, GT, 1, RES, HEADS>(wm);
+        case 2: return reg_wm<T, GT, 2, RES, HEADS>(wm);
+        case 4: return reg_wm<T, GT, 4, RES, HEADS>(wm);
+        case 8: return reg_wm<T, GT, 8, RES, HEADS>(wm);
+        default: return nullptr;
+    }
+}
+
+template <typename T, bool RES, bool HEADS, int MAXGT>
+const void *reg_gt(int gt, int ch, int wm) {
+    switch (gt) {
+        case 4: return reg_ch<T, 4, RES, HEADS>(ch, wm);
+        case 8: return reg_ch<T, 8, RES, HEADS>(ch, wm);
+        case 16: return reg_ch<T, 16, RES, HEADS>(ch, wm);
+        case 32: return reg_ch<T, 32, RES, HEADS>(ch, wm);
+        default: break;
+    }
+    if constexpr (MAXGT >= 512) {
+        switch (gt) {
+            case 64: return reg_ch<T, 64, RES, HEADS>(ch, wm);
+            case 128: return reg_ch<T, 128, RES, HEADS>(ch, wm);
+            case 256: return reg_ch<T, 256, RES, HEADS>(ch, wm);
+            case 512: return reg_ch<T, 512, RES, HEADS>(ch, wm);
+            default: break;
+        }
+    }
+    return nullptr;
+}
+
+template <typename T, int VE, int BLOCK, bool RES, bool HEADS>
+const void *loop_wm(int wm) {
+    switch (wm) {
+        case kNoWeight: return reinterpret_cast<const void *>(&rms_loop_kernel<T, VE, BLOCK, RES, kNoWeight, HEADS>);
+        case kWeight: return reinterpret_cast<const void *>(&rms_loop_kernel<T, VE, BLOCK, RES, kWeight, HEADS>);
+        case kWeightBias:
+            return reinterpret_cast<const void *>(&rms_loop_kernel<T, VE, BLOCK, RES, kWeightBias, HEADS>);
+        default: return nullptr;
+    }
+}
+
+template <typename T, bool RES, bool HEADS>
+const void *loop_block(int block, bool vec, int wm) {
+    switch (block) {
+        case 64: return vec ? loop_wm<T, T::kVec, 64, RES, HEADS>(wm) : loop_wm<T, 1, 64, RES, HEADS>(wm);
+        case 256: return vec ? loop_wm<T, T::kVec, 256, RES, HEADS>(wm) : loop_wm<T, 1, 256, RES, HEADS>(wm);
+        case 1024: return vec ? loop_wm<T, T::kVec, 1024, RES, HEADS>(wm) : loop_wm<T, 1, 1024, RES, HEADS>(wm);
+        default: return nullptr;
+    }
+}
+
+}  // namespace pick
+}  // namespace rrn

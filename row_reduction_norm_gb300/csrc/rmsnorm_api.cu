@@ -50,52 +50,56 @@ int64_t next_pow2(int64_t v) {
     return p;
 }
 
-bool aligned16(const void *p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned_to(const void *p, int a) {
     return p == nullptr || (reinterpret_cast<uintptr_t>(p) % (uintptr_t)a) == 0;
 }
 
-int check_args(const void *x, const void *residual, const void *y, const void *residual_out,
-               int64_t rows, int64_t hidden, float eps, int dtype) {
-    if (dtype != RMSNORM_F32 && dtype != RMSNORM_BF16) return RMSNORM_EINVAL;
-    if (rows < 0 || hidden <= 0) return RMSNORM_EINVAL;
-    if (!std::isfinite(eps) || eps < 0.f) return RMSNORM_EINVAL;
-    if (hidden > kMaxHidden) return RMSNORM_EUNSUPPORTED;
-    if (rows > INT64_MAX / (hidden * elem_size(dtype))) return RMSNORM_EINVAL;
-    if (rows == 0) return RMSNORM_OK;   // nothing is accessed: pointers may be NULL
-    if (x == nullptr || y == nullptr) return RMSNORM_EINVAL;
-    if ((residual == nullptr) != (residual_out == nullptr)) return RMSNORM_EINVAL;
-    return RMSNORM_OK;
+// Everything one launch needs, for contiguous rows and for head rows.
+struct Op {
+    const void *x = nullptr, *res = nullptr, *w = nullptr, *w2 = nullptr;
+    void *y = nullptr, *res_out = nullptr;
+    int64_t rows = 0;          // launch rows: rows, or tokens * heads
+    int64_t row_elems = 0;     // hidden or head_dim
+    int64_t x_stride = 0;      // elements between rows (tokens for head rows)
+    int64_t y_stride = 0;
+    int32_t heads = 1, q_heads = 1;
+    bool head_rows = false;
+    float eps = 0.f, w_bias = 0.f;
+    int wm = 0;                // rrn::WeightMode
+    int dtype = RMSNORM_BF16;
+};
+
+bool elem_aligned(const Op &o) {
+    const int a = elem_size(o.dtype);
+    return aligned_to(o.x, a) && aligned_to(o.res, a) && aligned_to(o.w, a) && aligned_to(o.w2, a) &&
+           aligned_to(o.y, a) && aligned_to(o.res_out, a);
 }
 
-// Element alignment is required on every path (a misaligned element access
-// would fault); 16-byte alignment selects the vector path.
-bool elem_aligned(const void *x, const void *r, const void *w, const void *y, const void *ro, int dtype) {
-    const int a = elem_size(dtype);
-    return aligned_to(x, a) && aligned_to(r, a) && aligned_to(w, a) && aligned_to(y, a) && aligned_to(ro, a);
-}
-
-int vec_ok_of(const void *x, const void *r, const void *w, const void *y, const void *ro,
-              int64_t hidden, int dtype) {
-    return aligned16(x) && aligned16(r) && aligned16(w) && aligned16(y) && aligned16(ro) &&
-           (hidden * elem_size(dtype)) % 16 == 0;
+// 16-byte units are possible when every pointer, the row size and the row
+// strides are multiples of 16 bytes.
+int vec_ok_of(const Op &o) {
+    const int s = elem_size(o.dtype);
+    return aligned_to(o.x, 16) && aligned_to(o.res, 16) && aligned_to(o.w, 16) && aligned_to(o.w2, 16) &&
+           aligned_to(o.y, 16) && aligned_to(o.res_out, 16) && (o.row_elems * s) % 16 == 0 &&
+           (o.x_stride * s) % 16 == 0 && (o.y_stride * s) % 16 == 0;
 }
 
 // The per-row schedule: everything but the grid.
-void schedule(int64_t hidden, int dtype, int vec_ok, rmsnorm_plan_t *p) {
+void schedule(int64_t hidden, int dtype, int vec_ok, bool head_rows, rmsnorm_plan_t *p) {
     std::memset(p, 0, sizeof(*p));
     const int V = vec_elems_of(dtype);
+    const int max_gt = head_rows ? rrn::kRegMaxGTHeads : rrn::kRegMaxGT;
     if (vec_ok) {
         const int64_t nch = hidden / V;
         // Aim at 4 chunks (64 bytes of each input) per thread with at least 4
         // lanes per row: measured on GB300, this keeps every row-group block
         // resident in one wave at the occupancy the registers allow and beats
-        // 8 chunks per thread.  Rows longer than 512 threads x 4 chunks take
-        // up to 8 chunks per thread.
+        // 8 chunks per thread.  Rows longer than max_gt threads x 4 chunks
+        // take up to 8 chunks per thread.
         int64_t gt = next_pow2(ceil_div(nch, kRegTargetCH));
         if (gt < 4) gt = 4;
-        if (gt > rrn::kRegMaxGT && ceil_div(nch, rrn::kRegMaxGT) <= rrn::kRegMaxCH) gt = rrn::kRegMaxGT;
-        if (gt <= rrn::kRegMaxGT) {
+        if (gt > max_gt && ceil_div(nch, max_gt) <= rrn::kRegMaxCH) gt = max_gt;
+        if (gt <= max_gt) {
             int64_t need = ceil_div(nch, gt);
             int ch = 1;
             while (ch < need) ch <<= 1;
@@ -137,33 +141,31 @@ void size_grid(int64_t rows, int sm_count, int blocks_per_sm, rmsnorm_plan_t *p)
     if (p->persistent && p->kernel == RMSNORM_KERNEL_REG) p->regime = RMSNORM_REGIME_PERSISTENT;
 }
 
-size_t dyn_smem_of(const rmsnorm_plan_t *p, int64_t hidden, int dtype, bool has_w) {
-    if (p->kernel != RMSNORM_KERNEL_REG || !has_w) return 0;
-    return (size_t)(hidden / vec_elems_of(dtype)) * 16;
+size_t dyn_smem_of(const rmsnorm_plan_t *p, const Op &o) {
+    if (p->kernel != RMSNORM_KERNEL_REG || o.wm == rrn::kNoWeight) return 0;
+    return (size_t)(o.row_elems / vec_elems_of(o.dtype)) * 16 * (o.head_rows ? 2 : 1);
 }
 
-const void *kernel_of(const rmsnorm_plan_t *p, int dtype, bool res, bool w) {
-    if (p->kernel == RMSNORM_KERNEL_REG) {
-        return dtype == RMSNORM_BF16 ? rrn::reg_kernel_bf16(p->threads_per_row, p->chunks_per_thread, res, w)
-                                     : rrn::reg_kernel_f32(p->threads_per_row, p->chunks_per_thread, res, w);
-    }
-    const bool vec = p->vec_elems != 1;
-    return dtype == RMSNORM_BF16 ? rrn::loop_kernel_bf16(p->block_threads, vec, res, w)
-                                 : rrn::loop_kernel_f32(p->block_threads, vec, res, w);
+const void *kernel_of(const rmsnorm_plan_t *p, const Op &o) {
+    const bool res = o.res != nullptr;
+    if (p->kernel == RMSNORM_KERNEL_REG)
+        return rrn::reg_kernel(o.dtype, p->threads_per_row, p->chunks_per_thread, res, o.wm, o.head_rows);
+    return rrn::loop_kernel(o.dtype, p->block_threads, p->vec_elems != 1, res, o.wm, o.head_rows);
 }
 
 // Checks a plan against the shape and pointers (caller-made plans included).
-int validate_plan(const rmsnorm_plan_t *p, int64_t rows, int64_t hidden, int dtype, int vec_ok) {
+int validate_plan(const rmsnorm_plan_t *p, const Op &o, int vec_ok) {
     if (p == nullptr) return RMSNORM_EINVAL;
-    const int V = vec_elems_of(dtype);
-    if (rows > 0 && (p->grid < 1 || p->grid > INT_MAX)) return RMSNORM_EINVAL;
+    const int V = vec_elems_of(o.dtype);
+    if (o.rows > 0 && (p->grid < 1 || p->grid > INT_MAX)) return RMSNORM_EINVAL;
     if (p->pdl != 0 && p->pdl != 1) return RMSNORM_EINVAL;
     if (p->kernel == RMSNORM_KERNEL_REG) {
         const int gt = p->threads_per_row, ch = p->chunks_per_thread;
+        const int max_gt = o.head_rows ? rrn::kRegMaxGTHeads : rrn::kRegMaxGT;
         if (!vec_ok || p->vec_elems != V) return RMSNORM_EINVAL;
-        if (gt < 4 || gt > rrn::kRegMaxGT || (gt & (gt - 1)) != 0) return RMSNORM_EINVAL;
+        if (gt < 4 || gt > max_gt || (gt & (gt - 1)) != 0) return RMSNORM_EINVAL;
         if (ch < 1 || ch > rrn::kRegMaxCH || (ch & (ch - 1)) != 0) return RMSNORM_EINVAL;
-        if ((int64_t)gt * ch * V < hidden) return RMSNORM_EINVAL;
+        if ((int64_t)gt * ch * V < o.row_elems) return RMSNORM_EINVAL;
         if (p->block_threads != rrn::reg_block_threads(gt)) return RMSNORM_EINVAL;
         if (p->rows_per_block != p->block_threads / gt) return RMSNORM_EINVAL;
         return RMSNORM_OK;
@@ -174,7 +176,7 @@ int validate_plan(const rmsnorm_plan_t *p, int64_t rows, int64_t hidden, int dty
         for (int b : rrn::kLoopBlocks) known = known || (b == p->block_threads);
         if (!known) return RMSNORM_EINVAL;
         if (p->rows_per_block != 1) return RMSNORM_EINVAL;
-        if (ceil_div(hidden / p->vec_elems, p->block_threads) * p->vec_elems > kLoopMaxTermsPerThread)
+        if (ceil_div(o.row_elems / p->vec_elems, p->block_threads) * p->vec_elems > kLoopMaxTermsPerThread)
             return RMSNORM_EINVAL;
         return RMSNORM_OK;
     }
@@ -192,7 +194,7 @@ struct OccEntry {
     size_t smem;
     int blocks;
 };
-constexpr int kOccSlots = 512;
+constexpr int kOccSlots = 1024;
 OccEntry g_occ[kOccSlots];
 int g_occ_used = 0;
 
@@ -251,40 +253,52 @@ int blocks_per_sm_of(int dev, const void *fn, int block, size_t smem, int *out) 
     return RMSNORM_OK;
 }
 
-// Full device-side planning for concrete pointers.
-int plan_for_device(const void *x, const void *residual, const void *w, const void *y,
-                    const void *residual_out, int64_t rows, int64_t hidden, int dtype,
-                    rmsnorm_plan_t *plan, int *dev_out) {
-    const int vec_ok = vec_ok_of(x, residual, w, y, residual_out, hidden, dtype);
-    schedule(hidden, dtype, vec_ok, plan);
+// Full device-side planning for an op.
+int plan_for_device(const Op &o, rmsnorm_plan_t *plan, int *dev_out) {
+    schedule(o.row_elems, o.dtype, vec_ok_of(o), o.head_rows, plan);
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return RMSNORM_ECUDA;
     int sms = 0;
     int st = sm_count_of(dev, &sms);
     if (st != RMSNORM_OK) return st;
-    const bool res = residual != nullptr, hw = w != nullptr;
-    const void *fn = kernel_of(plan, dtype, res, hw);
+    const void *fn = kernel_of(plan, o);
     if (fn == nullptr) return RMSNORM_EINVAL;
-    const size_t smem = dyn_smem_of(plan, hidden, dtype, hw);
+    const size_t smem = dyn_smem_of(plan, o);
     if (smem > 0 && (st = ensure_smem_attr(dev, fn)) != RMSNORM_OK) return st;
     int bps = 0;
     if ((st = blocks_per_sm_of(dev, fn, plan->block_threads, smem, &bps)) != RMSNORM_OK) return st;
-    size_grid(rows, sms, bps, plan);
+    size_grid(o.rows, sms, bps, plan);
     if (dev_out) *dev_out = dev;
     return RMSNORM_OK;
 }
 
-int launch(const rrn::Params &prm, const rmsnorm_plan_t *plan, int dtype, int dev,
-           rmsnorm_stream_t stream) {
-    const bool res = prm.res != nullptr, hw = prm.w != nullptr;
-    const void *fn = kernel_of(plan, dtype, res, hw);
+int launch(const Op &o, const rmsnorm_plan_t *plan, int dev, rmsnorm_stream_t stream) {
+    const void *fn = kernel_of(plan, o);
     if (fn == nullptr) return RMSNORM_EINVAL;
-    const size_t smem = dyn_smem_of(plan, prm.row_elems, dtype, hw);
+    const size_t smem = dyn_smem_of(plan, o);
     if (smem > 0) {
         int st = ensure_smem_attr(dev, fn);
         if (st != RMSNORM_OK) return st;
     }
-    rrn::Params args = prm;
+    const int64_t s = elem_size(o.dtype);
+    rrn::Params args;
+    args.x = o.x;
+    args.res = o.res;
+    args.w = o.w;
+    args.w2 = o.w2;
+    args.y = o.y;
+    args.res_out = o.res_out;
+    args.rows = o.rows;
+    args.row_elems = o.row_elems;
+    args.row_bytes = o.row_elems * s;
+    args.x_stride = o.x_stride * s;
+    args.y_stride = o.y_stride * s;
+    args.units = (int32_t)(o.row_elems / plan->vec_elems);
+    args.heads = o.heads;
+    args.q_heads = o.q_heads;
+    args.hidden_f = (float)o.row_elems;
+    args.eps = o.eps;
+    args.w_bias = o.w_bias;
     void *argv[] = {&args};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -304,20 +318,94 @@ int launch(const rrn::Params &prm, const rmsnorm_plan_t *plan, int dtype, int de
     return RMSNORM_OK;
 }
 
-rrn::Params make_params(const void *x, const void *residual, const void *w, void *y, void *residual_out,
-                        int64_t rows, int64_t hidden, float eps, int vec_elems) {
-    rrn::Params prm;
-    prm.x = x;
-    prm.res = residual;
-    prm.w = w;
-    prm.y = y;
-    prm.res_out = residual_out;
-    prm.rows = rows;
-    prm.row_elems = hidden;
-    prm.units = (int32_t)(hidden / vec_elems);
-    prm.hidden_f = (float)hidden;
-    prm.eps = eps;
-    return prm;
+// Plan (if none is given), validate and launch.
+int run(const Op &o, const rmsnorm_plan_t *user_plan, rmsnorm_stream_t stream) {
+    if (!elem_aligned(o)) return RMSNORM_EINVAL;
+    const int vec_ok = vec_ok_of(o);
+    if (user_plan != nullptr) {
+        int st = validate_plan(user_plan, o, vec_ok);
+        if (st != RMSNORM_OK) return st;
+    }
+    if (o.rows == 0) return RMSNORM_OK;
+    rmsnorm_plan_t plan;
+    int dev = 0;
+    if (user_plan == nullptr) {
+        int st = plan_for_device(o, &plan, &dev);
+        if (st != RMSNORM_OK) return st;
+    } else {
+        plan = *user_plan;
+        if (cudaGetDevice(&dev) != cudaSuccess) return RMSNORM_ECUDA;
+    }
+    return launch(o, &plan, dev, stream);
+}
+
+int check_common(int64_t rows, int64_t row_elems, float eps, float w_bias, int dtype) {
+    if (dtype != RMSNORM_F32 && dtype != RMSNORM_BF16) return RMSNORM_EINVAL;
+    if (rows < 0 || row_elems <= 0) return RMSNORM_EINVAL;
+    if (!std::isfinite(eps) || eps < 0.f || !std::isfinite(w_bias)) return RMSNORM_EINVAL;
+    if (row_elems > kMaxHidden) return RMSNORM_EUNSUPPORTED;
+    return RMSNORM_OK;
+}
+
+int make_contig(const void *x, const void *residual, const void *w, void *y, void *residual_out, int64_t rows,
+                int64_t hidden, float eps, float w_bias, int dtype, Op *o) {
+    int st = check_common(rows, hidden, eps, w_bias, dtype);
+    if (st != RMSNORM_OK) return st;
+    if (rows > INT64_MAX / (hidden * elem_size(dtype))) return RMSNORM_EINVAL;
+    if (rows > 0) {
+        if (x == nullptr || y == nullptr) return RMSNORM_EINVAL;
+        if ((residual == nullptr) != (residual_out == nullptr)) return RMSNORM_EINVAL;
+    }
+    if (w_bias != 0.f && w == nullptr) return RMSNORM_EINVAL;
+    o->x = x;
+    o->res = residual;
+    o->w = w;
+    o->y = y;
+    o->res_out = residual_out;
+    o->rows = rows;
+    o->row_elems = hidden;
+    o->x_stride = hidden;
+    o->y_stride = hidden;
+    o->eps = eps;
+    o->w_bias = w_bias;
+    o->wm = w == nullptr ? rrn::kNoWeight : (w_bias != 0.f ? rrn::kWeightBias : rrn::kWeight);
+    o->dtype = dtype;
+    return RMSNORM_OK;
+}
+
+int make_heads(const void *x, void *y, int64_t tokens, int64_t x_token_stride, int64_t y_token_stride,
+               int32_t q_heads, int32_t k_heads, int64_t head_dim, const void *q_w, const void *k_w, float w_bias,
+               float eps, int dtype, Op *o) {
+    int st = check_common(tokens, head_dim, eps, w_bias, dtype);
+    if (st != RMSNORM_OK) return st;
+    if (q_heads < 0 || k_heads < 0 || (int64_t)q_heads + k_heads < 1 || (int64_t)q_heads + k_heads > INT_MAX)
+        return RMSNORM_EINVAL;
+    const int64_t heads = (int64_t)q_heads + k_heads;
+    const int64_t span = heads * head_dim;
+    if (x_token_stride < span || y_token_stride < span) return RMSNORM_EINVAL;
+    const int64_t s = elem_size(dtype);
+    const int64_t big = x_token_stride > y_token_stride ? x_token_stride : y_token_stride;
+    if (tokens > INT64_MAX / (big * s) || tokens > INT64_MAX / heads) return RMSNORM_EINVAL;
+    if ((q_w == nullptr) != (k_w == nullptr)) return RMSNORM_EINVAL;
+    if (w_bias != 0.f && q_w == nullptr) return RMSNORM_EINVAL;
+    if (tokens > 0 && (x == nullptr || y == nullptr)) return RMSNORM_EINVAL;
+    if (x == y && x_token_stride != y_token_stride) return RMSNORM_EINVAL;
+    o->x = x;
+    o->y = y;
+    o->w = q_w;
+    o->w2 = k_w;
+    o->rows = tokens * heads;
+    o->row_elems = head_dim;
+    o->x_stride = x_token_stride;
+    o->y_stride = y_token_stride;
+    o->heads = (int32_t)heads;
+    o->q_heads = q_heads;
+    o->head_rows = true;
+    o->eps = eps;
+    o->w_bias = w_bias;
+    o->wm = q_w == nullptr ? rrn::kNoWeight : (w_bias != 0.f ? rrn::kWeightBias : rrn::kWeight);
+    o->dtype = dtype;
+    return RMSNORM_OK;
 }
 
 }  // namespace
@@ -330,7 +418,7 @@ int rmsnorm_plan(int64_t rows, int64_t hidden, int dtype, int vec_ok, int sm_cou
         return RMSNORM_EINVAL;
     if (hidden > kMaxHidden) return RMSNORM_EUNSUPPORTED;
     if (vec_ok && (hidden * elem_size(dtype)) % 16 != 0) return RMSNORM_EINVAL;
-    schedule(hidden, dtype, vec_ok ? 1 : 0, plan);
+    schedule(hidden, dtype, vec_ok ? 1 : 0, false, plan);
     size_grid(rows, sm_count, blocks_per_sm, plan);
     return RMSNORM_OK;
 }
@@ -339,39 +427,62 @@ int rmsnorm_plan_for(const void *x, const void *residual, const void *w, const v
                      const void *residual_out, int64_t rows, int64_t hidden, int dtype,
                      rmsnorm_plan_t *plan) {
     if (plan == nullptr) return RMSNORM_EINVAL;
-    int st = check_args(x, residual, y, residual_out, rows, hidden, 0.f, dtype);
+    Op o;
+    int st = make_contig(x, residual, w, const_cast<void *>(y), const_cast<void *>(residual_out), rows, hidden,
+                         0.f, 0.f, dtype, &o);
     if (st != RMSNORM_OK) return st;
-    if (!elem_aligned(x, residual, w, y, residual_out, dtype)) return RMSNORM_EINVAL;
-    return plan_for_device(x, residual, w, y, residual_out, rows, hidden, dtype, plan, nullptr);
+    if (!elem_aligned(o)) return RMSNORM_EINVAL;
+    return plan_for_device(o, plan, nullptr);
 }
 
 int rmsnorm_fwd(const void *x, const void *residual, const void *w, void *y, void *residual_out,
                 int64_t rows, int64_t hidden, float eps, int dtype, rmsnorm_stream_t stream) {
-    int st = check_args(x, residual, y, residual_out, rows, hidden, eps, dtype);
+    Op o;
+    int st = make_contig(x, residual, w, y, residual_out, rows, hidden, eps, 0.f, dtype, &o);
     if (st != RMSNORM_OK) return st;
-    if (!elem_aligned(x, residual, w, y, residual_out, dtype)) return RMSNORM_EINVAL;
-    if (rows == 0) return RMSNORM_OK;
-    rmsnorm_plan_t plan;
-    int dev = 0;
-    st = plan_for_device(x, residual, w, y, residual_out, rows, hidden, dtype, &plan, &dev);
-    if (st != RMSNORM_OK) return st;
-    return launch(make_params(x, residual, w, y, residual_out, rows, hidden, eps, plan.vec_elems), &plan,
-                  dtype, dev, stream);
+    return run(o, nullptr, stream);
 }
 
 int rmsnorm_fwd_plan(const void *x, const void *residual, const void *w, void *y, void *residual_out,
                      int64_t rows, int64_t hidden, float eps, int dtype, const rmsnorm_plan_t *plan,
                      rmsnorm_stream_t stream) {
-    int st = check_args(x, residual, y, residual_out, rows, hidden, eps, dtype);
+    if (plan == nullptr) return RMSNORM_EINVAL;
+    Op o;
+    int st = make_contig(x, residual, w, y, residual_out, rows, hidden, eps, 0.f, dtype, &o);
     if (st != RMSNORM_OK) return st;
-    if (!elem_aligned(x, residual, w, y, residual_out, dtype)) return RMSNORM_EINVAL;
-    const int vec_ok = vec_ok_of(x, residual, w, y, residual_out, hidden, dtype);
-    if ((st = validate_plan(plan, rows, hidden, dtype, vec_ok)) != RMSNORM_OK) return st;
-    if (rows == 0) return RMSNORM_OK;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return RMSNORM_ECUDA;
-    return launch(make_params(x, residual, w, y, residual_out, rows, hidden, eps, plan->vec_elems), plan,
-                  dtype, dev, stream);
+    return run(o, plan, stream);
+}
+
+int rmsnorm_fwd_ex(const void *x, const void *residual, const void *w, void *y, void *residual_out,
+                   int64_t rows, int64_t hidden, float eps, float weight_bias, int dtype,
+                   const rmsnorm_plan_t *plan, rmsnorm_stream_t stream) {
+    Op o;
+    int st = make_contig(x, residual, w, y, residual_out, rows, hidden, eps, weight_bias, dtype, &o);
+    if (st != RMSNORM_OK) return st;
+    return run(o, plan, stream);
+}
+
+int rmsnorm_qk_fwd(const void *x, void *y, int64_t tokens, int64_t x_token_stride, int64_t y_token_stride,
+                   int32_t q_heads, int32_t k_heads, int64_t head_dim, const void *q_w, const void *k_w,
+                   float weight_bias, float eps, int dtype, const rmsnorm_plan_t *plan,
+                   rmsnorm_stream_t stream) {
+    Op o;
+    int st = make_heads(x, y, tokens, x_token_stride, y_token_stride, q_heads, k_heads, head_dim, q_w, k_w,
+                        weight_bias, eps, dtype, &o);
+    if (st != RMSNORM_OK) return st;
+    return run(o, plan, stream);
+}
+
+int rmsnorm_qk_plan_for(const void *x, const void *y, int64_t tokens, int64_t x_token_stride,
+                        int64_t y_token_stride, int32_t q_heads, int32_t k_heads, int64_t head_dim,
+                        const void *q_w, const void *k_w, int dtype, rmsnorm_plan_t *plan) {
+    if (plan == nullptr) return RMSNORM_EINVAL;
+    Op o;
+    int st = make_heads(x, const_cast<void *>(y), tokens, x_token_stride, y_token_stride, q_heads, k_heads,
+                        head_dim, q_w, k_w, 0.f, 0.f, dtype, &o);
+    if (st != RMSNORM_OK) return st;
+    if (!elem_aligned(o)) return RMSNORM_EINVAL;
+    return plan_for_device(o, plan, nullptr);
 }
 
 int64_t rmsnorm_max_hidden(int dtype) {
@@ -391,8 +502,8 @@ const char *rmsnorm_strerror(int status) {
 }
 
 const char *rmsnorm_build_info(void) {
-    return "row_reduction_norm_gb300 fused RMSNorm 0.1; target sm_103a; kernels: register (warp/CTA/"
-           "persistent), two-pass";
+    return "row_reduction_norm_gb300 fused RMSNorm 0.2; target sm_103a; kernels: register (warp/CTA/"
+           "persistent), two-pass; contiguous rows and Q/K head rows; weight, weight + bias, no weight";
 }
 
 }  // extern "C"

@@ -24,6 +24,9 @@
 //    over row groups, so a grid capped at the resident capacity is the
 //    persistent regime, and w (the same for every row) is staged once per
 //    block in shared memory.
+//  * Both kernels also serve head rows (the fused Q+K norm of the Perplexity
+//    page's "QK Norm" section): rows are the heads of each token inside a
+//    packed projection, and query and key heads take different weights.
 //  * rms_loop_kernel -- one block per row, the row streamed twice: the first
 //    pass forms h (and writes residual_out) and the sum of squares, the second
 //    re-reads h (an L2 hit: the rows in flight are far smaller than L2) and
@@ -44,18 +47,62 @@
 namespace rrn {
 
 // Kernel arguments (passed by value).
+//
+// Row addressing.  Contiguous rows: row r starts x_stride * r bytes into x
+// (residual shares x's layout) and y_stride * r bytes into y (residual_out
+// shares y's).  Head rows (the fused Q+K norm): row r is head j = r % heads of
+// token t = r / heads, at t * x_stride + j * row_bytes in x and likewise in y;
+// heads j < q_heads take weight w, the others w2.
 struct Params {
     const void *x;
     const void *res;     // nullable
     const void *w;       // nullable
+    const void *w2;      // second weight (head rows: the key heads' weight)
     void *y;
     void *res_out;       // nullable
-    int64_t rows;
-    int64_t row_elems;   // hidden
-    int32_t units;       // loads per row: hidden / vec_elems
-    float hidden_f;      // hidden as float (exact for hidden <= 2^24)
+    int64_t rows;        // rows, or tokens * heads
+    int64_t row_elems;   // elements per row (hidden or head_dim)
+    int64_t row_bytes;   // row_elems * sizeof(T)
+    int64_t x_stride;    // bytes between consecutive rows (tokens for head rows) of x
+    int64_t y_stride;    // same for y
+    int32_t units;       // loads per row: row_elems / vec_elems
+    int32_t heads;       // heads per token (head rows), else 1
+    int32_t q_heads;     // heads per token that take w
+    float hidden_f;      // row_elems as float (exact for row_elems <= 2^24)
     float eps;
+    float w_bias;        // added to every weight element (weight mode kWeightBias)
 };
+
+// How the weight enters y: none, w, or (w + w_bias).
+enum WeightMode { kNoWeight = 0, kWeight = 1, kWeightBias = 2 };
+
+template <int WM>
+__device__ __forceinline__ float scale_out(float h, float r, float w, float bias) {
+    if constexpr (WM == kNoWeight) {
+        return h * r;
+    } else if constexpr (WM == kWeight) {
+        return (h * r) * w;
+    } else {
+        return (h * r) * (w + bias);
+    }
+}
+
+// Byte offsets of row `row` in x and y, and which weight it takes.
+template <bool HEADS>
+__device__ __forceinline__ void row_offsets(const Params &p, int64_t row, int64_t &xo, int64_t &yo, int &wsel) {
+    if constexpr (HEADS) {
+        const int64_t tok = row / p.heads;
+        const int j = (int)(row - tok * p.heads);
+        const int64_t hoff = (int64_t)j * p.row_bytes;
+        xo = tok * p.x_stride + hoff;
+        yo = tok * p.y_stride + hoff;
+        wsel = j >= p.q_heads ? 1 : 0;
+    } else {
+        xo = row * p.x_stride;
+        yo = row * p.y_stride;
+        wsel = 0;
+    }
+}
 
 struct BF16 {
     using storage = uint16_t;
@@ -186,9 +233,11 @@ __device__ __forceinline__ float tree_sum(float (&v)[N]) {
 
 // ------------------------------------------------------- register kernel
 
-template <typename T, int GT, int CH, bool RES, bool W>
+template <typename T, int GT, int CH, bool RES, int WM, bool HEADS>
 __global__ void __launch_bounds__(reg_block_threads(GT))
 rms_reg_kernel(const Params p) {
+    constexpr bool W = WM != kNoWeight;
+    static_assert(!(HEADS && RES), "head rows take no residual");
     constexpr int V = T::kVec;
     constexpr int BLOCK = reg_block_threads(GT);
     constexpr int RPB = BLOCK / GT;               // rows per block iteration
@@ -201,15 +250,14 @@ rms_reg_kernel(const Params p) {
     const int slot = tid / GT;
     const int t = tid % GT;
     const int nch = p.units;
-    const int64_t row_bytes = p.row_elems * (int64_t)sizeof(typename T::storage);
 
     pdl_wait_for_inputs();
     pdl_allow_dependents();
 
-    // w is the same for every row: staged once per block in shared memory
-    // (dynamic, units * 16 bytes) and read from there in every epilogue.  The
-    // staging happens after the first row's loads are issued, so the two
-    // memory round trips overlap.
+    // w (and w2 for head rows) is the same for every row: staged once per
+    // block in shared memory (dynamic, units * 16 bytes per weight) and read
+    // from there in every epilogue.  The staging happens after the first
+    // row's loads are issued, so the two memory round trips overlap.
     extern __shared__ Chunk w_smem[];
     bool w_staged = false;
 
@@ -217,7 +265,9 @@ rms_reg_kernel(const Params p) {
     for (int64_t rb = blockIdx.x; rb * RPB < p.rows; rb += gridDim.x) {
         const int64_t row = rb * RPB + slot;
         const bool row_ok = row < p.rows;
-        const int64_t off = row * row_bytes;
+        int64_t off = 0, yoff = 0;
+        int wsel = 0;
+        if (row_ok) row_offsets<HEADS>(p, row, off, yoff, wsel);
 
         // A1: load the row's chunks (zeros where a slot is past the row end)
         Chunk hc[CH];
@@ -244,6 +294,10 @@ rms_reg_kernel(const Params p) {
             if (!w_staged) {   // first iteration of the block (uniform across it)
                 for (int i = tid; i < nch; i += BLOCK)
                     w_smem[i] = ld_readonly16(static_cast<const char *>(p.w) + (int64_t)i * 16);
+                if constexpr (HEADS) {
+                    for (int i = tid; i < nch; i += BLOCK)
+                        w_smem[nch + i] = ld_readonly16(static_cast<const char *>(p.w2) + (int64_t)i * 16);
+                }
                 __syncthreads();
                 w_staged = true;
             }
@@ -260,7 +314,7 @@ rms_reg_kernel(const Params p) {
                 for (int e = 0; e < V; ++e) a[e] = add_round(a[e], b[e], T{});
                 hc[c] = pack(a, T{});
                 if (row_ok && u < nch)
-                    st16(static_cast<char *>(p.res_out) + off + (int64_t)u * 16, hc[c]);
+                    st16(static_cast<char *>(p.res_out) + yoff + (int64_t)u * 16, hc[c]);
             }
         }
         // A3: squares into V accumulators, chunk order; zero slots add +0 exactly
@@ -289,23 +343,23 @@ rms_reg_kernel(const Params p) {
         }
         // A6: the row's scale
         const float r = rsqrtf(sum / p.hidden_f + p.eps);
-        // A7: y = RN_T(h * r * w)
+        // A7: y = RN_T(h * r * w)   (or h * r, or h * r * (w + bias))
 #pragma unroll
         for (int c = 0; c < CH; ++c) {
             const int u = c * GT + t;
             if (row_ok && u < nch) {
                 float a[V];
                 unpack(hc[c], a, T{});
+                float wv[V];
                 if constexpr (W) {
-                    float wv[V];
-                    unpack(w_smem[u], wv, T{});
-#pragma unroll
-                    for (int e = 0; e < V; ++e) a[e] = (a[e] * r) * wv[e];
+                    unpack(w_smem[wsel * nch + u], wv, T{});
                 } else {
 #pragma unroll
-                    for (int e = 0; e < V; ++e) a[e] = a[e] * r;
+                    for (int e = 0; e < V; ++e) wv[e] = 1.f;
                 }
-                st16(static_cast<char *>(p.y) + off + (int64_t)u * 16, pack(a, T{}));
+#pragma unroll
+                for (int e = 0; e < V; ++e) a[e] = scale_out<WM>(a[e], r, wv[e], p.w_bias);
+                st16(static_cast<char *>(p.y) + yoff + (int64_t)u * 16, pack(a, T{}));
             }
         }
     }
@@ -386,9 +440,11 @@ struct UnitIO<T, 1> {
     }
 };
 
-template <typename T, int VE, int BLOCK, bool RES, bool W>
+template <typename T, int VE, int BLOCK, bool RES, int WM, bool HEADS>
 __global__ void __launch_bounds__(BLOCK, 1)
 rms_loop_kernel(const Params p) {
+    constexpr bool W = WM != kNoWeight;
+    static_assert(!(HEADS && RES), "head rows take no residual");
     using IO = UnitIO<T, VE>;
     using Raw = typename IO::Raw;
     constexpr int NACC = 8;                          // per-thread accumulators
@@ -400,17 +456,19 @@ rms_loop_kernel(const Params p) {
 
     const int tid = threadIdx.x;
     const int64_t nunits = p.units;
-    const int64_t row_bytes = p.row_elems * (int64_t)sizeof(typename T::storage);
     int parity = 0;
     pdl_wait_for_inputs();
     pdl_allow_dependents();
 
     for (int64_t row = blockIdx.x; row < p.rows; row += gridDim.x) {
-        const int64_t off = row * row_bytes;
+        int64_t off, yoff;
+        int wsel;
+        row_offsets<HEADS>(p, row, off, yoff, wsel);
         const void *xr = static_cast<const char *>(p.x) + off;
         const void *rr = RES ? static_cast<const char *>(p.res) + off : nullptr;
-        void *hr = RES ? static_cast<char *>(p.res_out) + off : nullptr;
-        void *yr = static_cast<char *>(p.y) + off;
+        void *hr = RES ? static_cast<char *>(p.res_out) + yoff : nullptr;
+        void *yr = static_cast<char *>(p.y) + yoff;
+        const void *wr = wsel ? p.w2 : p.w;
 
         // pass 1: h (and residual_out), sum of squares.  Element e of the
         // j-th unit of a step feeds accumulator (j * VE + e) % NACC.
@@ -474,22 +532,22 @@ rms_loop_kernel(const Params p) {
             for (int j = 0; j < U; ++j) {
                 const int64_t u = base + (int64_t)j * BLOCK;
                 ha[j] = u < nunits ? IO::load_last(src, u) : IO::zero();
-                if constexpr (W) wa[j] = u < nunits ? IO::load_w(p.w, u) : IO::zero();
+                if constexpr (W) wa[j] = u < nunits ? IO::load_w(wr, u) : IO::zero();
             }
 #pragma unroll
             for (int j = 0; j < U; ++j) {
                 const int64_t u = base + (int64_t)j * BLOCK;
                 float a[VE];
                 IO::widen(ha[j], a);
+                float wv[VE];
                 if constexpr (W) {
-                    float wv[VE];
                     IO::widen(wa[j], wv);
-#pragma unroll
-                    for (int e = 0; e < VE; ++e) a[e] = (a[e] * r) * wv[e];
                 } else {
 #pragma unroll
-                    for (int e = 0; e < VE; ++e) a[e] = a[e] * r;
+                    for (int e = 0; e < VE; ++e) wv[e] = 1.f;
                 }
+#pragma unroll
+                for (int e = 0; e < VE; ++e) a[e] = scale_out<WM>(a[e], r, wv[e], p.w_bias);
                 if (u < nunits) IO::store(yr, u, a);
             }
         }

@@ -144,3 +144,67 @@ def from_numpy_bits(a, dtype: str) -> torch.Tensor:
     if dtype == "bf16":
         return torch.from_numpy(a.view("int16").copy()).view(torch.bfloat16)
     return torch.from_numpy(a.copy())
+
+
+@dataclasses.dataclass(frozen=True)
+class QKWorkload:
+    """Packed token rows [q heads | k heads | v heads] for the fused Q+K norm."""
+    name: str
+    dtype: str
+    tokens: int
+    q_heads: int
+    k_heads: int
+    v_heads: int
+    head_dim: int
+    eps: float
+    x_std: float
+    w_std: Optional[float]        # None: no weights
+    weight_bias: float = 0.0      # added to every weight element
+    w_mean: float = 1.0           # weights ~ w_mean + N(0, w_std)
+    note: str = ""
+
+    @property
+    def width(self) -> int:
+        return (self.q_heads + self.k_heads + self.v_heads) * self.head_dim
+
+    @property
+    def elem_bytes(self) -> int:
+        return 2 if self.dtype == "bf16" else 4
+
+    def algorithmic_bytes(self) -> int:
+        """Read and write every query and key head once, read both weights."""
+        heads = self.tokens * (self.q_heads + self.k_heads)
+        w = 2 * self.head_dim * self.elem_bytes if self.w_std is not None else 0
+        return heads * self.head_dim * self.elem_bytes * 2 + w
+
+
+QK_WORKLOADS = {
+    w.name: w
+    for w in [
+        QKWorkload("qk_bf16_8192tok_q32_k8_v8_hd128", "bf16", 8192, 32, 8, 8, 128, 1e-6, 2.0, 0.1,
+                   note="Qwen3-8B-like fused projection, query and key norms in one launch"),
+        QKWorkload("qk_bf16_8192tok_q32_k8_v8_hd128_1pw", "bf16", 8192, 32, 8, 8, 128, 1e-6, 2.0, 0.1,
+                   weight_bias=1.0, w_mean=0.0, note="same, (1 + w) weight form"),
+        QKWorkload("qk_bf16_64tok_q32_k8_v8_hd128", "bf16", 64, 32, 8, 8, 128, 1e-6, 2.0, 0.1,
+                   note="decode batch"),
+    ]
+}
+
+
+def make_qk_inputs(wl: QKWorkload, seed: int = 0, device="cpu", tokens: Optional[int] = None,
+                   stride: Optional[int] = None):
+    """Draw (qkv, q_w, k_w): qkv [tokens, stride] (stride >= width; value heads and
+    padding drawn like the rest), weights ~ w_mean + N(0, w_std) or None."""
+    device = torch.device(device)
+    t = wl.tokens if tokens is None else int(tokens)
+    width = wl.width if stride is None else int(stride)
+    dt = TORCH_DTYPE[wl.dtype]
+    qkv = torch.randn((t, width), generator=_gen(device, seed), device=device,
+                      dtype=torch.float32).mul_(wl.x_std).to(dt)
+    q_w = k_w = None
+    if wl.w_std is not None:
+        q_w = (torch.randn((wl.head_dim,), generator=_gen(device, seed + 2), device=device,
+                           dtype=torch.float32).mul_(wl.w_std).add_(wl.w_mean)).to(dt)
+        k_w = (torch.randn((wl.head_dim,), generator=_gen(device, seed + 4), device=device,
+                           dtype=torch.float32).mul_(wl.w_std).add_(wl.w_mean)).to(dt)
+    return qkv, q_w, k_w

@@ -98,11 +98,12 @@ def midpoint_distance(sign_q: Fraction, fmt: str) -> Fraction:
     return best
 
 
-def rmsnorm_row_exact(x, w, residual, eps_bits_value: Fraction, fmt: str):
+def rmsnorm_row_exact(x, w, residual, eps_bits_value: Fraction, fmt: str, weight_bias: Fraction = Fraction(0)):
     """Exact RMSNorm of one row given as lists of encodings (ints).
 
-    Returns (y_bits, residual_out_bits or None, q_list, signs) where y_i =
-    sign_i * sqrt(q_i) exactly, before rounding.
+    The weight enters as (w_i + weight_bias).  Returns (y_bits,
+    residual_out_bits or None, q_list, signs) where y_i = sign_i * sqrt(q_i)
+    exactly, before rounding.
     """
     n = len(x)
     xs = [decode(b, fmt) for b in x]
@@ -113,7 +114,7 @@ def rmsnorm_row_exact(x, w, residual, eps_bits_value: Fraction, fmt: str):
     else:
         h_bits = None
         hs = xs
-    ws = [decode(b, fmt) for b in w] if w is not None else [Fraction(1)] * n
+    ws = [decode(b, fmt) + weight_bias for b in w] if w is not None else [Fraction(1)] * n
     s = sum(h * h for h in hs)
     denom = s / n + eps_bits_value
     qs, signs, y_bits = [], [], []
@@ -126,8 +127,15 @@ def rmsnorm_row_exact(x, w, residual, eps_bits_value: Fraction, fmt: str):
         else:
             # IEEE sign of a zero product: XOR of the operand signs (r > 0)
             hb = (h_bits[i] if h_bits is not None else x[i]) & sign_mask
-            wb = (w[i] & sign_mask) if w is not None else 0
-            sg = -1 if (hb != 0) != (wb != 0) else 1
+            if w is None:
+                wneg = False
+            elif ws[i] != 0:
+                wneg = ws[i] < 0
+            elif weight_bias == 0:
+                wneg = (w[i] & sign_mask) != 0
+            else:
+                wneg = False   # w + b == 0 exactly: IEEE round-to-nearest sum is +0
+            sg = -1 if (hb != 0) != wneg else 1
         qs.append(q)
         signs.append(sg)
         y_bits.append(round_sqrt(sg, q, fmt))

@@ -20,6 +20,9 @@ MISTAKES = [
     "ties_away", "abs_output", "residual_out_is_x", "sum_of_abs", "stats_from_x",
     "eps_as_double", "round_via_f32",
 ]
+# Planted mistakes of the weight-bias form and of the per-head Q/K layout.
+BIAS_MISTAKES = ["bias_ignored", "bias_added_to_output", "bias_scaled_by_r"]
+QK_MISTAKES = ["qk_weights_swapped", "qk_one_weight", "qk_stats_over_token", "qk_head_offset"]
 
 
 def _round(v, dt, mode="rne"):
@@ -57,8 +60,9 @@ def _encode(v, dt):
     return f
 
 
-def reference(x, w, residual, eps, dt, mistake=None):
+def reference(x, w, residual, eps, dt, mistake=None, weight_bias=0.0):
     mode = {"trunc_rounding": "trunc", "ties_away": "away"}.get(mistake, "rne")
+    b = float(np.float32(weight_bias or 0.0))
     xv = _decode(x, dt)
     e = float(eps) if mistake == "eps_as_double" else float(np.float32(eps))
     if residual is not None:
@@ -98,7 +102,14 @@ def reference(x, w, residual, eps, dt, mistake=None):
             wv = _decode(w, dt)
             if mistake == "weight_reversed":
                 wv = wv[::-1]
-            y = y * wv
+            if mistake == "bias_added_to_output":
+                y = y * wv + b
+            elif mistake == "bias_scaled_by_r":
+                y = h * (r * wv + b)
+            elif mistake == "bias_ignored":
+                y = y * wv
+            else:
+                y = y * (wv + b)
         if mistake == "abs_output":
             y = np.abs(y)
     if mistake == "round_via_f32":
@@ -107,3 +118,28 @@ def reference(x, w, residual, eps, dt, mistake=None):
     out_y = _encode(yr, dt)
     out_h = None if h_store is None else _encode(h_store, dt)
     return out_y, out_h, y
+
+
+def reference_qk(x, q_heads, k_heads, head_dim, q_w, k_w, eps, dt, weight_bias=0.0, mistake=None):
+    """Per-head Q/K norm of packed token rows built on ``reference``."""
+    tokens = x.shape[0]
+    qc, kc = q_heads * head_dim, k_heads * head_dim
+    if mistake == "qk_head_offset":
+        qc_start = head_dim // 2
+    else:
+        qc_start = 0
+    q_rows = np.ascontiguousarray(x[:, qc_start:qc_start + qc]).reshape(tokens * q_heads, head_dim)
+    k_rows = np.ascontiguousarray(x[:, qc:qc + kc]).reshape(tokens * k_heads, head_dim)
+    qw, kw = (k_w, q_w) if mistake == "qk_weights_swapped" else (q_w, k_w)
+    if mistake == "qk_one_weight":
+        kw = qw
+    if mistake == "qk_stats_over_token":
+        both = np.concatenate([x[:, :qc], x[:, qc:qc + kc]], axis=1)
+        yall, _, _ = reference(both, None, None, eps, dt)
+        # rescale as if a whole-token norm were taken: wrong statistics per head
+        qy = yall[:, :qc].reshape(tokens, q_heads, head_dim)
+        ky = yall[:, qc:].reshape(tokens, k_heads, head_dim)
+        return qy, ky
+    qy, _, _ = reference(q_rows, qw, None, eps, dt, weight_bias=weight_bias)
+    ky, _, _ = reference(k_rows, kw, None, eps, dt, weight_bias=weight_bias)
+    return qy.reshape(tokens, q_heads, head_dim), ky.reshape(tokens, k_heads, head_dim)

@@ -369,6 +369,76 @@ def pin_near_ties(impl, trials=400_000, seed=77):
     return fails
 
 
+def pin_weight_bias(impl_b):
+    """y = h * r * (w + b): random tiny rows, b in {1, 1/2, -1/4, 3}, with and
+    without a residual, bit-exact against exact rational arithmetic; and
+    b = 0 gives the plain weighted op bit for bit."""
+    rng = np.random.default_rng(31)
+    fails = []
+    for k in range(40):
+        dt = ("bf16", "f32")[k % 2]
+        has_res = bool((k // 2) % 2)
+        b = (1.0, 0.5, -0.25, 3.0)[(k // 4) % 4]
+        hidden = int(rng.integers(1, 9))
+        rows = 3
+        eps = (0.0, 1e-6, 0.25)[k % 3]
+        xb = [random_bits(rng, dt, hidden) for _ in range(rows)]
+        rb = [random_bits(rng, dt, hidden) for _ in range(rows)] if has_res else None
+        wb = random_bits(rng, dt, hidden, -2, 2)
+        x = to_array(sum(xb, []), dt).reshape(rows, hidden)
+        res = to_array(sum(rb, []), dt).reshape(rows, hidden) if has_res else None
+        w = to_array(wb, dt)
+        y, _, _ = impl_b(x, w, res, eps, dt, b)
+        yb = bits_of(y, dt).reshape(rows, hidden)
+        for r in range(rows):
+            want, _, qs, _ = exact.rmsnorm_row_exact(xb[r], wb, rb[r] if has_res else None, f32_exact(eps),
+                                                     dt, Fraction(b))
+            for i in range(hidden):
+                if int(yb[r, i]) != want[i]:
+                    d = exact.midpoint_distance(qs[i], dt)
+                    if d is None or d > Fraction(1, 2 ** 44):
+                        fails.append(f"weight bias {b} case {k} ({dt}, res={has_res}) row {r} elem {i}: "
+                                     f"{int(yb[r, i]):#x} != {want[i]:#x}")
+        y0, _, _ = impl_b(x, w, res, eps, dt, 0.0)
+        y1, _, _ = impl_b(x, w, res, eps, dt, None)
+        if not np.array_equal(bits_of(y0, dt), bits_of(y1, dt)):
+            fails.append(f"weight bias 0 differs from the plain weighted op (case {k})")
+    return fails
+
+
+def pin_qk_heads(impl_qk):
+    """Packed token rows [q heads | k heads | v heads]: every query head is the
+    op on that head with q_w, every key head with k_w, each head on its own
+    (exact rational check); a head's result does not depend on the others."""
+    rng = np.random.default_rng(41)
+    fails = []
+    for k, (dt, qh, kh, hd, b) in enumerate([("bf16", 4, 2, 8, 0.0), ("f32", 3, 1, 5, 1.0),
+                                              ("bf16", 2, 2, 4, 1.0), ("f32", 1, 3, 8, 0.0)]):
+        tokens = 3
+        cols = (qh + kh + 1) * hd          # one value head after the keys
+        xb = random_bits(rng, dt, tokens * cols, -4, 4)
+        x = to_array(xb, dt).reshape(tokens, cols)
+        qwb = random_bits(rng, dt, hd, -1, 1)
+        kwb = random_bits(rng, dt, hd, -1, 1)
+        qy, ky = impl_qk(x, qh, kh, hd, to_array(qwb, dt), to_array(kwb, dt), 1e-6, dt, b)
+        qy = bits_of(qy, dt).reshape(tokens, qh, hd)
+        ky = bits_of(ky, dt).reshape(tokens, kh, hd)
+        for t in range(tokens):
+            row = xb[t * cols:(t + 1) * cols]
+            for j in range(qh + kh):
+                head = row[j * hd:(j + 1) * hd]
+                wb = qwb if j < qh else kwb
+                want, _, qs, _ = exact.rmsnorm_row_exact(head, wb, None, f32_exact(1e-6), dt, Fraction(b))
+                got = qy[t, j] if j < qh else ky[t, j - qh]
+                for i in range(hd):
+                    if int(got[i]) != want[i]:
+                        d = exact.midpoint_distance(qs[i], dt)
+                        if d is None or d > Fraction(1, 2 ** 44):
+                            fails.append(f"qk case {k} token {t} head {j} elem {i}: "
+                                         f"{int(got[i]):#x} != {want[i]:#x}")
+    return fails
+
+
 ALL_PINS = [pin_golden, pin_bruteforce, pin_constant_row, pin_scale_invariance,
             pin_unit_rms, pin_special_values, pin_single_element, pin_row_independence,
             pin_eps_dominated, pin_near_ties]

@@ -157,3 +157,44 @@ def test_torch_api_refuses_cpu_tensors():
     x = torch.zeros(4, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         R.rms_norm(x)
+
+
+def _qk(*a):
+    return N.rmsnorm_qk_fwd_status(*a)
+
+
+def test_qk_and_ex_arguments_rejected_without_cuda():
+    P = 1 << 20
+    # x, y, tokens, xs, ys, qh, kh, hd, q_w, k_w, bias, eps, dtype
+    ok = (P, P, 4, 48 * 128, 48 * 128, 32, 8, 128, P, P, 0.0, 1e-6, 1)
+    bad = [
+        (P, P, 4, 48 * 128, 48 * 128, -1, 8, 128, P, P, 0.0, 1e-6, 1),          # negative heads
+        (P, P, 4, 48 * 128, 48 * 128, 0, 0, 128, P, P, 0.0, 1e-6, 1),          # no heads
+        (P, P, 4, 39 * 128, 48 * 128, 32, 8, 128, P, P, 0.0, 1e-6, 1),         # x stride too short
+        (P, P, 4, 48 * 128, 39 * 128, 32, 8, 128, P, P, 0.0, 1e-6, 1),         # y stride too short
+        (P, P, 4, 48 * 128, 64 * 128, 32, 8, 128, P, P, 0.0, 1e-6, 1),         # in place, strides differ
+        (P, P, 4, 48 * 128, 48 * 128, 32, 8, 128, P, None, 0.0, 1e-6, 1),      # one weight only
+        (P, P, 4, 48 * 128, 48 * 128, 32, 8, 128, None, None, 1.0, 1e-6, 1),   # bias without weights
+        (P, P, 4, 48 * 128, 48 * 128, 32, 8, 0, P, P, 0.0, 1e-6, 1),           # head_dim 0
+        (P, P, 4, 48 * 128, 48 * 128, 32, 8, 128, P, P, float("nan"), 1e-6, 1),  # bias not finite
+        (P, P, -1, 48 * 128, 48 * 128, 32, 8, 128, P, P, 0.0, 1e-6, 1),        # negative tokens
+        (None, P, 4, 48 * 128, 48 * 128, 32, 8, 128, P, P, 0.0, 1e-6, 1),      # null x
+        (P + 1, P, 4, 48 * 128, 48 * 128, 32, 8, 128, P, P, 0.0, 1e-6, 1),     # misaligned element
+    ]
+    for a in bad:
+        assert _qk(*a) == N.RMSNORM_EINVAL, a
+    assert _qk(P, P, 4, 48 * 128, 48 * 128, 32, 8, 1 << 17, P, P, 0.0, 1e-6, 1) == N.RMSNORM_EUNSUPPORTED
+    # zero tokens: a successful no-op, pointers unused
+    assert _qk(None, None, 0, 48 * 128, 48 * 128, 32, 8, 128, None, None, 0.0, 1e-6, 1) == N.RMSNORM_OK
+    # weight bias needs a weight; non-finite bias rejected
+    assert N.rmsnorm_fwd_ex_status(P, None, None, P, None, 4, 64, 1e-6, 1.0, 1) == N.RMSNORM_EINVAL
+    assert N.rmsnorm_fwd_ex_status(P, None, P, P, None, 4, 64, 1e-6, float("inf"), 1) == N.RMSNORM_EINVAL
+    assert N.rmsnorm_fwd_ex_status(P, None, P, P, None, 0, 64, 1e-6, 1.0, 1) == N.RMSNORM_OK
+    bad_plan = R.rmsnorm_plan(4, 64, 1, True, 152, 1)
+    bad_plan.threads_per_row = 64    # head rows allow at most 32 threads per row
+    bad_plan.block_threads = 256
+    bad_plan.rows_per_block = 4
+    bad_plan.chunks_per_thread = 1
+    assert N.rmsnorm_qk_fwd_status(P, P, 4, 48 * 512, 48 * 512, 32, 8, 512, P, P, 0.0, 1e-6, 1,
+                                   bad_plan) == N.RMSNORM_EINVAL
+    del ok

@@ -82,3 +82,41 @@ def test_bf16_conversion_definition():
     finite = ~np.isnan(vals)
     back = oracle.bf16_from_double(vals[finite])
     assert np.array_equal(back, bits[finite])
+
+
+def oracle_impl_b(x, w, residual, eps, dtype, weight_bias):
+    if weight_bias is None:
+        return oracle.rmsnorm(x, w=w, residual=residual, eps=eps, dtype=dtype, want_exact=True)
+    return oracle.rmsnorm(x, w=w, residual=residual, eps=eps, dtype=dtype, want_exact=True,
+                          weight_bias=weight_bias)
+
+
+def oracle_impl_qk(x, qh, kh, hd, q_w, k_w, eps, dtype, weight_bias):
+    return oracle.rmsnorm_qk(x, qh, kh, hd, q_w=q_w, k_w=k_w, eps=eps, dtype=dtype, weight_bias=weight_bias)
+
+
+def test_oracle_weight_bias_pin():
+    assert pins.pin_weight_bias(oracle_impl_b) == []
+
+
+def test_oracle_qk_pin():
+    assert pins.pin_qk_heads(oracle_impl_qk) == []
+
+
+def test_restatement_passes_bias_and_qk_pins():
+    assert pins.pin_weight_bias(lambda x, w, r, e, d, b: mutants.reference(x, w, r, e, d, weight_bias=b)) == []
+    assert pins.pin_qk_heads(lambda x, qh, kh, hd, qw, kw, e, d, b:
+                             mutants.reference_qk(x, qh, kh, hd, qw, kw, e, d, weight_bias=b)) == []
+
+
+@pytest.mark.parametrize("mistake", mutants.BIAS_MISTAKES)
+def test_weight_bias_pin_catches(mistake):
+    impl = lambda x, w, r, e, d, b: mutants.reference(x, w, r, e, d, mistake=mistake, weight_bias=b)
+    assert pins.pin_weight_bias(impl) != []
+
+
+@pytest.mark.parametrize("mistake", mutants.QK_MISTAKES)
+def test_qk_pin_catches(mistake):
+    impl = lambda x, qh, kh, hd, qw, kw, e, d, b: mutants.reference_qk(x, qh, kh, hd, qw, kw, e, d,
+                                                                       weight_bias=b, mistake=mistake)
+    assert pins.pin_qk_heads(impl) != []
