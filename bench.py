@@ -274,6 +274,26 @@ class Launcher:
         return g
 
 
+class LNLauncher(Launcher):
+    """LayerNorm workloads: the Launcher's buffer sets plus a bias."""
+
+    def __init__(self, wl, device, stream, min_footprint, seed=0):
+        import torch
+        from row_reduction_norm_gb300 import api, workloads as W
+        super().__init__(wl, device, stream, min_footprint, seed)
+        _, _, _, b = W.make_ln_inputs(wl, seed=seed, device=device, rows=1)
+        self.b = b
+        self.b_ptr = None if b is None else b.data_ptr()
+        x0, r0, y0, h0 = self.sets[0]
+        self.plan = api.layer_norm_plan_for(x0, w=self.w, b=b, residual=r0, out=y0, residual_out=h0)
+        del torch
+
+    def launch(self, i):
+        x, r, y, h = self.ptrs[i % self.n_sets]
+        self.N.layernorm_fwd(x, r, self.w_ptr, self.b_ptr, y, h, self.wl.rows, self.wl.hidden, self.wl.eps,
+                             self.code, None, self.stream.cuda_stream)
+
+
 class QKLauncher(Launcher):
     """Buffer sets of a fused Q+K workload, normalised in place (the usual use on
     a packed projection), with the same launch interface as Launcher."""
@@ -579,10 +599,11 @@ def run_ours(args):
     if not args.no_per_config:
         del L
         torch.cuda.empty_cache()
-        for name in PER_CONFIG + list(W.QK_WORKLOADS):
+        for name in PER_CONFIG + list(W.QK_WORKLOADS) + list(W.LN_WORKLOADS):
             qk = name in W.QK_WORKLOADS
-            cw = W.QK_WORKLOADS[name] if qk else W.WORKLOADS[name]
-            CL = (QKLauncher if qk else Launcher)(cw, device, stream, min_footprint)
+            ln = name in W.LN_WORKLOADS
+            cw = W.QK_WORKLOADS[name] if qk else W.LN_WORKLOADS[name] if ln else W.WORKLOADS[name]
+            CL = (QKLauncher if qk else LNLauncher if ln else Launcher)(cw, device, stream, min_footprint)
             # calibrate: about 0.3 s of launches
             cal = time_launches(CL, 64, 8)
             k = int(max(64, min(200000, 0.3 / max(cal / 1e3 / 64, 1e-9))))
@@ -601,6 +622,8 @@ def run_ours(args):
                               "weight_bias": cw.weight_bias})
             else:
                 entry.update({"residual": cw.has_res, "weight": cw.has_w})
+            if ln:
+                entry.update({"op": "layernorm", "bias": cw.has_b})
             if rows <= 64 or (qk and cw.tokens <= 64):
                 entry["single_launch_latency_us"] = round(single_launch_latency_us(CL), 2)
             per_config.append(entry)

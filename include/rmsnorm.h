@@ -1,5 +1,6 @@
 /*
- * rmsnorm.h -- C ABI of the GB300 (sm_103a) fused row-wise RMSNorm library.
+ * rmsnorm.h -- C ABI of the GB300 (sm_103a) fused row-wise RMSNorm library
+ * (with its LayerNorm and fused Q+K head-norm variants).
  *
  * The operation (one row at a time, rows of a row-major [rows, hidden] tensor):
  *
@@ -206,6 +207,28 @@ int rmsnorm_qk_plan_for(const void *x, const void *y, int64_t tokens, int64_t x_
                         int64_t y_token_stride, int32_t q_heads, int32_t k_heads,
                         int64_t head_dim, const void *q_w, const void *k_w, int dtype,
                         rmsnorm_plan_t *plan);
+
+/*
+ * Fused row-wise LayerNorm ("GPT-2 on the GPU", section "The Whole Model as
+ * One Kernel": mean, variance, (x - mean) / sqrt(var + eps), weight times the
+ * normalised value plus bias):
+ *   h    = x, or RN_T(x + residual) written to residual_out
+ *   mu   = mean(h),  var = mean((h - mu)^2)   (population variance)
+ *   y_i  = RN_T( (h_i - mu) * rsqrt(var + eps) * w_i + b_i )
+ * w and b are optional [hidden] tensors (b requires w); without w the
+ * normalised value is returned.  Layout, aliasing, alignment, plan and
+ * status codes as rmsnorm_fwd_ex (REG plans up to 256 threads per row).
+ * The statistics are formed in fp32 in a fixed order; the variance is taken
+ * of the centred values (a second pass over the row held on chip).
+ */
+int layernorm_fwd(const void *x, const void *residual, const void *w, const void *b, void *y,
+                  void *residual_out, int64_t rows, int64_t hidden, float eps, int dtype,
+                  const rmsnorm_plan_t *plan, rmsnorm_stream_t stream);
+
+/* The plan layernorm_fwd would use for these pointers on the current device. */
+int layernorm_plan_for(const void *x, const void *residual, const void *w, const void *b,
+                       const void *y, const void *residual_out, int64_t rows, int64_t hidden,
+                       int dtype, rmsnorm_plan_t *plan);
 
 /* Largest supported hidden size for a dtype (0 for an unknown dtype). */
 int64_t rmsnorm_max_hidden(int dtype);

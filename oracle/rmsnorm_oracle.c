@@ -173,6 +173,66 @@ int oracle_rmsnorm_rows(const void *x, const void *residual, const void *w,
     return 0;
 }
 
+/*
+ * LayerNorm, rows [row_begin, row_end) ("GPT-2 on the GPU", section "The
+ * Whole Model as One Kernel": the traced block takes the mean and the
+ * variance of the row, normalises as (x - mean) / sqrt(variance + eps) and
+ * returns weight * normalised + bias):
+ *   h      = x, or RN_T(x + residual) as above
+ *   mean   = sum_i h_i / hidden
+ *   var    = sum_i (h_i - mean)^2 / hidden        (population variance)
+ *   n_i    = (h_i - mean) / sqrt(var + eps)
+ *   y_i    = RN_T(w_i * n_i + b_i)                (w, b optional; b needs w)
+ * n_exact, y_exact: optional fp64 copies of n and of y before rounding.
+ * Returns 0, or -1 on an invalid argument.
+ */
+int oracle_layernorm_rows(const void *x, const void *residual, const void *w, const void *b,
+                          void *y, double *n_exact, double *y_exact, void *residual_out,
+                          int64_t row_begin, int64_t row_end, int64_t hidden, float eps, int dtype)
+{
+    if (x == NULL || y == NULL || hidden <= 0 || row_begin < 0 || row_end < row_begin)
+        return -1;
+    if (dtype != ORACLE_F32 && dtype != ORACLE_BF16)
+        return -1;
+    if ((residual == NULL) != (residual_out == NULL))
+        return -1;
+    if (b != NULL && w == NULL)
+        return -1;
+
+    const double e = (double)eps;
+    for (int64_t row = row_begin; row < row_end; ++row) {
+        const int64_t base = row * hidden;
+        double sum = 0.0;
+        for (int64_t i = 0; i < hidden; ++i)
+            sum += row_input(x, residual, base + i, dtype);
+        const double mean = sum / (double)hidden;
+        double sq = 0.0;
+        for (int64_t i = 0; i < hidden; ++i) {
+            double d = row_input(x, residual, base + i, dtype) - mean;
+            sq += d * d;
+        }
+        const double var = sq / (double)hidden;
+        const double denom = sqrt(var + e);
+        for (int64_t i = 0; i < hidden; ++i) {
+            double h = row_input(x, residual, base + i, dtype);
+            double n = (h - mean) / denom;
+            double v = n;
+            if (w != NULL)
+                v = load_elem(w, i, dtype) * n;
+            if (b != NULL)
+                v = v + load_elem(b, i, dtype);
+            if (n_exact != NULL)
+                n_exact[base + i] = n;
+            if (y_exact != NULL)
+                y_exact[base + i] = v;
+            store_elem(y, base + i, dtype, v);
+            if (residual_out != NULL)
+                store_elem(residual_out, base + i, dtype, h);
+        }
+    }
+    return 0;
+}
+
 /* Elementwise conversions, exposed so that tests can pin them on their own. */
 void oracle_bf16_from_double(const double *v, uint16_t *out, int64_t n)
 {

@@ -36,8 +36,8 @@ KERNEL_NAMES = {0: "reg", 1: "loop"}
 
 # Every symbol the header declares (checked by the CPU tests).
 EXPORTED = ["rmsnorm_fwd", "rmsnorm_plan", "rmsnorm_plan_for", "rmsnorm_fwd_plan", "rmsnorm_fwd_ex",
-            "rmsnorm_qk_fwd", "rmsnorm_qk_plan_for", "rmsnorm_max_hidden", "rmsnorm_reg_max_chunks",
-            "rmsnorm_strerror", "rmsnorm_build_info"]
+            "rmsnorm_qk_fwd", "rmsnorm_qk_plan_for", "layernorm_fwd", "layernorm_plan_for",
+            "rmsnorm_max_hidden", "rmsnorm_reg_max_chunks", "rmsnorm_strerror", "rmsnorm_build_info"]
 
 
 class RmsNormError(RuntimeError):
@@ -111,6 +111,11 @@ def load():
         lib.rmsnorm_qk_plan_for.argtypes = [vp, vp, i64, i64, i64, ctypes.c_int32, ctypes.c_int32, i64, vp, vp,
                                             i32, ctypes.POINTER(Plan)]
         lib.rmsnorm_qk_plan_for.restype = i32
+        lib.layernorm_fwd.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, ctypes.c_float, i32,
+                                      ctypes.POINTER(Plan), vp]
+        lib.layernorm_fwd.restype = i32
+        lib.layernorm_plan_for.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i32, ctypes.POINTER(Plan)]
+        lib.layernorm_plan_for.restype = i32
         lib.rmsnorm_plan.argtypes = [i64, i64, i32, i32, i32, i32, ctypes.POINTER(Plan)]
         lib.rmsnorm_plan.restype = i32
         lib.rmsnorm_plan_for.argtypes = [vp, vp, vp, vp, vp, i64, i64, i32, ctypes.POINTER(Plan)]
@@ -185,6 +190,24 @@ def rmsnorm_qk_plan_for(x, y, tokens, x_token_stride, y_token_stride, q_heads, k
     p = Plan()
     _check(load().rmsnorm_qk_plan_for(x, y, tokens, x_token_stride, y_token_stride, q_heads, k_heads,
                                       head_dim, q_w, k_w, dtype, ctypes.byref(p)), "rmsnorm_qk_plan_for")
+    return p
+
+
+def layernorm_fwd(x, residual, w, b, y, residual_out, rows, hidden, eps, dtype, plan=None, stream=0):
+    _check(layernorm_fwd_status(x, residual, w, b, y, residual_out, rows, hidden, eps, dtype, plan, stream),
+           "layernorm_fwd")
+
+
+def layernorm_fwd_status(x, residual, w, b, y, residual_out, rows, hidden, eps, dtype, plan=None,
+                         stream=0) -> int:
+    return load().layernorm_fwd(x, residual, w, b, y, residual_out, rows, hidden, eps, dtype, _plan_ref(plan),
+                                stream)
+
+
+def layernorm_plan_for(x, residual, w, b, y, residual_out, rows, hidden, dtype) -> Plan:
+    p = Plan()
+    _check(load().layernorm_plan_for(x, residual, w, b, y, residual_out, rows, hidden, dtype, ctypes.byref(p)),
+           "layernorm_plan_for")
     return p
 
 

@@ -144,3 +144,42 @@ def plan_for(x: torch.Tensor, w=None, residual=None, out=None, residual_out=None
     with torch.cuda.device(x.device):
         return N.rmsnorm_plan_for(_ptr(x), _ptr(residual), _ptr(w), _ptr(y), _ptr(ro), rows, hidden,
                                   dtype_code(x.dtype))
+
+
+def layer_norm(x: torch.Tensor, w: Optional[torch.Tensor] = None, b: Optional[torch.Tensor] = None,
+               residual: Optional[torch.Tensor] = None, eps: float = 1e-5, out: Optional[torch.Tensor] = None,
+               residual_out: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None,
+               plan: Optional[N.Plan] = None):
+    """y = (h - mean(h)) / sqrt(var(h) + eps) * w + b over the last dimension
+    (h = x, or x + residual written to ``residual_out``).  Returns y, or
+    (y, residual_out) with a residual."""
+    _check_tensor(x, "x", x)
+    code = dtype_code(x.dtype)
+    hidden = x.shape[-1]
+    rows = x.numel() // hidden if hidden else 0
+    for name, t in (("residual", residual), ("out", out), ("residual_out", residual_out)):
+        if t is not None and t.shape != x.shape:
+            raise ValueError(f"{name} has shape {tuple(t.shape)}, x has {tuple(x.shape)}")
+    for name, t in (("w", w), ("b", b)):
+        if t is not None and tuple(t.shape) != (hidden,):
+            raise ValueError(f"{name} must have shape ({hidden},)")
+    y = torch.empty_like(x) if out is None else out
+    if residual is not None and residual_out is None:
+        residual_out = torch.empty_like(x)
+    for name, t in (("w", w), ("b", b), ("residual", residual), ("out", y), ("residual_out", residual_out)):
+        _check_tensor(t, name, x)
+    with torch.cuda.device(x.device):
+        s = stream if stream is not None else torch.cuda.current_stream(x.device)
+        N.layernorm_fwd(_ptr(x), _ptr(residual), _ptr(w), _ptr(b), _ptr(y), _ptr(residual_out), rows, hidden,
+                        float(eps), code, plan, s.cuda_stream)
+    return (y, residual_out) if residual is not None else y
+
+
+def layer_norm_plan_for(x, w=None, b=None, residual=None, out=None, residual_out=None) -> N.Plan:
+    hidden = x.shape[-1]
+    rows = x.numel() // hidden
+    y = out if out is not None else x
+    ro = residual_out if residual_out is not None else residual
+    with torch.cuda.device(x.device):
+        return N.layernorm_plan_for(_ptr(x), _ptr(residual), _ptr(w), _ptr(b), _ptr(y), _ptr(ro), rows, hidden,
+                                    dtype_code(x.dtype))

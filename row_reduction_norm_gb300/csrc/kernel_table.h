@@ -22,6 +22,12 @@ const void *reg_heads_bf16(int gt, int ch, int wm);
 const void *loop_contig(int dtype, int block, bool vec, bool res, int wm);
 const void *loop_heads(int dtype, int block, bool vec, int wm);
 
+// LayerNorm (contiguous rows); aff: 0 none, 1 weight, 2 weight and bias.
+constexpr int kLnMaxGT = 256;
+const void *ln_reg_f32(int gt, int ch, bool res, int aff);
+const void *ln_reg_bf16(int gt, int ch, bool res, int aff);
+const void *ln_loop(int dtype, int block, bool vec, bool res, int aff);
+
 inline const void *reg_kernel(int dtype, int gt, int ch, bool res, int wm, bool heads) {
     if (heads) return res ? nullptr : (dtype == 1 ? reg_heads_bf16(gt, ch, wm) : reg_heads_f32(gt, ch, wm));
     if (dtype == 1) return res ? reg_contig_bf16_res(gt, ch, wm) : reg_contig_bf16_plain(gt, ch, wm);

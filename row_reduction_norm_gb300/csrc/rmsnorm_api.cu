@@ -17,6 +17,7 @@
 #include <mutex>
 
 #include "kernel_table.h"
+#include "layernorm_kernels.cuh"
 #include "rmsnorm.h"
 #include "rmsnorm_kernels.cuh"
 
@@ -64,15 +65,21 @@ struct Op {
     int64_t y_stride = 0;
     int32_t heads = 1, q_heads = 1;
     bool head_rows = false;
+    bool ln = false;           // LayerNorm instead of RMSNorm
+    const void *b = nullptr;   // LayerNorm bias
     float eps = 0.f, w_bias = 0.f;
-    int wm = 0;                // rrn::WeightMode
+    int wm = 0;                // rrn::WeightMode (RMSNorm) or rrn::AffineMode (LayerNorm)
     int dtype = RMSNORM_BF16;
 };
+
+int max_threads_per_row(const Op &o) {
+    return o.ln ? rrn::kLnMaxGT : (o.head_rows ? rrn::kRegMaxGTHeads : rrn::kRegMaxGT);
+}
 
 bool elem_aligned(const Op &o) {
     const int a = elem_size(o.dtype);
     return aligned_to(o.x, a) && aligned_to(o.res, a) && aligned_to(o.w, a) && aligned_to(o.w2, a) &&
-           aligned_to(o.y, a) && aligned_to(o.res_out, a);
+           aligned_to(o.b, a) && aligned_to(o.y, a) && aligned_to(o.res_out, a);
 }
 
 // 16-byte units are possible when every pointer, the row size and the row
@@ -80,15 +87,14 @@ bool elem_aligned(const Op &o) {
 int vec_ok_of(const Op &o) {
     const int s = elem_size(o.dtype);
     return aligned_to(o.x, 16) && aligned_to(o.res, 16) && aligned_to(o.w, 16) && aligned_to(o.w2, 16) &&
-           aligned_to(o.y, 16) && aligned_to(o.res_out, 16) && (o.row_elems * s) % 16 == 0 &&
+           aligned_to(o.b, 16) && aligned_to(o.y, 16) && aligned_to(o.res_out, 16) && (o.row_elems * s) % 16 == 0 &&
            (o.x_stride * s) % 16 == 0 && (o.y_stride * s) % 16 == 0;
 }
 
 // The per-row schedule: everything but the grid.
-void schedule(int64_t hidden, int dtype, int vec_ok, bool head_rows, rmsnorm_plan_t *p) {
+void schedule(int64_t hidden, int dtype, int vec_ok, int max_gt, rmsnorm_plan_t *p) {
     std::memset(p, 0, sizeof(*p));
     const int V = vec_elems_of(dtype);
-    const int max_gt = head_rows ? rrn::kRegMaxGTHeads : rrn::kRegMaxGT;
     if (vec_ok) {
         const int64_t nch = hidden / V;
         // Aim at 4 chunks (64 bytes of each input) per thread with at least 4
@@ -142,12 +148,19 @@ void size_grid(int64_t rows, int sm_count, int blocks_per_sm, rmsnorm_plan_t *p)
 }
 
 size_t dyn_smem_of(const rmsnorm_plan_t *p, const Op &o) {
-    if (p->kernel != RMSNORM_KERNEL_REG || o.wm == rrn::kNoWeight) return 0;
-    return (size_t)(o.row_elems / vec_elems_of(o.dtype)) * 16 * (o.head_rows ? 2 : 1);
+    if (p->kernel != RMSNORM_KERNEL_REG || o.wm == 0) return 0;
+    const int copies = o.ln ? (o.wm == rrn::kAffWB ? 2 : 1) : (o.head_rows ? 2 : 1);
+    return (size_t)(o.row_elems / vec_elems_of(o.dtype)) * 16 * copies;
 }
 
 const void *kernel_of(const rmsnorm_plan_t *p, const Op &o) {
     const bool res = o.res != nullptr;
+    if (o.ln) {
+        if (p->kernel == RMSNORM_KERNEL_REG)
+            return o.dtype == RMSNORM_BF16 ? rrn::ln_reg_bf16(p->threads_per_row, p->chunks_per_thread, res, o.wm)
+                                           : rrn::ln_reg_f32(p->threads_per_row, p->chunks_per_thread, res, o.wm);
+        return rrn::ln_loop(o.dtype, p->block_threads, p->vec_elems != 1, res, o.wm);
+    }
     if (p->kernel == RMSNORM_KERNEL_REG)
         return rrn::reg_kernel(o.dtype, p->threads_per_row, p->chunks_per_thread, res, o.wm, o.head_rows);
     return rrn::loop_kernel(o.dtype, p->block_threads, p->vec_elems != 1, res, o.wm, o.head_rows);
@@ -161,7 +174,7 @@ int validate_plan(const rmsnorm_plan_t *p, const Op &o, int vec_ok) {
     if (p->pdl != 0 && p->pdl != 1) return RMSNORM_EINVAL;
     if (p->kernel == RMSNORM_KERNEL_REG) {
         const int gt = p->threads_per_row, ch = p->chunks_per_thread;
-        const int max_gt = o.head_rows ? rrn::kRegMaxGTHeads : rrn::kRegMaxGT;
+        const int max_gt = max_threads_per_row(o);
         if (!vec_ok || p->vec_elems != V) return RMSNORM_EINVAL;
         if (gt < 4 || gt > max_gt || (gt & (gt - 1)) != 0) return RMSNORM_EINVAL;
         if (ch < 1 || ch > rrn::kRegMaxCH || (ch & (ch - 1)) != 0) return RMSNORM_EINVAL;
@@ -255,7 +268,7 @@ int blocks_per_sm_of(int dev, const void *fn, int block, size_t smem, int *out) 
 
 // Full device-side planning for an op.
 int plan_for_device(const Op &o, rmsnorm_plan_t *plan, int *dev_out) {
-    schedule(o.row_elems, o.dtype, vec_ok_of(o), o.head_rows, plan);
+    schedule(o.row_elems, o.dtype, vec_ok_of(o), max_threads_per_row(o), plan);
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return RMSNORM_ECUDA;
     int sms = 0;
@@ -282,6 +295,25 @@ int launch(const Op &o, const rmsnorm_plan_t *plan, int dev, rmsnorm_stream_t st
     }
     const int64_t s = elem_size(o.dtype);
     rrn::Params args;
+    rrn::LnParams largs;
+    void *argv[1];
+    if (o.ln) {
+        largs.x = o.x;
+        largs.res = o.res;
+        largs.w = o.w;
+        largs.b = o.b;
+        largs.y = o.y;
+        largs.res_out = o.res_out;
+        largs.rows = o.rows;
+        largs.row_elems = o.row_elems;
+        largs.row_bytes = o.row_elems * s;
+        largs.units = (int32_t)(o.row_elems / plan->vec_elems);
+        largs.hidden_f = (float)o.row_elems;
+        largs.eps = o.eps;
+        argv[0] = &largs;
+    } else {
+        argv[0] = &args;
+    }
     args.x = o.x;
     args.res = o.res;
     args.w = o.w;
@@ -299,7 +331,6 @@ int launch(const Op &o, const rmsnorm_plan_t *plan, int dev, rmsnorm_stream_t st
     args.hidden_f = (float)o.row_elems;
     args.eps = o.eps;
     args.w_bias = o.w_bias;
-    void *argv[] = {&args};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -408,9 +439,40 @@ int make_heads(const void *x, void *y, int64_t tokens, int64_t x_token_stride, i
     return RMSNORM_OK;
 }
 
+int make_ln(const void *x, const void *residual, const void *w, const void *b, void *y, void *residual_out,
+            int64_t rows, int64_t hidden, float eps, int dtype, Op *o) {
+    int st = make_contig(x, residual, w, y, residual_out, rows, hidden, eps, 0.f, dtype, o);
+    if (st != RMSNORM_OK) return st;
+    if (b != nullptr && w == nullptr) return RMSNORM_EINVAL;
+    o->ln = true;
+    o->b = b;
+    o->wm = w == nullptr ? rrn::kAffNone : (b == nullptr ? rrn::kAffW : rrn::kAffWB);
+    return RMSNORM_OK;
+}
+
 }  // namespace
 
 extern "C" {
+
+int layernorm_fwd(const void *x, const void *residual, const void *w, const void *b, void *y, void *residual_out,
+                  int64_t rows, int64_t hidden, float eps, int dtype, const rmsnorm_plan_t *plan,
+                  rmsnorm_stream_t stream) {
+    Op o;
+    int st = make_ln(x, residual, w, b, y, residual_out, rows, hidden, eps, dtype, &o);
+    if (st != RMSNORM_OK) return st;
+    return run(o, plan, stream);
+}
+
+int layernorm_plan_for(const void *x, const void *residual, const void *w, const void *b, const void *y,
+                       const void *residual_out, int64_t rows, int64_t hidden, int dtype, rmsnorm_plan_t *plan) {
+    if (plan == nullptr) return RMSNORM_EINVAL;
+    Op o;
+    int st = make_ln(x, residual, w, b, const_cast<void *>(y), const_cast<void *>(residual_out), rows, hidden, 0.f,
+                     dtype, &o);
+    if (st != RMSNORM_OK) return st;
+    if (!elem_aligned(o)) return RMSNORM_EINVAL;
+    return plan_for_device(o, plan, nullptr);
+}
 
 int rmsnorm_plan(int64_t rows, int64_t hidden, int dtype, int vec_ok, int sm_count, int blocks_per_sm,
                  rmsnorm_plan_t *plan) {
@@ -418,7 +480,7 @@ int rmsnorm_plan(int64_t rows, int64_t hidden, int dtype, int vec_ok, int sm_cou
         return RMSNORM_EINVAL;
     if (hidden > kMaxHidden) return RMSNORM_EUNSUPPORTED;
     if (vec_ok && (hidden * elem_size(dtype)) % 16 != 0) return RMSNORM_EINVAL;
-    schedule(hidden, dtype, vec_ok ? 1 : 0, false, plan);
+    schedule(hidden, dtype, vec_ok ? 1 : 0, rrn::kRegMaxGT, plan);
     size_grid(rows, sm_count, blocks_per_sm, plan);
     return RMSNORM_OK;
 }
@@ -502,8 +564,8 @@ const char *rmsnorm_strerror(int status) {
 }
 
 const char *rmsnorm_build_info(void) {
-    return "row_reduction_norm_gb300 fused RMSNorm 0.2; target sm_103a; kernels: register (warp/CTA/"
-           "persistent), two-pass; contiguous rows and Q/K head rows; weight, weight + bias, no weight";
+    return "row_reduction_norm_gb300 fused RMSNorm / LayerNorm 0.3; target sm_103a; kernels: register (warp/"
+           "CTA/persistent), two/three-pass; contiguous rows and Q/K head rows; weight, weight + bias, no weight";
 }
 
 }  // extern "C"

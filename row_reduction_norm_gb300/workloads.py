@@ -39,6 +39,8 @@ class Workload:
     outlier_frac: float = 0.0
     outlier_scale: float = 1.0
     note: str = ""
+    b_std: Optional[float] = None   # LayerNorm bias ~ N(0, b_std) (None: no bias)
+    x_mean: float = 0.0             # x ~ x_mean + N(0, x_std)
 
     @property
     def has_res(self) -> bool:
@@ -52,11 +54,15 @@ class Workload:
     def elem_bytes(self) -> int:
         return 2 if self.dtype == "bf16" else 4
 
+    @property
+    def has_b(self) -> bool:
+        return self.b_std is not None
+
     def algorithmic_bytes(self, rows: Optional[int] = None) -> int:
-        """Bytes one pass must move: read x (+ residual), write y (+ residual_out), read w once."""
+        """Bytes one pass must move: read x (+ residual), write y (+ residual_out), read w (and b) once."""
         r = self.rows if rows is None else rows
         per_row = self.hidden * self.elem_bytes * (2 + (2 if self.has_res else 0))
-        return r * per_row + (self.hidden * self.elem_bytes if self.has_w else 0)
+        return r * per_row + self.hidden * self.elem_bytes * ((1 if self.has_w else 0) + (1 if self.has_b else 0))
 
     def with_rows(self, rows: int) -> "Workload":
         return dataclasses.replace(self, rows=rows, name=f"{self.name}@rows={rows}")
@@ -106,6 +112,8 @@ def make_inputs(wl: Workload, seed: int = 0, device="cpu", rows: Optional[int] =
     dt = TORCH_DTYPE[wl.dtype]
     x = torch.randn((r, h), generator=_gen(device, seed), device=device, dtype=torch.float32)
     x.mul_(wl.x_std)
+    if wl.x_mean:
+        x.add_(wl.x_mean)
     if wl.outlier_frac > 0.0:
         u = torch.rand((r, h), generator=_gen(device, seed + 3), device=device, dtype=torch.float32)
         x = torch.where(u < wl.outlier_frac, x * wl.outlier_scale, x)
@@ -208,3 +216,30 @@ def make_qk_inputs(wl: QKWorkload, seed: int = 0, device="cpu", tokens: Optional
         k_w = (torch.randn((wl.head_dim,), generator=_gen(device, seed + 4), device=device,
                            dtype=torch.float32).mul_(wl.w_std).add_(wl.w_mean)).to(dt)
     return qkv, q_w, k_w
+
+
+# LayerNorm workloads: GPT-2 (width 768, eps 1e-5, weight and bias) from "GPT-2
+# on the GPU", section "The Whole Model as One Kernel", plus a wider fused
+# residual case.  Weights ~ 1 + N(0, 0.1), biases ~ N(0, 0.1).
+LN_WORKLOADS = {
+    w.name: w
+    for w in [
+        Workload("ln_f32_64x768_wb", "f32", 64, 768, 1e-5, 1.0, None, 0.1, b_std=0.1,
+                 note="GPT-2 width, fp32 as the tutorial runs it"),
+        Workload("ln_bf16_16384x768_wb", "bf16", 16384, 768, 1e-5, 1.0, None, 0.1, b_std=0.1, x_mean=0.5,
+                 note="GPT-2 width, 16384 tokens"),
+        Workload("ln_bf16_res_16384x4096_wb", "bf16", 16384, 4096, 1e-5, 1.0, 1.0, 0.1, b_std=0.1,
+                 note="fused residual add, width 4096"),
+    ]
+}
+
+
+def make_ln_inputs(wl: Workload, seed: int = 0, device="cpu", rows: Optional[int] = None):
+    """(x, residual, w, b) for a LayerNorm workload; b drawn with seed + 5."""
+    x, r, w = make_inputs(wl, seed=seed, device=device, rows=rows)
+    b = None
+    if wl.has_b:
+        dev = torch.device(device)
+        b = torch.randn((wl.hidden,), generator=_gen(dev, seed + 5), device=dev,
+                        dtype=torch.float32).mul_(wl.b_std).to(TORCH_DTYPE[wl.dtype])
+    return x, r, w, b

@@ -140,3 +140,81 @@ def rmsnorm_row_exact(x, w, residual, eps_bits_value: Fraction, fmt: str, weight
         signs.append(sg)
         y_bits.append(round_sqrt(sg, q, fmt))
     return y_bits, h_bits, qs, signs
+
+
+def _cmp_affine_sqrt(a: Fraction, d: Fraction, b: Fraction, v: Fraction) -> int:
+    """Sign of (a / sqrt(d) + b) - v, exactly (d > 0)."""
+    c = v - b                      # compare a / sqrt(d) with c
+    if a >= 0 and c <= 0:
+        return 0 if (a == 0 and c == 0) else 1
+    if a <= 0 and c >= 0:
+        return -1
+    lhs, rhs = a * a, c * c * d    # same signs: compare squares
+    if a > 0:
+        return (lhs > rhs) - (lhs < rhs)
+    return (rhs > lhs) - (rhs < lhs)
+
+
+def round_affine_sqrt(a: Fraction, d: Fraction, b: Fraction, fmt: str) -> int:
+    """Bits of the correctly rounded value of a / sqrt(d) + b (d > 0), ties to even."""
+    e_bits, f_bits, bias, inf_ord = _fmt(fmt)
+    sign_bit = 1 << (e_bits + f_bits)
+    s0 = _cmp_affine_sqrt(a, d, b, Fraction(0))
+    if s0 == 0:
+        return 0
+    neg = s0 < 0
+    if neg:                        # round the magnitude of -(value)
+        a, b = -a, -b
+    # largest ordinal k with value(k) <= value (positive side)
+    lo, hi = 0, inf_ord
+    if _cmp_affine_sqrt(a, d, b, _ord_value(inf_ord, fmt)) >= 0:
+        return (sign_bit if neg else 0) | inf_ord
+    while hi - lo > 1:
+        mid = (lo + hi) // 2
+        if _cmp_affine_sqrt(a, d, b, _ord_value(mid, fmt)) >= 0:
+            lo = mid
+        else:
+            hi = mid
+    m = (_ord_value(lo, fmt) + _ord_value(hi, fmt)) / 2
+    c = _cmp_affine_sqrt(a, d, b, m)
+    k = lo if c < 0 else hi if c > 0 else (lo if lo % 2 == 0 else hi)
+    return (sign_bit if neg else 0) | k
+
+
+def near_midpoint_affine(a: Fraction, d: Fraction, b: Fraction, bits1: int, bits2: int, fmt: str,
+                         rel: Fraction = Fraction(1, 2 ** 44)) -> bool:
+    """True if a / sqrt(d) + b lies within `rel` (relative) of the midpoint of
+    two adjacent encodings bits1, bits2 (an fp64 computation may round it either way)."""
+    v1, v2 = decode(bits1, fmt), decode(bits2, fmt)
+    if v1 is None or v2 is None:
+        return False
+    m = (v1 + v2) / 2
+    lo, hi = m - abs(m) * rel, m + abs(m) * rel
+    return _cmp_affine_sqrt(a, d, b, lo) >= 0 and _cmp_affine_sqrt(a, d, b, hi) <= 0
+
+
+def layernorm_row_exact(x, w, b, residual, eps_value: Fraction, fmt: str, want_terms: bool = False):
+    """Exact LayerNorm of one row of encodings: y_i = w_i (h_i - mean) / sqrt(var + eps) + b_i,
+    correctly rounded.  Returns (y_bits, residual_out_bits or None), plus the
+    exact terms (a_i, d, b_i) of y_i = a_i / sqrt(d) + b_i with ``want_terms``."""
+    n = len(x)
+    xs = [decode(v, fmt) for v in x]
+    if residual is not None:
+        rs = [decode(v, fmt) for v in residual]
+        h_bits = [round_value(p + q, fmt) for p, q in zip(xs, rs)]
+        hs = [decode(v, fmt) for v in h_bits]
+    else:
+        h_bits, hs = None, xs
+    mean = sum(hs) / n
+    var = sum((h - mean) ** 2 for h in hs) / n
+    d = var + eps_value
+    ws = [decode(v, fmt) for v in w] if w is not None else [Fraction(1)] * n
+    bs = [decode(v, fmt) for v in b] if b is not None else [Fraction(0)] * n
+    out = []
+    terms = []
+    for i in range(n):
+        out.append(round_affine_sqrt(ws[i] * (hs[i] - mean), d, bs[i], fmt))
+        terms.append((ws[i] * (hs[i] - mean), d, bs[i]))
+    if want_terms:
+        return out, h_bits, terms
+    return out, h_bits

@@ -143,3 +143,40 @@ def reference_qk(x, q_heads, k_heads, head_dim, q_w, k_w, eps, dt, weight_bias=0
     qy, _, _ = reference(q_rows, qw, None, eps, dt, weight_bias=weight_bias)
     ky, _, _ = reference(k_rows, kw, None, eps, dt, weight_bias=weight_bias)
     return qy.reshape(tokens, q_heads, head_dim), ky.reshape(tokens, k_heads, head_dim)
+
+
+LN_MISTAKES = ["bessel", "eps_outside_sqrt", "no_centering", "bias_inside_weight", "no_bias",
+               "stats_from_x", "unrounded_residual", "mean_over_h_minus_1"]
+
+
+def reference_ln(x, w, b, residual, eps, dt, mistake=None):
+    """Independent numpy fp64 LayerNorm with optional planted mistakes."""
+    xv = _decode(x, dt)
+    e = float(np.float32(eps))
+    if residual is not None:
+        sm = xv + _decode(residual, dt)
+        h_store = _round(sm, dt)
+        h = sm if mistake == "unrounded_residual" else h_store
+    else:
+        h, h_store = xv, None
+    st = xv if mistake == "stats_from_x" else h
+    n = h.shape[1]
+    with np.errstate(invalid="ignore", divide="ignore"):
+        mean = st.sum(axis=1, keepdims=True) / (n - 1 if mistake == "mean_over_h_minus_1" else n)
+        if mistake == "no_centering":
+            mean = np.zeros_like(mean)
+        var = ((st - mean) ** 2).sum(axis=1, keepdims=True) / (n - 1 if mistake == "bessel" else n)
+        if mistake == "eps_outside_sqrt":
+            nrm = (h - mean) / (np.sqrt(var) + e)
+        else:
+            nrm = (h - mean) / np.sqrt(var + e)
+        y = nrm
+        if w is not None:
+            wv = _decode(w, dt)
+            if b is not None and mistake not in ("no_bias",):
+                bv = _decode(b, dt)
+                y = wv * (nrm + bv) if mistake == "bias_inside_weight" else wv * nrm + bv
+            else:
+                y = wv * nrm
+    out = _encode(_round(y, dt), dt)
+    return out, (None if h_store is None else _encode(h_store, dt)), nrm, y

@@ -68,3 +68,47 @@ def bits_equal(a, b):
     a = np.ascontiguousarray(a)
     b = np.ascontiguousarray(b)
     return a.shape == b.shape and a.view(np.uint8).tobytes() == b.view(np.uint8).tobytes()
+
+
+# LayerNorm: y = w * n + b can cancel, so a relative bound per element does not
+# hold; the bound is on the terms instead.  The kernels form the mean and the
+# centred sum of squares along fixed trees at most 21 levels deep, so
+#   |n' - n| <= 18u |n| + 21u mean|h| / sigma      (sigma = sqrt(var + eps))
+# and the fused multiply-add of the output adds u |y|:
+#   |y' - y| <= 2e-6 * ( |w| (|n| + mean|h| / sigma) + |b| )
+# before the final rounding to the I/O type, which adds at most half an ulp of
+# the stored value.
+LN_TERM_TOL = 2e-6
+
+
+def _half_ulp(vals, dtype):
+    v = np.abs(vals.astype(np.float64))
+    p = 8 if dtype == "bf16" else 24
+    qmin = -133 if dtype == "bf16" else -149
+    _, e = np.frexp(np.where(v > 0, v, 1.0))
+    q = np.maximum(e - p, qmin)
+    return np.ldexp(0.5, q)
+
+
+def decode(a, dtype):
+    a = np.asarray(a)
+    if dtype == "bf16":
+        return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return a.astype(np.float64)
+
+
+def compare_ln(got, y64, n64, w, b, mean_abs_h, sigma, dtype):
+    """CUDA LayerNorm output against the oracle's fp64 value with the term bound above."""
+    g = decode(got, dtype)
+    wv = np.ones_like(y64) if w is None else decode(w, dtype)[None, :]
+    bv = np.zeros_like(y64) if b is None else decode(b, dtype)[None, :]
+    bound = LN_TERM_TOL * (np.abs(wv) * (np.abs(n64) + (mean_abs_h / sigma)[:, None]) + np.abs(bv))
+    lim = bound + _half_ulp(g, dtype)
+    gn, rn = np.isnan(g), np.isnan(y64)
+    with np.errstate(invalid="ignore"):
+        err = np.where(gn | rn, 0.0, np.abs(g - y64))
+    bad = err > lim
+    nan_ok = np.array_equal(gn, rn)
+    ratio = float((err / np.where(lim > 0, lim, 1)).max()) if err.size else 0.0
+    return nan_ok and not bad.any(), {"worst_err_over_bound": ratio, "n_bad": int(bad.sum()), "nan_ok": nan_ok,
+                                      "n": int(err.size)}

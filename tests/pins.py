@@ -439,6 +439,104 @@ def pin_qk_heads(impl_qk):
     return fails
 
 
+# ------------------------------------------------------------- LayerNorm pins
+# impl_ln(x, w, b, residual, eps, dtype) -> (y, residual_out, n_exact, y_exact)
+# Definition: "GPT-2 on the GPU", section "The Whole Model as One Kernel".
+
+def pin_ln_bruteforce(impl_ln, n_cases=80, seed=4321):
+    """Random tiny rows, every option, bit-exact against exact rational arithmetic."""
+    rng = np.random.default_rng(seed)
+    fails = []
+    for k in range(n_cases):
+        dt = ("bf16", "f32")[k % 2]
+        has_w = bool((k // 2) % 2)
+        has_b = has_w and bool((k // 4) % 2)
+        has_res = bool((k // 8) % 2)
+        hidden = int(rng.integers(2, 9))
+        eps = (0.0, 1e-5, 0.25)[k % 3]
+        rows = 3
+        xb = [random_bits(rng, dt, hidden) for _ in range(rows)]
+        rb = [random_bits(rng, dt, hidden) for _ in range(rows)] if has_res else None
+        wb = random_bits(rng, dt, hidden, -2, 2) if has_w else None
+        bb = random_bits(rng, dt, hidden, -2, 2) if has_b else None
+        x = to_array(sum(xb, []), dt).reshape(rows, hidden)
+        res = to_array(sum(rb, []), dt).reshape(rows, hidden) if has_res else None
+        w = to_array(wb, dt) if has_w else None
+        b = to_array(bb, dt) if has_b else None
+        y, rout, _, _ = impl_ln(x, w, b, res, eps, dt)
+        yb = bits_of(y, dt).reshape(rows, hidden)
+        for r in range(rows):
+            want, want_h, terms = exact.layernorm_row_exact(xb[r], wb, bb, rb[r] if has_res else None,
+                                                            f32_exact(eps), dt, want_terms=True)
+            got = [int(v) for v in yb[r]]
+            for i in range(hidden):
+                # a mismatch is allowed only for a value within 2^-44 of a rounding midpoint
+                if got[i] != want[i] and not exact.near_midpoint_affine(*terms[i], got[i], want[i], dt):
+                    fails.append(f"ln bruteforce case {k} ({dt}, w={has_w}, b={has_b}, res={has_res},"
+                                 f" eps={eps}) row {r} elem {i}: {got[i]:#x} != {want[i]:#x}")
+            if has_res and [int(v) for v in bits_of(rout, dt).reshape(rows, hidden)[r]] != want_h:
+                fails.append(f"ln bruteforce case {k}: residual_out row {r}")
+    return fails
+
+
+def pin_ln_closed_forms(impl_ln):
+    """Hand-derived cases: [1, 2, 3, 4] (mean 5/2, variance 5/4: n_i^2 =
+    (x_i - 5/2)^2 / (5/4) = 9/5, 1/5, 1/5, 9/5); a constant row gives y = b
+    exactly (n = 0, eps > 0); [a, -a] gives n = +-a / sqrt(a^2 + eps)."""
+    fails = []
+    for dt in ("bf16", "f32"):
+        x = to_array([encode_exact(Fraction(v), dt) for v in (1, 2, 3, 4)], dt).reshape(1, 4)
+        y, _, _, _ = impl_ln(x, None, None, None, 0.0, dt)
+        want = [exact.round_sqrt(s, q, dt) for s, q in zip((-1, -1, 1, 1),
+                                                              (Fraction(9, 5), Fraction(1, 5), Fraction(1, 5),
+                                                               Fraction(9, 5)))]
+        if [int(v) for v in bits_of(y, dt).reshape(-1)] != want:
+            fails.append(f"ln [1,2,3,4] {dt}")
+        c = encode_exact(Fraction(3, 4), dt)
+        bvals = [Fraction(1, 8), Fraction(-5, 2), Fraction(0), Fraction(7)]
+        w = to_array([encode_exact(Fraction(2), dt)] * 4, dt)
+        b = to_array([encode_exact(v, dt) for v in bvals], dt)
+        y, _, _, _ = impl_ln(to_array([c] * 4, dt).reshape(1, 4), w, b, None, 1e-5, dt)
+        if [int(v) for v in bits_of(y, dt).reshape(-1)] != [encode_exact(v, dt) for v in bvals]:
+            fails.append(f"ln constant row {dt}: y != b")
+        a = Fraction(3, 2)
+        x2 = to_array([encode_exact(a, dt), encode_exact(-a, dt)], dt).reshape(1, 2)
+        y, _, _, _ = impl_ln(x2, None, None, None, 0.5, dt)
+        q = a * a / (a * a + f32_exact(0.5))
+        want = [exact.round_sqrt(1, q, dt), exact.round_sqrt(-1, q, dt)]
+        if [int(v) for v in bits_of(y, dt).reshape(-1)] != want:
+            fails.append(f"ln [a,-a] {dt}")
+    return fails
+
+
+def pin_ln_invariances(impl_ln):
+    """With eps = 0: y(2^k x + c) == y(x) bit for bit for integer rows whose
+    shifted and scaled values stay exact; and without affine, mean(n) = 0 and
+    mean(n^2) = 1 in fp64."""
+    fails = []
+    rng = np.random.default_rng(55)
+    for dt in ("bf16", "f32"):
+        hidden = 64
+        vals = rng.integers(-50, 51, size=(3, hidden)).astype(np.float64)
+        vals[:, 0] = 60.0          # rows are never constant
+        def enc(v):
+            return to_array([encode_exact(Fraction(int(t)), dt) for t in v.reshape(-1)], dt).reshape(v.shape)
+        base, _, n64, _ = impl_ln(enc(vals), None, None, None, 0.0, dt)
+        for scale, shift in ((2, 0), (1, 64), (4, -32)):
+            y2, _, _, _ = impl_ln(enc(vals * scale + shift), None, None, None, 0.0, dt)
+            if not np.array_equal(bits_of(base, dt), bits_of(y2, dt)):
+                fails.append(f"ln invariance {dt} scale={scale} shift={shift}")
+        if n64 is None:
+            fails.append("ln: no fp64 normalised values")
+        else:
+            if not (np.all(np.abs(n64.mean(axis=1)) < 1e-12) and np.all(np.abs((n64 ** 2).mean(axis=1) - 1) < 1e-12)):
+                fails.append(f"ln moments {dt}")
+    return fails
+
+
+LN_PINS = [pin_ln_closed_forms, pin_ln_invariances, pin_ln_bruteforce]
+
+
 ALL_PINS = [pin_golden, pin_bruteforce, pin_constant_row, pin_scale_invariance,
             pin_unit_rms, pin_special_values, pin_single_element, pin_row_independence,
             pin_eps_dominated, pin_near_ties]

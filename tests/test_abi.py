@@ -15,7 +15,7 @@ HEADER = B.os.path.join(B.INCLUDE, "rmsnorm.h")
 def header_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(rmsnorm_\w+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b((?:rmsnorm|layernorm)_\w+)\s*\(", text)))
 
 
 def test_library_builds_and_loads():

@@ -120,3 +120,37 @@ def test_qk_pin_catches(mistake):
     impl = lambda x, qh, kh, hd, qw, kw, e, d, b: mutants.reference_qk(x, qh, kh, hd, qw, kw, e, d,
                                                                        weight_bias=b, mistake=mistake)
     assert pins.pin_qk_heads(impl) != []
+
+
+
+def oracle_impl_ln(x, w, b, residual, eps, dtype):
+    return oracle.layernorm(x, w=w, b=b, residual=residual, eps=eps, dtype=dtype, want_exact=True)
+
+
+@pytest.mark.parametrize("pin", pins.LN_PINS, ids=lambda p: p.__name__)
+def test_oracle_ln_pin(pin):
+    assert pin(oracle_impl_ln) == []
+
+
+def test_ln_restatement_passes_pins():
+    impl = lambda x, w, b, r, e, d: mutants.reference_ln(x, w, b, r, e, d)
+    for pin in pins.LN_PINS:
+        assert pin(impl) == [], pin.__name__
+
+
+@pytest.mark.parametrize("mistake", mutants.LN_MISTAKES)
+def test_ln_pins_catch_planted_mistake(mistake):
+    impl = lambda x, w, b, r, e, d: mutants.reference_ln(x, w, b, r, e, d, mistake=mistake)
+    caught = [p.__name__ for p in pins.LN_PINS if p(impl)]
+    assert caught, mistake
+
+
+def test_ln_oracle_matches_restatement_on_workload_shapes():
+    from row_reduction_norm_gb300 import workloads as W
+    for dt, h in (("bf16", 768), ("f32", 1024), ("bf16", 4096)):
+        x = W.to_numpy_bits(W.random_rows(dt, 64, h, seed=h, std=3.0))
+        wv = W.to_numpy_bits(W.random_rows(dt, 1, h, seed=h + 1).reshape(-1))
+        bv = W.to_numpy_bits(W.random_rows(dt, 1, h, seed=h + 2).reshape(-1))
+        y1 = oracle.layernorm(x, w=wv, b=bv, eps=1e-5, dtype=dt)[0]
+        y2 = mutants.reference_ln(x, wv, bv, None, 1e-5, dt)[0]
+        assert np.array_equal(pins.bits_of(y1, dt), pins.bits_of(y2, dt))
