@@ -209,6 +209,36 @@ int rmsnorm_qk_plan_for(const void *x, const void *y, int64_t tokens, int64_t x_
                         rmsnorm_plan_t *plan);
 
 /*
+ * RMSNorm with a block-scaled MXFP8 output (OCP Microscaling Formats v1.0:
+ * E4M3 elements, one E8M0 scale per 32 elements; block-scaled low-precision
+ * formats are named in "CuTeDSL at Perplexity", section "Blackwell
+ * support").  The op's fp32 values v_i = h_i * r * (w_i + weight_bias) (as
+ * rmsnorm_fwd_ex, before any rounding to the I/O type) are quantised in
+ * blocks of 32 consecutive elements of a row:
+ *   s       = floor(log2(max |v|)) - 8, clamped to [-127, 127] (-127 for a zero block)
+ *   scales  [rows, hidden / 32] bytes: E8M0 code s + 127
+ *   codes   [rows, hidden] bytes: E4M3 of v_i / 2^s, nearest-even, saturated at 448
+ * A block holding NaN or Inf is a NaN block (scale 0xFF, every code 0x7F).
+ * hidden must be a multiple of 32 and x, residual, w, codes and
+ * residual_out 16-byte aligned (else RMSNORM_EINVAL); hidden up to 32768
+ * (bf16) or 16384 (fp32), else RMSNORM_EUNSUPPORTED.  residual_out
+ * (required with a residual) receives h in the I/O type.  A code chosen by
+ * the kernel may differ from the correctly rounded one only when the exact
+ * value lies within the fp32 error of the op (about 1e-6 relative) of an
+ * E4M3 rounding midpoint, and likewise a scale when the block's maximum lies
+ * that close to a power of two.
+ */
+int rmsnorm_fwd_mxfp8(const void *x, const void *residual, const void *w, void *codes,
+                      void *scales, void *residual_out, int64_t rows, int64_t hidden,
+                      float eps, float weight_bias, int dtype, const rmsnorm_plan_t *plan,
+                      rmsnorm_stream_t stream);
+
+/* The plan rmsnorm_fwd_mxfp8 would use for these pointers on the current device. */
+int rmsnorm_mxfp8_plan_for(const void *x, const void *residual, const void *w,
+                           const void *codes, const void *scales, const void *residual_out,
+                           int64_t rows, int64_t hidden, int dtype, rmsnorm_plan_t *plan);
+
+/*
  * Fused row-wise LayerNorm ("GPT-2 on the GPU", section "The Whole Model as
  * One Kernel": mean, variance, (x - mean) / sqrt(var + eps), weight times the
  * normalised value plus bias):

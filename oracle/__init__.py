@@ -67,6 +67,13 @@ def _load():
             lib.oracle_layernorm_rows.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64,
                                                   ctypes.c_float, ctypes.c_int]
             lib.oracle_layernorm_rows.restype = ctypes.c_int
+            lib.oracle_rmsnorm_mxfp8_rows.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64,
+                                                      ctypes.c_float, ctypes.c_float, ctypes.c_int]
+            lib.oracle_rmsnorm_mxfp8_rows.restype = ctypes.c_int
+            lib.oracle_e4m3_from_double.argtypes = [vp, vp, i64]
+            lib.oracle_e4m3_from_double.restype = None
+            lib.oracle_double_from_e4m3.argtypes = [vp, vp, i64]
+            lib.oracle_double_from_e4m3.restype = None
             lib.oracle_bf16_from_double.argtypes = [vp, vp, i64]
             lib.oracle_bf16_from_double.restype = None
             lib.oracle_double_from_bf16.argtypes = [vp, vp, i64]
@@ -173,6 +180,62 @@ def layernorm(x, w=None, b=None, residual=None, eps: float = 1e-5, dtype: str = 
         with ThreadPoolExecutor(max_workers=threads) as ex:
             list(ex.map(lambda i: run(int(bounds[i]), int(bounds[i + 1])), range(threads)))
     return y, res_out, n64, y64
+
+
+def rmsnorm_mxfp8(x, w=None, residual=None, eps: float = 1e-6, dtype: str = "bf16", weight_bias: float = 0.0,
+                  threads: int = 1):
+    """Reference RMSNorm with MXFP8 output (E4M3 codes, one E8M0 scale per 32
+    elements of a row; see the C file for the exact rule).
+
+    Returns ``(codes, scales, residual_out, v_exact)``: uint8 codes [rows,
+    hidden], uint8 scales [rows, hidden/32], the rounded residual sum or None,
+    and the op's fp64 values before quantisation.
+    """
+    x = np.ascontiguousarray(x)
+    rows, hidden = x.shape
+    x = _check(x, "x", dtype, (rows, hidden))
+    residual = _check(residual, "residual", dtype, (rows, hidden))
+    w = _check(w, "w", dtype, (hidden,))
+    if hidden % 32:
+        raise ValueError("hidden must be a multiple of 32")
+    codes = np.empty((rows, hidden), dtype=np.uint8)
+    scales = np.empty((rows, hidden // 32), dtype=np.uint8)
+    res_out = None if residual is None else np.empty((rows, hidden), dtype=_NP_TYPE[dtype])
+    v64 = np.empty((rows, hidden), dtype=np.float64)
+    if rows == 0:
+        return codes, scales, res_out, v64
+    lib = _load()
+    args = (_ptr(x), _ptr(residual), _ptr(w), _ptr(codes), _ptr(scales), _ptr(v64), _ptr(res_out))
+
+    def run(lo, hi):
+        rc = lib.oracle_rmsnorm_mxfp8_rows(*args, lo, hi, hidden, float(eps), float(weight_bias), DTYPES[dtype])
+        if rc != 0:
+            raise ValueError("oracle rejected its arguments")
+
+    threads = max(1, min(int(threads), rows))
+    if threads == 1:
+        run(0, rows)
+    else:
+        bounds = np.linspace(0, rows, threads + 1).astype(np.int64)
+        with ThreadPoolExecutor(max_workers=threads) as ex:
+            list(ex.map(lambda i: run(int(bounds[i]), int(bounds[i + 1])), range(threads)))
+    return codes, scales, res_out, v64
+
+
+def e4m3_from_double(v) -> np.ndarray:
+    """Round fp64 values to E4M3 codes (nearest-even, saturated at 448)."""
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    out = np.empty(v.shape, dtype=np.uint8)
+    _load().oracle_e4m3_from_double(_ptr(v), _ptr(out), v.size)
+    return out
+
+
+def double_from_e4m3(c) -> np.ndarray:
+    """Decode E4M3 codes."""
+    c = np.ascontiguousarray(c, dtype=np.uint8)
+    out = np.empty(c.shape, dtype=np.float64)
+    _load().oracle_double_from_e4m3(_ptr(c), _ptr(out), c.size)
+    return out
 
 
 def rmsnorm_qk(x, q_heads: int, k_heads: int, head_dim: int, q_w=None, k_w=None, eps: float = 1e-6,

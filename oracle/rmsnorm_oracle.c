@@ -48,6 +48,7 @@
 #include <math.h>
 #include <stddef.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 enum { ORACLE_F32 = 0, ORACLE_BF16 = 1 };
@@ -119,6 +120,38 @@ static double row_input(const void *x, const void *residual, int64_t i, int dtyp
 }
 
 /*
+ * The op's fp64 values v_i (y_i before its rounding to the I/O type) for one
+ * row, and h written to residual_out when a residual is given.
+ */
+static void rms_row_values(const void *x, const void *residual, const void *w, int64_t row,
+                           int64_t hidden, double e, double b, int dtype, double *v,
+                           void *residual_out)
+{
+    const int64_t base = row * hidden;
+
+    /* square and sum */
+    double sum_sq = 0.0;
+    for (int64_t i = 0; i < hidden; ++i) {
+        double h = row_input(x, residual, base + i, dtype);
+        sum_sq += h * h;
+    }
+    /* divide by the count, add epsilon, inverse square root */
+    double mean_sq = sum_sq / (double)hidden;
+    double inv_rms = 1.0 / sqrt(mean_sq + e);
+
+    /* two multiplications */
+    for (int64_t i = 0; i < hidden; ++i) {
+        double h = row_input(x, residual, base + i, dtype);
+        double t = h * inv_rms;
+        if (w != NULL)
+            t = t * (load_elem(w, i, dtype) + b);
+        v[i] = t;
+        if (residual_out != NULL)
+            store_elem(residual_out, base + i, dtype, h);
+    }
+}
+
+/*
  * Rows [row_begin, row_end) of the op.
  *   x, residual, w : inputs in the I/O type (residual and w may be NULL)
  *   y              : output in the I/O type
@@ -141,35 +174,19 @@ int oracle_rmsnorm_rows(const void *x, const void *residual, const void *w,
         return -1;
     if (w == NULL && weight_bias != 0.0f)
         return -1;
-
-    const double e = (double)eps;
-    const double b = (double)weight_bias;
+    double *v = (double *)malloc((size_t)hidden * sizeof(double));
+    if (v == NULL)
+        return -1;
     for (int64_t row = row_begin; row < row_end; ++row) {
-        const int64_t base = row * hidden;
-
-        /* square and sum */
-        double sum_sq = 0.0;
+        rms_row_values(x, residual, w, row, hidden, (double)eps, (double)weight_bias, dtype, v,
+                       residual_out);
         for (int64_t i = 0; i < hidden; ++i) {
-            double h = row_input(x, residual, base + i, dtype);
-            sum_sq += h * h;
-        }
-        /* divide by the count, add epsilon, inverse square root */
-        double mean_sq = sum_sq / (double)hidden;
-        double inv_rms = 1.0 / sqrt(mean_sq + e);
-
-        /* two multiplications, then one rounding to the I/O type */
-        for (int64_t i = 0; i < hidden; ++i) {
-            double h = row_input(x, residual, base + i, dtype);
-            double v = h * inv_rms;
-            if (w != NULL)
-                v = v * (load_elem(w, i, dtype) + b);
             if (y_exact != NULL)
-                y_exact[base + i] = v;
-            store_elem(y, base + i, dtype, v);
-            if (residual_out != NULL)
-                store_elem(residual_out, base + i, dtype, h);
+                y_exact[row * hidden + i] = v[i];
+            store_elem(y, row * hidden + i, dtype, v[i]);   /* one rounding to the I/O type */
         }
     }
+    free(v);
     return 0;
 }
 
@@ -231,6 +248,130 @@ int oracle_layernorm_rows(const void *x, const void *residual, const void *w, co
         }
     }
     return 0;
+}
+
+/*
+ * FP8 E4M3 (OCP 8-bit floating point): 1 sign bit, 4 exponent bits (bias 7),
+ * 3 fraction bits; no infinities; S.1111.111 is NaN, so the largest finite
+ * magnitude is 1.75 * 2^8 = 448; subnormals have the fixed quantum 2^-9.
+ * Rounding to E4M3 here: round to nearest, ties to even, on 4 significant
+ * bits, then saturate magnitudes above 448 to 448 ("satfinite").
+ */
+static uint8_t double_to_e4m3_sat(double v)
+{
+    uint8_t sign = signbit(v) ? 0x80u : 0u;
+    if (isnan(v))
+        return (uint8_t)(sign | 0x7Fu);
+    double a = fabs(v);
+    if (a == 0.0)
+        return sign;
+    if (isinf(a))
+        return (uint8_t)(sign | 0x7Eu);
+    int e;
+    frexp(a, &e);                 /* a in [2^(e-1), 2^e)                     */
+    int q = e - 4;                /* 4 significant bits: quantum 2^(e-1-3)   */
+    if (q < -9)
+        q = -9;                   /* subnormal quantum                        */
+    double r = ldexp(nearbyint(ldexp(a, -q)), q);
+    if (r > 448.0)
+        r = 448.0;
+    /* encode r (exactly representable) */
+    if (r < ldexp(1.0, -6)) {                   /* subnormal: r = m * 2^-9   */
+        int m = (int)ldexp(r, 9);
+        return (uint8_t)(sign | (uint8_t)m);
+    }
+    int re;
+    double f = frexp(r, &re);                   /* r = f * 2^re, f in [0.5,1) */
+    int exp_field = re - 1 + 7;
+    int mant = (int)ldexp(f * 2.0 - 1.0, 3);    /* 3 fraction bits            */
+    return (uint8_t)(sign | (uint8_t)(exp_field << 3) | (uint8_t)mant);
+}
+
+static double e4m3_to_double(uint8_t c)
+{
+    double s = (c & 0x80u) ? -1.0 : 1.0;
+    int ef = (c >> 3) & 0xF;
+    int m = c & 0x7;
+    if (ef == 0xF && m == 0x7)
+        return NAN;
+    if (ef == 0)
+        return s * ldexp((double)m, -9);
+    return s * ldexp(1.0 + m / 8.0, ef - 7);
+}
+
+/*
+ * RMSNorm with MXFP8 output (OCP Microscaling Formats v1.0, MXFP8 with E4M3
+ * elements; block-scaled low-precision output is named in "CuTeDSL at
+ * Perplexity", section "Blackwell support").  The op's values v_i (y_i of
+ * oracle_rmsnorm_rows before its rounding, weight bias included) are grouped
+ * in blocks of 32 consecutive elements of a row.  For each block:
+ *   amax   = max_i |v_i|
+ *   s      = floor(log2(amax)) - 8, clamped to [-127, 127] (s = -127 when amax is 0)
+ *   scale  = E8M0 code s + 127
+ *   code_i = E4M3 of v_i / 2^s, nearest-even, saturated at 448
+ * A block holding a NaN or an infinity is a NaN block: scale 0xFF (the E8M0
+ * NaN) and every code 0x7F (the E4M3 NaN).
+ * hidden must be a multiple of 32.  codes [rows, hidden], scales [rows, hidden/32];
+ * v_exact (optional) receives the fp64 values.
+ */
+int oracle_rmsnorm_mxfp8_rows(const void *x, const void *residual, const void *w,
+                              uint8_t *codes, uint8_t *scales, double *v_exact, void *residual_out,
+                              int64_t row_begin, int64_t row_end, int64_t hidden,
+                              float eps, float weight_bias, int dtype)
+{
+    if (x == NULL || codes == NULL || scales == NULL || hidden <= 0 || hidden % 32 != 0)
+        return -1;
+    if (row_begin < 0 || row_end < row_begin || (dtype != ORACLE_F32 && dtype != ORACLE_BF16))
+        return -1;
+    if ((residual == NULL) != (residual_out == NULL) || (w == NULL && weight_bias != 0.0f))
+        return -1;
+    double *v = (double *)malloc((size_t)hidden * sizeof(double));
+    if (v == NULL)
+        return -1;
+    for (int64_t row = row_begin; row < row_end; ++row) {
+        rms_row_values(x, residual, w, row, hidden, (double)eps, (double)weight_bias, dtype, v,
+                       residual_out);
+        if (v_exact != NULL)
+            memcpy(v_exact + row * hidden, v, (size_t)hidden * sizeof(double));
+        for (int64_t k = 0; k < hidden / 32; ++k) {
+            const double *vb = v + k * 32;
+            double amax = 0.0;
+            int special = 0;
+            for (int j = 0; j < 32; ++j) {
+                if (isnan(vb[j]) || isinf(vb[j]))
+                    special = 1;
+                else if (fabs(vb[j]) > amax)
+                    amax = fabs(vb[j]);
+            }
+            int s = -127;
+            if (amax > 0.0) {
+                int e;
+                frexp(amax, &e);          /* amax in [2^(e-1), 2^e): floor(log2(amax)) = e - 1 */
+                s = (e - 1) - 8;          /* 8: exponent of the largest E4M3 value, 1.75 * 2^8  */
+                if (s < -127)
+                    s = -127;
+                if (s > 127)
+                    s = 127;
+            }
+            scales[row * (hidden / 32) + k] = special ? 0xFFu : (uint8_t)(s + 127);
+            for (int j = 0; j < 32; ++j)
+                codes[row * hidden + k * 32 + j] = special ? 0x7Fu : double_to_e4m3_sat(ldexp(vb[j], -s));
+        }
+    }
+    free(v);
+    return 0;
+}
+
+void oracle_e4m3_from_double(const double *v, uint8_t *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = double_to_e4m3_sat(v[i]);
+}
+
+void oracle_double_from_e4m3(const uint8_t *c, double *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = e4m3_to_double(c[i]);
 }
 
 /* Elementwise conversions, exposed so that tests can pin them on their own. */

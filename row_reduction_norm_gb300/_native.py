@@ -36,7 +36,8 @@ KERNEL_NAMES = {0: "reg", 1: "loop"}
 
 # Every symbol the header declares (checked by the CPU tests).
 EXPORTED = ["rmsnorm_fwd", "rmsnorm_plan", "rmsnorm_plan_for", "rmsnorm_fwd_plan", "rmsnorm_fwd_ex",
-            "rmsnorm_qk_fwd", "rmsnorm_qk_plan_for", "layernorm_fwd", "layernorm_plan_for",
+            "rmsnorm_qk_fwd", "rmsnorm_qk_plan_for", "rmsnorm_fwd_mxfp8", "rmsnorm_mxfp8_plan_for",
+            "layernorm_fwd", "layernorm_plan_for",
             "rmsnorm_max_hidden", "rmsnorm_reg_max_chunks", "rmsnorm_strerror", "rmsnorm_build_info"]
 
 
@@ -111,6 +112,11 @@ def load():
         lib.rmsnorm_qk_plan_for.argtypes = [vp, vp, i64, i64, i64, ctypes.c_int32, ctypes.c_int32, i64, vp, vp,
                                             i32, ctypes.POINTER(Plan)]
         lib.rmsnorm_qk_plan_for.restype = i32
+        lib.rmsnorm_fwd_mxfp8.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, ctypes.c_float, ctypes.c_float, i32,
+                                          ctypes.POINTER(Plan), vp]
+        lib.rmsnorm_fwd_mxfp8.restype = i32
+        lib.rmsnorm_mxfp8_plan_for.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i32, ctypes.POINTER(Plan)]
+        lib.rmsnorm_mxfp8_plan_for.restype = i32
         lib.layernorm_fwd.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, ctypes.c_float, i32,
                                       ctypes.POINTER(Plan), vp]
         lib.layernorm_fwd.restype = i32
@@ -190,6 +196,25 @@ def rmsnorm_qk_plan_for(x, y, tokens, x_token_stride, y_token_stride, q_heads, k
     p = Plan()
     _check(load().rmsnorm_qk_plan_for(x, y, tokens, x_token_stride, y_token_stride, q_heads, k_heads,
                                       head_dim, q_w, k_w, dtype, ctypes.byref(p)), "rmsnorm_qk_plan_for")
+    return p
+
+
+def rmsnorm_fwd_mxfp8(x, residual, w, codes, scales, residual_out, rows, hidden, eps, weight_bias, dtype,
+                      plan=None, stream=0):
+    _check(rmsnorm_fwd_mxfp8_status(x, residual, w, codes, scales, residual_out, rows, hidden, eps, weight_bias,
+                                    dtype, plan, stream), "rmsnorm_fwd_mxfp8")
+
+
+def rmsnorm_fwd_mxfp8_status(x, residual, w, codes, scales, residual_out, rows, hidden, eps, weight_bias, dtype,
+                             plan=None, stream=0) -> int:
+    return load().rmsnorm_fwd_mxfp8(x, residual, w, codes, scales, residual_out, rows, hidden, eps, weight_bias,
+                                    dtype, _plan_ref(plan), stream)
+
+
+def rmsnorm_mxfp8_plan_for(x, residual, w, codes, scales, residual_out, rows, hidden, dtype) -> Plan:
+    p = Plan()
+    _check(load().rmsnorm_mxfp8_plan_for(x, residual, w, codes, scales, residual_out, rows, hidden, dtype,
+                                         ctypes.byref(p)), "rmsnorm_mxfp8_plan_for")
     return p
 
 

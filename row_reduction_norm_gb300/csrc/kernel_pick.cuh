@@ -49,6 +49,48 @@ const void *reg_gt(int gt, int ch, int wm) {
     return nullptr;
 }
 
+// MXFP8 output (contiguous rows; at least 32 / V lanes per row).
+template <typename T, int GT, int CH, bool RES>
+const void *mx_wm(int wm) {
+    switch (wm) {
+        case kNoWeight: return reinterpret_cast<const void *>(&rms_reg_kernel<T, GT, CH, RES, kNoWeight, false, kOutMxfp8>);
+        case kWeight: return reinterpret_cast<const void *>(&rms_reg_kernel<T, GT, CH, RES, kWeight, false, kOutMxfp8>);
+        case kWeightBias:
+            return reinterpret_cast<const void *>(&rms_reg_kernel<T, GT, CH, RES, kWeightBias, false, kOutMxfp8>);
+        default: return nullptr;
+    }
+}
+
+template <typename T, int GT, bool RES>
+const void *mx_ch(int ch, int wm) {
+    if constexpr (GT < 32 / T::kVec) {
+        return nullptr;
+    } else {
+        switch (ch) {
+            case 1: return mx_wm<T, GT, 1, RES>(wm);
+            case 2: return mx_wm<T, GT, 2, RES>(wm);
+            case 4: return mx_wm<T, GT, 4, RES>(wm);
+            case 8: return mx_wm<T, GT, 8, RES>(wm);
+            default: return nullptr;
+        }
+    }
+}
+
+template <typename T, bool RES>
+const void *mx_gt(int gt, int ch, int wm) {
+    switch (gt) {
+        case 4: return mx_ch<T, 4, RES>(ch, wm);
+        case 8: return mx_ch<T, 8, RES>(ch, wm);
+        case 16: return mx_ch<T, 16, RES>(ch, wm);
+        case 32: return mx_ch<T, 32, RES>(ch, wm);
+        case 64: return mx_ch<T, 64, RES>(ch, wm);
+        case 128: return mx_ch<T, 128, RES>(ch, wm);
+        case 256: return mx_ch<T, 256, RES>(ch, wm);
+        case 512: return mx_ch<T, 512, RES>(ch, wm);
+        default: return nullptr;
+    }
+}
+
 template <typename T, int VE, int BLOCK, bool RES, bool HEADS>
 const void *loop_wm(int wm) {
     switch (wm) {

@@ -22,6 +22,17 @@ const void *reg_heads_bf16(int gt, int ch, int wm);
 const void *loop_contig(int dtype, int block, bool vec, bool res, int wm);
 const void *loop_heads(int dtype, int block, bool vec, int wm);
 
+// RMSNorm with MXFP8 output (contiguous rows, register kernel only).
+const void *mx_reg_f32_plain(int gt, int ch, int wm);
+const void *mx_reg_f32_res(int gt, int ch, int wm);
+const void *mx_reg_bf16_plain(int gt, int ch, int wm);
+const void *mx_reg_bf16_res(int gt, int ch, int wm);
+
+inline const void *mx_kernel(int dtype, int gt, int ch, bool res, int wm) {
+    if (dtype == 1) return res ? mx_reg_bf16_res(gt, ch, wm) : mx_reg_bf16_plain(gt, ch, wm);
+    return res ? mx_reg_f32_res(gt, ch, wm) : mx_reg_f32_plain(gt, ch, wm);
+}
+
 // LayerNorm (contiguous rows); aff: 0 none, 1 weight, 2 weight and bias.
 constexpr int kLnMaxGT = 256;
 const void *ln_reg_f32(int gt, int ch, bool res, int aff);

@@ -1,0 +1,9 @@
+// mx_reg_bf16_res.cu -- RMSNorm with MXFP8 output: register-kernel instantiations, bf16 I/O, fused residual add.
+#include "kernel_pick.cuh"
+#include "kernel_table.h"
+
+namespace rrn {
+
+const void *mx_reg_bf16_res(int gt, int ch, int wm) { return pick::mx_gt<BF16, true>(gt, ch, wm); }
+
+}  // namespace rrn

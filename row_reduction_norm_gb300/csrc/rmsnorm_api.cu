@@ -67,6 +67,8 @@ struct Op {
     bool head_rows = false;
     bool ln = false;           // LayerNorm instead of RMSNorm
     const void *b = nullptr;   // LayerNorm bias
+    bool mx = false;           // MXFP8 output: y holds E4M3 codes, scales the E8M0 scales
+    void *scales = nullptr;
     float eps = 0.f, w_bias = 0.f;
     int wm = 0;                // rrn::WeightMode (RMSNorm) or rrn::AffineMode (LayerNorm)
     int dtype = RMSNORM_BF16;
@@ -153,8 +155,15 @@ size_t dyn_smem_of(const rmsnorm_plan_t *p, const Op &o) {
     return (size_t)(o.row_elems / vec_elems_of(o.dtype)) * 16 * copies;
 }
 
+// Smallest row group of the MXFP8 form: the lanes of one 32-element block.
+int mx_min_gt(int dtype) { return 32 / vec_elems_of(dtype); }
+
 const void *kernel_of(const rmsnorm_plan_t *p, const Op &o) {
     const bool res = o.res != nullptr;
+    if (o.mx) {
+        if (p->kernel != RMSNORM_KERNEL_REG) return nullptr;
+        return rrn::mx_kernel(o.dtype, p->threads_per_row, p->chunks_per_thread, res, o.wm);
+    }
     if (o.ln) {
         if (p->kernel == RMSNORM_KERNEL_REG)
             return o.dtype == RMSNORM_BF16 ? rrn::ln_reg_bf16(p->threads_per_row, p->chunks_per_thread, res, o.wm)
@@ -177,6 +186,7 @@ int validate_plan(const rmsnorm_plan_t *p, const Op &o, int vec_ok) {
         const int max_gt = max_threads_per_row(o);
         if (!vec_ok || p->vec_elems != V) return RMSNORM_EINVAL;
         if (gt < 4 || gt > max_gt || (gt & (gt - 1)) != 0) return RMSNORM_EINVAL;
+        if (o.mx && gt < mx_min_gt(o.dtype)) return RMSNORM_EINVAL;
         if (ch < 1 || ch > rrn::kRegMaxCH || (ch & (ch - 1)) != 0) return RMSNORM_EINVAL;
         if ((int64_t)gt * ch * V < o.row_elems) return RMSNORM_EINVAL;
         if (p->block_threads != rrn::reg_block_threads(gt)) return RMSNORM_EINVAL;
@@ -184,6 +194,7 @@ int validate_plan(const rmsnorm_plan_t *p, const Op &o, int vec_ok) {
         return RMSNORM_OK;
     }
     if (p->kernel == RMSNORM_KERNEL_LOOP) {
+        if (o.mx) return RMSNORM_EINVAL;   // the MXFP8 form runs on the register kernel only
         if (p->vec_elems != 1 && !(p->vec_elems == V && vec_ok)) return RMSNORM_EINVAL;
         bool known = false;
         for (int b : rrn::kLoopBlocks) known = known || (b == p->block_threads);
@@ -269,6 +280,18 @@ int blocks_per_sm_of(int dev, const void *fn, int block, size_t smem, int *out) 
 // Full device-side planning for an op.
 int plan_for_device(const Op &o, rmsnorm_plan_t *plan, int *dev_out) {
     schedule(o.row_elems, o.dtype, vec_ok_of(o), max_threads_per_row(o), plan);
+    if (o.mx) {
+        if (plan->kernel != RMSNORM_KERNEL_REG) return RMSNORM_EUNSUPPORTED;
+        const int V = vec_elems_of(o.dtype);
+        while (plan->threads_per_row < mx_min_gt(o.dtype)) plan->threads_per_row <<= 1;
+        int64_t need = ceil_div(o.row_elems / V, plan->threads_per_row);
+        int ch = 1;
+        while (ch < need) ch <<= 1;
+        plan->chunks_per_thread = ch;
+        plan->block_threads = rrn::reg_block_threads(plan->threads_per_row);
+        plan->rows_per_block = plan->block_threads / plan->threads_per_row;
+        plan->regime = plan->threads_per_row <= 32 ? RMSNORM_REGIME_WARP : RMSNORM_REGIME_CTA;
+    }
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return RMSNORM_ECUDA;
     int sms = 0;
@@ -331,6 +354,7 @@ int launch(const Op &o, const rmsnorm_plan_t *plan, int dev, rmsnorm_stream_t st
     args.hidden_f = (float)o.row_elems;
     args.eps = o.eps;
     args.w_bias = o.w_bias;
+    args.scales = o.scales;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -439,6 +463,19 @@ int make_heads(const void *x, void *y, int64_t tokens, int64_t x_token_stride, i
     return RMSNORM_OK;
 }
 
+int make_mx(const void *x, const void *residual, const void *w, void *codes, void *scales, void *residual_out,
+            int64_t rows, int64_t hidden, float eps, float w_bias, int dtype, Op *o) {
+    int st = make_contig(x, residual, w, codes, residual_out, rows, hidden, eps, w_bias, dtype, o);
+    if (st != RMSNORM_OK) return st;
+    if (hidden % 32 != 0) return RMSNORM_EINVAL;
+    if (rows > 0 && scales == nullptr) return RMSNORM_EINVAL;
+    o->mx = true;
+    o->scales = scales;
+    // the codes are bytes: their row stride is hidden bytes, which the register
+    // kernel derives from row_elems; y_stride (in elements of T) is unused
+    return RMSNORM_OK;
+}
+
 int make_ln(const void *x, const void *residual, const void *w, const void *b, void *y, void *residual_out,
             int64_t rows, int64_t hidden, float eps, int dtype, Op *o) {
     int st = make_contig(x, residual, w, y, residual_out, rows, hidden, eps, 0.f, dtype, o);
@@ -453,6 +490,28 @@ int make_ln(const void *x, const void *residual, const void *w, const void *b, v
 }  // namespace
 
 extern "C" {
+
+int rmsnorm_fwd_mxfp8(const void *x, const void *residual, const void *w, void *codes, void *scales,
+                      void *residual_out, int64_t rows, int64_t hidden, float eps, float weight_bias, int dtype,
+                      const rmsnorm_plan_t *plan, rmsnorm_stream_t stream) {
+    Op o;
+    int st = make_mx(x, residual, w, codes, scales, residual_out, rows, hidden, eps, weight_bias, dtype, &o);
+    if (st != RMSNORM_OK) return st;
+    if (rows > 0 && !vec_ok_of(o)) return RMSNORM_EINVAL;   // 16-byte aligned rows required
+    return run(o, plan, stream);
+}
+
+int rmsnorm_mxfp8_plan_for(const void *x, const void *residual, const void *w, const void *codes,
+                           const void *scales, const void *residual_out, int64_t rows, int64_t hidden, int dtype,
+                           rmsnorm_plan_t *plan) {
+    if (plan == nullptr) return RMSNORM_EINVAL;
+    Op o;
+    int st = make_mx(x, residual, w, const_cast<void *>(codes), const_cast<void *>(scales),
+                     const_cast<void *>(residual_out), rows, hidden, 0.f, 0.f, dtype, &o);
+    if (st != RMSNORM_OK) return st;
+    if (!elem_aligned(o) || !vec_ok_of(o)) return RMSNORM_EINVAL;
+    return plan_for_device(o, plan, nullptr);
+}
 
 int layernorm_fwd(const void *x, const void *residual, const void *w, const void *b, void *y, void *residual_out,
                   int64_t rows, int64_t hidden, float eps, int dtype, const rmsnorm_plan_t *plan,

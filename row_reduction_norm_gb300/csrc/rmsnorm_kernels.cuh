@@ -41,6 +41,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -71,7 +72,12 @@ struct Params {
     float hidden_f;      // row_elems as float (exact for row_elems <= 2^24)
     float eps;
     float w_bias;        // added to every weight element (weight mode kWeightBias)
+    void *scales;        // MXFP8 output: E8M0 scales [rows, row_elems / 32] (y holds the codes)
 };
+
+// Output form of the register kernel: the I/O type, or MXFP8 (E4M3 codes in
+// y, one E8M0 scale per 32 elements in scales).
+enum OutputMode { kOutT = 0, kOutMxfp8 = 1 };
 
 // How the weight enters y: none, w, or (w + w_bias).
 enum WeightMode { kNoWeight = 0, kWeight = 1, kWeightBias = 2 };
@@ -233,11 +239,42 @@ __device__ __forceinline__ float tree_sum(float (&v)[N]) {
 
 // ------------------------------------------------------- register kernel
 
-template <typename T, int GT, int CH, bool RES, int WM, bool HEADS>
+// MXFP8 (OCP Microscaling v1.0, E4M3 elements): a block of 32 consecutive
+// elements of a row shares the scale 2^s, s = floor(log2(amax)) - 8 clamped
+// to [-127, 127] (-127 for an all-zero block); elements are E4M3 of v / 2^s,
+// nearest-even, saturated at 448.  A block holding NaN or Inf is all NaN
+// (scale 0xFF, codes 0x7F).  With the row's chunk c*GT + t owned by thread
+// t, the 32 elements of a block sit in LPB = 32 / V consecutive lanes, which
+// combine their maxima with xor shuffles.
+template <int LPB>
+__device__ __forceinline__ void mx_block_stats(float &amax, bool &special) {
+    unsigned sp = special ? 1u : 0u;
+#pragma unroll
+    for (int off = LPB / 2; off > 0; off >>= 1) {
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+        sp |= __shfl_xor_sync(0xffffffffu, sp, off);
+    }
+    special = sp != 0u;
+}
+
+// E8M0 exponent of a block from its (finite, non-negative) amax.
+__device__ __forceinline__ int mx_scale_exponent(float amax) {
+    const int ef = (__float_as_int(amax) >> 23) & 0xFF;   // 0: zero or subnormal
+    const int s = ef == 0 ? -127 : ef - 127 - 8;
+    return s < -127 ? -127 : s;
+}
+
+__device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
+    return (uint16_t)__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
+}
+
+template <typename T, int GT, int CH, bool RES, int WM, bool HEADS, int OUT = kOutT>
 __global__ void __launch_bounds__(reg_block_threads(GT))
 rms_reg_kernel(const Params p) {
     constexpr bool W = WM != kNoWeight;
     static_assert(!(HEADS && RES), "head rows take no residual");
+    static_assert(OUT == kOutT || (!HEADS && GT >= 32 / T::kVec), "MXFP8 output: contiguous rows, "
+                                                                  "a block's lanes in one row group");
     constexpr int V = T::kVec;
     constexpr int BLOCK = reg_block_threads(GT);
     constexpr int RPB = BLOCK / GT;               // rows per block iteration
@@ -343,6 +380,56 @@ rms_reg_kernel(const Params p) {
         }
         // A6: the row's scale
         const float r = rsqrtf(sum / p.hidden_f + p.eps);
+        // A7 (MXFP8 form): values, block scale, E4M3 codes
+        if constexpr (OUT == kOutMxfp8) {
+            constexpr int LPB = 32 / V;
+#pragma unroll
+            for (int c = 0; c < CH; ++c) {
+                const int u = c * GT + t;
+                const bool valid = row_ok && u < nch;     // uniform over a block's lanes
+                float a[V];
+                unpack(hc[c], a, T{});
+                float wv[V];
+                if constexpr (W) {
+                    unpack(w_smem[valid ? u : 0], wv, T{});
+                } else {
+#pragma unroll
+                    for (int e = 0; e < V; ++e) wv[e] = 1.f;
+                }
+                float amax = 0.f;
+                bool special = false;
+#pragma unroll
+                for (int e = 0; e < V; ++e) {
+                    a[e] = scale_out<WM>(a[e], r, wv[e], p.w_bias);
+                    const float m = fabsf(a[e]);
+                    special |= !(m <= 3.402823466e38f);     // NaN or Inf
+                    amax = fmaxf(amax, m);
+                }
+                mx_block_stats<LPB>(amax, special);
+                const int s = mx_scale_exponent(amax);
+                const float mult = __int_as_float((127 - s) << 23);   // 2^-s, a normal float
+                uint32_t q[V / 4];
+#pragma unroll
+                for (int k = 0; k < V / 4; ++k) {
+                    const uint32_t lo = e4m3x2(a[4 * k] * mult, a[4 * k + 1] * mult);
+                    const uint32_t hi = e4m3x2(a[4 * k + 2] * mult, a[4 * k + 3] * mult);
+                    q[k] = special ? 0x7F7F7F7Fu : (lo | (hi << 16));
+                }
+                if (valid) {
+                    char *dst = static_cast<char *>(p.y) + row * p.row_elems + (int64_t)u * V;
+                    if constexpr (V == 8) {
+                        asm volatile("st.global.v2.u32 [%0], {%1, %2};" : : "l"(dst), "r"(q[0]), "r"(q[1]) : "memory");
+                    } else {
+                        asm volatile("st.global.u32 [%0], %1;" : : "l"(dst), "r"(q[0]) : "memory");
+                    }
+                    if (t % LPB == 0) {
+                        const uint8_t sc = special ? (uint8_t)0xFF : (uint8_t)(s + 127);
+                        static_cast<uint8_t *>(p.scales)[row * (p.row_elems / 32) + u / LPB] = sc;
+                    }
+                }
+            }
+            continue;
+        }
         // A7: y = RN_T(h * r * w)   (or h * r, or h * r * (w + bias))
 #pragma unroll
         for (int c = 0; c < CH; ++c) {

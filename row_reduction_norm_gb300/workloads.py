@@ -243,3 +243,24 @@ def make_ln_inputs(wl: Workload, seed: int = 0, device="cpu", rows: Optional[int
         b = torch.randn((wl.hidden,), generator=_gen(dev, seed + 5), device=dev,
                         dtype=torch.float32).mul_(wl.b_std).to(TORCH_DTYPE[wl.dtype])
     return x, r, w, b
+
+
+# RMSNorm with MXFP8 output (E4M3 codes + one E8M0 scale per 32 elements):
+# the Llama-3.2-1B-width residual case and the 65536 x 8192 bandwidth case.
+MX_WORKLOADS = {
+    w.name: w
+    for w in [
+        Workload("mx_bf16_res_16384x2048", "bf16", 16384, 2048, 1e-5, 0.5, 1.0, 0.05,
+                 note="fused residual add, MXFP8 output"),
+        Workload("mx_bf16_res_65536x8192_w", "bf16", 65536, 8192, 1e-6, 1.0, 1.0, 0.1,
+                 outlier_frac=1e-3, outlier_scale=100.0, note="bandwidth case, MXFP8 output"),
+    ]
+}
+
+
+def mx_algorithmic_bytes(wl: Workload) -> int:
+    """Read x (+ residual), write the codes (1 byte an element) and scales (1 per
+    32) (+ residual_out), read w once."""
+    e = wl.rows * wl.hidden
+    b = e * wl.elem_bytes * (1 + (2 if wl.has_res else 0)) + e + e // 32
+    return b + (wl.hidden * wl.elem_bytes if wl.has_w else 0)

@@ -218,3 +218,78 @@ def layernorm_row_exact(x, w, b, residual, eps_value: Fraction, fmt: str, want_t
     if want_terms:
         return out, h_bits, terms
     return out, h_bits
+
+
+
+# ---------------------------------------------------------------- E4M3, MXFP8
+# FP8 E4M3 (OCP): 4 exponent bits (bias 7), 3 fraction bits, no infinities,
+# S.1111.111 is NaN, largest finite 448, subnormal quantum 2^-9.
+
+def e4m3_decode(code: int):
+    """Exact value of an E4M3 code (None for NaN)."""
+    sign = -1 if code & 0x80 else 1
+    ef = (code >> 3) & 0xF
+    m = code & 0x7
+    if ef == 0xF and m == 0x7:
+        return None
+    if ef == 0:
+        return sign * Fraction(m, 8) * Fraction(1, 64)
+    return sign * (1 + Fraction(m, 8)) * Fraction(2) ** (ef - 7)
+
+
+def e4m3_round_sqrt_sat(sign: int, q: Fraction) -> int:
+    """E4M3 code of sign*sqrt(q): nearest, ties to even, magnitudes above 448 -> 448."""
+    sign_bit = 0x80 if sign < 0 else 0
+    if q == 0:
+        return sign_bit
+    if q >= 448 * 448:
+        return sign_bit | 0x7E
+    lo, hi = 0, 0x7E          # positive codes are ordered by value
+    while hi - lo > 1:
+        mid = (lo + hi) // 2
+        if e4m3_decode(mid) ** 2 <= q:
+            lo = mid
+        else:
+            hi = mid
+    if e4m3_decode(hi) ** 2 <= q:
+        lo = hi
+    if lo == 0x7E:
+        return sign_bit | 0x7E
+    a, b = e4m3_decode(lo), e4m3_decode(lo + 1)
+    m2 = ((a + b) / 2) ** 2
+    k = lo if q < m2 else lo + 1 if q > m2 else (lo if lo % 2 == 0 else lo + 1)
+    return sign_bit | k
+
+
+def floor_log2_sqrt(q: Fraction) -> int:
+    """floor(log2(sqrt(q))) for q > 0, exactly."""
+    e = 0
+    while Fraction(4) ** e > q:
+        e -= 1
+    while Fraction(4) ** (e + 1) <= q:
+        e += 1
+    return e
+
+
+def mxfp8_row_exact(x, w, residual, eps_value: Fraction, fmt: str, weight_bias: Fraction = Fraction(0)):
+    """Exact MXFP8 codes and E8M0 scales of one row (hidden a multiple of 32)."""
+    n = len(x)
+    xs = [decode(b, fmt) for b in x]
+    if residual is not None:
+        rs = [decode(b, fmt) for b in residual]
+        hs = [decode(round_value(a + b, fmt), fmt) for a, b in zip(xs, rs)]
+    else:
+        hs = xs
+    ws = [decode(b, fmt) + weight_bias for b in w] if w is not None else [Fraction(1)] * n
+    denom = sum(h * h for h in hs) / n + eps_value
+    codes, scales, qs = [], [], []
+    for k in range(n // 32):
+        ps = [hs[i] * ws[i] for i in range(32 * k, 32 * k + 32)]
+        q_block = [p * p / denom for p in ps]        # v_i^2
+        amax2 = max(q_block)
+        s = -127 if amax2 == 0 else max(-127, min(127, floor_log2_sqrt(amax2) - 8))
+        scales.append(s + 127)
+        for p, q in zip(ps, q_block):
+            codes.append(e4m3_round_sqrt_sat(-1 if p < 0 else 1, q * Fraction(4) ** (-s)))
+            qs.append(q * Fraction(4) ** (-s))
+    return codes, scales, qs

@@ -180,3 +180,56 @@ def reference_ln(x, w, b, residual, eps, dt, mistake=None):
                 y = wv * nrm
     out = _encode(_round(y, dt), dt)
     return out, (None if h_store is None else _encode(h_store, dt)), nrm, y
+
+
+MX_MISTAKES = ["scale_without_offset", "scale_ceil", "no_saturation", "blocks_of_16", "truncate_codes",
+               "ties_away_codes", "scale_off_by_one"]
+
+
+def _e4m3(v, mode="rne", saturate=True):
+    """Numpy E4M3 encoder (values -> codes) with a selectable rounding rule."""
+    v = np.asarray(v, dtype=np.float64)
+    sign = np.where(np.signbit(v), 0x80, 0).astype(np.uint8)
+    a = np.abs(v)
+    with np.errstate(invalid="ignore", divide="ignore", over="ignore"):
+        _, e = np.frexp(np.where(a > 0, a, 1.0))
+        q = np.maximum(e - 4, -9)
+        s = np.ldexp(a, -q)
+        n = np.rint(s) if mode == "rne" else np.floor(s) if mode == "trunc" else np.floor(s + 0.5)
+        r = np.ldexp(n, q)
+    over = r > 448.0
+    r = np.where(over, 448.0, r)
+    codes = np.zeros(v.shape, dtype=np.uint8)
+    sub = r < 2.0 ** -6
+    codes = np.where(sub, np.ldexp(r, 9).astype(np.int64), 0)
+    _, re_ = np.frexp(np.where(r > 0, r, 1.0))
+    f = np.ldexp(r, -(re_ - 1)) - 1.0
+    norm = ((re_ - 1 + 7) << 3) | np.rint(f * 8).astype(np.int64)
+    codes = np.where(sub, codes, norm).astype(np.uint8)
+    if not saturate:
+        codes = np.where(over, 0x7F, codes).astype(np.uint8)
+    return (codes | sign).astype(np.uint8)
+
+
+def reference_mx(x, w, residual, eps, dt, weight_bias=0.0, mistake=None):
+    """Numpy MXFP8 RMSNorm on top of ``reference`` (fp64 values), with planted mistakes."""
+    _, h_out, v = reference(x, w, residual, eps, dt, weight_bias=weight_bias)
+    rows, hidden = v.shape
+    blk = 16 if mistake == "blocks_of_16" else 32
+    vb = v.reshape(rows, hidden // blk, blk)
+    amax = np.abs(vb).max(axis=2)
+    with np.errstate(divide="ignore"):
+        lg = np.log2(np.where(amax > 0, amax, 1.0))
+    e = np.ceil(lg) if mistake == "scale_ceil" else np.floor(lg)
+    off = 0 if mistake == "scale_without_offset" else 8
+    s = np.where(amax > 0, e - off, -127)
+    if mistake == "scale_off_by_one":
+        s = s + 1
+    s = np.clip(s, -127, 127).astype(np.int64)
+    scaled = vb * np.ldexp(1.0, -s)[:, :, None]
+    mode = {"truncate_codes": "trunc", "ties_away_codes": "away"}.get(mistake, "rne")
+    codes = _e4m3(scaled, mode=mode, saturate=mistake != "no_saturation").reshape(rows, hidden)
+    scales = (s + 127).astype(np.uint8)
+    if blk == 16:
+        scales = scales[:, ::2]
+    return codes, scales, h_out, v

@@ -112,3 +112,62 @@ def compare_ln(got, y64, n64, w, b, mean_abs_h, sigma, dtype):
     ratio = float((err / np.where(lim > 0, lim, 1)).max()) if err.size else 0.0
     return nan_ok and not bad.any(), {"worst_err_over_bound": ratio, "n_bad": int(bad.sum()), "nan_ok": nan_ok,
                                       "n": int(err.size)}
+
+
+# MXFP8: integers (E4M3 codes, E8M0 scales) decided by floating point.  The
+# kernel decides them from its fp32 values of the op, which are within
+# MX_REL_TOL (the fp32 bound derived above) of the exact values; a code or a
+# scale may therefore differ from the oracle's only where the exact value lies
+# that close to the decision boundary.  Everything else must match exactly.
+MX_REL_TOL = 2e-6
+
+
+def _e4m3_values(codes):
+    c = np.asarray(codes, dtype=np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    ef = (c >> 3) & 0xF
+    m = c & 0x7
+    val = np.where(ef == 0, m / 8.0 * 2.0 ** -6, (1 + m / 8.0) * np.ldexp(1.0, ef - 7))
+    return np.where((ef == 0xF) & (m == 0x7), np.nan, sign * val)
+
+
+def compare_mx(codes_g, scales_g, codes_o, scales_o, v64, e4m3_encode):
+    """Check GPU MXFP8 output against the oracle's; ``e4m3_encode`` is the
+    oracle's encoder (used to re-derive the codes under an alternative scale)."""
+    codes_g = np.asarray(codes_g)
+    rows, hidden = codes_g.shape
+    nb = hidden // 32
+    vb = v64.reshape(rows, nb, 32)
+    special = ~np.isfinite(vb).all(axis=2)
+    amax = np.where(special, 0.0, np.abs(np.where(np.isfinite(vb), vb, 0.0)).max(axis=2))
+    sg = np.asarray(scales_g).astype(np.int64)
+    so = np.asarray(scales_o).astype(np.int64)
+    report = {"scale_flips": 0, "code_flips": 0, "bad": 0}
+    # scales: equal, or amax within tolerance of the power of two between them
+    diff = sg != so
+    if diff.any():
+        with np.errstate(divide="ignore"):
+            lg = np.log2(np.where(amax > 0, amax, 1.0))
+        near = np.abs(lg - np.round(lg)) < MX_REL_TOL * 1.45
+        ok_flip = diff & ~special & (np.abs(sg - so) == 1) & near
+        report["scale_flips"] = int(ok_flip.sum())
+        if (diff & ~ok_flip).any():
+            report["bad"] += int((diff & ~ok_flip).sum())
+            return False, report
+    # expected codes under the GPU's scales
+    scaled = vb * np.ldexp(1.0, -(sg - 127))[:, :, None]
+    want = e4m3_encode(np.where(np.isfinite(scaled), scaled, 0.0)).reshape(rows, nb, 32)
+    want = np.where(special[:, :, None], 0x7F, want)
+    got = codes_g.reshape(rows, nb, 32).astype(np.int64)
+    mism = got != want
+    if mism.any():
+        vg = _e4m3_values(got)
+        vw = _e4m3_values(want)
+        mid = (vg + vw) / 2
+        adjacent = np.abs((got & 0x7F) - (want & 0x7F)) == 1
+        near = np.abs(scaled - mid) <= MX_REL_TOL * np.abs(scaled)
+        sat = (np.abs(scaled) > 448.0) & ((got & 0x7F) == 0x7E)      # saturated either way
+        ok = mism & ((adjacent & near) | sat)
+        report["code_flips"] = int(ok.sum())
+        report["bad"] += int((mism & ~ok).sum())
+    return report["bad"] == 0, report

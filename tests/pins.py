@@ -537,6 +537,120 @@ def pin_ln_invariances(impl_ln):
 LN_PINS = [pin_ln_closed_forms, pin_ln_invariances, pin_ln_bruteforce]
 
 
+# ----------------------------------------------------------------- MXFP8 pins
+# impl_mx(x, w, residual, eps, dtype, weight_bias) -> (codes, scales, residual_out, v_exact)
+# e4m3(v) -> codes ; e4m3_inv(codes) -> values.  Format: OCP FP8 E4M3 and MX v1.0.
+
+def pin_e4m3_codec(e4m3, e4m3_inv):
+    """Every code decodes to the value its bit fields define; every finite
+    code encodes back to itself; the table's landmarks (448, 2^-6, 2^-9, 1, NaN)."""
+    fails = []
+    codes = np.arange(256, dtype=np.uint8)
+    vals = e4m3_inv(codes)
+    for c in range(256):
+        want = exact.e4m3_decode(c)
+        got = vals[c]
+        if want is None:
+            if not np.isnan(got):
+                fails.append(f"e4m3 {c:#x} should be NaN")
+        elif Fraction(float(got)) != want:
+            fails.append(f"e4m3 {c:#x}: {got} != {float(want)}")
+    finite = [c for c in range(256) if exact.e4m3_decode(c) is not None]
+    back = e4m3(vals[finite])
+    for c, b in zip(finite, back):
+        if c != 0x80 and int(b) != c:
+            fails.append(f"e4m3 round trip {c:#x} -> {int(b):#x}")
+    for c, v in ((0x7E, 448.0), (0x08, 2.0 ** -6), (0x01, 2.0 ** -9), (0x38, 1.0), (0x40, 2.0)):
+        if vals[c] != v:
+            fails.append(f"e4m3 landmark {c:#x}")
+    return fails
+
+
+def pin_e4m3_rounding(e4m3):
+    """Midpoints between adjacent codes round to the even code; values just
+    off a midpoint round to the nearer one; magnitudes above 448 saturate."""
+    fails = []
+    pts, want = [], []
+    for c in range(0x00, 0x7E):
+        a, b = exact.e4m3_decode(c), exact.e4m3_decode(c + 1)
+        m = (a + b) / 2
+        pts += [float(m), float(m) * (1 - 2 ** -40), float(m) * (1 + 2 ** -40)]
+        want += [c if c % 2 == 0 else c + 1, c, c + 1]
+    pts += [448.0, 463.9, 464.0, 500.0, 1e30, -1e30]
+    want += [0x7E, 0x7E, 0x7E, 0x7E, 0x7E, 0xFE]
+    got = e4m3(np.array(pts, dtype=np.float64))
+    for p, w_, g in zip(pts, want, got):
+        if int(g) != w_:
+            fails.append(f"e4m3({p!r}) = {int(g):#x}, want {w_:#x}")
+    return fails
+
+
+def pin_mx_bruteforce(impl_mx, n_cases=24, seed=909):
+    """Random rows of 32 or 64 elements: codes and scales equal the exact
+    rational answer (except values within 2^-44 of an E4M3 rounding midpoint)."""
+    rng = np.random.default_rng(seed)
+    fails = []
+    for k in range(n_cases):
+        dt = ("bf16", "f32")[k % 2]
+        hidden = (32, 64)[(k // 2) % 2]
+        has_w = bool((k // 4) % 2)
+        has_res = bool((k // 8) % 2)
+        b = (0.0, 1.0)[(k // 3) % 2] if has_w else 0.0
+        eps = (0.0, 1e-6, 0.5)[k % 3]
+        rows = 2
+        lo_e, hi_e = ((-20, 20) if k % 5 == 0 else (-4, 4))     # some rows with a wide dynamic range
+        xb = [random_bits(rng, dt, hidden, lo_e, hi_e) for _ in range(rows)]
+        rb = [random_bits(rng, dt, hidden, -4, 4) for _ in range(rows)] if has_res else None
+        wb = random_bits(rng, dt, hidden, -2, 2) if has_w else None
+        x = to_array(sum(xb, []), dt).reshape(rows, hidden)
+        res = to_array(sum(rb, []), dt).reshape(rows, hidden) if has_res else None
+        w = to_array(wb, dt) if has_w else None
+        codes, scales, _, _ = impl_mx(x, w, res, eps, dt, b)
+        for r in range(rows):
+            wc, ws, qs = exact.mxfp8_row_exact(xb[r], wb, rb[r] if has_res else None, f32_exact(eps), dt,
+                                              Fraction(b))
+            if [int(v) for v in scales[r]] != ws:
+                fails.append(f"mx case {k} row {r}: scales {list(scales[r])} != {ws}")
+                continue
+            for i in range(hidden):
+                if int(codes[r, i]) != wc[i]:
+                    a, c2 = exact.e4m3_decode(int(codes[r, i]) & 0x7F), exact.e4m3_decode(wc[i] & 0x7F)
+                    near = False
+                    if a is not None and c2 is not None:
+                        m2 = ((a + c2) / 2) ** 2
+                        near = m2 > 0 and abs(qs[i] - m2) / m2 < Fraction(1, 2 ** 43)
+                    if not near:
+                        fails.append(f"mx case {k} ({dt}, H={hidden}) row {r} elem {i}: "
+                                     f"{int(codes[r, i]):#x} != {wc[i]:#x}")
+    return fails
+
+
+def pin_mx_closed_forms(impl_mx):
+    """A constant row with eps = 0 and no weight normalises to +-1 exactly:
+    amax 1, scale 2^(0-8) (E8M0 code 119), every code E4M3(256) = 0x78 (sign
+    kept).  Scaling a row by 2^k leaves codes and scales unchanged (eps = 0)."""
+    fails = []
+    for dt in ("bf16", "f32"):
+        c = encode_exact(Fraction(-3, 2), dt)
+        x = to_array([c] * 64, dt).reshape(1, 64)
+        codes, scales, _, _ = impl_mx(x, None, None, 0.0, dt, 0.0)
+        if [int(v) for v in scales[0]] != [119, 119] or any(int(v) != 0xF8 for v in codes[0]):
+            fails.append(f"mx constant row {dt}: scales {list(scales[0])} codes {set(int(v) for v in codes[0])}")
+        rng = np.random.default_rng(3)
+        xb = random_bits(rng, dt, 64, -3, 3)
+        x1 = to_array(xb, dt).reshape(1, 64)
+        c1, s1, _, _ = impl_mx(x1, None, None, 0.0, dt, 0.0)
+        xs = (x1.astype(np.float32) * np.float32(8.0)) if dt == "f32" else \
+            ((((x1.astype(np.uint32) << 16).view(np.float32) * np.float32(8.0)).view(np.uint32)) >> 16).astype(np.uint16)
+        c2, s2, _, _ = impl_mx(xs, None, None, 0.0, dt, 0.0)
+        if not (np.array_equal(c1, c2) and np.array_equal(s1, s2)):
+            fails.append(f"mx scale invariance {dt}")
+    return fails
+
+
+MX_PINS = [pin_mx_closed_forms, pin_mx_bruteforce]
+
+
 ALL_PINS = [pin_golden, pin_bruteforce, pin_constant_row, pin_scale_invariance,
             pin_unit_rms, pin_special_values, pin_single_element, pin_row_independence,
             pin_eps_dominated, pin_near_ties]

@@ -154,3 +154,63 @@ def test_ln_oracle_matches_restatement_on_workload_shapes():
         y1 = oracle.layernorm(x, w=wv, b=bv, eps=1e-5, dtype=dt)[0]
         y2 = mutants.reference_ln(x, wv, bv, None, 1e-5, dt)[0]
         assert np.array_equal(pins.bits_of(y1, dt), pins.bits_of(y2, dt))
+
+
+
+def oracle_impl_mx(x, w, residual, eps, dtype, weight_bias):
+    return oracle.rmsnorm_mxfp8(x, w=w, residual=residual, eps=eps, dtype=dtype, weight_bias=weight_bias)
+
+
+def test_oracle_e4m3_codec_and_rounding():
+    assert pins.pin_e4m3_codec(oracle.e4m3_from_double, oracle.double_from_e4m3) == []
+    assert pins.pin_e4m3_rounding(oracle.e4m3_from_double) == []
+
+
+@pytest.mark.parametrize("pin", pins.MX_PINS, ids=lambda p: p.__name__)
+def test_oracle_mx_pin(pin):
+    assert pin(oracle_impl_mx) == []
+
+
+def test_mx_restatement_passes_pins_and_matches_oracle():
+    impl = lambda x, w, r, e, d, b: mutants.reference_mx(x, w, r, e, d, weight_bias=b)
+    for pin in pins.MX_PINS:
+        assert pin(impl) == [], pin.__name__
+    assert pins.pin_e4m3_rounding(lambda v: mutants._e4m3(v)) == []
+    from row_reduction_norm_gb300 import workloads as W
+    x = W.to_numpy_bits(W.random_rows("bf16", 64, 2048, seed=5))
+    a = oracle.rmsnorm_mxfp8(x, eps=1e-6, dtype="bf16")
+    b = mutants.reference_mx(x, None, None, 1e-6, "bf16")
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("mistake", mutants.MX_MISTAKES)
+def test_mx_pins_catch_planted_mistake(mistake):
+    impl = lambda x, w, r, e, d, b: mutants.reference_mx(x, w, r, e, d, weight_bias=b, mistake=mistake)
+    caught = [p.__name__ for p in pins.MX_PINS if p(impl)]
+    if not caught and mistake in ("truncate_codes", "ties_away_codes", "no_saturation"):
+        # rounding-rule mistakes also show on the bare encoder's midpoints
+        enc = lambda v: mutants._e4m3(v, mode={"truncate_codes": "trunc", "ties_away_codes": "away"}.get(
+            mistake, "rne"), saturate=mistake != "no_saturation")
+        caught = ["pin_e4m3_rounding"] if pins.pin_e4m3_rounding(enc) else []
+    assert caught, mistake
+
+
+def test_compare_helpers_flag_planted_differences():
+    """The GPU-side comparison helpers accept the oracle against itself and
+    reject a flipped code, a shifted scale and a 2-ulp bf16 difference."""
+    import parity
+    from row_reduction_norm_gb300 import workloads as W
+    x = W.to_numpy_bits(W.random_rows("bf16", 16, 576, seed=1))
+    co, so, _, v = oracle.rmsnorm_mxfp8(x, eps=1e-5, dtype="bf16")
+    assert parity.compare_mx(co, so, co, so, v, oracle.e4m3_from_double)[0]
+    c2 = co.copy()
+    c2[3, 7] ^= 1
+    assert not parity.compare_mx(c2, so, co, so, v, oracle.e4m3_from_double)[0]
+    s2 = so.copy()
+    s2[2, 1] += 1
+    assert not parity.compare_mx(co, s2, co, so, v, oracle.e4m3_from_double)[0]
+    y, _, _ = oracle.rmsnorm(x, eps=1e-5, dtype="bf16")
+    assert parity.compare_y(y, y, "bf16")[0]
+    y2 = y.copy()
+    y2[0, 0] += 2
+    assert not parity.compare_y(y2, y, "bf16")[0]
