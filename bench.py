@@ -740,6 +740,22 @@ def run_profile_case(args, device, stream):
     import torch
     from row_reduction_norm_gb300 import _native as N
     from row_reduction_norm_gb300 import api, workloads as W
+    if args.ncu_case in W.QK_WORKLOADS or args.ncu_case in W.LN_WORKLOADS or args.ncu_case in W.MX_WORKLOADS:
+        qk = args.ncu_case in W.QK_WORKLOADS
+        ln = args.ncu_case in W.LN_WORKLOADS
+        wl = W.QK_WORKLOADS.get(args.ncu_case) or W.LN_WORKLOADS.get(args.ncu_case) or W.MX_WORKLOADS[args.ncu_case]
+        if not qk and (args.rows or args.hidden):
+            wl = dataclasses.replace(wl, rows=args.rows or wl.rows, hidden=args.hidden or wl.hidden)
+        L = (QKLauncher if qk else LNLauncher if ln else MXLauncher)(wl, device, stream, 0)
+        with torch.cuda.stream(stream):
+            for i in range(args.launches):
+                L.launch(i)
+        stream.synchronize()
+        nbytes = wl.algorithmic_bytes() if (qk or ln) else W.mx_algorithmic_bytes(wl)
+        rows = wl.tokens * (wl.q_heads + wl.k_heads) if qk else wl.rows
+        print(json.dumps({"ncu_case": wl.name, "rows": rows, "hidden": wl.head_dim if qk else wl.hidden,
+                          "launches": args.launches, "bytes_per_launch": nbytes, "plan": plan_summary(L.plan)}))
+        return
     wl = W.WORKLOADS[args.ncu_case]
     if args.rows or args.hidden:
         wl = dataclasses.replace(wl, rows=args.rows or wl.rows, hidden=args.hidden or wl.hidden)
