@@ -75,7 +75,10 @@ __device__ __forceinline__ float row_combine(float v, float (&red)[2][RPB][WPR],
 // enough loads in flight per SM; two (128 registers) for 8 chunks.
 __host__ __device__ constexpr int ln_min_blocks(int ch) { return ch <= 4 ? 4 : 2; }
 
-template <typename T, int GT, int CH, bool RES, int AFF>
+// PIPE: software-pipelined grid-stride loop -- a block issues the loads of
+// its next row group before it reduces and writes the current one, so loads
+// stay in flight through the reductions (for grids capped at a few waves).
+template <typename T, int GT, int CH, bool RES, int AFF, bool PIPE = false>
 __global__ void __launch_bounds__(reg_block_threads(GT), ln_min_blocks(CH))
 ln_reg_kernel(const LnParams p) {
     constexpr int V = T::kVec;
@@ -101,30 +104,54 @@ ln_reg_kernel(const LnParams p) {
     bool staged = false;
     int parity = 0;
 
+    // loads of row group rbi into (dx, dr); zeros past the row end
+    auto load_group = [&](int64_t rbi, Chunk (&dx)[CH], Chunk (&dr)[RES ? CH : 1]) {
+        const int64_t rw = rbi * RPB + slot;
+        const bool ok = rw < p.rows;
+        const int64_t o = ok ? rw * p.row_bytes : 0;
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+            const int u = c * GT + t;
+            if (ok && u < nch)
+                dx[c] = ld_stream16(static_cast<const char *>(p.x) + o + (int64_t)u * 16);
+            else
+                dx[c] = Chunk{{0u, 0u, 0u, 0u}};
+        }
+        if constexpr (RES) {
+#pragma unroll
+            for (int c = 0; c < CH; ++c) {
+                const int u = c * GT + t;
+                if (ok && u < nch)
+                    dr[c] = ld_stream16(static_cast<const char *>(p.res) + o + (int64_t)u * 16);
+                else
+                    dr[c] = Chunk{{0u, 0u, 0u, 0u}};
+            }
+        }
+    };
+    Chunk nx[PIPE ? CH : 1];
+    Chunk nr[PIPE && RES ? CH : 1];
+    if constexpr (PIPE) {
+        if ((int64_t)blockIdx.x * RPB < p.rows) load_group(blockIdx.x, nx, nr);
+    }
+
     for (int64_t rb = blockIdx.x; rb * RPB < p.rows; rb += gridDim.x) {
         const int64_t row = rb * RPB + slot;
         const bool row_ok = row < p.rows;
         const int64_t off = row_ok ? row * p.row_bytes : 0;
 
         Chunk hc[CH];
-#pragma unroll
-        for (int c = 0; c < CH; ++c) {
-            const int u = c * GT + t;
-            if (row_ok && u < nch)
-                hc[c] = ld_stream16(static_cast<const char *>(p.x) + off + (int64_t)u * 16);
-            else
-                hc[c] = Chunk{{0u, 0u, 0u, 0u}};
-        }
         Chunk rc[RES ? CH : 1];
-        if constexpr (RES) {
+        if constexpr (PIPE) {
 #pragma unroll
-            for (int c = 0; c < CH; ++c) {
-                const int u = c * GT + t;
-                if (row_ok && u < nch)
-                    rc[c] = ld_stream16(static_cast<const char *>(p.res) + off + (int64_t)u * 16);
-                else
-                    rc[c] = Chunk{{0u, 0u, 0u, 0u}};
+            for (int c = 0; c < CH; ++c) hc[c] = nx[c];
+            if constexpr (RES) {
+#pragma unroll
+                for (int c = 0; c < CH; ++c) rc[c] = nr[c];
             }
+            const int64_t rbn = rb + gridDim.x;
+            if (rbn * RPB < p.rows) load_group(rbn, nx, nr);   // next group's loads go out now
+        } else {
+            load_group(rb, hc, rc);
         }
         if constexpr (W) {
             if (!staged) {   // first iteration of the block (uniform across it)
@@ -160,8 +187,7 @@ ln_reg_kernel(const LnParams p) {
         for (int c = 0; c < CH; ++c) {
             float a[V];
             unpack(hc[c], a, T{});
-#pragma unroll
-            for (int e = 0; e < V; ++e) acc[e] += a[e];
+            add_pairs(acc, a);
         }
         const float mu = row_combine<LANES, WPR, RPB>(tree_sum(acc), red, parity, slot, t, tid) / p.hidden_f;
         // variance: centred squares of the valid elements (slots past the row end are skipped)
@@ -174,10 +200,8 @@ ln_reg_kernel(const LnParams p) {
                 float a[V];
                 unpack(hc[c], a, T{});
 #pragma unroll
-                for (int e = 0; e < V; ++e) {
-                    const float d = a[e] - mu;
-                    acc[e] = fmaf(d, d, acc[e]);
-                }
+                for (int e = 0; e < V; ++e) a[e] = a[e] - mu;
+                sq_accumulate(a, acc);
             }
         }
         const float var = row_combine<LANES, WPR, RPB>(tree_sum(acc), red, parity, slot, t, tid) / p.hidden_f;
@@ -190,11 +214,18 @@ ln_reg_kernel(const LnParams p) {
                 unpack(hc[c], a, T{});
                 if constexpr (W) unpack(wb_smem[u], wv, T{});
                 if constexpr (B) unpack(wb_smem[nch + u], bv, T{});
+                const float2 mu2 = make_float2(-mu, -mu), r2 = make_float2(r, r);
 #pragma unroll
-                for (int e = 0; e < V; ++e) {
-                    const float wi = W ? wv[e] : 1.f;
-                    const float bi = B ? bv[e] : 0.f;
-                    a[e] = ln_out<AFF>(a[e], mu, r, wi, bi);
+                for (int k = 0; k < V / 2; ++k) {
+                    // n = (h - mu) * r, then n * w or fma(n, w, b): two lanes at a time
+                    float2 n = __fmul2_rn(__fadd2_rn(make_float2(a[2 * k], a[2 * k + 1]), mu2), r2);
+                    if constexpr (AFF == kAffW) {
+                        n = __fmul2_rn(n, make_float2(wv[2 * k], wv[2 * k + 1]));
+                    } else if constexpr (AFF == kAffWB) {
+                        n = __ffma2_rn(n, make_float2(wv[2 * k], wv[2 * k + 1]), make_float2(bv[2 * k], bv[2 * k + 1]));
+                    }
+                    a[2 * k] = n.x;
+                    a[2 * k + 1] = n.y;
                 }
                 st16(static_cast<char *>(p.y) + off + (int64_t)u * 16, pack(a, T{}));
             }

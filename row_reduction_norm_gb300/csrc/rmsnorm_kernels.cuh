@@ -214,6 +214,50 @@ __device__ __forceinline__ float add_round(float a, float b, BF16) {
 }
 __device__ __forceinline__ float add_round(float a, float b, F32) { return __fadd_rn(a, b); }
 
+// ------------------------------------------------------- packed fp32 math
+// sm_100+ issues two fp32 operations per instruction on register pairs
+// (FFMA2 / FMUL2 / FADD2).  Each half rounds exactly as the scalar operation
+// does, so these helpers change instruction counts, not results.
+
+template <int N>
+__device__ __forceinline__ void sq_accumulate(const float (&a)[N], float (&acc)[N]) {
+#pragma unroll
+    for (int k = 0; k < N / 2; ++k) {
+        const float2 v = make_float2(a[2 * k], a[2 * k + 1]);
+        const float2 r = __ffma2_rn(v, v, make_float2(acc[2 * k], acc[2 * k + 1]));
+        acc[2 * k] = r.x;
+        acc[2 * k + 1] = r.y;
+    }
+}
+
+template <int N>
+__device__ __forceinline__ void add_pairs(float (&acc)[N], const float (&a)[N]) {
+#pragma unroll
+    for (int k = 0; k < N / 2; ++k) {
+        const float2 r = __fadd2_rn(make_float2(acc[2 * k], acc[2 * k + 1]), make_float2(a[2 * k], a[2 * k + 1]));
+        acc[2 * k] = r.x;
+        acc[2 * k + 1] = r.y;
+    }
+}
+
+// a[e] = scale_out<WM>(a[e], r, w[e], bias) for every e, two lanes at a time.
+template <int WM, int N>
+__device__ __forceinline__ void scale_out_pairs(float (&a)[N], float r, const float (&w)[N], float bias) {
+    const float2 r2 = make_float2(r, r);
+#pragma unroll
+    for (int k = 0; k < N / 2; ++k) {
+        float2 v = __fmul2_rn(make_float2(a[2 * k], a[2 * k + 1]), r2);
+        if constexpr (WM == kWeight) {
+            v = __fmul2_rn(v, make_float2(w[2 * k], w[2 * k + 1]));
+        } else if constexpr (WM == kWeightBias) {
+            const float2 wb = __fadd2_rn(make_float2(w[2 * k], w[2 * k + 1]), make_float2(bias, bias));
+            v = __fmul2_rn(v, wb);
+        }
+        a[2 * k] = v.x;
+        a[2 * k + 1] = v.y;
+    }
+}
+
 // ----------------------------------------------------------------- helpers
 
 __host__ __device__ constexpr int reg_block_threads(int gt) { return gt >= 256 ? gt : 256; }
@@ -362,8 +406,7 @@ rms_reg_kernel(const Params p) {
         for (int c = 0; c < CH; ++c) {
             float a[V];
             unpack(hc[c], a, T{});
-#pragma unroll
-            for (int e = 0; e < V; ++e) acc[e] = fmaf(a[e], a[e], acc[e]);
+            sq_accumulate(a, acc);
         }
         float sum = tree_sum(acc);
         // A4: butterfly across the row's lanes of this warp
@@ -398,9 +441,9 @@ rms_reg_kernel(const Params p) {
                 }
                 float amax = 0.f;
                 bool special = false;
+                scale_out_pairs<WM>(a, r, wv, p.w_bias);
 #pragma unroll
                 for (int e = 0; e < V; ++e) {
-                    a[e] = scale_out<WM>(a[e], r, wv[e], p.w_bias);
                     const float m = fabsf(a[e]);
                     special |= !(m <= 3.402823466e38f);     // NaN or Inf
                     amax = fmaxf(amax, m);
@@ -444,8 +487,7 @@ rms_reg_kernel(const Params p) {
 #pragma unroll
                     for (int e = 0; e < V; ++e) wv[e] = 1.f;
                 }
-#pragma unroll
-                for (int e = 0; e < V; ++e) a[e] = scale_out<WM>(a[e], r, wv[e], p.w_bias);
+                scale_out_pairs<WM>(a, r, wv, p.w_bias);
                 st16(static_cast<char *>(p.y) + yoff + (int64_t)u * 16, pack(a, T{}));
             }
         }
