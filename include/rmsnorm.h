@@ -107,10 +107,7 @@ typedef struct {
                                    (the kernel may start while the previous kernel on
                                    the stream drains; it reads no input before that
                                    kernel has completed).  Planning sets 1.          */
-    int32_t pipeline;           /* 1: software-pipelined grid-stride loop (a block
-                                   issues its next row group's loads before it reduces
-                                   the current one); LayerNorm register plans with 2
-                                   or 4 chunks.  Planning sets 0.                    */
+    int32_t reserved;           /* must be 0                                          */
     int64_t grid;               /* blocks launched (0 when rows == 0)                 */
 } rmsnorm_plan_t;
 

@@ -59,7 +59,7 @@ class Plan(ctypes.Structure):
         ("rows_per_block", ctypes.c_int32),
         ("persistent", ctypes.c_int32),
         ("pdl", ctypes.c_int32),
-        ("pipeline", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
         ("grid", ctypes.c_int64),
     ]
 

@@ -35,8 +35,8 @@ inline const void *mx_kernel(int dtype, int gt, int ch, bool res, int wm) {
 
 // LayerNorm (contiguous rows); aff: 0 none, 1 weight, 2 weight and bias.
 constexpr int kLnMaxGT = 256;
-const void *ln_reg_f32(int gt, int ch, bool res, int aff, bool pipe);
-const void *ln_reg_bf16(int gt, int ch, bool res, int aff, bool pipe);
+const void *ln_reg_f32(int gt, int ch, bool res, int aff);
+const void *ln_reg_bf16(int gt, int ch, bool res, int aff);
 const void *ln_loop(int dtype, int block, bool vec, bool res, int aff);
 
 inline const void *reg_kernel(int dtype, int gt, int ch, bool res, int wm, bool heads) {

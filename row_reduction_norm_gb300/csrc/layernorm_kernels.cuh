@@ -75,10 +75,7 @@ __device__ __forceinline__ float row_combine(float v, float (&red)[2][RPB][WPR],
 // enough loads in flight per SM; two (128 registers) for 8 chunks.
 __host__ __device__ constexpr int ln_min_blocks(int ch) { return ch <= 4 ? 4 : 2; }
 
-// PIPE: software-pipelined grid-stride loop -- a block issues the loads of
-// its next row group before it reduces and writes the current one, so loads
-// stay in flight through the reductions (for grids capped at a few waves).
-template <typename T, int GT, int CH, bool RES, int AFF, bool PIPE = false>
+template <typename T, int GT, int CH, bool RES, int AFF>
 __global__ void __launch_bounds__(reg_block_threads(GT), ln_min_blocks(CH))
 ln_reg_kernel(const LnParams p) {
     constexpr int V = T::kVec;
@@ -128,11 +125,6 @@ ln_reg_kernel(const LnParams p) {
             }
         }
     };
-    Chunk nx[PIPE ? CH : 1];
-    Chunk nr[PIPE && RES ? CH : 1];
-    if constexpr (PIPE) {
-        if ((int64_t)blockIdx.x * RPB < p.rows) load_group(blockIdx.x, nx, nr);
-    }
 
     for (int64_t rb = blockIdx.x; rb * RPB < p.rows; rb += gridDim.x) {
         const int64_t row = rb * RPB + slot;
@@ -141,18 +133,7 @@ ln_reg_kernel(const LnParams p) {
 
         Chunk hc[CH];
         Chunk rc[RES ? CH : 1];
-        if constexpr (PIPE) {
-#pragma unroll
-            for (int c = 0; c < CH; ++c) hc[c] = nx[c];
-            if constexpr (RES) {
-#pragma unroll
-                for (int c = 0; c < CH; ++c) rc[c] = nr[c];
-            }
-            const int64_t rbn = rb + gridDim.x;
-            if (rbn * RPB < p.rows) load_group(rbn, nx, nr);   // next group's loads go out now
-        } else {
-            load_group(rb, hc, rc);
-        }
+        load_group(rb, hc, rc);
         if constexpr (W) {
             if (!staged) {   // first iteration of the block (uniform across it)
                 for (int i = tid; i < nch; i += BLOCK)

@@ -7,45 +7,37 @@
 namespace rrn {
 namespace lnpick {
 
-template <typename T, int GT, int CH, bool RES, bool PIPE>
+template <typename T, int GT, int CH, bool RES>
 const void *reg_aff(int aff) {
     switch (aff) {
-        case kAffNone: return reinterpret_cast<const void *>(&ln_reg_kernel<T, GT, CH, RES, kAffNone, PIPE>);
-        case kAffW: return reinterpret_cast<const void *>(&ln_reg_kernel<T, GT, CH, RES, kAffW, PIPE>);
-        case kAffWB: return reinterpret_cast<const void *>(&ln_reg_kernel<T, GT, CH, RES, kAffWB, PIPE>);
+        case kAffNone: return reinterpret_cast<const void *>(&ln_reg_kernel<T, GT, CH, RES, kAffNone>);
+        case kAffW: return reinterpret_cast<const void *>(&ln_reg_kernel<T, GT, CH, RES, kAffW>);
+        case kAffWB: return reinterpret_cast<const void *>(&ln_reg_kernel<T, GT, CH, RES, kAffWB>);
         default: return nullptr;
     }
 }
 
-// The pipelined form is compiled for 2 and 4 chunks a thread.
 template <typename T, int GT, bool RES>
-const void *reg_ch(int ch, int aff, bool pipe) {
-    if (pipe) {
-        switch (ch) {
-            case 2: return reg_aff<T, GT, 2, RES, true>(aff);
-            case 4: return reg_aff<T, GT, 4, RES, true>(aff);
-            default: return nullptr;
-        }
-    }
+const void *reg_ch(int ch, int aff) {
     switch (ch) {
-        case 1: return reg_aff<T, GT, 1, RES, false>(aff);
-        case 2: return reg_aff<T, GT, 2, RES, false>(aff);
-        case 4: return reg_aff<T, GT, 4, RES, false>(aff);
-        case 8: return reg_aff<T, GT, 8, RES, false>(aff);
+        case 1: return reg_aff<T, GT, 1, RES>(aff);
+        case 2: return reg_aff<T, GT, 2, RES>(aff);
+        case 4: return reg_aff<T, GT, 4, RES>(aff);
+        case 8: return reg_aff<T, GT, 8, RES>(aff);
         default: return nullptr;
     }
 }
 
 template <typename T, bool RES>
-const void *reg_gt(int gt, int ch, int aff, bool pipe) {
+const void *reg_gt(int gt, int ch, int aff) {
     switch (gt) {
-        case 4: return reg_ch<T, 4, RES>(ch, aff, pipe);
-        case 8: return reg_ch<T, 8, RES>(ch, aff, pipe);
-        case 16: return reg_ch<T, 16, RES>(ch, aff, pipe);
-        case 32: return reg_ch<T, 32, RES>(ch, aff, pipe);
-        case 64: return reg_ch<T, 64, RES>(ch, aff, pipe);
-        case 128: return reg_ch<T, 128, RES>(ch, aff, pipe);
-        case 256: return reg_ch<T, 256, RES>(ch, aff, pipe);
+        case 4: return reg_ch<T, 4, RES>(ch, aff);
+        case 8: return reg_ch<T, 8, RES>(ch, aff);
+        case 16: return reg_ch<T, 16, RES>(ch, aff);
+        case 32: return reg_ch<T, 32, RES>(ch, aff);
+        case 64: return reg_ch<T, 64, RES>(ch, aff);
+        case 128: return reg_ch<T, 128, RES>(ch, aff);
+        case 256: return reg_ch<T, 256, RES>(ch, aff);
         default: return nullptr;
     }
 }

@@ -4,8 +4,8 @@
 
 namespace rrn {
 
-const void *ln_reg_bf16(int gt, int ch, bool res, int aff, bool pipe) {
-    return res ? lnpick::reg_gt<BF16, true>(gt, ch, aff, pipe) : lnpick::reg_gt<BF16, false>(gt, ch, aff, pipe);
+const void *ln_reg_bf16(int gt, int ch, bool res, int aff) {
+    return res ? lnpick::reg_gt<BF16, true>(gt, ch, aff) : lnpick::reg_gt<BF16, false>(gt, ch, aff);
 }
 
 }  // namespace rrn

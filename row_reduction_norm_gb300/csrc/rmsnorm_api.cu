@@ -166,9 +166,8 @@ const void *kernel_of(const rmsnorm_plan_t *p, const Op &o) {
     }
     if (o.ln) {
         if (p->kernel == RMSNORM_KERNEL_REG)
-            return o.dtype == RMSNORM_BF16
-                       ? rrn::ln_reg_bf16(p->threads_per_row, p->chunks_per_thread, res, o.wm, p->pipeline != 0)
-                       : rrn::ln_reg_f32(p->threads_per_row, p->chunks_per_thread, res, o.wm, p->pipeline != 0);
+            return o.dtype == RMSNORM_BF16 ? rrn::ln_reg_bf16(p->threads_per_row, p->chunks_per_thread, res, o.wm)
+                                           : rrn::ln_reg_f32(p->threads_per_row, p->chunks_per_thread, res, o.wm);
         return rrn::ln_loop(o.dtype, p->block_threads, p->vec_elems != 1, res, o.wm);
     }
     if (p->kernel == RMSNORM_KERNEL_REG)
@@ -182,11 +181,7 @@ int validate_plan(const rmsnorm_plan_t *p, const Op &o, int vec_ok) {
     const int V = vec_elems_of(o.dtype);
     if (o.rows > 0 && (p->grid < 1 || p->grid > INT_MAX)) return RMSNORM_EINVAL;
     if (p->pdl != 0 && p->pdl != 1) return RMSNORM_EINVAL;
-    if (p->pipeline != 0 && p->pipeline != 1) return RMSNORM_EINVAL;
-    // the pipelined loop is compiled for the LayerNorm register kernel, 2 or 4 chunks
-    if (p->pipeline && !(o.ln && p->kernel == RMSNORM_KERNEL_REG &&
-                         (p->chunks_per_thread == 2 || p->chunks_per_thread == 4)))
-        return RMSNORM_EINVAL;
+    if (p->reserved != 0) return RMSNORM_EINVAL;
     if (p->kernel == RMSNORM_KERNEL_REG) {
         const int gt = p->threads_per_row, ch = p->chunks_per_thread;
         const int max_gt = max_threads_per_row(o);
