@@ -330,6 +330,44 @@ class MXLauncher(Launcher):
                                  self.wl.hidden, self.wl.eps, 0.0, self.code, None, self.stream.cuda_stream)
 
 
+class NVLauncher(MXLauncher):
+    """RMSNorm with NVFP4 output: codes are half a byte an element, one scale per 16."""
+
+    def __init__(self, wl, device, stream, min_footprint, seed=0):
+        import torch
+        from row_reduction_norm_gb300 import api, workloads as W
+        self.N = api.N
+        self.wl = wl
+        self.stream = stream
+        e = wl.rows * wl.hidden
+        per_set = e * wl.elem_bytes * (1 + (2 if wl.has_res else 0)) + e // 2 + e // 16
+        self.n_sets = max(1, math.ceil(min_footprint / max(per_set, 1)))
+        self.sets, self.scales = [], []
+        w = None
+        for s in range(self.n_sets):
+            x, r, w_s = W.make_inputs(wl, seed=seed + 16 * s, device=device)
+            w = w_s if w is None else w
+            codes = torch.empty((wl.rows, wl.hidden // 2), dtype=torch.uint8, device=device)
+            sc = torch.empty((wl.rows, wl.hidden // 16), dtype=torch.uint8, device=device)
+            h = torch.empty_like(x) if r is not None else None
+            self.sets.append((x, r, codes, h))
+            self.scales.append(sc)
+        self.w = w
+        self.code = api.dtype_code(self.sets[0][0].dtype)
+        self.ptrs = [(x.data_ptr(), None if r is None else r.data_ptr(), c.data_ptr(),
+                      None if h is None else h.data_ptr()) for x, r, c, h in self.sets]
+        self.w_ptr = None if w is None else w.data_ptr()
+        self.footprint = per_set * self.n_sets
+        self.tensor_scale = W.NV_TENSOR_SCALE
+        self.plan = api.rms_norm_nvfp4_plan_for(self.sets[0][0], w=w, residual=self.sets[0][1])
+
+    def launch(self, i):
+        x, r, c, h = self.ptrs[i % self.n_sets]
+        self.N.rmsnorm_fwd_nvfp4(x, r, self.w_ptr, c, self.scales[i % self.n_sets].data_ptr(), h, self.wl.rows,
+                                 self.wl.hidden, self.wl.eps, 0.0, self.tensor_scale, self.code, None,
+                                 self.stream.cuda_stream)
+
+
 class QKLauncher(Launcher):
     """Buffer sets of a fused Q+K workload, normalised in place (the usual use on
     a packed projection), with the same launch interface as Launcher."""
@@ -635,20 +673,22 @@ def run_ours(args):
     if not args.no_per_config:
         del L
         torch.cuda.empty_cache()
-        for name in PER_CONFIG + list(W.QK_WORKLOADS) + list(W.LN_WORKLOADS) + list(W.MX_WORKLOADS):
+        for name in (PER_CONFIG + list(W.QK_WORKLOADS) + list(W.LN_WORKLOADS) + list(W.MX_WORKLOADS)
+                     + list(W.NV_WORKLOADS)):
             qk = name in W.QK_WORKLOADS
             ln = name in W.LN_WORKLOADS
             mx = name in W.MX_WORKLOADS
+            nv = name in W.NV_WORKLOADS
             cw = (W.QK_WORKLOADS[name] if qk else W.LN_WORKLOADS[name] if ln else
-                  W.MX_WORKLOADS[name] if mx else W.WORKLOADS[name])
-            CL = (QKLauncher if qk else LNLauncher if ln else MXLauncher if mx else Launcher)(
+                  W.MX_WORKLOADS[name] if mx else W.NV_WORKLOADS[name] if nv else W.WORKLOADS[name])
+            CL = (QKLauncher if qk else LNLauncher if ln else MXLauncher if mx else NVLauncher if nv else Launcher)(
                 cw, device, stream, min_footprint)
             # calibrate: about 0.3 s of launches
             cal = time_launches(CL, 64, 8)
             k = int(max(64, min(200000, 0.3 / max(cal / 1e3 / 64, 1e-9))))
             cms = time_launches(CL, k, max(3, k // 20), barrier=barrier)
             t_launch = cms / 1e3 / k
-            b = W.mx_algorithmic_bytes(cw) if mx else cw.algorithmic_bytes()
+            b = W.mx_algorithmic_bytes(cw) if mx else W.nv_algorithmic_bytes(cw) if nv else cw.algorithmic_bytes()
             rows = cw.tokens * (cw.q_heads + cw.k_heads) if qk else cw.rows
             entry = {"workload": name, "rows": rows, "hidden": cw.head_dim if qk else cw.hidden,
                      "dtype": cw.dtype, "bytes_per_launch": b, "us_per_launch": round(t_launch * 1e6, 3),
@@ -665,6 +705,9 @@ def run_ours(args):
                 entry.update({"op": "layernorm", "bias": cw.has_b})
             if mx:
                 entry.update({"op": "rmsnorm, MXFP8 output (E4M3 codes, E8M0 scale per 32)"})
+            if nv:
+                entry.update({"op": "rmsnorm, NVFP4 output (E2M1 codes, E4M3 scale per 16, tensor scale "
+                                    f"{W.NV_TENSOR_SCALE})"})
             if rows <= 64 or (qk and cw.tokens <= 64):
                 entry["single_launch_latency_us"] = round(single_launch_latency_us(CL), 2)
             per_config.append(entry)
@@ -740,18 +783,21 @@ def run_profile_case(args, device, stream):
     import torch
     from row_reduction_norm_gb300 import _native as N
     from row_reduction_norm_gb300 import api, workloads as W
-    if args.ncu_case in W.QK_WORKLOADS or args.ncu_case in W.LN_WORKLOADS or args.ncu_case in W.MX_WORKLOADS:
+    special = {**W.QK_WORKLOADS, **W.LN_WORKLOADS, **W.MX_WORKLOADS, **W.NV_WORKLOADS}
+    if args.ncu_case in special:
         qk = args.ncu_case in W.QK_WORKLOADS
         ln = args.ncu_case in W.LN_WORKLOADS
-        wl = W.QK_WORKLOADS.get(args.ncu_case) or W.LN_WORKLOADS.get(args.ncu_case) or W.MX_WORKLOADS[args.ncu_case]
+        nv = args.ncu_case in W.NV_WORKLOADS
+        wl = special[args.ncu_case]
         if not qk and (args.rows or args.hidden):
             wl = dataclasses.replace(wl, rows=args.rows or wl.rows, hidden=args.hidden or wl.hidden)
-        L = (QKLauncher if qk else LNLauncher if ln else MXLauncher)(wl, device, stream, 0)
+        L = (QKLauncher if qk else LNLauncher if ln else NVLauncher if nv else MXLauncher)(wl, device, stream, 0)
         with torch.cuda.stream(stream):
             for i in range(args.launches):
                 L.launch(i)
         stream.synchronize()
-        nbytes = wl.algorithmic_bytes() if (qk or ln) else W.mx_algorithmic_bytes(wl)
+        nbytes = (wl.algorithmic_bytes() if (qk or ln) else
+                  W.nv_algorithmic_bytes(wl) if nv else W.mx_algorithmic_bytes(wl))
         rows = wl.tokens * (wl.q_heads + wl.k_heads) if qk else wl.rows
         print(json.dumps({"ncu_case": wl.name, "rows": rows, "hidden": wl.head_dim if qk else wl.hidden,
                           "launches": args.launches, "bytes_per_launch": nbytes, "plan": plan_summary(L.plan)}))

@@ -239,6 +239,34 @@ int rmsnorm_mxfp8_plan_for(const void *x, const void *residual, const void *w,
                            int64_t rows, int64_t hidden, int dtype, rmsnorm_plan_t *plan);
 
 /*
+ * RMSNorm with a block-scaled NVFP4 output: E2M1 elements (magnitudes 0, 0.5,
+ * 1, 1.5, 2, 3, 4, 6), one E4M3 scale per 16 elements and a per-tensor fp32
+ * scale S given by the caller ("CuTeDSL at Perplexity", section "Blackwell
+ * support", names NVFP4 without a recipe; the reading taken is that a value
+ * decodes as code * scale * S).  For each block of 16 consecutive elements of
+ * a row, with the op's fp32 values v_i as for rmsnorm_fwd_mxfp8:
+ *   scales  [rows, hidden / 16] bytes: E4M3(amax / (6 S)), nearest-even, saturating
+ *   codes   [rows, hidden / 2] bytes: E2M1(v_i / (scale * S)), nearest-even,
+ *           saturated at 6, two a byte, element 2k in the low nibble
+ *           (all 0 when the block's scale is 0)
+ * A block holding NaN or Inf gets the E4M3 NaN 0x7F as its scale and codes 0.
+ * bf16 I/O only (fp32: RMSNORM_EUNSUPPORTED); hidden a multiple of 16;
+ * tensor_scale > 0 and finite; x, residual, w, codes, residual_out 16-byte
+ * aligned.  Codes and scales may differ from the correctly rounded ones only
+ * where the exact value lies within the op's fp32 error of a rounding
+ * boundary, as for MXFP8.
+ */
+int rmsnorm_fwd_nvfp4(const void *x, const void *residual, const void *w, void *codes,
+                      void *scales, void *residual_out, int64_t rows, int64_t hidden,
+                      float eps, float weight_bias, float tensor_scale, int dtype,
+                      const rmsnorm_plan_t *plan, rmsnorm_stream_t stream);
+
+/* The plan rmsnorm_fwd_nvfp4 would use for these pointers on the current device. */
+int rmsnorm_nvfp4_plan_for(const void *x, const void *residual, const void *w,
+                           const void *codes, const void *scales, const void *residual_out,
+                           int64_t rows, int64_t hidden, int dtype, rmsnorm_plan_t *plan);
+
+/*
  * Fused row-wise LayerNorm ("GPT-2 on the GPU", section "The Whole Model as
  * One Kernel": mean, variance, (x - mean) / sqrt(var + eps), weight times the
  * normalised value plus bias):

@@ -70,6 +70,14 @@ def _load():
             lib.oracle_rmsnorm_mxfp8_rows.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64,
                                                       ctypes.c_float, ctypes.c_float, ctypes.c_int]
             lib.oracle_rmsnorm_mxfp8_rows.restype = ctypes.c_int
+            lib.oracle_rmsnorm_nvfp4_rows.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64,
+                                                      ctypes.c_float, ctypes.c_float, ctypes.c_float,
+                                                      ctypes.c_int]
+            lib.oracle_rmsnorm_nvfp4_rows.restype = ctypes.c_int
+            lib.oracle_e2m1_from_double.argtypes = [vp, vp, i64]
+            lib.oracle_e2m1_from_double.restype = None
+            lib.oracle_double_from_e2m1.argtypes = [vp, vp, i64]
+            lib.oracle_double_from_e2m1.restype = None
             lib.oracle_e4m3_from_double.argtypes = [vp, vp, i64]
             lib.oracle_e4m3_from_double.restype = None
             lib.oracle_double_from_e4m3.argtypes = [vp, vp, i64]
@@ -220,6 +228,59 @@ def rmsnorm_mxfp8(x, w=None, residual=None, eps: float = 1e-6, dtype: str = "bf1
         with ThreadPoolExecutor(max_workers=threads) as ex:
             list(ex.map(lambda i: run(int(bounds[i]), int(bounds[i + 1])), range(threads)))
     return codes, scales, res_out, v64
+
+
+def rmsnorm_nvfp4(x, w=None, residual=None, eps: float = 1e-6, dtype: str = "bf16", weight_bias: float = 0.0,
+                  tensor_scale: float = 1.0, threads: int = 1):
+    """Reference RMSNorm with NVFP4 output (E2M1 codes packed two a byte, one
+    E4M3 scale per 16 elements, per-tensor scale ``tensor_scale``; see the C
+    file).  Returns ``(codes [rows, hidden/2], scales [rows, hidden/16],
+    residual_out, v_exact)``."""
+    x = np.ascontiguousarray(x)
+    rows, hidden = x.shape
+    x = _check(x, "x", dtype, (rows, hidden))
+    residual = _check(residual, "residual", dtype, (rows, hidden))
+    w = _check(w, "w", dtype, (hidden,))
+    if hidden % 16:
+        raise ValueError("hidden must be a multiple of 16")
+    codes = np.empty((rows, hidden // 2), dtype=np.uint8)
+    scales = np.empty((rows, hidden // 16), dtype=np.uint8)
+    res_out = None if residual is None else np.empty((rows, hidden), dtype=_NP_TYPE[dtype])
+    v64 = np.empty((rows, hidden), dtype=np.float64)
+    if rows == 0:
+        return codes, scales, res_out, v64
+    lib = _load()
+    args = (_ptr(x), _ptr(residual), _ptr(w), _ptr(codes), _ptr(scales), _ptr(v64), _ptr(res_out))
+
+    def run(lo, hi):
+        rc = lib.oracle_rmsnorm_nvfp4_rows(*args, lo, hi, hidden, float(eps), float(weight_bias),
+                                           float(tensor_scale), DTYPES[dtype])
+        if rc != 0:
+            raise ValueError("oracle rejected its arguments")
+
+    threads = max(1, min(int(threads), rows))
+    if threads == 1:
+        run(0, rows)
+    else:
+        bounds = np.linspace(0, rows, threads + 1).astype(np.int64)
+        with ThreadPoolExecutor(max_workers=threads) as ex:
+            list(ex.map(lambda i: run(int(bounds[i]), int(bounds[i + 1])), range(threads)))
+    return codes, scales, res_out, v64
+
+
+def e2m1_from_double(v) -> np.ndarray:
+    """Round fp64 values to 4-bit E2M1 codes (nearest-even, saturated at 6)."""
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    out = np.empty(v.shape, dtype=np.uint8)
+    _load().oracle_e2m1_from_double(_ptr(v), _ptr(out), v.size)
+    return out
+
+
+def double_from_e2m1(c) -> np.ndarray:
+    c = np.ascontiguousarray(c, dtype=np.uint8)
+    out = np.empty(c.shape, dtype=np.float64)
+    _load().oracle_double_from_e2m1(_ptr(c), _ptr(out), c.size)
+    return out
 
 
 def e4m3_from_double(v) -> np.ndarray:

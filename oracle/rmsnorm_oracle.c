@@ -362,6 +362,111 @@ int oracle_rmsnorm_mxfp8_rows(const void *x, const void *residual, const void *w
     return 0;
 }
 
+/*
+ * FP4 E2M1: 1 sign bit, 2 exponent bits (bias 1), 1 fraction bit; magnitudes
+ * 0, 0.5, 1, 1.5, 2, 3, 4, 6; no infinities or NaN.  Rounding to E2M1 here:
+ * round to nearest on the format's grid (quantum 0.5 below 2, 1 in [2, 4),
+ * 2 in [4, 8)), ties to the even code, then saturate above 6 to 6.  The
+ * 4-bit code is sign << 3 | magnitude index (0 .. 7 in value order).
+ */
+static uint8_t double_to_e2m1_sat(double v)
+{
+    uint8_t sign = signbit(v) ? 0x8u : 0u;
+    double a = fabs(v);
+    if (isnan(a))
+        return 0x7u;                     /* NaN is not encodable: largest positive */
+    double q = a < 2.0 ? 0.5 : (a < 4.0 ? 1.0 : 2.0);
+    double r = nearbyint(a / q) * q;     /* a / q is exact (q a power of two)     */
+    if (r > 6.0)
+        r = 6.0;
+    static const double mags[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+    uint8_t idx = 0;
+    for (uint8_t i = 0; i < 8; ++i)
+        if (mags[i] == r)
+            idx = i;
+    return (uint8_t)(sign | idx);
+}
+
+static double e2m1_to_double(uint8_t c)
+{
+    static const double mags[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+    return ((c & 0x8u) ? -1.0 : 1.0) * mags[c & 0x7u];
+}
+
+/*
+ * RMSNorm with NVFP4 output (E2M1 elements, one E4M3 scale per 16 elements,
+ * and a per-tensor fp32 scale S given by the caller; the format is named in
+ * "CuTeDSL at Perplexity", section "Blackwell support", without a recipe).
+ * Reading taken: the value decodes as code * scale * S.  For each block of 16
+ * consecutive elements of a row, with the op's values v_i (as for MXFP8):
+ *   scale  = E4M3(amax / (6 * S)), nearest-even, saturated at 448
+ *   code_i = E2M1(v_i / (scale * S)), nearest-even, saturated at 6
+ *            (all codes 0 when the scale is 0)
+ * A block holding NaN or Inf gets the E4M3 NaN (0x7F) as its scale and codes 0.
+ * codes: [rows, hidden / 2] bytes, element 2k in the low nibble of byte k;
+ * scales: [rows, hidden / 16].  hidden must be a multiple of 16; S > 0 finite.
+ */
+int oracle_rmsnorm_nvfp4_rows(const void *x, const void *residual, const void *w,
+                              uint8_t *codes, uint8_t *scales, double *v_exact, void *residual_out,
+                              int64_t row_begin, int64_t row_end, int64_t hidden,
+                              float eps, float weight_bias, float tensor_scale, int dtype)
+{
+    if (x == NULL || codes == NULL || scales == NULL || hidden <= 0 || hidden % 16 != 0)
+        return -1;
+    if (row_begin < 0 || row_end < row_begin || (dtype != ORACLE_F32 && dtype != ORACLE_BF16))
+        return -1;
+    if ((residual == NULL) != (residual_out == NULL) || (w == NULL && weight_bias != 0.0f))
+        return -1;
+    if (!(tensor_scale > 0.0f) || isinf(tensor_scale))
+        return -1;
+    const double S = (double)tensor_scale;
+    double *v = (double *)malloc((size_t)hidden * sizeof(double));
+    if (v == NULL)
+        return -1;
+    for (int64_t row = row_begin; row < row_end; ++row) {
+        rms_row_values(x, residual, w, row, hidden, (double)eps, (double)weight_bias, dtype, v,
+                       residual_out);
+        if (v_exact != NULL)
+            memcpy(v_exact + row * hidden, v, (size_t)hidden * sizeof(double));
+        for (int64_t k = 0; k < hidden / 16; ++k) {
+            const double *vb = v + k * 16;
+            double amax = 0.0;
+            int special = 0;
+            for (int j = 0; j < 16; ++j) {
+                if (isnan(vb[j]) || isinf(vb[j]))
+                    special = 1;
+                else if (fabs(vb[j]) > amax)
+                    amax = fabs(vb[j]);
+            }
+            uint8_t sc = special ? 0x7Fu : double_to_e4m3_sat(amax / (6.0 * S));
+            scales[row * (hidden / 16) + k] = sc;
+            const double sv = special ? 0.0 : e4m3_to_double(sc);
+            for (int j = 0; j < 16; j += 2) {
+                uint8_t lo = 0, hi = 0;
+                if (sv > 0.0) {
+                    lo = double_to_e2m1_sat(vb[j] / (sv * S));
+                    hi = double_to_e2m1_sat(vb[j + 1] / (sv * S));
+                }
+                codes[row * (hidden / 2) + (k * 16 + j) / 2] = (uint8_t)(lo | (hi << 4));
+            }
+        }
+    }
+    free(v);
+    return 0;
+}
+
+void oracle_e2m1_from_double(const double *v, uint8_t *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = double_to_e2m1_sat(v[i]);
+}
+
+void oracle_double_from_e2m1(const uint8_t *c, double *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = e2m1_to_double(c[i]);
+}
+
 void oracle_e4m3_from_double(const double *v, uint8_t *out, int64_t n)
 {
     for (int64_t i = 0; i < n; ++i)

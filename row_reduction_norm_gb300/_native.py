@@ -37,6 +37,7 @@ KERNEL_NAMES = {0: "reg", 1: "loop"}
 # Every symbol the header declares (checked by the CPU tests).
 EXPORTED = ["rmsnorm_fwd", "rmsnorm_plan", "rmsnorm_plan_for", "rmsnorm_fwd_plan", "rmsnorm_fwd_ex",
             "rmsnorm_qk_fwd", "rmsnorm_qk_plan_for", "rmsnorm_fwd_mxfp8", "rmsnorm_mxfp8_plan_for",
+            "rmsnorm_fwd_nvfp4", "rmsnorm_nvfp4_plan_for",
             "layernorm_fwd", "layernorm_plan_for",
             "rmsnorm_max_hidden", "rmsnorm_reg_max_chunks", "rmsnorm_strerror", "rmsnorm_build_info"]
 
@@ -117,6 +118,11 @@ def load():
         lib.rmsnorm_fwd_mxfp8.restype = i32
         lib.rmsnorm_mxfp8_plan_for.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i32, ctypes.POINTER(Plan)]
         lib.rmsnorm_mxfp8_plan_for.restype = i32
+        lib.rmsnorm_fwd_nvfp4.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, ctypes.c_float, ctypes.c_float,
+                                          ctypes.c_float, i32, ctypes.POINTER(Plan), vp]
+        lib.rmsnorm_fwd_nvfp4.restype = i32
+        lib.rmsnorm_nvfp4_plan_for.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i32, ctypes.POINTER(Plan)]
+        lib.rmsnorm_nvfp4_plan_for.restype = i32
         lib.layernorm_fwd.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, ctypes.c_float, i32,
                                       ctypes.POINTER(Plan), vp]
         lib.layernorm_fwd.restype = i32
@@ -215,6 +221,25 @@ def rmsnorm_mxfp8_plan_for(x, residual, w, codes, scales, residual_out, rows, hi
     p = Plan()
     _check(load().rmsnorm_mxfp8_plan_for(x, residual, w, codes, scales, residual_out, rows, hidden, dtype,
                                          ctypes.byref(p)), "rmsnorm_mxfp8_plan_for")
+    return p
+
+
+def rmsnorm_fwd_nvfp4(x, residual, w, codes, scales, residual_out, rows, hidden, eps, weight_bias, tensor_scale,
+                      dtype, plan=None, stream=0):
+    _check(rmsnorm_fwd_nvfp4_status(x, residual, w, codes, scales, residual_out, rows, hidden, eps, weight_bias,
+                                    tensor_scale, dtype, plan, stream), "rmsnorm_fwd_nvfp4")
+
+
+def rmsnorm_fwd_nvfp4_status(x, residual, w, codes, scales, residual_out, rows, hidden, eps, weight_bias,
+                             tensor_scale, dtype, plan=None, stream=0) -> int:
+    return load().rmsnorm_fwd_nvfp4(x, residual, w, codes, scales, residual_out, rows, hidden, eps, weight_bias,
+                                    tensor_scale, dtype, _plan_ref(plan), stream)
+
+
+def rmsnorm_nvfp4_plan_for(x, residual, w, codes, scales, residual_out, rows, hidden, dtype) -> Plan:
+    p = Plan()
+    _check(load().rmsnorm_nvfp4_plan_for(x, residual, w, codes, scales, residual_out, rows, hidden, dtype,
+                                         ctypes.byref(p)), "rmsnorm_nvfp4_plan_for")
     return p
 
 

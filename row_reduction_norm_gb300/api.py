@@ -222,3 +222,44 @@ def rms_norm_mxfp8_plan_for(x, w=None, residual=None) -> N.Plan:
     with torch.cuda.device(x.device):
         return N.rmsnorm_mxfp8_plan_for(_ptr(x), _ptr(residual), _ptr(w), codes.data_ptr(), codes.data_ptr(),
                                         _ptr(residual), rows, hidden, dtype_code(x.dtype))
+
+
+def rms_norm_nvfp4(x: torch.Tensor, w: Optional[torch.Tensor] = None, residual: Optional[torch.Tensor] = None,
+                   eps: float = 1e-6, tensor_scale: float = 1.0, weight_bias: float = 0.0,
+                   codes: Optional[torch.Tensor] = None, scales: Optional[torch.Tensor] = None,
+                   residual_out: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None,
+                   plan: Optional[N.Plan] = None):
+    """RMSNorm with NVFP4 output (bf16 input): returns (codes uint8 [rows,
+    hidden/2] with two E2M1 codes a byte, scales uint8 [rows, hidden/16]
+    E4M3) and, with a residual, residual_out."""
+    _check_tensor(x, "x", x)
+    code = dtype_code(x.dtype)
+    hidden = x.shape[-1]
+    rows = x.numel() // hidden if hidden else 0
+    if w is not None and tuple(w.shape) != (hidden,):
+        raise ValueError(f"w must have shape ({hidden},)")
+    if codes is None:
+        codes = torch.empty(tuple(x.shape[:-1]) + (hidden // 2,), dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty(tuple(x.shape[:-1]) + (hidden // 16,), dtype=torch.uint8, device=x.device)
+    if residual is not None and residual_out is None:
+        residual_out = torch.empty_like(x)
+    for name, t in (("w", w), ("residual", residual), ("residual_out", residual_out)):
+        _check_tensor(t, name, x)
+    for name, t in (("codes", codes), ("scales", scales)):
+        if not t.is_cuda or t.dtype != torch.uint8 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA uint8 tensor")
+    with torch.cuda.device(x.device):
+        s = stream if stream is not None else torch.cuda.current_stream(x.device)
+        N.rmsnorm_fwd_nvfp4(_ptr(x), _ptr(residual), _ptr(w), _ptr(codes), _ptr(scales), _ptr(residual_out), rows,
+                            hidden, float(eps), float(weight_bias), float(tensor_scale), code, plan, s.cuda_stream)
+    return (codes, scales, residual_out) if residual is not None else (codes, scales)
+
+
+def rms_norm_nvfp4_plan_for(x, w=None, residual=None) -> N.Plan:
+    hidden = x.shape[-1]
+    rows = x.numel() // hidden
+    codes = torch.empty(1, dtype=torch.uint8, device=x.device)
+    with torch.cuda.device(x.device):
+        return N.rmsnorm_nvfp4_plan_for(_ptr(x), _ptr(residual), _ptr(w), codes.data_ptr(), codes.data_ptr(),
+                                        _ptr(residual), rows, hidden, dtype_code(x.dtype))

@@ -91,6 +91,44 @@ const void *mx_gt(int gt, int ch, int wm) {
     }
 }
 
+// NVFP4 output (contiguous rows).
+template <typename T, int GT, int CH, bool RES>
+const void *nv_wm(int wm) {
+    switch (wm) {
+        case kNoWeight: return reinterpret_cast<const void *>(&rms_reg_kernel<T, GT, CH, RES, kNoWeight, false, kOutNvfp4>);
+        case kWeight: return reinterpret_cast<const void *>(&rms_reg_kernel<T, GT, CH, RES, kWeight, false, kOutNvfp4>);
+        case kWeightBias:
+            return reinterpret_cast<const void *>(&rms_reg_kernel<T, GT, CH, RES, kWeightBias, false, kOutNvfp4>);
+        default: return nullptr;
+    }
+}
+
+template <typename T, int GT, bool RES>
+const void *nv_ch(int ch, int wm) {
+    switch (ch) {
+        case 1: return nv_wm<T, GT, 1, RES>(wm);
+        case 2: return nv_wm<T, GT, 2, RES>(wm);
+        case 4: return nv_wm<T, GT, 4, RES>(wm);
+        case 8: return nv_wm<T, GT, 8, RES>(wm);
+        default: return nullptr;
+    }
+}
+
+template <typename T, bool RES>
+const void *nv_gt(int gt, int ch, int wm) {
+    switch (gt) {
+        case 4: return nv_ch<T, 4, RES>(ch, wm);
+        case 8: return nv_ch<T, 8, RES>(ch, wm);
+        case 16: return nv_ch<T, 16, RES>(ch, wm);
+        case 32: return nv_ch<T, 32, RES>(ch, wm);
+        case 64: return nv_ch<T, 64, RES>(ch, wm);
+        case 128: return nv_ch<T, 128, RES>(ch, wm);
+        case 256: return nv_ch<T, 256, RES>(ch, wm);
+        case 512: return nv_ch<T, 512, RES>(ch, wm);
+        default: return nullptr;
+    }
+}
+
 template <typename T, int VE, int BLOCK, bool RES, bool HEADS>
 const void *loop_wm(int wm) {
     switch (wm) {

@@ -33,6 +33,15 @@ inline const void *mx_kernel(int dtype, int gt, int ch, bool res, int wm) {
     return res ? mx_reg_f32_res(gt, ch, wm) : mx_reg_f32_plain(gt, ch, wm);
 }
 
+// RMSNorm with NVFP4 output (bf16 I/O, contiguous rows, register kernel only).
+const void *nv_reg_bf16_plain(int gt, int ch, int wm);
+const void *nv_reg_bf16_res(int gt, int ch, int wm);
+
+inline const void *nv_kernel(int dtype, int gt, int ch, bool res, int wm) {
+    if (dtype != 1) return nullptr;
+    return res ? nv_reg_bf16_res(gt, ch, wm) : nv_reg_bf16_plain(gt, ch, wm);
+}
+
 // LayerNorm (contiguous rows); aff: 0 none, 1 weight, 2 weight and bias.
 constexpr int kLnMaxGT = 256;
 const void *ln_reg_f32(int gt, int ch, bool res, int aff);

@@ -68,7 +68,9 @@ struct Op {
     bool ln = false;           // LayerNorm instead of RMSNorm
     const void *b = nullptr;   // LayerNorm bias
     bool mx = false;           // MXFP8 output: y holds E4M3 codes, scales the E8M0 scales
+    bool nv = false;           // NVFP4 output: y holds packed E2M1 codes, scales the E4M3 scales
     void *scales = nullptr;
+    float q_scale = 1.f;       // NVFP4 per-tensor scale
     float eps = 0.f, w_bias = 0.f;
     int wm = 0;                // rrn::WeightMode (RMSNorm) or rrn::AffineMode (LayerNorm)
     int dtype = RMSNORM_BF16;
@@ -160,9 +162,10 @@ int mx_min_gt(int dtype) { return 32 / vec_elems_of(dtype); }
 
 const void *kernel_of(const rmsnorm_plan_t *p, const Op &o) {
     const bool res = o.res != nullptr;
-    if (o.mx) {
+    if (o.mx || o.nv) {
         if (p->kernel != RMSNORM_KERNEL_REG) return nullptr;
-        return rrn::mx_kernel(o.dtype, p->threads_per_row, p->chunks_per_thread, res, o.wm);
+        return o.mx ? rrn::mx_kernel(o.dtype, p->threads_per_row, p->chunks_per_thread, res, o.wm)
+                    : rrn::nv_kernel(o.dtype, p->threads_per_row, p->chunks_per_thread, res, o.wm);
     }
     if (o.ln) {
         if (p->kernel == RMSNORM_KERNEL_REG)
@@ -195,7 +198,7 @@ int validate_plan(const rmsnorm_plan_t *p, const Op &o, int vec_ok) {
         return RMSNORM_OK;
     }
     if (p->kernel == RMSNORM_KERNEL_LOOP) {
-        if (o.mx) return RMSNORM_EINVAL;   // the MXFP8 form runs on the register kernel only
+        if (o.mx || o.nv) return RMSNORM_EINVAL;   // block-scaled forms run on the register kernel only
         if (p->vec_elems != 1 && !(p->vec_elems == V && vec_ok)) return RMSNORM_EINVAL;
         bool known = false;
         for (int b : rrn::kLoopBlocks) known = known || (b == p->block_threads);
@@ -281,8 +284,8 @@ int blocks_per_sm_of(int dev, const void *fn, int block, size_t smem, int *out) 
 // Full device-side planning for an op.
 int plan_for_device(const Op &o, rmsnorm_plan_t *plan, int *dev_out) {
     schedule(o.row_elems, o.dtype, vec_ok_of(o), max_threads_per_row(o), plan);
+    if ((o.mx || o.nv) && plan->kernel != RMSNORM_KERNEL_REG) return RMSNORM_EUNSUPPORTED;
     if (o.mx) {
-        if (plan->kernel != RMSNORM_KERNEL_REG) return RMSNORM_EUNSUPPORTED;
         const int V = vec_elems_of(o.dtype);
         while (plan->threads_per_row < mx_min_gt(o.dtype)) plan->threads_per_row <<= 1;
         int64_t need = ceil_div(o.row_elems / V, plan->threads_per_row);
@@ -356,6 +359,8 @@ int launch(const Op &o, const rmsnorm_plan_t *plan, int dev, rmsnorm_stream_t st
     args.eps = o.eps;
     args.w_bias = o.w_bias;
     args.scales = o.scales;
+    args.q_scale = o.q_scale;
+    args.q_inv6s = (float)(1.0 / (6.0 * (double)o.q_scale));
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -477,6 +482,20 @@ int make_mx(const void *x, const void *residual, const void *w, void *codes, voi
     return RMSNORM_OK;
 }
 
+int make_nv(const void *x, const void *residual, const void *w, void *codes, void *scales, void *residual_out,
+            int64_t rows, int64_t hidden, float eps, float w_bias, float tensor_scale, int dtype, Op *o) {
+    int st = make_contig(x, residual, w, codes, residual_out, rows, hidden, eps, w_bias, dtype, o);
+    if (st != RMSNORM_OK) return st;
+    if (hidden % 16 != 0) return RMSNORM_EINVAL;
+    if (!(tensor_scale > 0.f) || !std::isfinite(tensor_scale)) return RMSNORM_EINVAL;
+    if (dtype != RMSNORM_BF16) return RMSNORM_EUNSUPPORTED;
+    if (rows > 0 && scales == nullptr) return RMSNORM_EINVAL;
+    o->nv = true;
+    o->scales = scales;
+    o->q_scale = tensor_scale;
+    return RMSNORM_OK;
+}
+
 int make_ln(const void *x, const void *residual, const void *w, const void *b, void *y, void *residual_out,
             int64_t rows, int64_t hidden, float eps, int dtype, Op *o) {
     int st = make_contig(x, residual, w, y, residual_out, rows, hidden, eps, 0.f, dtype, o);
@@ -500,6 +519,29 @@ int rmsnorm_fwd_mxfp8(const void *x, const void *residual, const void *w, void *
     if (st != RMSNORM_OK) return st;
     if (rows > 0 && !vec_ok_of(o)) return RMSNORM_EINVAL;   // 16-byte aligned rows required
     return run(o, plan, stream);
+}
+
+int rmsnorm_fwd_nvfp4(const void *x, const void *residual, const void *w, void *codes, void *scales,
+                      void *residual_out, int64_t rows, int64_t hidden, float eps, float weight_bias,
+                      float tensor_scale, int dtype, const rmsnorm_plan_t *plan, rmsnorm_stream_t stream) {
+    Op o;
+    int st = make_nv(x, residual, w, codes, scales, residual_out, rows, hidden, eps, weight_bias, tensor_scale,
+                     dtype, &o);
+    if (st != RMSNORM_OK) return st;
+    if (rows > 0 && !vec_ok_of(o)) return RMSNORM_EINVAL;   // 16-byte aligned rows required
+    return run(o, plan, stream);
+}
+
+int rmsnorm_nvfp4_plan_for(const void *x, const void *residual, const void *w, const void *codes,
+                           const void *scales, const void *residual_out, int64_t rows, int64_t hidden, int dtype,
+                           rmsnorm_plan_t *plan) {
+    if (plan == nullptr) return RMSNORM_EINVAL;
+    Op o;
+    int st = make_nv(x, residual, w, const_cast<void *>(codes), const_cast<void *>(scales),
+                     const_cast<void *>(residual_out), rows, hidden, 0.f, 0.f, 1.f, dtype, &o);
+    if (st != RMSNORM_OK) return st;
+    if (!elem_aligned(o) || !vec_ok_of(o)) return RMSNORM_EINVAL;
+    return plan_for_device(o, plan, nullptr);
 }
 
 int rmsnorm_mxfp8_plan_for(const void *x, const void *residual, const void *w, const void *codes,

@@ -41,6 +41,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp4.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -72,12 +73,15 @@ struct Params {
     float hidden_f;      // row_elems as float (exact for row_elems <= 2^24)
     float eps;
     float w_bias;        // added to every weight element (weight mode kWeightBias)
-    void *scales;        // MXFP8 output: E8M0 scales [rows, row_elems / 32] (y holds the codes)
+    void *scales;        // block-scaled outputs: the scales (y holds the codes)
+    float q_scale;       // NVFP4: per-tensor scale S
+    float q_inv6s;       // NVFP4: 1 / (6 S), rounded once to float
 };
 
-// Output form of the register kernel: the I/O type, or MXFP8 (E4M3 codes in
-// y, one E8M0 scale per 32 elements in scales).
-enum OutputMode { kOutT = 0, kOutMxfp8 = 1 };
+// Output form of the register kernel: the I/O type; MXFP8 (E4M3 codes in y,
+// one E8M0 scale per 32 elements in scales); NVFP4 (E2M1 codes packed two a
+// byte in y, one E4M3 scale per 16 elements in scales).
+enum OutputMode { kOutT = 0, kOutMxfp8 = 1, kOutNvfp4 = 2 };
 
 // How the weight enters y: none, w, or (w + w_bias).
 enum WeightMode { kNoWeight = 0, kWeight = 1, kWeightBias = 2 };
@@ -312,12 +316,33 @@ __device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
     return (uint16_t)__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
 }
 
+// NVFP4: a block of 16 consecutive elements of a row (16 / V lanes) takes the
+// scale E4M3(amax / (6 S)) (nearest-even, saturating) and the codes
+// E2M1(v / (scale * S)), nearest-even, saturated at 6, two per byte with the
+// even element in the low nibble; codes are 0 when the scale is 0.  A block
+// holding NaN or Inf gets the E4M3 NaN 0x7F as its scale and codes 0.
+__device__ __forceinline__ uint8_t e4m3_of(float v) {
+    return (uint8_t)__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3);
+}
+
+// Value of a finite E4M3 code from its bit fields (4 exponent bits, bias 7;
+// 3 fraction bits; subnormals m * 2^-9).
+__device__ __forceinline__ float e4m3_value(uint8_t c) {
+    const int ef = (c >> 3) & 0xF, m = c & 0x7;
+    const float mag = ef == 0 ? (float)m * 0.001953125f : __int_as_float(((ef + 120) << 23) | (m << 20));
+    return (c & 0x80) ? -mag : mag;
+}
+
+__device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
+    return (uint32_t)__nv_cvt_float2_to_fp4x2(make_float2(lo, hi), __NV_E2M1, cudaRoundNearest);
+}
+
 template <typename T, int GT, int CH, bool RES, int WM, bool HEADS, int OUT = kOutT>
 __global__ void __launch_bounds__(reg_block_threads(GT))
 rms_reg_kernel(const Params p) {
     constexpr bool W = WM != kNoWeight;
     static_assert(!(HEADS && RES), "head rows take no residual");
-    static_assert(OUT == kOutT || (!HEADS && GT >= 32 / T::kVec), "MXFP8 output: contiguous rows, "
+    static_assert(OUT == kOutT || (!HEADS && GT >= 32 / T::kVec), "block-scaled output: contiguous rows, "
                                                                   "a block's lanes in one row group");
     constexpr int V = T::kVec;
     constexpr int BLOCK = reg_block_threads(GT);
@@ -469,6 +494,54 @@ rms_reg_kernel(const Params p) {
                         const uint8_t sc = special ? (uint8_t)0xFF : (uint8_t)(s + 127);
                         static_cast<uint8_t *>(p.scales)[row * (p.row_elems / 32) + u / LPB] = sc;
                     }
+                }
+            }
+            continue;
+        }
+        // A7 (NVFP4 form): values, block scale, packed E2M1 codes
+        if constexpr (OUT == kOutNvfp4) {
+            constexpr int LPB = 16 / V;
+#pragma unroll
+            for (int c = 0; c < CH; ++c) {
+                const int u = c * GT + t;
+                const bool valid = row_ok && u < nch;     // uniform over a block's lanes
+                float a[V];
+                unpack(hc[c], a, T{});
+                float wv[V];
+                if constexpr (W) {
+                    unpack(w_smem[valid ? u : 0], wv, T{});
+                } else {
+#pragma unroll
+                    for (int e = 0; e < V; ++e) wv[e] = 1.f;
+                }
+                scale_out_pairs<WM>(a, r, wv, p.w_bias);
+                float amax = 0.f;
+                bool special = false;
+#pragma unroll
+                for (int e = 0; e < V; ++e) {
+                    const float m = fabsf(a[e]);
+                    special |= !(m <= 3.402823466e38f);     // NaN or Inf
+                    amax = fmaxf(amax, m);
+                }
+                mx_block_stats<LPB>(amax, special);
+                const uint8_t sc = special ? (uint8_t)0x7F : e4m3_of(amax * p.q_inv6s);
+                const float sv = special ? 0.f : e4m3_value(sc);
+                uint32_t packed = 0u;
+                if (sv > 0.f) {
+                    const float rcp = 1.f / (sv * p.q_scale);
+#pragma unroll
+                    for (int k = 0; k < V / 2; ++k)
+                        packed |= e2m1x2(a[2 * k] * rcp, a[2 * k + 1] * rcp) << (8 * k);
+                }
+                if (valid) {
+                    char *dst = static_cast<char *>(p.y) + row * (p.row_elems / 2) + (int64_t)u * (V / 2);
+                    if constexpr (V == 8) {
+                        asm volatile("st.global.u32 [%0], %1;" : : "l"(dst), "r"(packed) : "memory");
+                    } else {
+                        asm volatile("st.global.u16 [%0], %1;" : : "l"(dst), "h"((unsigned short)packed) : "memory");
+                    }
+                    if (t % LPB == 0)
+                        static_cast<uint8_t *>(p.scales)[row * (p.row_elems / 16) + u / LPB] = sc;
                 }
             }
             continue;

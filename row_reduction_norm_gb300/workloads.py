@@ -264,3 +264,26 @@ def mx_algorithmic_bytes(wl: Workload) -> int:
     e = wl.rows * wl.hidden
     b = e * wl.elem_bytes * (1 + (2 if wl.has_res else 0)) + e + e // 32
     return b + (wl.hidden * wl.elem_bytes if wl.has_w else 0)
+
+
+# RMSNorm with NVFP4 output (bf16 in): the same shapes as the MXFP8 rows, with a
+# per-tensor scale of 1/64 (block scales stay inside E4M3's range for these
+# distributions: amax / (6 S) <= 448 for amax up to 42).
+NV_TENSOR_SCALE = 1.0 / 64.0
+NV_WORKLOADS = {
+    w.name: w
+    for w in [
+        Workload("nv_bf16_res_16384x2048", "bf16", 16384, 2048, 1e-5, 0.5, 1.0, 0.05,
+                 note="fused residual add, NVFP4 output"),
+        Workload("nv_bf16_res_65536x8192_w", "bf16", 65536, 8192, 1e-6, 1.0, 1.0, 0.1,
+                 outlier_frac=1e-3, outlier_scale=100.0, note="bandwidth case, NVFP4 output"),
+    ]
+}
+
+
+def nv_algorithmic_bytes(wl: Workload) -> int:
+    """Read x (+ residual), write the codes (half a byte an element) and scales
+    (1 per 16) (+ residual_out), read w once."""
+    e = wl.rows * wl.hidden
+    b = e * wl.elem_bytes * (1 + (2 if wl.has_res else 0)) + e // 2 + e // 16
+    return b + (wl.hidden * wl.elem_bytes if wl.has_w else 0)

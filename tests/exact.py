@@ -293,3 +293,58 @@ def mxfp8_row_exact(x, w, residual, eps_value: Fraction, fmt: str, weight_bias: 
             codes.append(e4m3_round_sqrt_sat(-1 if p < 0 else 1, q * Fraction(4) ** (-s)))
             qs.append(q * Fraction(4) ** (-s))
     return codes, scales, qs
+
+
+
+# ---------------------------------------------------------------- E2M1, NVFP4
+E2M1_MAGS = [Fraction(0), Fraction(1, 2), Fraction(1), Fraction(3, 2), Fraction(2), Fraction(3), Fraction(4),
+             Fraction(6)]
+
+
+def e2m1_decode(code: int) -> Fraction:
+    return (-1 if code & 0x8 else 1) * E2M1_MAGS[code & 0x7]
+
+
+def e2m1_round_sqrt_sat(sign: int, q: Fraction) -> int:
+    """E2M1 code of sign*sqrt(q): nearest, ties to the even code, saturated at 6."""
+    sign_bit = 0x8 if sign < 0 else 0
+    if q >= 36:
+        return sign_bit | 7
+    lo = max(i for i in range(8) if E2M1_MAGS[i] ** 2 <= q)
+    if lo == 7:
+        return sign_bit | 7
+    m2 = ((E2M1_MAGS[lo] + E2M1_MAGS[lo + 1]) / 2) ** 2
+    k = lo if q < m2 else lo + 1 if q > m2 else (lo if lo % 2 == 0 else lo + 1)
+    return sign_bit | k
+
+
+def nvfp4_row_exact(x, w, residual, eps_value: Fraction, fmt: str, tensor_scale: Fraction,
+                    weight_bias: Fraction = Fraction(0)):
+    """Exact NVFP4 codes (4-bit, unpacked) and E4M3 block scales of one row
+    (hidden a multiple of 16), with the reading: scale = E4M3(amax / (6 S)),
+    code = E2M1(v / (scale S)).  Returns (codes, scales, q_code_list)."""
+    n = len(x)
+    xs = [decode(b, fmt) for b in x]
+    if residual is not None:
+        rs = [decode(b, fmt) for b in residual]
+        hs = [decode(round_value(a + b, fmt), fmt) for a, b in zip(xs, rs)]
+    else:
+        hs = xs
+    ws = [decode(b, fmt) + weight_bias for b in w] if w is not None else [Fraction(1)] * n
+    denom = sum(h * h for h in hs) / n + eps_value
+    codes, scales, qs = [], [], []
+    for k in range(n // 16):
+        ps = [hs[i] * ws[i] for i in range(16 * k, 16 * k + 16)]
+        q_block = [p * p / denom for p in ps]                   # v_i^2
+        sc = e4m3_round_sqrt_sat(1, max(q_block) / (6 * tensor_scale) ** 2)
+        scales.append(sc)
+        sv = e4m3_decode(sc)
+        for p, q in zip(ps, q_block):
+            if sv == 0:
+                codes.append(0)
+                qs.append(Fraction(0))
+            else:
+                qq = q / (sv * tensor_scale) ** 2
+                codes.append(e2m1_round_sqrt_sat(-1 if p < 0 else 1, qq))
+                qs.append(qq)
+    return codes, scales, qs

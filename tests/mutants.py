@@ -233,3 +233,52 @@ def reference_mx(x, w, residual, eps, dt, weight_bias=0.0, mistake=None):
     if blk == 16:
         scales = scales[:, ::2]
     return codes, scales, h_out, v
+
+
+NV_MISTAKES = ["nv_no_div6", "nv_blocks_of_32", "nv_truncate", "nv_no_saturation", "nv_nibbles_swapped",
+               "nv_tensor_scale_ignored", "nv_scale_ceil"]
+
+
+def _e2m1(v, mode="rne", saturate=True):
+    a = np.abs(np.asarray(v, dtype=np.float64))
+    sign = np.where(np.signbit(v), 0x8, 0)
+    q = np.where(a < 2, 0.5, np.where(a < 4, 1.0, 2.0))
+    s = a / q
+    n = np.rint(s) if mode == "rne" else np.floor(s) if mode == "trunc" else np.ceil(s)
+    r = n * q
+    mags = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6])
+    if saturate:
+        r = np.minimum(r, 6.0)
+        idx = np.searchsorted(mags, r)
+    else:
+        idx = np.where(r > 6.0, 0, np.searchsorted(mags, np.minimum(r, 6.0)))   # overflow wraps to 0
+    return (sign | idx).astype(np.uint8)
+
+
+def reference_nv(x, w, residual, eps, dt, weight_bias=0.0, tensor_scale=1.0, mistake=None):
+    """Numpy NVFP4 RMSNorm on top of ``reference`` with planted mistakes."""
+    _, h_out, v = reference(x, w, residual, eps, dt, weight_bias=weight_bias)
+    rows, hidden = v.shape
+    blk = 32 if mistake == "nv_blocks_of_32" else 16
+    S = 1.0 if mistake == "nv_tensor_scale_ignored" else float(np.float32(tensor_scale))
+    vb = v.reshape(rows, hidden // blk, blk)
+    amax = np.abs(vb).max(axis=2)
+    div = 1.0 if mistake == "nv_no_div6" else 6.0
+    t = amax / (div * S)
+    sc = _e4m3(t) if mistake != "nv_scale_ceil" else _e4m3(t * (1 + 2 ** -4))
+    sv = np.where((sc & 0x7F) == 0, 0.0, _e4m3_values_np(sc))
+    with np.errstate(divide="ignore", invalid="ignore"):
+        scaled = np.where(sv[:, :, None] > 0, vb / (sv[:, :, None] * S), 0.0)
+    mode = "trunc" if mistake == "nv_truncate" else "rne"
+    codes = _e2m1(scaled, mode=mode, saturate=mistake != "nv_no_saturation").reshape(rows, hidden)
+    lo, hi = codes[:, 0::2], codes[:, 1::2]
+    packed = (hi | (lo << 4)) if mistake == "nv_nibbles_swapped" else (lo | (hi << 4))
+    scales = sc if blk == 16 else np.repeat(sc, 2, axis=1)
+    return packed.astype(np.uint8), scales.astype(np.uint8), h_out, v
+
+
+def _e4m3_values_np(codes):
+    c = np.asarray(codes, dtype=np.int64)
+    ef = (c >> 3) & 0xF
+    m = c & 0x7
+    return np.where(ef == 0, m / 8.0 * 2.0 ** -6, (1 + m / 8.0) * np.ldexp(1.0, ef - 7))

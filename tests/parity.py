@@ -171,3 +171,58 @@ def compare_mx(codes_g, scales_g, codes_o, scales_o, v64, e4m3_encode):
         report["code_flips"] = int(ok.sum())
         report["bad"] += int((mism & ~ok).sum())
     return report["bad"] == 0, report
+
+
+# NVFP4: as MXFP8, integers decided by fp32.  The kernel's block scale comes
+# from amax * RN(1 / (6 S)) and its codes from v * RN(1 / RN(scale * S)),
+# three more roundings than the exact quotients: NV_REL_TOL covers them.
+NV_REL_TOL = 2.5e-6
+E2M1_MAGS = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+
+def _e4m3_mid_near(t, a, b, tol):
+    """t (>= 0) lies within tol (relative) of the midpoint of E4M3 codes a, b."""
+    va, vb = _e4m3_values(a), _e4m3_values(b)
+    m = (va + vb) / 2
+    return np.abs(t - m) <= tol * np.maximum(m, 1e-300)
+
+
+def compare_nv(packed_g, scales_g, packed_o, scales_o, v64, tensor_scale, e2m1_encode):
+    g = np.asarray(packed_g)
+    rows = g.shape[0]
+    cg = np.empty((rows, g.shape[1] * 2), dtype=np.int64)
+    cg[:, 0::2], cg[:, 1::2] = g & 0xF, g >> 4
+    hidden = cg.shape[1]
+    nb = hidden // 16
+    vb = v64.reshape(rows, nb, 16)
+    S = float(np.float32(tensor_scale))
+    special = ~np.isfinite(vb).all(axis=2)
+    amax = np.where(special, 0.0, np.abs(np.where(np.isfinite(vb), vb, 0.0)).max(axis=2))
+    sg = np.asarray(scales_g).astype(np.int64)
+    so = np.asarray(scales_o).astype(np.int64)
+    rep = {"scale_flips": 0, "code_flips": 0, "bad": 0}
+    diff = sg != so
+    if diff.any():
+        t = amax / (6.0 * S)
+        ok_flip = diff & ~special & (np.abs(sg - so) == 1) & _e4m3_mid_near(t, sg, so, NV_REL_TOL)
+        rep["scale_flips"] = int(ok_flip.sum())
+        if (diff & ~ok_flip).any():
+            rep["bad"] += int((diff & ~ok_flip).sum())
+            return False, rep
+    sv = np.where(special, 0.0, _e4m3_values(sg))
+    with np.errstate(divide="ignore", invalid="ignore"):
+        scaled = np.where(sv[:, :, None] > 0, vb / (sv[:, :, None] * S), 0.0)
+    want = e2m1_encode(np.where(np.isfinite(scaled), scaled, 0.0)).reshape(rows, nb, 16).astype(np.int64)
+    want = np.where(special[:, :, None], 0, want)
+    got = cg.reshape(rows, nb, 16)
+    mism = got != want
+    if mism.any():
+        lo = np.minimum(got & 7, want & 7)
+        hi = np.maximum(got & 7, want & 7)
+        mid = (E2M1_MAGS[lo] + E2M1_MAGS[np.minimum(hi, 7)]) / 2
+        adjacent = (hi - lo == 1) & ((got & 8) == (want & 8))
+        near = np.abs(np.abs(scaled) - mid) <= NV_REL_TOL * np.maximum(mid, 1e-300)
+        ok = mism & adjacent & near
+        rep["code_flips"] = int(ok.sum())
+        rep["bad"] += int((mism & ~ok).sum())
+    return rep["bad"] == 0, rep

@@ -651,6 +651,106 @@ def pin_mx_closed_forms(impl_mx):
 MX_PINS = [pin_mx_closed_forms, pin_mx_bruteforce]
 
 
+# ----------------------------------------------------------------- NVFP4 pins
+# impl_nv(x, w, residual, eps, dtype, weight_bias, tensor_scale) -> (codes packed, scales, residual_out, v_exact)
+
+def unpack_nibbles(packed):
+    p = np.asarray(packed, dtype=np.uint8)
+    out = np.empty(p.shape[:-1] + (p.shape[-1] * 2,), dtype=np.uint8)
+    out[..., 0::2] = p & 0xF
+    out[..., 1::2] = p >> 4
+    return out
+
+
+def pin_e2m1_codec(e2m1, e2m1_inv):
+    """The 16 codes decode to their definition's values; every midpoint rounds
+    to the even code; magnitudes above 6 saturate."""
+    fails = []
+    vals = e2m1_inv(np.arange(16, dtype=np.uint8))
+    for c in range(16):
+        if Fraction(float(vals[c])) != exact.e2m1_decode(c):
+            fails.append(f"e2m1 {c:#x}: {vals[c]}")
+    pts, want = [], []
+    for i in range(7):
+        a, b = exact.E2M1_MAGS[i], exact.E2M1_MAGS[i + 1]
+        m = float((a + b) / 2)
+        pts += [m, m * (1 - 2 ** -40), m * (1 + 2 ** -40), -m]
+        want += [i if i % 2 == 0 else i + 1, i, i + 1, 0x8 | (i if i % 2 == 0 else i + 1)]
+    pts += [6.0, 6.9, 7.0, 1e9]
+    want += [7, 7, 7, 7]
+    got = e2m1(np.array(pts))
+    for p, w_, g in zip(pts, want, got):
+        if int(g) != w_:
+            fails.append(f"e2m1({p}) = {int(g):#x}, want {w_:#x}")
+    return fails
+
+
+def pin_nv_bruteforce(impl_nv, n_cases=24, seed=707):
+    """Random rows of 16 or 32 elements, several tensor scales: packed codes and
+    scales equal the exact rational answer (except values within 2^-43 of a
+    rounding midpoint)."""
+    rng = np.random.default_rng(seed)
+    fails = []
+    for k in range(n_cases):
+        dt = ("bf16", "f32")[k % 2]
+        hidden = (16, 32)[(k // 2) % 2]
+        has_w = bool((k // 4) % 2)
+        has_res = bool((k // 8) % 2)
+        S = (1.0, 0.125, 1.0 / 6.0, 3.0)[k % 4]
+        b = 1.0 if (has_w and k % 3 == 0) else 0.0
+        eps = (0.0, 1e-6, 0.5)[k % 3]
+        rows = 2
+        xb = [random_bits(rng, dt, hidden, -6, 6) for _ in range(rows)]
+        rb = [random_bits(rng, dt, hidden, -4, 4) for _ in range(rows)] if has_res else None
+        wb = random_bits(rng, dt, hidden, -2, 2) if has_w else None
+        x = to_array(sum(xb, []), dt).reshape(rows, hidden)
+        res = to_array(sum(rb, []), dt).reshape(rows, hidden) if has_res else None
+        w = to_array(wb, dt) if has_w else None
+        codes, scales, _, _ = impl_nv(x, w, res, eps, dt, b, S)
+        codes = unpack_nibbles(codes)
+        for r in range(rows):
+            wc, ws, qs = exact.nvfp4_row_exact(xb[r], wb, rb[r] if has_res else None, f32_exact(eps), dt,
+                                              Fraction(float(np.float32(S))), Fraction(b))
+            if [int(v) for v in scales[r]] != ws:
+                fails.append(f"nv case {k} row {r}: scales {list(scales[r])} != {ws}")
+                continue
+            for i in range(hidden):
+                if int(codes[r, i]) != wc[i]:
+                    lo, hi = sorted([int(codes[r, i]) & 7, wc[i] & 7])
+                    near = False
+                    if hi == lo + 1:
+                        m2 = ((exact.E2M1_MAGS[lo] + exact.E2M1_MAGS[hi]) / 2) ** 2
+                        near = abs(qs[i] - m2) / m2 < Fraction(1, 2 ** 43)
+                    if not near:
+                        fails.append(f"nv case {k} ({dt}, H={hidden}, S={S}) row {r} elem {i}: "
+                                     f"{int(codes[r, i]):#x} != {wc[i]:#x}")
+    return fails
+
+
+def pin_nv_closed_forms(impl_nv):
+    """A constant row with eps = 0 normalises to +-1; with tensor scale 1/6
+    the block scale is E4M3(1) = 0x38 and every code is +-6 (0x7 / 0xF),
+    packed low nibble first.  A zero row gives scale 0 and codes 0."""
+    fails = []
+    for dt in ("bf16", "f32"):
+        S = float(np.float32(1.0 / 6.0))
+        c = encode_exact(Fraction(-5, 4), dt)
+        codes, scales, _, _ = impl_nv(to_array([c] * 32, dt).reshape(1, 32), None, None, 0.0, dt, 0.0, S)
+        if [int(v) for v in scales[0]] != [0x38, 0x38] or any(int(v) != 0xFF for v in codes[0]):
+            fails.append(f"nv constant row {dt}: {list(scales[0])} {list(codes[0])}")
+        xs = to_array([encode_exact(Fraction(1), dt), encode_exact(Fraction(-1), dt)] * 8, dt)
+        codes, scales, _, _ = impl_nv(xs.reshape(1, 16), None, None, 0.0, dt, 0.0, S)
+        if [int(v) for v in codes[0]] != [0xF7] * 8:       # +6 (0x7) in the low nibble, -6 (0xF) high
+            fails.append(f"nv nibble order {dt}: {list(codes[0])}")
+        codes, scales, _, _ = impl_nv(to_array([0] * 16, dt).reshape(1, 16), None, None, 1e-5, dt, 0.0, 1.0)
+        if int(scales[0, 0]) != 0 or any(int(v) != 0 for v in codes[0]):
+            fails.append(f"nv zero row {dt}")
+    return fails
+
+
+NV_PINS = [pin_nv_closed_forms, pin_nv_bruteforce]
+
+
 ALL_PINS = [pin_golden, pin_bruteforce, pin_constant_row, pin_scale_invariance,
             pin_unit_rms, pin_special_values, pin_single_element, pin_row_independence,
             pin_eps_dominated, pin_near_ties]

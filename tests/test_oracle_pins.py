@@ -214,3 +214,63 @@ def test_compare_helpers_flag_planted_differences():
     y2 = y.copy()
     y2[0, 0] += 2
     assert not parity.compare_y(y2, y, "bf16")[0]
+
+
+
+def oracle_impl_nv(x, w, residual, eps, dtype, weight_bias, tensor_scale):
+    return oracle.rmsnorm_nvfp4(x, w=w, residual=residual, eps=eps, dtype=dtype, weight_bias=weight_bias,
+                                tensor_scale=tensor_scale)
+
+
+def test_oracle_e2m1_codec():
+    assert pins.pin_e2m1_codec(oracle.e2m1_from_double, oracle.double_from_e2m1) == []
+
+
+@pytest.mark.parametrize("pin", pins.NV_PINS, ids=lambda p: p.__name__)
+def test_oracle_nv_pin(pin):
+    assert pin(oracle_impl_nv) == []
+
+
+def test_nv_restatement_passes_pins_and_matches_oracle():
+    impl = lambda x, w, r, e, d, b, S: mutants.reference_nv(x, w, r, e, d, weight_bias=b, tensor_scale=S)
+    for pin in pins.NV_PINS:
+        assert pin(impl) == [], pin.__name__
+    assert pins.pin_e2m1_codec(lambda v: mutants._e2m1(v), oracle.double_from_e2m1) == []
+    from row_reduction_norm_gb300 import workloads as W
+    x = W.to_numpy_bits(W.random_rows("bf16", 64, 2048, seed=6))
+    a = oracle.rmsnorm_nvfp4(x, eps=1e-6, dtype="bf16", tensor_scale=0.25)
+    b = mutants.reference_nv(x, None, None, 1e-6, "bf16", tensor_scale=0.25)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("mistake", mutants.NV_MISTAKES)
+def test_nv_pins_catch_planted_mistake(mistake):
+    impl = lambda x, w, r, e, d, b, S: mutants.reference_nv(x, w, r, e, d, weight_bias=b, tensor_scale=S,
+                                                            mistake=mistake)
+    caught = []
+    for p in pins.NV_PINS:
+        try:
+            if p(impl):
+                caught.append(p.__name__)
+        except Exception as ex:   # a crash also counts as caught
+            caught.append(f"{p.__name__}: {ex!r}")
+    if not caught and mistake in ("nv_truncate", "nv_no_saturation"):
+        enc = lambda v: mutants._e2m1(v, mode="trunc" if mistake == "nv_truncate" else "rne",
+                                      saturate=mistake != "nv_no_saturation")
+        caught = ["pin_e2m1_codec"] if pins.pin_e2m1_codec(enc, oracle.double_from_e2m1) else []
+    assert caught, mistake
+
+
+
+def test_compare_nv_flags_planted_differences():
+    import parity
+    from row_reduction_norm_gb300 import workloads as W
+    x = W.to_numpy_bits(W.random_rows("bf16", 16, 512, seed=2))
+    co, so, _, v = oracle.rmsnorm_nvfp4(x, eps=1e-5, dtype="bf16", tensor_scale=1 / 64)
+    assert parity.compare_nv(co, so, co, so, v, 1 / 64, oracle.e2m1_from_double)[0]
+    c2 = co.copy()
+    c2[1, 3] ^= 0x02
+    assert not parity.compare_nv(c2, so, co, so, v, 1 / 64, oracle.e2m1_from_double)[0]
+    s2 = so.copy()
+    s2[4, 2] += 1
+    assert not parity.compare_nv(co, s2, co, so, v, 1 / 64, oracle.e2m1_from_double)[0]
