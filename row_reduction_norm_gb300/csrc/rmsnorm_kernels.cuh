@@ -528,7 +528,9 @@ rms_reg_kernel(const Params p) {
                 const float sv = special ? 0.f : e4m3_value(sc);
                 uint32_t packed = 0u;
                 if (sv > 0.f) {
-                    const float rcp = 1.f / (sv * p.q_scale);
+                    // fast reciprocal (CUDA documents <= 2 ulp): the code decision
+                    // tolerance covers it (a few 1e-7 against 2.5e-6)
+                    const float rcp = __fdividef(1.f, sv * p.q_scale);
 #pragma unroll
                     for (int k = 0; k < V / 2; ++k)
                         packed |= e2m1x2(a[2 * k] * rcp, a[2 * k + 1] * rcp) << (8 * k);

@@ -174,8 +174,9 @@ def compare_mx(codes_g, scales_g, codes_o, scales_o, v64, e4m3_encode):
 
 
 # NVFP4: as MXFP8, integers decided by fp32.  The kernel's block scale comes
-# from amax * RN(1 / (6 S)) and its codes from v * RN(1 / RN(scale * S)),
-# three more roundings than the exact quotients: NV_REL_TOL covers them.
+# from amax * RN(1 / (6 S)) and its codes from v * rcp(RN(scale * S)) with a
+# fast reciprocal (<= 2 ulp): a few 1e-7 more than the exact quotients on top
+# of the op's 1.1e-6, inside NV_REL_TOL.
 NV_REL_TOL = 2.5e-6
 E2M1_MAGS = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
 
