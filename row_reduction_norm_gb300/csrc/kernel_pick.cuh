@@ -17,6 +17,8 @@ const void *reg_wm(int wm) {
     }
 }
 
+// Chunks per thread: powers of two, plus 3 and 6 for contiguous rows (rows of
+// 3 * 2^k or 6 * 2^k chunks, e.g. widths 576 and 768, then fill every slot).
 template <typename T, int GT, bool RES, bool HEADS>
 const void *reg_ch(int ch, int wm) {
     switch (ch) {
@@ -24,8 +26,16 @@ const void *reg_ch(int ch, int wm) {
         case 2: return reg_wm<T, GT, 2, RES, HEADS>(wm);
         case 4: return reg_wm<T, GT, 4, RES, HEADS>(wm);
         case 8: return reg_wm<T, GT, 8, RES, HEADS>(wm);
-        default: return nullptr;
+        default: break;
     }
+    if constexpr (!HEADS) {
+        switch (ch) {
+            case 3: return reg_wm<T, GT, 3, RES, HEADS>(wm);
+            case 6: return reg_wm<T, GT, 6, RES, HEADS>(wm);
+            default: break;
+        }
+    }
+    return nullptr;
 }
 
 template <typename T, bool RES, bool HEADS, int MAXGT>

@@ -22,7 +22,9 @@ const void *reg_ch(int ch, int aff) {
     switch (ch) {
         case 1: return reg_aff<T, GT, 1, RES>(aff);
         case 2: return reg_aff<T, GT, 2, RES>(aff);
+        case 3: return reg_aff<T, GT, 3, RES>(aff);
         case 4: return reg_aff<T, GT, 4, RES>(aff);
+        case 6: return reg_aff<T, GT, 6, RES>(aff);
         case 8: return reg_aff<T, GT, 8, RES>(aff);
         default: return nullptr;
     }

@@ -96,7 +96,9 @@ int vec_ok_of(const Op &o) {
 }
 
 // The per-row schedule: everything but the grid.
-void schedule(int64_t hidden, int dtype, int vec_ok, int max_gt, rmsnorm_plan_t *p) {
+// odd_ch: chunk counts 3 and 6 may be chosen (a row of 3 * 2^k chunks then
+// fills every slot); measured to help LayerNorm rows, not RMSNorm rows.
+void schedule(int64_t hidden, int dtype, int vec_ok, int max_gt, rmsnorm_plan_t *p, bool odd_ch = false) {
     std::memset(p, 0, sizeof(*p));
     const int V = vec_elems_of(dtype);
     if (vec_ok) {
@@ -113,6 +115,7 @@ void schedule(int64_t hidden, int dtype, int vec_ok, int max_gt, rmsnorm_plan_t 
             int64_t need = ceil_div(nch, gt);
             int ch = 1;
             while (ch < need) ch <<= 1;
+            if (odd_ch && (need == 3 || need == 5 || need == 6)) ch = need == 3 ? 3 : 6;
             p->kernel = RMSNORM_KERNEL_REG;
             p->threads_per_row = (int32_t)gt;
             p->chunks_per_thread = ch;
@@ -191,7 +194,9 @@ int validate_plan(const rmsnorm_plan_t *p, const Op &o, int vec_ok) {
         if (!vec_ok || p->vec_elems != V) return RMSNORM_EINVAL;
         if (gt < 4 || gt > max_gt || (gt & (gt - 1)) != 0) return RMSNORM_EINVAL;
         if (o.mx && gt < mx_min_gt(o.dtype)) return RMSNORM_EINVAL;
-        if (ch < 1 || ch > rrn::kRegMaxCH || (ch & (ch - 1)) != 0) return RMSNORM_EINVAL;
+        const bool odd_ch = ch == 3 || ch == 6;   // compiled for contiguous RMSNorm / LayerNorm rows
+        if (ch < 1 || ch > rrn::kRegMaxCH || ((ch & (ch - 1)) != 0 && !odd_ch)) return RMSNORM_EINVAL;
+        if (odd_ch && (o.head_rows || o.mx || o.nv)) return RMSNORM_EINVAL;
         if ((int64_t)gt * ch * V < o.row_elems) return RMSNORM_EINVAL;
         if (p->block_threads != rrn::reg_block_threads(gt)) return RMSNORM_EINVAL;
         if (p->rows_per_block != p->block_threads / gt) return RMSNORM_EINVAL;
@@ -283,7 +288,7 @@ int blocks_per_sm_of(int dev, const void *fn, int block, size_t smem, int *out) 
 
 // Full device-side planning for an op.
 int plan_for_device(const Op &o, rmsnorm_plan_t *plan, int *dev_out) {
-    schedule(o.row_elems, o.dtype, vec_ok_of(o), max_threads_per_row(o), plan);
+    schedule(o.row_elems, o.dtype, vec_ok_of(o), max_threads_per_row(o), plan, o.ln);
     if ((o.mx || o.nv) && plan->kernel != RMSNORM_KERNEL_REG) return RMSNORM_EUNSUPPORTED;
     if (o.mx) {
         const int V = vec_elems_of(o.dtype);

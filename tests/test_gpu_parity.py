@@ -91,17 +91,18 @@ def test_workload_large_sampled(name):
 
 # ------------------------------------------------------------ forced plans
 
-def all_plans(rows, hidden, dtype_code, vec_ok, sm_count=152):
+def all_plans(rows, hidden, dtype_code, vec_ok, sm_count=152, odd_ch=False):
     """Every launch plan that is valid for the shape: all REG (threads, chunks)
-    pairs that cover the row, the two-pass kernel (vector / scalar, each block
-    size that keeps the accuracy bound), each in a full grid and a small
+    pairs that cover the row (chunks 3 and 6 too with ``odd_ch``, compiled for
+    contiguous rows), the two-pass kernel (vector / scalar, each block size
+    that keeps the accuracy bound), each in a full grid and a small
     (persistent) grid."""
     V = 8 if dtype_code == N.RMSNORM_BF16 else 4
     plans = []
     if vec_ok:
         nch = hidden // V
         for gt in (4, 8, 16, 32, 64, 128, 256, 512):
-            for ch in (1, 2, 4, 8):
+            for ch in ((1, 2, 3, 4, 6, 8) if odd_ch else (1, 2, 4, 8)):
                 if gt * ch * V < hidden:
                     continue
                 p = N.Plan()
@@ -147,7 +148,7 @@ def test_every_plan_matches_oracle(rows, hidden, dtype):
     code = R.dtype_code(x.dtype)
     yr, hr = oracle_run(x, r, w, wl.eps, dtype)
     yr_nr, _ = oracle_run(x, None, None, wl.eps, dtype)
-    plans = all_plans(rows, hidden, code, True)
+    plans = all_plans(rows, hidden, code, True, odd_ch=True)
     assert plans
     for p in plans:
         y, h = R.rms_norm(x, w=w, residual=r, eps=wl.eps, plan=p)
