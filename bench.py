@@ -647,6 +647,7 @@ def run_ours(args):
         return
 
     L = Launcher(wl, device, stream, min_footprint)
+    headline_sets = L.n_sets
     sampler = ClockSampler(gpu_id_for(local)) if rank == 0 else None
     if sampler:
         sampler.start()
@@ -673,22 +674,15 @@ def run_ours(args):
     if not args.no_per_config:
         del L
         torch.cuda.empty_cache()
-        for name in (PER_CONFIG + list(W.QK_WORKLOADS) + list(W.LN_WORKLOADS) + list(W.MX_WORKLOADS)
-                     + list(W.NV_WORKLOADS)):
-            qk = name in W.QK_WORKLOADS
-            ln = name in W.LN_WORKLOADS
-            mx = name in W.MX_WORKLOADS
-            nv = name in W.NV_WORKLOADS
-            cw = (W.QK_WORKLOADS[name] if qk else W.LN_WORKLOADS[name] if ln else
-                  W.MX_WORKLOADS[name] if mx else W.NV_WORKLOADS[name] if nv else W.WORKLOADS[name])
-            CL = (QKLauncher if qk else LNLauncher if ln else MXLauncher if mx else NVLauncher if nv else Launcher)(
-                cw, device, stream, min_footprint)
+        for name, (cw, launcher_cls, bytes_of, kind) in per_config_table(W).items():
+            qk, ln, mx, nv = kind == "qk", kind == "ln", kind == "mx", kind == "nv"
+            CL = launcher_cls(cw, device, stream, min_footprint)
             # calibrate: about 0.3 s of launches
             cal = time_launches(CL, 64, 8)
             k = int(max(64, min(200000, 0.3 / max(cal / 1e3 / 64, 1e-9))))
             cms = time_launches(CL, k, max(3, k // 20), barrier=barrier)
             t_launch = cms / 1e3 / k
-            b = W.mx_algorithmic_bytes(cw) if mx else W.nv_algorithmic_bytes(cw) if nv else cw.algorithmic_bytes()
+            b = bytes_of(cw)
             rows = cw.tokens * (cw.q_heads + cw.k_heads) if qk else cw.rows
             entry = {"workload": name, "rows": rows, "hidden": cw.head_dim if qk else cw.hidden,
                      "dtype": cw.dtype, "bytes_per_launch": b, "us_per_launch": round(t_launch * 1e6, 3),
@@ -745,7 +739,7 @@ def run_ours(args):
         "config": {
             "workload": wl.name, "rows": wl.rows, "hidden": wl.hidden, "eps": wl.eps,
             "residual": wl.has_res, "weight": wl.has_w, "bytes_per_step": launch_bytes,
-            "l2": f"inputs larger than L2 in aggregate: launches rotate over {L_sets(args, wl, min_footprint)} "
+            "l2": f"inputs larger than L2 in aggregate: launches rotate over {headline_sets} "
                   f"buffer sets (>= 4x the {l2 // 2**20} MiB L2)",
             "timing": "CUDA graphs of C-ABI launches, CUDA events on the launching stream",
             "plan": plan_summary(L.plan),
@@ -777,27 +771,41 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def per_config_table(W):
+    """name -> (workload, launcher class, algorithmic bytes of one launch, kind)
+    for every workload the per-config table times, in order."""
+    table = {}
+    for name in PER_CONFIG:
+        table[name] = (W.WORKLOADS[name], Launcher, lambda w: w.algorithmic_bytes(), "rms")
+    for name, wl in W.QK_WORKLOADS.items():
+        table[name] = (wl, QKLauncher, lambda w: w.algorithmic_bytes(), "qk")
+    for name, wl in W.LN_WORKLOADS.items():
+        table[name] = (wl, LNLauncher, lambda w: w.algorithmic_bytes(), "ln")
+    for name, wl in W.MX_WORKLOADS.items():
+        table[name] = (wl, MXLauncher, W.mx_algorithmic_bytes, "mx")
+    for name, wl in W.NV_WORKLOADS.items():
+        table[name] = (wl, NVLauncher, W.nv_algorithmic_bytes, "nv")
+    return table
+
+
 def run_profile_case(args, device, stream):
     """A few launches of one workload, for ncu (no timing)."""
     import dataclasses
     import torch
     from row_reduction_norm_gb300 import _native as N
     from row_reduction_norm_gb300 import api, workloads as W
-    special = {**W.QK_WORKLOADS, **W.LN_WORKLOADS, **W.MX_WORKLOADS, **W.NV_WORKLOADS}
-    if args.ncu_case in special:
-        qk = args.ncu_case in W.QK_WORKLOADS
-        ln = args.ncu_case in W.LN_WORKLOADS
-        nv = args.ncu_case in W.NV_WORKLOADS
-        wl = special[args.ncu_case]
+    table = per_config_table(W)
+    if args.ncu_case in table and table[args.ncu_case][3] != "rms":
+        wl, launcher_cls, bytes_of, kind = table[args.ncu_case]
+        qk = kind == "qk"
         if not qk and (args.rows or args.hidden):
             wl = dataclasses.replace(wl, rows=args.rows or wl.rows, hidden=args.hidden or wl.hidden)
-        L = (QKLauncher if qk else LNLauncher if ln else NVLauncher if nv else MXLauncher)(wl, device, stream, 0)
+        L = launcher_cls(wl, device, stream, 0)
         with torch.cuda.stream(stream):
             for i in range(args.launches):
                 L.launch(i)
         stream.synchronize()
-        nbytes = (wl.algorithmic_bytes() if (qk or ln) else
-                  W.nv_algorithmic_bytes(wl) if nv else W.mx_algorithmic_bytes(wl))
+        nbytes = bytes_of(wl)
         rows = wl.tokens * (wl.q_heads + wl.k_heads) if qk else wl.rows
         print(json.dumps({"ncu_case": wl.name, "rows": rows, "hidden": wl.head_dim if qk else wl.hidden,
                           "launches": args.launches, "bytes_per_launch": nbytes, "plan": plan_summary(L.plan)}))
@@ -830,11 +838,6 @@ def run_profile_case(args, device, stream):
     print(json.dumps({"ncu_case": wl.name, "rows": wl.rows, "hidden": wl.hidden,
                       "launches": args.launches, "bytes_per_launch": wl.algorithmic_bytes(),
                       "plan": plan_summary(plan)}))
-
-
-def L_sets(args, wl, min_footprint):
-    per_set = wl.rows * wl.hidden * wl.elem_bytes * (4 if wl.has_res else 2)
-    return max(1, math.ceil(min_footprint / max(per_set, 1)))
 
 
 def run_reference(args):

@@ -97,8 +97,10 @@ typedef struct {
     int32_t regime;             /* RMSNORM_REGIME_*                                   */
     int32_t threads_per_row;    /* REG: 4..512 (4..32 for head rows), power of two;
                                    LOOP: block_threads                                */
-    int32_t chunks_per_thread;  /* REG: upper bound of vector chunks per thread; LOOP:
-                                   0                                                  */
+    int32_t chunks_per_thread;  /* REG: vector chunks per thread (an upper bound:
+                                   slots past the row end stay idle); 1, 2, 4 or 8,
+                                   and 3 or 6 for contiguous RMSNorm / LayerNorm rows
+                                   in the I/O type; LOOP: 0                          */
     int32_t vec_elems;          /* elements per load: 16 / sizeof(T), or 1 (scalar)  */
     int32_t block_threads;      /* threads per block                                  */
     int32_t rows_per_block;     /* rows one block handles per loop iteration          */
@@ -148,10 +150,11 @@ int rmsnorm_plan_for(const void *x, const void *residual, const void *w, const v
 /*
  * rmsnorm_fwd with a caller-chosen plan (tests and schedule sweeps).  The plan
  * is validated against the shape and the pointers: a REG plan must cover the
- * row (threads_per_row * chunks_per_thread * vec_elems >= hidden, with
- * chunks_per_thread <= the compiled bound), block_threads and rows_per_block
- * must match threads_per_row, a vector plan needs aligned pointers, and
- * grid >= 1.  Returns RMSNORM_EINVAL for a plan that does not fit.
+ * row (threads_per_row * chunks_per_thread * vec_elems >= hidden, with a
+ * compiled chunks_per_thread, see rmsnorm_plan_t), block_threads and
+ * rows_per_block must match threads_per_row, a vector plan needs aligned
+ * pointers, grid >= 1, pdl 0 or 1 and reserved 0.  Returns RMSNORM_EINVAL for
+ * a plan that does not fit.
  */
 int rmsnorm_fwd_plan(const void *x, const void *residual, const void *w, void *y,
                      void *residual_out, int64_t rows, int64_t hidden, float eps,
