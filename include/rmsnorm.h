@@ -74,8 +74,12 @@ enum {
 /* Kernel families (rmsnorm_plan_t.kernel). */
 enum {
     RMSNORM_KERNEL_REG = 0,   /* row held in registers, 128-bit I/O, one pass     */
-    RMSNORM_KERNEL_LOOP = 1   /* row streamed twice (second read from L2): any
-                                 alignment, and rows too long for registers       */
+    RMSNORM_KERNEL_LOOP = 1,  /* row streamed twice (second read from L2): any
+                                 alignment, and rows too long for the ring below  */
+    RMSNORM_KERNEL_TMA = 2    /* row staged in shared memory by bulk (TMA) copies:
+                                 rings for x, residual and weight fed by three
+                                 producer warps, 512 threads a row; contiguous
+                                 RMSNorm rows too long for registers              */
 };
 
 /* Regimes (rmsnorm_plan_t.regime), a summary of how rows map to threads. */
@@ -84,7 +88,9 @@ enum {
     RMSNORM_REGIME_CTA = 1,         /* several warps per row, shared-memory combine  */
     RMSNORM_REGIME_PERSISTENT = 2,  /* grid capped at the resident capacity; blocks
                                        stride over the rows                          */
-    RMSNORM_REGIME_LOOPED = 3       /* RMSNORM_KERNEL_LOOP                           */
+    RMSNORM_REGIME_LOOPED = 3,      /* RMSNORM_KERNEL_LOOP                           */
+    RMSNORM_REGIME_SMEM = 4         /* RMSNORM_KERNEL_TMA: one block per SM, blocks
+                                       stride over the rows                          */
 };
 
 /*
@@ -96,13 +102,20 @@ typedef struct {
     int32_t kernel;             /* RMSNORM_KERNEL_*                                   */
     int32_t regime;             /* RMSNORM_REGIME_*                                   */
     int32_t threads_per_row;    /* REG: 4..512 (4..32 for head rows), power of two;
-                                   LOOP: block_threads                                */
+                                   LOOP: block_threads; TMA: 512                      */
     int32_t chunks_per_thread;  /* REG: vector chunks per thread (an upper bound:
                                    slots past the row end stay idle); 1, 2, 4 or 8,
                                    and 3 or 6 for contiguous RMSNorm / LayerNorm rows
-                                   in the I/O type; LOOP: 0                          */
+                                   in the I/O type; LOOP: 0; TMA: chunks per thread
+                                   in one ring piece: 1, 2 or 4 (8, 16 or 32 KB
+                                   pieces; 28, 14 or 7 slots of shared memory, of
+                                   which avail / 7 (at least 1) go to a streamed
+                                   residual ring and as many to a streamed weight
+                                   ring -- one per piece when the weight stays
+                                   resident -- and the rest, which must hold a
+                                   whole row, to x)                                  */
     int32_t vec_elems;          /* elements per load: 16 / sizeof(T), or 1 (scalar)  */
-    int32_t block_threads;      /* threads per block                                  */
+    int32_t block_threads;      /* threads per block (TMA: 608)                       */
     int32_t rows_per_block;     /* rows one block handles per loop iteration          */
     int32_t persistent;         /* 1 if grid < row blocks (blocks stride over rows)   */
     int32_t pdl;                /* 1: launch with programmatic stream serialisation
@@ -152,7 +165,8 @@ int rmsnorm_plan_for(const void *x, const void *residual, const void *w, const v
  * is validated against the shape and the pointers: a REG plan must cover the
  * row (threads_per_row * chunks_per_thread * vec_elems >= hidden, with a
  * compiled chunks_per_thread, see rmsnorm_plan_t), block_threads and
- * rows_per_block must match threads_per_row, a vector plan needs aligned
+ * rows_per_block must match threads_per_row, a TMA plan must fit the row in
+ * its ring (see rmsnorm_plan_t), a vector plan (REG, TMA) needs aligned
  * pointers, grid >= 1, pdl 0 or 1 and reserved 0.  Returns RMSNORM_EINVAL for
  * a plan that does not fit.
  */
@@ -296,6 +310,19 @@ int64_t rmsnorm_max_hidden(int dtype);
 
 /* Largest chunks_per_thread a REG plan may use. */
 int rmsnorm_reg_max_chunks(void);
+
+/*
+ * Every wait inside the RMSNORM_KERNEL_TMA kernel (for a bulk copy to land,
+ * for a ring slot to be released) gives up after one second; the block then
+ * finishes its rows without waiting (its outputs are not valid), waits, again
+ * at most a second each, for its copies still in flight, and adds 1 to a
+ * per-device counter.  This reads that counter for the current device (the
+ * count since the library was loaded; 0 unless a launch went wrong).  It is a
+ * blocking device-to-host read: call it after synchronising the streams that
+ * ran the kernels, and not while a stream is being captured.
+ * Returns RMSNORM_OK, RMSNORM_EINVAL (count NULL) or RMSNORM_ECUDA.
+ */
+int rmsnorm_wait_timeouts(uint32_t *count);
 
 /* Static text for a status code. */
 const char *rmsnorm_strerror(int status);

@@ -12,7 +12,7 @@ from ._native import (  # noqa: F401  (the C ABI, same names)
     rmsnorm_max_hidden, rmsnorm_plan, rmsnorm_plan_for, rmsnorm_qk_fwd, rmsnorm_qk_plan_for,
     layernorm_fwd, layernorm_plan_for, rmsnorm_fwd_mxfp8, rmsnorm_mxfp8_plan_for, rmsnorm_fwd_nvfp4,
     rmsnorm_nvfp4_plan_for,
-    rmsnorm_reg_max_chunks, rmsnorm_strerror,
+    rmsnorm_reg_max_chunks, rmsnorm_wait_timeouts, rmsnorm_strerror,
     RMSNORM_BF16, RMSNORM_F32, RMSNORM_OK, RMSNORM_EINVAL, RMSNORM_EUNSUPPORTED, RMSNORM_ECUDA,
 )
 from .api import (  # noqa: F401

@@ -25,21 +25,46 @@ RMSNORM_ECUDA = -3
 
 RMSNORM_KERNEL_REG = 0
 RMSNORM_KERNEL_LOOP = 1
+RMSNORM_KERNEL_TMA = 2
 
 RMSNORM_REGIME_WARP = 0
 RMSNORM_REGIME_CTA = 1
 RMSNORM_REGIME_PERSISTENT = 2
 RMSNORM_REGIME_LOOPED = 3
+RMSNORM_REGIME_SMEM = 4
 
-REGIME_NAMES = {0: "warp", 1: "cta", 2: "persistent", 3: "looped"}
-KERNEL_NAMES = {0: "reg", 1: "loop"}
+REGIME_NAMES = {0: "warp", 1: "cta", 2: "persistent", 3: "looped", 4: "smem"}
+KERNEL_NAMES = {0: "reg", 1: "loop", 2: "tma"}
+
+# Shape of the bulk-copy (TMA) kernel's block and rings (include/rmsnorm.h).
+TMA_THREADS_PER_ROW = 512
+TMA_BLOCK_THREADS = 608
+TMA_PIECE_CHUNKS = (1, 2, 4)
+_TMA_SMEM_BUDGET = 227 * 1024 - 1024
+_TMA_BAR_BYTES = 2 * 32 * 8
+
+
+def tma_rings(row_bytes, pc, res, w):
+    """(x, residual, weight) ring slots of the bulk-copy kernel for rows of
+    ``row_bytes`` and pieces of ``pc`` chunks a thread, or None when the row
+    does not fit -- the rule of ``rmsnorm_plan_t.chunks_per_thread``, restated
+    so tests can tell which forced plans are valid."""
+    piece = 512 * 16 * pc
+    avail = min(32, (_TMA_SMEM_BUDGET - _TMA_BAR_BYTES) // piece)
+    pieces = -(-row_bytes // piece)
+    streamed = max(1, avail // 7)
+    sr = streamed if res else 0
+    sw = (pieces if avail - sr - pieces >= pieces + 1 else streamed) if w else 0
+    sx = avail - sr - sw
+    return (sx, sr, sw) if sx >= pieces else None
 
 # Every symbol the header declares (checked by the CPU tests).
 EXPORTED = ["rmsnorm_fwd", "rmsnorm_plan", "rmsnorm_plan_for", "rmsnorm_fwd_plan", "rmsnorm_fwd_ex",
             "rmsnorm_qk_fwd", "rmsnorm_qk_plan_for", "rmsnorm_fwd_mxfp8", "rmsnorm_mxfp8_plan_for",
             "rmsnorm_fwd_nvfp4", "rmsnorm_nvfp4_plan_for",
             "layernorm_fwd", "layernorm_plan_for",
-            "rmsnorm_max_hidden", "rmsnorm_reg_max_chunks", "rmsnorm_strerror", "rmsnorm_build_info"]
+            "rmsnorm_max_hidden", "rmsnorm_reg_max_chunks", "rmsnorm_wait_timeouts", "rmsnorm_strerror",
+            "rmsnorm_build_info"]
 
 
 class RmsNormError(RuntimeError):
@@ -136,6 +161,8 @@ def load():
         lib.rmsnorm_max_hidden.restype = i64
         lib.rmsnorm_reg_max_chunks.argtypes = []
         lib.rmsnorm_reg_max_chunks.restype = i32
+        lib.rmsnorm_wait_timeouts.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+        lib.rmsnorm_wait_timeouts.restype = i32
         lib.rmsnorm_strerror.argtypes = [i32]
         lib.rmsnorm_strerror.restype = ctypes.c_char_p
         lib.rmsnorm_build_info.argtypes = []
@@ -289,3 +316,11 @@ def rmsnorm_strerror(status) -> str:
 
 def rmsnorm_build_info() -> str:
     return load().rmsnorm_build_info().decode()
+
+
+def rmsnorm_wait_timeouts() -> int:
+    """Blocks of the bulk-copy kernel on the current device whose bounded
+    waits ran out since the library was loaded (a blocking read)."""
+    n = ctypes.c_uint32(0)
+    _check(load().rmsnorm_wait_timeouts(ctypes.byref(n)), "rmsnorm_wait_timeouts")
+    return int(n.value)

@@ -42,6 +42,21 @@ inline const void *nv_kernel(int dtype, int gt, int ch, bool res, int wm) {
     return res ? nv_reg_bf16_res(gt, ch, wm) : nv_reg_bf16_plain(gt, ch, wm);
 }
 
+// RMSNorm with the row staged in shared memory by bulk copies (contiguous
+// rows, 16-byte units): 512 consumer threads and three producer warps a
+// block; rings of pieces of 512 x 16 x pc bytes (pc: 1, 2 or 4) for x, the
+// residual and the weight, kTmaMaxSlots slots in all, after the
+// 2 x kTmaMaxSlots mbarriers.
+constexpr int kTmaGT = 512;
+constexpr int kTmaBlock = kTmaGT + 3 * 32;
+constexpr int kTmaMaxSlots = 32;
+constexpr int kTmaBarBytes = 2 * kTmaMaxSlots * 8;
+constexpr int tma_piece_bytes(int pc) { return kTmaGT * 16 * pc; }
+constexpr int tma_smem_bytes(int pc, int slots) { return kTmaBarBytes + slots * tma_piece_bytes(pc); }
+const void *tma_kernel(int dtype, int pc, bool res, int wm);
+// Reads the count of blocks whose bounded waits ran out (current device); 0 or -1.
+int tma_timeouts_read(unsigned int *out);
+
 // LayerNorm (contiguous rows); aff: 0 none, 1 weight, 2 weight and bias.
 constexpr int kLnMaxGT = 256;
 const void *ln_reg_f32(int gt, int ch, bool res, int aff);

@@ -39,6 +39,14 @@ constexpr int64_t kLoopMaxTermsPerThread = 64;
 // Dynamic shared memory of a register-kernel block with a weight: the weight
 // row, at most kRegMaxGT * kRegMaxCH chunks of 16 bytes.
 constexpr int kRegMaxWeightSmem = rrn::kRegMaxGT * rrn::kRegMaxCH * 16;
+// Dynamic shared memory the bulk-copy kernel's ring may take: the 227 KB a
+// block may opt in to on sm_103a, less 1 KB for the kernel's static arrays.
+constexpr int kTmaSmemBudget = 227 * 1024 - 1024;
+// Chunks per consumer thread per ring piece chosen by planning (16 KB pieces).
+constexpr int kTmaPlanPC = 2;
+// 16-byte units of a row past which contiguous RMSNorm rows leave the
+// register kernel for the bulk-copy kernel (2048 units: 32 KB).
+constexpr int64_t kRegWideUnits = 256 * rrn::kRegMaxCH;
 
 int elem_size(int dtype) { return dtype == RMSNORM_BF16 ? 2 : 4; }
 int vec_elems_of(int dtype) { return 16 / elem_size(dtype); }
@@ -53,6 +61,32 @@ int64_t next_pow2(int64_t v) {
 
 bool aligned_to(const void *p, int a) {
     return p == nullptr || (reinterpret_cast<uintptr_t>(p) % (uintptr_t)a) == 0;
+}
+
+// Slots of the bulk-copy kernel's three rings (x, residual, weight).
+struct TmaRings {
+    int sx = 0, sr = 0, sw = 0;
+};
+
+// Ring sizes for rows of row_bytes with pieces of pc chunks a thread: the
+// slots that fit the shared-memory budget are shared out as a streamed ring
+// of avail / 7 slots (at least 1) for the residual, the same for the weight
+// -- or one slot per piece, so the weight stays resident, when the x ring
+// still gets a row and a spare slot -- and the rest for x.  False when the
+// x ring cannot hold a whole row.
+bool tma_rings(int64_t row_bytes, int pc, bool res, bool w, TmaRings *out) {
+    const int piece = rrn::tma_piece_bytes(pc);
+    int avail = (kTmaSmemBudget - rrn::kTmaBarBytes) / piece;
+    if (avail > rrn::kTmaMaxSlots) avail = rrn::kTmaMaxSlots;
+    const int64_t pieces = ceil_div(row_bytes, piece);
+    const int streamed = avail / 7 > 0 ? avail / 7 : 1;
+    TmaRings R;
+    R.sr = res ? streamed : 0;
+    if (w) R.sw = (avail - R.sr - pieces >= pieces + 1) ? (int)pieces : streamed;
+    R.sx = avail - R.sr - R.sw;
+    if (R.sx < pieces) return false;
+    if (out) *out = R;
+    return true;
 }
 
 // Everything one launch needs, for contiguous rows and for head rows.
@@ -98,11 +132,31 @@ int vec_ok_of(const Op &o) {
 // The per-row schedule: everything but the grid.
 // odd_ch: chunk counts 3 and 6 may be chosen (a row of 3 * 2^k chunks then
 // fills every slot); measured to help LayerNorm rows, not RMSNorm rows.
-void schedule(int64_t hidden, int dtype, int vec_ok, int max_gt, rmsnorm_plan_t *p, bool odd_ch = false) {
+// tma_ok: the op has a bulk-copy kernel (contiguous RMSNorm rows).  For
+// these ops, measured on GB300: rows of 16 to 32 KB run best as 256 threads
+// x 8 chunks (not 512 x 4), and longer rows on the bulk-copy kernel (not
+// 512 x 8 in registers) when they fit its rings.
+void schedule(int64_t hidden, int dtype, int vec_ok, int max_gt, rmsnorm_plan_t *p, bool odd_ch = false,
+              bool tma_ok = false) {
     std::memset(p, 0, sizeof(*p));
     const int V = vec_elems_of(dtype);
     if (vec_ok) {
         const int64_t nch = hidden / V;
+        // Planning must not depend on which optional tensors are given: a row
+        // goes to the bulk-copy kernel only if it fits with a residual and a
+        // weight.
+        const bool to_tma = tma_ok && nch > kRegWideUnits &&
+                            tma_rings(hidden * elem_size(dtype), kTmaPlanPC, true, true, nullptr);
+        if (to_tma) {
+            p->kernel = RMSNORM_KERNEL_TMA;
+            p->regime = RMSNORM_REGIME_SMEM;
+            p->threads_per_row = rrn::kTmaGT;
+            p->chunks_per_thread = kTmaPlanPC;
+            p->vec_elems = V;
+            p->block_threads = rrn::kTmaBlock;
+            p->rows_per_block = 1;
+            return;
+        }
         // Aim at 4 chunks (64 bytes of each input) per thread with at least 4
         // lanes per row: measured on GB300, this keeps every row-group block
         // resident in one wave at the occupancy the registers allow and beats
@@ -111,6 +165,7 @@ void schedule(int64_t hidden, int dtype, int vec_ok, int max_gt, rmsnorm_plan_t 
         int64_t gt = next_pow2(ceil_div(nch, kRegTargetCH));
         if (gt < 4) gt = 4;
         if (gt > max_gt && ceil_div(nch, max_gt) <= rrn::kRegMaxCH) gt = max_gt;
+        if (tma_ok && gt > 256 && ceil_div(nch, 256) <= rrn::kRegMaxCH) gt = 256;
         if (gt <= max_gt) {
             int64_t need = ceil_div(nch, gt);
             int ch = 1;
@@ -145,8 +200,14 @@ void schedule(int64_t hidden, int dtype, int vec_ok, int max_gt, rmsnorm_plan_t 
 
 void size_grid(int64_t rows, int sm_count, int blocks_per_sm, rmsnorm_plan_t *p) {
     const int64_t row_blocks = ceil_div(rows, p->rows_per_block);
-    int64_t cap = (int64_t)(sm_count > 0 ? sm_count : 1) * (blocks_per_sm > 0 ? blocks_per_sm : 1) *
-                  kPersistentWaves;
+    const int64_t resident = (int64_t)(sm_count > 0 ? sm_count : 1) * (blocks_per_sm > 0 ? blocks_per_sm : 1);
+    p->pdl = 1;
+    if (p->kernel == RMSNORM_KERNEL_TMA) {   // one wave; blocks stride over the rows
+        p->grid = row_blocks < resident ? row_blocks : resident;
+        p->persistent = row_blocks > p->grid;
+        return;
+    }
+    int64_t cap = resident * kPersistentWaves;
     if (cap > INT_MAX) cap = INT_MAX;
     p->persistent = row_blocks > cap;
     p->grid = row_blocks > cap ? cap : row_blocks;
@@ -155,6 +216,12 @@ void size_grid(int64_t rows, int sm_count, int blocks_per_sm, rmsnorm_plan_t *p)
 }
 
 size_t dyn_smem_of(const rmsnorm_plan_t *p, const Op &o) {
+    if (p->kernel == RMSNORM_KERNEL_TMA) {
+        TmaRings R;
+        if (!tma_rings(o.row_elems * elem_size(o.dtype), p->chunks_per_thread, o.res != nullptr, o.w != nullptr, &R))
+            return 0;
+        return (size_t)rrn::tma_smem_bytes(p->chunks_per_thread, R.sx + R.sr + R.sw);
+    }
     if (p->kernel != RMSNORM_KERNEL_REG || o.wm == 0) return 0;
     const int copies = o.ln ? (o.wm == rrn::kAffWB ? 2 : 1) : (o.head_rows ? 2 : 1);
     return (size_t)(o.row_elems / vec_elems_of(o.dtype)) * 16 * copies;
@@ -165,6 +232,10 @@ int mx_min_gt(int dtype) { return 32 / vec_elems_of(dtype); }
 
 const void *kernel_of(const rmsnorm_plan_t *p, const Op &o) {
     const bool res = o.res != nullptr;
+    if (p->kernel == RMSNORM_KERNEL_TMA) {
+        if (o.mx || o.nv || o.ln || o.head_rows) return nullptr;
+        return rrn::tma_kernel(o.dtype, p->chunks_per_thread, res, o.wm);
+    }
     if (o.mx || o.nv) {
         if (p->kernel != RMSNORM_KERNEL_REG) return nullptr;
         return o.mx ? rrn::mx_kernel(o.dtype, p->threads_per_row, p->chunks_per_thread, res, o.wm)
@@ -200,6 +271,17 @@ int validate_plan(const rmsnorm_plan_t *p, const Op &o, int vec_ok) {
         if ((int64_t)gt * ch * V < o.row_elems) return RMSNORM_EINVAL;
         if (p->block_threads != rrn::reg_block_threads(gt)) return RMSNORM_EINVAL;
         if (p->rows_per_block != p->block_threads / gt) return RMSNORM_EINVAL;
+        return RMSNORM_OK;
+    }
+    if (p->kernel == RMSNORM_KERNEL_TMA) {
+        if (o.mx || o.nv || o.ln || o.head_rows) return RMSNORM_EINVAL;   // contiguous RMSNorm rows only
+        if (!vec_ok || p->vec_elems != V) return RMSNORM_EINVAL;
+        if (p->threads_per_row != rrn::kTmaGT || p->block_threads != rrn::kTmaBlock || p->rows_per_block != 1)
+            return RMSNORM_EINVAL;
+        const int pc = p->chunks_per_thread;
+        if (pc != 1 && pc != 2 && pc != 4) return RMSNORM_EINVAL;
+        if (!tma_rings(o.row_elems * elem_size(o.dtype), pc, o.res != nullptr, o.w != nullptr, nullptr))
+            return RMSNORM_EINVAL;
         return RMSNORM_OK;
     }
     if (p->kernel == RMSNORM_KERNEL_LOOP) {
@@ -256,12 +338,14 @@ int sm_count_of(int dev, int *out) {
     return RMSNORM_OK;
 }
 
-// Opt a kernel in to the largest dynamic shared memory it may be given.
-int ensure_smem_attr(int dev, const void *fn) {
+// Opt a kernel in to the largest dynamic shared memory its family may be
+// given (the weight row of the register kernel, the bulk-copy kernel's ring).
+int ensure_smem_attr(int dev, const void *fn, const rmsnorm_plan_t *p) {
     std::lock_guard<std::mutex> lk(g_mu);
     for (int i = 0; i < g_attr_used; ++i)
         if (g_attr[i].dev == dev && g_attr[i].fn == fn) return RMSNORM_OK;
-    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kRegMaxWeightSmem) != cudaSuccess)
+    const int bytes = p->kernel == RMSNORM_KERNEL_TMA ? kTmaSmemBudget : kRegMaxWeightSmem;
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
         return RMSNORM_ECUDA;
     if (g_attr_used < kOccSlots) g_attr[g_attr_used++] = AttrEntry{dev, fn};
     return RMSNORM_OK;
@@ -288,7 +372,8 @@ int blocks_per_sm_of(int dev, const void *fn, int block, size_t smem, int *out) 
 
 // Full device-side planning for an op.
 int plan_for_device(const Op &o, rmsnorm_plan_t *plan, int *dev_out) {
-    schedule(o.row_elems, o.dtype, vec_ok_of(o), max_threads_per_row(o), plan, o.ln);
+    schedule(o.row_elems, o.dtype, vec_ok_of(o), max_threads_per_row(o), plan, o.ln,
+             !(o.ln || o.head_rows || o.mx || o.nv));
     if ((o.mx || o.nv) && plan->kernel != RMSNORM_KERNEL_REG) return RMSNORM_EUNSUPPORTED;
     if (o.mx) {
         const int V = vec_elems_of(o.dtype);
@@ -309,7 +394,7 @@ int plan_for_device(const Op &o, rmsnorm_plan_t *plan, int *dev_out) {
     const void *fn = kernel_of(plan, o);
     if (fn == nullptr) return RMSNORM_EINVAL;
     const size_t smem = dyn_smem_of(plan, o);
-    if (smem > 0 && (st = ensure_smem_attr(dev, fn)) != RMSNORM_OK) return st;
+    if (smem > 0 && (st = ensure_smem_attr(dev, fn, plan)) != RMSNORM_OK) return st;
     int bps = 0;
     if ((st = blocks_per_sm_of(dev, fn, plan->block_threads, smem, &bps)) != RMSNORM_OK) return st;
     size_grid(o.rows, sms, bps, plan);
@@ -322,13 +407,14 @@ int launch(const Op &o, const rmsnorm_plan_t *plan, int dev, rmsnorm_stream_t st
     if (fn == nullptr) return RMSNORM_EINVAL;
     const size_t smem = dyn_smem_of(plan, o);
     if (smem > 0) {
-        int st = ensure_smem_attr(dev, fn);
+        int st = ensure_smem_attr(dev, fn, plan);
         if (st != RMSNORM_OK) return st;
     }
     const int64_t s = elem_size(o.dtype);
     rrn::Params args;
     rrn::LnParams largs;
-    void *argv[1];
+    TmaRings rings;
+    void *argv[4];
     if (o.ln) {
         largs.x = o.x;
         largs.res = o.res;
@@ -366,6 +452,13 @@ int launch(const Op &o, const rmsnorm_plan_t *plan, int dev, rmsnorm_stream_t st
     args.scales = o.scales;
     args.q_scale = o.q_scale;
     args.q_inv6s = (float)(1.0 / (6.0 * (double)o.q_scale));
+    if (plan->kernel == RMSNORM_KERNEL_TMA) {
+        if (!tma_rings(o.row_elems * s, plan->chunks_per_thread, o.res != nullptr, o.w != nullptr, &rings))
+            return RMSNORM_EINVAL;
+        argv[1] = &rings.sx;
+        argv[2] = &rings.sr;
+        argv[3] = &rings.sw;
+    }
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -587,7 +680,7 @@ int rmsnorm_plan(int64_t rows, int64_t hidden, int dtype, int vec_ok, int sm_cou
         return RMSNORM_EINVAL;
     if (hidden > kMaxHidden) return RMSNORM_EUNSUPPORTED;
     if (vec_ok && (hidden * elem_size(dtype)) % 16 != 0) return RMSNORM_EINVAL;
-    schedule(hidden, dtype, vec_ok ? 1 : 0, rrn::kRegMaxGT, plan);
+    schedule(hidden, dtype, vec_ok ? 1 : 0, rrn::kRegMaxGT, plan, false, true);
     size_grid(rows, sm_count, blocks_per_sm, plan);
     return RMSNORM_OK;
 }
@@ -660,6 +753,17 @@ int64_t rmsnorm_max_hidden(int dtype) {
 
 int rmsnorm_reg_max_chunks(void) { return rrn::kRegMaxCH; }
 
+int rmsnorm_wait_timeouts(uint32_t *count) {
+    if (count == nullptr) return RMSNORM_EINVAL;
+    unsigned int n = 0;
+    if (rrn::tma_timeouts_read(&n) != 0) {
+        (void)cudaGetLastError();
+        return RMSNORM_ECUDA;
+    }
+    *count = n;
+    return RMSNORM_OK;
+}
+
 const char *rmsnorm_strerror(int status) {
     switch (status) {
         case RMSNORM_OK: return "ok";
@@ -672,7 +776,8 @@ const char *rmsnorm_strerror(int status) {
 
 const char *rmsnorm_build_info(void) {
     return "row_reduction_norm_gb300 fused RMSNorm / LayerNorm 0.3; target sm_103a; kernels: register (warp/"
-           "CTA/persistent), two/three-pass; contiguous rows and Q/K head rows; weight, weight + bias, no weight";
+           "CTA/persistent), shared-memory ring fed by bulk copies, two/three-pass; contiguous rows and Q/K head "
+           "rows; weight, weight + bias, no weight; MXFP8 / NVFP4 outputs";
 }
 
 }  // extern "C"

@@ -1,0 +1,40 @@
+// tma.cu -- instantiations of the shared-memory (bulk copy) RMSNorm kernel,
+// and the device counter its bounded waits report to.
+#include "kernel_table.h"
+#include "rmsnorm_tma.cuh"
+
+namespace rrn {
+namespace {
+
+template <typename T, bool RES, int PC>
+const void *tma_wm(int wm) {
+    switch (wm) {
+        case kNoWeight: return reinterpret_cast<const void *>(&rms_tma_kernel<T, RES, kNoWeight, PC>);
+        case kWeight: return reinterpret_cast<const void *>(&rms_tma_kernel<T, RES, kWeight, PC>);
+        case kWeightBias: return reinterpret_cast<const void *>(&rms_tma_kernel<T, RES, kWeightBias, PC>);
+        default: return nullptr;
+    }
+}
+
+template <typename T, bool RES>
+const void *tma_pc(int pc, int wm) {
+    switch (pc) {
+        case 1: return tma_wm<T, RES, 1>(wm);
+        case 2: return tma_wm<T, RES, 2>(wm);
+        case 4: return tma_wm<T, RES, 4>(wm);
+        default: return nullptr;
+    }
+}
+
+}  // namespace
+
+const void *tma_kernel(int dtype, int pc, bool res, int wm) {
+    if (dtype == 1) return res ? tma_pc<BF16, true>(pc, wm) : tma_pc<BF16, false>(pc, wm);
+    return res ? tma_pc<F32, true>(pc, wm) : tma_pc<F32, false>(pc, wm);
+}
+
+int tma_timeouts_read(unsigned int *out) {
+    return cudaMemcpyFromSymbol(out, g_tma_timeouts, sizeof(unsigned int)) == cudaSuccess ? 0 : -1;
+}
+
+}  // namespace rrn

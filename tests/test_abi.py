@@ -88,13 +88,14 @@ def test_plan_properties(dtype, hidden):
             continue
         plans = [R.rmsnorm_plan(rows, hidden, dtype, vec_ok, 152, 2) for rows in (1, 7, 1000, 10 ** 6)]
         huge = R.rmsnorm_plan(10 ** 12, hidden, dtype, vec_ok, 152, 2)
-        assert huge.persistent == 1 and huge.grid == 152 * 2 * 4096
+        tma = huge.kernel == N.RMSNORM_KERNEL_TMA
+        assert huge.persistent == 1 and huge.grid == (152 * 2 if tma else 152 * 2 * 4096)
         if huge.kernel == N.RMSNORM_KERNEL_REG:
             assert huge.regime == N.RMSNORM_REGIME_PERSISTENT
         sched = {(p.kernel, p.threads_per_row, p.chunks_per_thread, p.vec_elems, p.block_threads,
                   p.rows_per_block) for p in plans}
         assert len(sched) == 1, "the per-row schedule must not depend on the row count"
-        cap = 152 * 2 * 4096
+        cap = 152 * 2 if tma else 152 * 2 * 4096
         for rows, p in zip((1, 7, 1000, 10 ** 6), plans):
             row_blocks = -(-rows // p.rows_per_block)
             assert 1 <= p.grid <= min(row_blocks, cap)
@@ -109,6 +110,12 @@ def test_plan_properties(dtype, hidden):
                 want = (N.RMSNORM_REGIME_PERSISTENT if p.persistent else
                         N.RMSNORM_REGIME_WARP if gt <= 32 else N.RMSNORM_REGIME_CTA)
                 assert p.regime == want
+            elif p.kernel == N.RMSNORM_KERNEL_TMA:
+                # rows past 256 threads x 8 chunks, short enough for the rings
+                assert vec_ok and p.vec_elems == V and hidden * esz > 256 * 8 * 16
+                assert p.regime == N.RMSNORM_REGIME_SMEM
+                assert (p.threads_per_row, p.block_threads, p.rows_per_block) == (512, 608, 1)
+                assert N.tma_rings(hidden * esz, p.chunks_per_thread, True, True) is not None
             else:
                 assert p.kernel == N.RMSNORM_KERNEL_LOOP and p.regime == N.RMSNORM_REGIME_LOOPED
                 assert p.vec_elems == (V if vec_ok else 1)
@@ -116,6 +123,78 @@ def test_plan_properties(dtype, hidden):
                 assert -(-units // p.block_threads) * p.vec_elems <= 64
         if not vec_ok:
             assert plans[0].kernel == N.RMSNORM_KERNEL_LOOP
+
+
+@pytest.mark.parametrize("dtype,hidden,kernel", [
+    (N.RMSNORM_BF16, 16384, N.RMSNORM_KERNEL_REG), (N.RMSNORM_BF16, 16392, N.RMSNORM_KERNEL_TMA),
+    (N.RMSNORM_BF16, 40000, N.RMSNORM_KERNEL_TMA), (N.RMSNORM_BF16, 65536, N.RMSNORM_KERNEL_TMA),
+    (N.RMSNORM_F32, 8192, N.RMSNORM_KERNEL_REG), (N.RMSNORM_F32, 8196, N.RMSNORM_KERNEL_TMA),
+    (N.RMSNORM_F32, 40960, N.RMSNORM_KERNEL_TMA), (N.RMSNORM_F32, 40964, N.RMSNORM_KERNEL_LOOP),
+    (N.RMSNORM_F32, 65536, N.RMSNORM_KERNEL_LOOP)])
+def test_long_rows_go_to_the_shared_memory_ring(dtype, hidden, kernel):
+    """Rows past 256 threads x 8 chunks of 16 bytes (32 KB) take the
+    bulk-copy kernel while they fit its rings (160 KB rows with a residual
+    and a weight), the two-pass kernel beyond that or when unaligned; rows of
+    16 to 32 KB take 256 threads x 8 chunks."""
+    p = R.rmsnorm_plan(1000, hidden, dtype, True, 152, 1)
+    assert p.kernel == kernel
+    if kernel == N.RMSNORM_KERNEL_REG:
+        assert (p.threads_per_row, p.chunks_per_thread) == (256, 8)
+    if kernel == N.RMSNORM_KERNEL_TMA:
+        assert p.chunks_per_thread == 2 and p.grid == 152 and p.persistent == 1
+        assert R.rmsnorm_plan(100, hidden, dtype, True, 152, 1).grid == 100
+    assert R.rmsnorm_plan(1000, hidden, dtype, False, 152, 1).kernel == N.RMSNORM_KERNEL_LOOP
+
+
+def test_tma_plan_validation_without_cuda():
+    P = 1 << 20
+    good = R.rmsnorm_plan(4, 40000, N.RMSNORM_BF16, True, 152, 1)
+    assert good.kernel == N.RMSNORM_KERNEL_TMA
+
+    def st(plan, hidden=40000, dtype=N.RMSNORM_BF16, res=None, x=P):
+        return N.rmsnorm_fwd_plan_status(x, res, None, P, res, 4, hidden, 1e-6, dtype, plan, 0)
+
+    for field, value in (("chunks_per_thread", 3), ("chunks_per_thread", 8), ("threads_per_row", 256),
+                         ("block_threads", 544), ("rows_per_block", 2), ("vec_elems", 1)):
+        q = good.copy()
+        setattr(q, field, value)
+        assert st(q) == N.RMSNORM_EINVAL, field
+    # 65536 fp32 (256 KB) does not fit the x ring; 57344 fp32 (224 KB) fits it
+    # only without a residual and a weight
+    q = good.copy()
+    q.vec_elems = 4
+    assert st(q, hidden=65536, dtype=N.RMSNORM_F32) == N.RMSNORM_EINVAL
+    for res, status in ((None, N.RMSNORM_OK), (P, N.RMSNORM_EINVAL)):   # rows = 0: validation only
+        assert N.rmsnorm_fwd_plan_status(P, res, None, P, res, 0, 57344, 1e-6, N.RMSNORM_F32, q, 0) == status
+    # 32 KB pieces: 7 slots, 40000 bf16 (80 KB) fits, a misaligned x does not
+    q = good.copy()
+    q.chunks_per_thread = 4
+    assert st(q, x=P + 2) == N.RMSNORM_EINVAL
+    # rows == 0 validates the plan and launches nothing
+    assert N.rmsnorm_fwd_plan_status(P, None, None, P, None, 0, 40000, 1e-6, 1, good, 0) == N.RMSNORM_OK
+    # the other ops have no bulk-copy kernel
+    assert N.layernorm_fwd_status(P, None, None, None, P, None, 4, 40000, 1e-5, 1, good) == N.RMSNORM_EINVAL
+    assert N.rmsnorm_qk_fwd_status(P, P, 4, 40000, 40000, 1, 0, 40000, None, None, 0.0, 1e-6, 1,
+                                   good) == N.RMSNORM_EINVAL
+
+
+@pytest.mark.parametrize("pc", [1, 2, 4])
+@pytest.mark.parametrize("res", [False, True])
+@pytest.mark.parametrize("w", [False, True])
+def test_tma_ring_rule_matches_the_library(pc, res, w):
+    """The Python restatement of the ring sizing accepts exactly the plans the
+    library accepts (rows = 0 validates a plan and launches nothing)."""
+    P = 1 << 20
+    plan = R.rmsnorm_plan(4, 40000, N.RMSNORM_BF16, True, 152, 1)
+    plan.chunks_per_thread = pc
+    for dtype, esz in ((N.RMSNORM_BF16, 2), (N.RMSNORM_F32, 4)):
+        plan.vec_elems = 16 // esz
+        for hidden in range(4096, 65537, 4096 - 8):
+            hidden -= hidden % 8
+            want = N.tma_rings(hidden * esz, pc, res, w) is not None
+            got = N.rmsnorm_fwd_plan_status(P, P if res else None, P if w else None, P, P if res else None, 0,
+                                            hidden, 1e-6, dtype, plan, 0) == N.RMSNORM_OK
+            assert got == want, (dtype, hidden)
 
 
 def test_qk_norm_is_warp_regime_and_large_rows_cta():

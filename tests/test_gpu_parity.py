@@ -91,12 +91,13 @@ def test_workload_large_sampled(name):
 
 # ------------------------------------------------------------ forced plans
 
-def all_plans(rows, hidden, dtype_code, vec_ok, sm_count=152, odd_ch=False):
+def all_plans(rows, hidden, dtype_code, vec_ok, sm_count=152, odd_ch=False, tma=False):
     """Every launch plan that is valid for the shape: all REG (threads, chunks)
     pairs that cover the row (chunks 3 and 6 too with ``odd_ch``, compiled for
-    contiguous rows), the two-pass kernel (vector / scalar, each block size
-    that keeps the accuracy bound), each in a full grid and a small
-    (persistent) grid."""
+    contiguous rows), the bulk-copy kernel with both piece sizes that fit
+    (``tma``: contiguous RMSNorm rows), the two-pass kernel (vector / scalar,
+    each block size that keeps the accuracy bound), each in a full grid and a
+    small (persistent) grid."""
     V = 8 if dtype_code == N.RMSNORM_BF16 else 4
     plans = []
     if vec_ok:
@@ -113,6 +114,20 @@ def all_plans(rows, hidden, dtype_code, vec_ok, sm_count=152, odd_ch=False):
                 p.block_threads = gt if gt >= 256 else 256
                 p.rows_per_block = p.block_threads // gt
                 plans.append(p)
+    if vec_ok and tma:
+        esz = 16 // V
+        for pc in N.TMA_PIECE_CHUNKS:
+            if N.tma_rings(hidden * esz, pc, True, True) is None:
+                continue   # valid for every residual / weight form the callers run
+            p = N.Plan()
+            p.kernel = N.RMSNORM_KERNEL_TMA
+            p.regime = N.RMSNORM_REGIME_SMEM
+            p.threads_per_row = N.TMA_THREADS_PER_ROW
+            p.chunks_per_thread = pc
+            p.vec_elems = V
+            p.block_threads = N.TMA_BLOCK_THREADS
+            p.rows_per_block = 1
+            plans.append(p)
     for vec in ([True, False] if vec_ok else [False]):
         ve = V if vec else 1
         for blk in (64, 256, 1024):
@@ -148,7 +163,7 @@ def test_every_plan_matches_oracle(rows, hidden, dtype):
     code = R.dtype_code(x.dtype)
     yr, hr = oracle_run(x, r, w, wl.eps, dtype)
     yr_nr, _ = oracle_run(x, None, None, wl.eps, dtype)
-    plans = all_plans(rows, hidden, code, True, odd_ch=True)
+    plans = all_plans(rows, hidden, code, True, odd_ch=True, tma=True)
     assert plans
     for p in plans:
         y, h = R.rms_norm(x, w=w, residual=r, eps=wl.eps, plan=p)

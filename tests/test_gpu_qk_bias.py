@@ -132,7 +132,7 @@ def test_weight_bias_every_plan(rows, hidden, dtype):
     yr, hr, _ = oracle.rmsnorm(xn, w=wn, residual=rn, eps=wl.eps, dtype=dtype, threads=THREADS, weight_bias=1.0)
     code = R.dtype_code(x.dtype)
     esz = 2 if dtype == "bf16" else 4
-    plans = [None] + all_plans(rows, hidden, code, (hidden * esz) % 16 == 0, odd_ch=True)
+    plans = [None] + all_plans(rows, hidden, code, (hidden * esz) % 16 == 0, odd_ch=True, tma=True)
     for p in plans:
         y, h = R.rms_norm(x, w=w, residual=r, eps=wl.eps, weight_bias=1.0, plan=p)
         torch.cuda.synchronize()
