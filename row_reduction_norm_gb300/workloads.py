@@ -88,6 +88,14 @@ WORKLOADS = {
         Workload("bf16_res_65536x8192_nw", "bf16", 65536, 8192, 1e-6, 1.0, 1.0, None,
                  outlier_frac=1e-3, outlier_scale=100.0,
                  note="bandwidth-roofline case with outliers, no weight"),
+        # rows too long for registers (not among the pages' model widths):
+        # the shared-memory (bulk copy) regime and the two-pass regime
+        Workload("bf16_4096x32768_w", "bf16", 4096, 32768, 1e-6, 1.0, None, 0.1,
+                 note="long rows, shared-memory regime, weight resident"),
+        Workload("bf16_res_2048x65536_w", "bf16", 2048, 65536, 1e-6, 1.0, 1.0, 0.1,
+                 note="longest bf16 rows, shared-memory regime, weight streamed"),
+        Workload("f32_res_2048x65536_w", "f32", 2048, 65536, 1e-6, 1.0, 1.0, 0.1,
+                 note="fp32 rows past the shared-memory rings, two-pass regime"),
     ]
 }
 

@@ -72,19 +72,24 @@ def test_workload_full_size(name):
     check(y, h, x, r, w, wl.eps, wl.dtype, what=name)
 
 
-@pytest.mark.parametrize("name", ["bf16_res_65536x8192_w", "bf16_res_65536x8192_nw"])
+@pytest.mark.parametrize("name", ["bf16_res_65536x8192_w", "bf16_res_65536x8192_nw", "bf16_4096x32768_w",
+                                  "bf16_res_2048x65536_w", "f32_res_2048x65536_w"])
 def test_workload_large_sampled(name):
     wl = W.WORKLOADS[name]
     x, r, w = gpu_inputs(wl)
-    y, h = R.rms_norm(x, w=w, residual=r, eps=wl.eps)
+    out = R.rms_norm(x, w=w, residual=r, eps=wl.eps)
+    y, h = out if r is not None else (out, None)
     torch.cuda.synchronize()
     g = np.random.default_rng(17)
-    rows = np.unique(np.concatenate([[0, 1, wl.rows - 1], g.integers(0, wl.rows, 509)]))
+    n = 509 if wl.hidden <= 8192 else 61
+    rows = np.unique(np.concatenate([[0, 1, wl.rows - 1], g.integers(0, wl.rows, n)]))
     idx = torch.as_tensor(rows, device=DEV)
-    xs, rs, ys, hs = x[idx], r[idx], y[idx], h[idx]
+    xs, ys = x[idx], y[idx]
+    rs, hs = (None, None) if r is None else (r[idx], h[idx])
     check(ys, hs, xs, rs, w, wl.eps, wl.dtype, what=name)
-    # outliers are present in the sample (0.1% of entries scaled by 100)
-    assert float(xs.float().abs().max()) > 50.0
+    if wl.outlier_frac:
+        # outliers are present in the sample (0.1% of entries scaled by 100)
+        assert float(xs.float().abs().max()) > 50.0
     del x, r, y, h
     torch.cuda.empty_cache()
 
