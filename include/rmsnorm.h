@@ -20,9 +20,10 @@
  * residual_out is the sum rounded once to T and the norm is taken of it.
  *
  * Arithmetic: inputs are widened to fp32; the sum of squares is formed in
- * fp32 in a fixed order that depends only on (hidden, dtype, alignment), so
- * every call gives bit-identical results for a row, whatever the row count,
- * grid or stream ("batch invariant").  Accuracy: y is within 1 ulp of the
+ * fp32 in a fixed order that depends only on (hidden, dtype, alignment, and,
+ * for rows longer than 80 KB, whether a residual is given), so every call
+ * gives bit-identical results for a row, whatever the row count, grid or
+ * stream ("batch invariant").  Accuracy: y is within 1 ulp of the
  * correctly rounded result for bf16 and within 2e-6 relative for fp32;
  * residual_out is the correctly rounded sum (bit-exact).
  *
@@ -144,10 +145,12 @@ int rmsnorm_fwd(const void *x, const void *residual, const void *w, void *y,
                 int dtype, rmsnorm_stream_t stream);
 
 /*
- * Pure host planning (no CUDA call): the plan rmsnorm_fwd would use on a
- * device with `sm_count` SMs where the chosen kernel keeps `blocks_per_sm`
- * blocks resident.  vec_ok: 1 if every pointer is 16-byte aligned and
- * hidden * sizeof(T) is a multiple of 16.  Returns a status.
+ * Pure host planning (no CUDA call): the plan rmsnorm_fwd would use without
+ * a residual on a device with `sm_count` SMs where the chosen kernel keeps
+ * `blocks_per_sm` blocks resident (with a residual, rows longer than 80 KB
+ * take RMSNORM_KERNEL_LOOP instead of RMSNORM_KERNEL_TMA).  vec_ok: 1 if
+ * every pointer is 16-byte aligned and hidden * sizeof(T) is a multiple of
+ * 16.  Returns a status.
  */
 int rmsnorm_plan(int64_t rows, int64_t hidden, int dtype, int vec_ok, int sm_count,
                  int blocks_per_sm, rmsnorm_plan_t *plan);

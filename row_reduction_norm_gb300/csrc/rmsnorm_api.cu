@@ -42,8 +42,10 @@ constexpr int kRegMaxWeightSmem = rrn::kRegMaxGT * rrn::kRegMaxCH * 16;
 // Dynamic shared memory the bulk-copy kernel's ring may take: the 227 KB a
 // block may opt in to on sm_103a, less 1 KB for the kernel's static arrays.
 constexpr int kTmaSmemBudget = 227 * 1024 - 1024;
-// Chunks per consumer thread per ring piece chosen by planning (16 KB pieces).
+// Chunks per consumer thread per ring piece chosen by planning: 16 KB pieces,
+// and 32 KB pieces for rows past 80 KB without a residual.
 constexpr int kTmaPlanPC = 2;
+constexpr int kTmaLongPC = 4;
 // 16-byte units of a row past which contiguous RMSNorm rows leave the
 // register kernel for the bulk-copy kernel (2048 units: 32 KB).
 constexpr int64_t kRegWideUnits = 256 * rrn::kRegMaxCH;
@@ -137,21 +139,32 @@ int vec_ok_of(const Op &o) {
 // x 8 chunks (not 512 x 4), and longer rows on the bulk-copy kernel (not
 // 512 x 8 in registers) when they fit its rings.
 void schedule(int64_t hidden, int dtype, int vec_ok, int max_gt, rmsnorm_plan_t *p, bool odd_ch = false,
-              bool tma_ok = false) {
+              bool tma_ok = false, bool has_res = false) {
     std::memset(p, 0, sizeof(*p));
     const int V = vec_elems_of(dtype);
     if (vec_ok) {
         const int64_t nch = hidden / V;
-        // Planning must not depend on which optional tensors are given: a row
-        // goes to the bulk-copy kernel only if it fits with a residual and a
-        // weight.
-        const bool to_tma = tma_ok && nch > kRegWideUnits &&
-                            tma_rings(hidden * elem_size(dtype), kTmaPlanPC, true, true, nullptr);
-        if (to_tma) {
+        // Rows past 32 KB: the bulk-copy kernel when, with a residual and a
+        // weight, the weight stays resident beside the row (rows up to 80 KB,
+        // 16 KB pieces); longer rows without a residual also take it (32 KB
+        // pieces, the weight streamed), and longer rows with a residual the
+        // two-pass kernel -- each the faster one measured on GB300.  The
+        // piece size does not change any result; the kernel does.
+        const int64_t row_bytes = hidden * elem_size(dtype);
+        TmaRings tr;
+        int tma_pc = 0;
+        if (tma_ok && nch > kRegWideUnits) {
+            if (tma_rings(row_bytes, kTmaPlanPC, true, true, &tr) &&
+                tr.sw >= ceil_div(row_bytes, rrn::tma_piece_bytes(kTmaPlanPC)))
+                tma_pc = kTmaPlanPC;
+            else if (!has_res && tma_rings(row_bytes, kTmaLongPC, false, true, nullptr))
+                tma_pc = kTmaLongPC;
+        }
+        if (tma_pc > 0) {
             p->kernel = RMSNORM_KERNEL_TMA;
             p->regime = RMSNORM_REGIME_SMEM;
             p->threads_per_row = rrn::kTmaGT;
-            p->chunks_per_thread = kTmaPlanPC;
+            p->chunks_per_thread = tma_pc;
             p->vec_elems = V;
             p->block_threads = rrn::kTmaBlock;
             p->rows_per_block = 1;
@@ -373,7 +386,7 @@ int blocks_per_sm_of(int dev, const void *fn, int block, size_t smem, int *out) 
 // Full device-side planning for an op.
 int plan_for_device(const Op &o, rmsnorm_plan_t *plan, int *dev_out) {
     schedule(o.row_elems, o.dtype, vec_ok_of(o), max_threads_per_row(o), plan, o.ln,
-             !(o.ln || o.head_rows || o.mx || o.nv));
+             !(o.ln || o.head_rows || o.mx || o.nv), o.res != nullptr);
     if ((o.mx || o.nv) && plan->kernel != RMSNORM_KERNEL_REG) return RMSNORM_EUNSUPPORTED;
     if (o.mx) {
         const int V = vec_elems_of(o.dtype);

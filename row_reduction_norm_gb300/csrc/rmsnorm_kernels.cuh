@@ -652,7 +652,10 @@ rms_loop_kernel(const Params p) {
     using IO = UnitIO<T, VE>;
     using Raw = typename IO::Raw;
     constexpr int NACC = 8;                          // per-thread accumulators
-    constexpr int U = VE == 1 ? NACC : 2;            // units in flight per step
+    // units in flight per step: without a residual the first pass has no
+    // second input, so it takes twice the units to keep as many bytes in
+    // flight (an accumulator's sequence of units is the same for any U)
+    constexpr int U = VE == 1 ? NACC : (RES ? 2 : 4);
     constexpr int NW = BLOCK / 32;
     static_assert(BLOCK % 32 == 0 && (NW & (NW - 1)) == 0, "BLOCK: power-of-two warps");
     static_assert((U * VE) % NACC == 0 || NACC % (U * VE) == 0, "accumulator cycle");

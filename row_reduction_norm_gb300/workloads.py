@@ -92,10 +92,12 @@ WORKLOADS = {
         # the shared-memory (bulk copy) regime and the two-pass regime
         Workload("bf16_4096x32768_w", "bf16", 4096, 32768, 1e-6, 1.0, None, 0.1,
                  note="long rows, shared-memory regime, weight resident"),
+        Workload("bf16_res_4096x40960_w", "bf16", 4096, 40960, 1e-6, 1.0, 1.0, 0.1,
+                 note="longest rows of the shared-memory regime (80 KB), fused residual"),
         Workload("bf16_res_2048x65536_w", "bf16", 2048, 65536, 1e-6, 1.0, 1.0, 0.1,
-                 note="longest bf16 rows, shared-memory regime, weight streamed"),
+                 note="longest bf16 rows, two-pass regime"),
         Workload("f32_res_2048x65536_w", "f32", 2048, 65536, 1e-6, 1.0, 1.0, 0.1,
-                 note="fp32 rows past the shared-memory rings, two-pass regime"),
+                 note="longest fp32 rows, two-pass regime"),
     ]
 }
 

@@ -111,8 +111,10 @@ def test_plan_properties(dtype, hidden):
                         N.RMSNORM_REGIME_WARP if gt <= 32 else N.RMSNORM_REGIME_CTA)
                 assert p.regime == want
             elif p.kernel == N.RMSNORM_KERNEL_TMA:
-                # rows past 256 threads x 8 chunks, short enough for the rings
+                # rows past 256 threads x 8 chunks that fit the rings
                 assert vec_ok and p.vec_elems == V and hidden * esz > 256 * 8 * 16
+                assert p.chunks_per_thread == (2 if hidden * esz <= 80 * 1024 else 4)
+                assert N.tma_rings(hidden * esz, p.chunks_per_thread, False, True) is not None
                 assert p.regime == N.RMSNORM_REGIME_SMEM
                 assert (p.threads_per_row, p.block_threads, p.rows_per_block) == (512, 608, 1)
                 assert N.tma_rings(hidden * esz, p.chunks_per_thread, True, True) is not None
@@ -127,21 +129,27 @@ def test_plan_properties(dtype, hidden):
 
 @pytest.mark.parametrize("dtype,hidden,kernel", [
     (N.RMSNORM_BF16, 16384, N.RMSNORM_KERNEL_REG), (N.RMSNORM_BF16, 16392, N.RMSNORM_KERNEL_TMA),
-    (N.RMSNORM_BF16, 40000, N.RMSNORM_KERNEL_TMA), (N.RMSNORM_BF16, 65536, N.RMSNORM_KERNEL_TMA),
+    (N.RMSNORM_BF16, 40960, N.RMSNORM_KERNEL_TMA), (N.RMSNORM_BF16, 40968, N.RMSNORM_KERNEL_TMA),
+    (N.RMSNORM_BF16, 65536, N.RMSNORM_KERNEL_TMA),
     (N.RMSNORM_F32, 8192, N.RMSNORM_KERNEL_REG), (N.RMSNORM_F32, 8196, N.RMSNORM_KERNEL_TMA),
-    (N.RMSNORM_F32, 40960, N.RMSNORM_KERNEL_TMA), (N.RMSNORM_F32, 40964, N.RMSNORM_KERNEL_LOOP),
+    (N.RMSNORM_F32, 20480, N.RMSNORM_KERNEL_TMA), (N.RMSNORM_F32, 20484, N.RMSNORM_KERNEL_TMA),
+    (N.RMSNORM_F32, 49152, N.RMSNORM_KERNEL_TMA), (N.RMSNORM_F32, 49156, N.RMSNORM_KERNEL_LOOP),
     (N.RMSNORM_F32, 65536, N.RMSNORM_KERNEL_LOOP)])
 def test_long_rows_go_to_the_shared_memory_ring(dtype, hidden, kernel):
     """Rows past 256 threads x 8 chunks of 16 bytes (32 KB) take the
-    bulk-copy kernel while they fit its rings (160 KB rows with a residual
-    and a weight), the two-pass kernel beyond that or when unaligned; rows of
-    16 to 32 KB take 256 threads x 8 chunks."""
+    bulk-copy kernel: with 16 KB pieces while the weight stays resident beside
+    the row (80 KB), past that (planned without a residual, as this call
+    does) with 32 KB pieces while the row fits (192 KB); the two-pass kernel
+    beyond that or when unaligned; rows of 16 to 32 KB take 256 threads x 8
+    chunks."""
     p = R.rmsnorm_plan(1000, hidden, dtype, True, 152, 1)
     assert p.kernel == kernel
     if kernel == N.RMSNORM_KERNEL_REG:
         assert (p.threads_per_row, p.chunks_per_thread) == (256, 8)
     if kernel == N.RMSNORM_KERNEL_TMA:
-        assert p.chunks_per_thread == 2 and p.grid == 152 and p.persistent == 1
+        esz = 2 if dtype == N.RMSNORM_BF16 else 4
+        assert p.chunks_per_thread == (2 if hidden * esz <= 80 * 1024 else 4)
+        assert p.grid == 152 and p.persistent == 1
         assert R.rmsnorm_plan(100, hidden, dtype, True, 152, 1).grid == 100
     assert R.rmsnorm_plan(1000, hidden, dtype, False, 152, 1).kernel == N.RMSNORM_KERNEL_LOOP
 

@@ -69,10 +69,13 @@ def oracle_ref(x, r, w, eps, dtype, weight_bias=0.0):
     return y, h
 
 
-LONG = [("bf16", 32776), ("bf16", 40000), ("bf16", 65536), ("f32", 16388), ("f32", 24576), ("f32", 40960)]
+# rows the library plans on the bulk-copy kernel (32 to 80 KB), and longer
+# rows it can run when forced (up to 160 KB with a residual and a weight)
+PLANNED = [("bf16", 32776), ("bf16", 40000), ("bf16", 40960), ("f32", 16388), ("f32", 20480)]
+LONG = PLANNED + [("bf16", 65536), ("f32", 24576), ("f32", 40960)]
 
 
-@pytest.mark.parametrize("dtype,hidden", LONG)
+@pytest.mark.parametrize("dtype,hidden", PLANNED)
 def test_long_rows_library_plan(dtype, hidden):
     esz = 2 if dtype == "bf16" else 4
     for rows, has_res, has_w in ((1, False, False), (7, True, True), (40, True, False), (19, False, True)):
@@ -88,6 +91,29 @@ def test_long_rows_library_plan(dtype, hidden):
         yr, hr = oracle_ref(x, r, w, wl.eps, dtype)
         ok, rep = parity.compare_y(W.to_numpy_bits(y), yr, dtype)
         assert ok, f"rows={rows} res={has_res} w={has_w}: {rep}"
+        if r is not None:
+            assert parity.bits_equal(W.to_numpy_bits(h), hr)
+
+
+@pytest.mark.parametrize("dtype,hidden", [("bf16", 65536), ("f32", 24576), ("f32", 49152)])
+def test_rows_past_80kb_plan_by_residual(dtype, hidden):
+    """Past 80 KB the weight cannot stay resident beside the row: without a
+    residual the library plans the bulk-copy kernel with 32 KB pieces, with a
+    residual the two-pass kernel; both match the oracle."""
+    for has_res in (False, True):
+        wl = W.Workload("past80", dtype, 9, hidden, 1e-6, 1.0, 1.0 if has_res else None, 0.1)
+        x, r, w = W.make_inputs(wl, seed=hidden + has_res, device=DEV)
+        p = R.plan_for(x, w=w, residual=r)
+        if has_res:
+            assert p.kernel == N.RMSNORM_KERNEL_LOOP
+        else:
+            assert p.kernel == N.RMSNORM_KERNEL_TMA and p.chunks_per_thread == 4
+        out = R.rms_norm(x, w=w, residual=r, eps=wl.eps)
+        y, h = out if r is not None else (out, None)
+        torch.cuda.synchronize()
+        yr, hr = oracle_ref(x, r, w, wl.eps, dtype)
+        ok, rep = parity.compare_y(W.to_numpy_bits(y), yr, dtype)
+        assert ok, f"res={has_res}: {rep}"
         if r is not None:
             assert parity.bits_equal(W.to_numpy_bits(h), hr)
 
