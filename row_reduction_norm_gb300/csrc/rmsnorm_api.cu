@@ -43,7 +43,7 @@ constexpr int kRegMaxWeightSmem = rrn::kRegMaxGT * rrn::kRegMaxCH * 16;
 // block may opt in to on sm_103a, less 1 KB for the kernel's static arrays.
 constexpr int kTmaSmemBudget = 227 * 1024 - 1024;
 // Chunks per consumer thread per ring piece chosen by planning: 16 KB pieces,
-// and 32 KB pieces for rows past 80 KB without a residual.
+// and 32 KB pieces without a residual for bf16 rows and rows past 80 KB.
 constexpr int kTmaPlanPC = 2;
 constexpr int kTmaLongPC = 4;
 // 16-byte units of a row past which contiguous RMSNorm rows leave the
@@ -145,18 +145,19 @@ void schedule(int64_t hidden, int dtype, int vec_ok, int max_gt, rmsnorm_plan_t 
     if (vec_ok) {
         const int64_t nch = hidden / V;
         // Rows past 32 KB: the bulk-copy kernel when, with a residual and a
-        // weight, the weight stays resident beside the row (rows up to 80 KB,
-        // 16 KB pieces); longer rows without a residual also take it (32 KB
-        // pieces, the weight streamed), and longer rows with a residual the
-        // two-pass kernel -- each the faster one measured on GB300.  The
-        // piece size does not change any result; the kernel does.
+        // weight, the weight stays resident beside the row (rows up to 80 KB);
+        // longer rows without a residual also take it (the weight streamed),
+        // and longer rows with a residual the two-pass kernel.  Pieces of
+        // 16 KB, or 32 KB without a residual for bf16 rows and for rows past
+        // 80 KB -- each the faster choice measured on GB300.  The piece size
+        // changes no result; the kernel does.
         const int64_t row_bytes = hidden * elem_size(dtype);
         TmaRings tr;
         int tma_pc = 0;
         if (tma_ok && nch > kRegWideUnits) {
             if (tma_rings(row_bytes, kTmaPlanPC, true, true, &tr) &&
                 tr.sw >= ceil_div(row_bytes, rrn::tma_piece_bytes(kTmaPlanPC)))
-                tma_pc = kTmaPlanPC;
+                tma_pc = (!has_res && dtype == RMSNORM_BF16) ? kTmaLongPC : kTmaPlanPC;
             else if (!has_res && tma_rings(row_bytes, kTmaLongPC, false, true, nullptr))
                 tma_pc = kTmaLongPC;
         }

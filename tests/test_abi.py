@@ -113,7 +113,7 @@ def test_plan_properties(dtype, hidden):
             elif p.kernel == N.RMSNORM_KERNEL_TMA:
                 # rows past 256 threads x 8 chunks that fit the rings
                 assert vec_ok and p.vec_elems == V and hidden * esz > 256 * 8 * 16
-                assert p.chunks_per_thread == (2 if hidden * esz <= 80 * 1024 else 4)
+                assert p.chunks_per_thread == (2 if dtype == N.RMSNORM_F32 and hidden * esz <= 80 * 1024 else 4)
                 assert N.tma_rings(hidden * esz, p.chunks_per_thread, False, True) is not None
                 assert p.regime == N.RMSNORM_REGIME_SMEM
                 assert (p.threads_per_row, p.block_threads, p.rows_per_block) == (512, 608, 1)
@@ -148,7 +148,8 @@ def test_long_rows_go_to_the_shared_memory_ring(dtype, hidden, kernel):
         assert (p.threads_per_row, p.chunks_per_thread) == (256, 8)
     if kernel == N.RMSNORM_KERNEL_TMA:
         esz = 2 if dtype == N.RMSNORM_BF16 else 4
-        assert p.chunks_per_thread == (2 if hidden * esz <= 80 * 1024 else 4)
+        # planned without a residual: 32 KB pieces for bf16 and past 80 KB
+        assert p.chunks_per_thread == (2 if dtype == N.RMSNORM_F32 and hidden * esz <= 80 * 1024 else 4)
         assert p.grid == 152 and p.persistent == 1
         assert R.rmsnorm_plan(100, hidden, dtype, True, 152, 1).grid == 100
     assert R.rmsnorm_plan(1000, hidden, dtype, False, 152, 1).kernel == N.RMSNORM_KERNEL_LOOP

@@ -84,6 +84,7 @@ def test_long_rows_library_plan(dtype, hidden):
         x, r, w = W.make_inputs(wl, seed=hidden + rows, device=DEV)
         p = R.plan_for(x, w=w, residual=r)
         assert p.kernel == N.RMSNORM_KERNEL_TMA and p.regime == N.RMSNORM_REGIME_SMEM
+        assert p.chunks_per_thread == (4 if dtype == "bf16" and not has_res else 2)
         assert fits(hidden, esz, p.chunks_per_thread, has_res, has_w)
         out = R.rms_norm(x, w=w, residual=r, eps=wl.eps)
         y, h = out if r is not None else (out, None)
