@@ -95,9 +95,11 @@ enum {
 };
 
 /*
- * A launch plan.  The per-row schedule (kernel, threads_per_row,
- * chunks_per_thread, vec_elems, block_threads) depends only on hidden, dtype
- * and the alignment of the pointers; rows only sizes the grid.
+ * A launch plan.  The per-row schedule (kernel, threads_per_row, vec_elems,
+ * block_threads) depends only on hidden, dtype and the alignment of the
+ * pointers (and, for rows longer than 80 KB, on whether a residual is given);
+ * rows sizes the grid and may pick a chunk count that fits the row exactly,
+ * which never changes a result (chunks past the row end add exact zeros).
  */
 typedef struct {
     int32_t kernel;             /* RMSNORM_KERNEL_*                                   */
@@ -107,7 +109,9 @@ typedef struct {
     int32_t chunks_per_thread;  /* REG: vector chunks per thread (an upper bound:
                                    slots past the row end stay idle); 1, 2, 4 or 8,
                                    and 3 or 6 for contiguous RMSNorm / LayerNorm rows
-                                   in the I/O type; LOOP: 0; TMA: chunks per thread
+                                   in the I/O type (planning takes them for LayerNorm,
+                                   and for RMSNorm launches of more than one wave of
+                                   blocks); LOOP: 0; TMA: chunks per thread
                                    in one ring piece: 1, 2 or 4 (8, 16 or 32 KB
                                    pieces; 28, 14 or 7 slots of shared memory, of
                                    which avail / 7 (at least 1) go to a streamed

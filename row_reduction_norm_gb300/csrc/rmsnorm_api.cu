@@ -229,6 +229,27 @@ void size_grid(int64_t rows, int sm_count, int blocks_per_sm, rmsnorm_plan_t *p)
     if (p->persistent && p->kernel == RMSNORM_KERNEL_REG) p->regime = RMSNORM_REGIME_PERSISTENT;
 }
 
+// Chunk count that fits a register-kernel row exactly (3 or 6 chunks where
+// the power of two would leave slots idle).  Chunks past the row end add exact
+// zeros to the sum, so any count that covers the row gives the same result.
+int exact_ch(int64_t units, int gt, int ch) {
+    const int64_t need = ceil_div(units, gt);
+    if (need == 3) return 3;
+    if (need == 5 || need == 6) return 6;
+    return ch;
+}
+
+// Contiguous RMSNorm rows take the exact-fit chunk count when the launch has
+// more than one wave of blocks: measured on GB300 it is faster there (fewer
+// registers, more blocks resident: bf16 233016 x 576 without residual 0.874
+// -> 0.985 of peak, 26214 x 5120 0.855 -> 0.983) and slower for a single
+// wave (bf16 4096 x 576: 3.05 -> 3.17 us).
+void fit_chunks(int64_t rows, int64_t resident_blocks, bool contiguous_rms, int64_t units, rmsnorm_plan_t *p) {
+    if (!contiguous_rms || p->kernel != RMSNORM_KERNEL_REG) return;
+    if (ceil_div(rows, p->rows_per_block) <= resident_blocks) return;
+    p->chunks_per_thread = exact_ch(units, p->threads_per_row, p->chunks_per_thread);
+}
+
 size_t dyn_smem_of(const rmsnorm_plan_t *p, const Op &o) {
     if (p->kernel == RMSNORM_KERNEL_TMA) {
         TmaRings R;
@@ -412,6 +433,8 @@ int plan_for_device(const Op &o, rmsnorm_plan_t *plan, int *dev_out) {
     int bps = 0;
     if ((st = blocks_per_sm_of(dev, fn, plan->block_threads, smem, &bps)) != RMSNORM_OK) return st;
     size_grid(o.rows, sms, bps, plan);
+    fit_chunks(o.rows, (int64_t)sms * bps, !(o.ln || o.head_rows || o.mx || o.nv), o.row_elems / vec_elems_of(o.dtype),
+               plan);
     if (dev_out) *dev_out = dev;
     return RMSNORM_OK;
 }
@@ -696,6 +719,8 @@ int rmsnorm_plan(int64_t rows, int64_t hidden, int dtype, int vec_ok, int sm_cou
     if (vec_ok && (hidden * elem_size(dtype)) % 16 != 0) return RMSNORM_EINVAL;
     schedule(hidden, dtype, vec_ok ? 1 : 0, rrn::kRegMaxGT, plan, false, true);
     size_grid(rows, sm_count, blocks_per_sm, plan);
+    fit_chunks(rows, (int64_t)(sm_count > 0 ? sm_count : 1) * (blocks_per_sm > 0 ? blocks_per_sm : 1), true,
+               hidden / vec_elems_of(dtype), plan);
     return RMSNORM_OK;
 }
 

@@ -295,6 +295,27 @@ def test_deterministic_and_batch_invariant(name):
         assert parity.bits_equal(W.to_numpy_bits(yp), W.to_numpy_bits(ya[lo:hi]))
 
 
+@pytest.mark.parametrize("hidden,has_res", [(576, False), (576, True), (5120, False), (12288, True)])
+def test_batch_invariant_across_chunk_fit(hidden, has_res):
+    """A launch of many waves takes the chunk count that fits the row exactly
+    (3 or 6), a short one the power of two; a row's bits are the same in both."""
+    rows = max(40000 * 576 // hidden, 2000)
+    wl = W.Workload("fit", "bf16", rows, hidden, 1e-6, 1.0, 1.0 if has_res else None, 0.1)
+    x, r, w = gpu_inputs(wl, seed=hidden + has_res)
+    p_big = R.plan_for(x, w=w, residual=r)
+    p_small = R.plan_for(x[:13], w=w, residual=None if r is None else r[:13])
+    assert p_big.threads_per_row == p_small.threads_per_row
+    assert p_big.chunks_per_thread in (3, 6) and p_small.chunks_per_thread in (4, 8)
+    out = R.rms_norm(x, w=w, residual=r, eps=wl.eps)
+    y = out[0] if r is not None else out
+    part = R.rms_norm(x[:13].contiguous(), w=w, residual=None if r is None else r[:13].contiguous(), eps=wl.eps)
+    yp = part[0] if r is not None else part
+    torch.cuda.synchronize()
+    assert parity.bits_equal(W.to_numpy_bits(yp), W.to_numpy_bits(y[:13]))
+    check(y[:64], None if r is None else out[1][:64], x[:64], None if r is None else r[:64], w, wl.eps, "bf16",
+          what=f"H={hidden} res={has_res}")
+
+
 # ------------------------------------------------------------ special values
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
