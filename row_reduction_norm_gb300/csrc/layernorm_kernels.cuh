@@ -72,11 +72,16 @@ __device__ __forceinline__ float row_combine(float v, float (&red)[2][RPB][WPR],
 
 // Resident blocks per SM the register budget is sized for: four (64
 // registers a thread at 256 threads) for up to 4 chunks a thread, which keeps
-// enough loads in flight per SM; two (128 registers) for 8 chunks.
-__host__ __device__ constexpr int ln_min_blocks(int ch) { return ch <= 4 ? 4 : 2; }
+// enough loads in flight per SM; five (48 registers) for up to 3 chunks
+// without a residual, which fit them without spilling (measured on GB300:
+// bf16 16384 x 768 with weight and bias 11.47 -> 10.65 us; six spill and are
+// slower); two (128 registers) for 8 chunks.
+__host__ __device__ constexpr int ln_min_blocks(int ch, bool res) {
+    return (ch <= 3 && !res) ? 5 : (ch <= 4 ? 4 : 2);
+}
 
 template <typename T, int GT, int CH, bool RES, int AFF>
-__global__ void __launch_bounds__(reg_block_threads(GT), ln_min_blocks(CH))
+__global__ void __launch_bounds__(reg_block_threads(GT), ln_min_blocks(CH, RES))
 ln_reg_kernel(const LnParams p) {
     constexpr int V = T::kVec;
     constexpr int BLOCK = reg_block_threads(GT);
