@@ -86,3 +86,62 @@ def test_concurrent_host_threads_on_own_streams():
         yr, _ = _ref(x, None, w, wl.eps, "bf16")
         ok, rep = parity.compare_y(W.to_numpy_bits(outs[k]), yr, "bf16")
         assert ok, rep
+
+
+def test_bulk_copy_kernel_in_a_graph_and_from_threads():
+    """The shared-memory (bulk copy) kernel recorded in a CUDA graph and
+    replayed on new inputs, and launched from several host threads at once,
+    each on its own stream; no bounded wait runs out."""
+    from row_reduction_norm_gb300 import _native as N
+    wl = W.Workload("graph_long", "bf16", 40, 40960, 1e-6, 1.0, 1.0, 0.1)
+    x, r, w = W.make_inputs(wl, seed=3, device=DEV)
+    y, h = torch.empty_like(x), torch.empty_like(x)
+    assert R.plan_for(x, w=w, residual=r).kernel == N.RMSNORM_KERNEL_TMA
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        R.rms_norm(x, w=w, residual=r, eps=wl.eps, out=y, residual_out=h)   # fills the per-device caches
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        R.rms_norm(x, w=w, residual=r, eps=wl.eps, out=y, residual_out=h)
+    for seed in (21, 22):
+        x2, r2, _ = W.make_inputs(wl, seed=seed, device=DEV)
+        x.copy_(x2)
+        r.copy_(r2)
+        g.replay()
+        torch.cuda.synchronize()
+        yr, hr = _ref(x, r, w, wl.eps, "bf16")
+        ok, rep = parity.compare_y(W.to_numpy_bits(y), yr, "bf16")
+        assert ok, rep
+        assert parity.bits_equal(W.to_numpy_bits(h), hr)
+
+    n_threads = 3
+    inputs = [W.make_inputs(wl, seed=200 + k, device=DEV) for k in range(n_threads)]
+    outs = [(torch.empty_like(i[0]), torch.empty_like(i[0])) for i in inputs]
+    errors = []
+
+    def work(k):
+        try:
+            st = torch.cuda.Stream()
+            xk, rk, wk = inputs[k]
+            with torch.cuda.stream(st):
+                for _ in range(10):
+                    R.rms_norm(xk, w=wk, residual=rk, eps=wl.eps, out=outs[k][0], residual_out=outs[k][1])
+            st.synchronize()
+        except Exception as ex:   # reported below
+            errors.append(repr(ex))
+
+    ts = [threading.Thread(target=work, args=(k,)) for k in range(n_threads)]
+    for t in ts:
+        t.start()
+    for t in ts:
+        t.join()
+    assert not errors, errors
+    for k in range(n_threads):
+        xk, rk, wk = inputs[k]
+        yr, hr = _ref(xk, rk, wk, wl.eps, "bf16")
+        ok, rep = parity.compare_y(W.to_numpy_bits(outs[k][0]), yr, "bf16")
+        assert ok, rep
+        assert parity.bits_equal(W.to_numpy_bits(outs[k][1]), hr)
+    torch.cuda.synchronize()
+    assert N.rmsnorm_wait_timeouts() == 0
