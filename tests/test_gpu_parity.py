@@ -371,3 +371,33 @@ def test_status_codes_on_device():
     small.rows_per_block = 64
     assert N.rmsnorm_fwd_plan_status(p, None, None, q, None, 4, 64, 1e-6, 1, small, 0) == N.RMSNORM_EINVAL
     torch.cuda.synchronize()
+
+
+# ------------------------------------------------------ 64-bit addressing
+
+@pytest.mark.parametrize("hidden,rows,has_res,kind", [
+    (8192, 288000, False, "reg"),      # x 4.4 GiB: register kernel
+    (40960, 57600, False, "tma"),      # x 4.4 GiB: bulk-copy kernel
+    (65536, 36000, True, "loop"),      # x and residual 4.4 GiB each: two-pass kernel
+])
+def test_offsets_past_4gib(hidden, rows, has_res, kind):
+    """Tensors larger than 4 GiB: rows near the end sit at byte offsets past
+    2^32, checked against the oracle on sampled rows (first, last, and rows
+    either side of the 2^31 and 2^32 byte boundaries)."""
+    wl = W.Workload("big", "bf16", rows, hidden, 1e-6, 1.0, 1.0 if has_res else None, 0.1)
+    x, r, w = gpu_inputs(wl, seed=hidden)
+    p = R.plan_for(x, w=w, residual=r)
+    assert p.as_dict()["kernel_name"] == kind
+    out = R.rms_norm(x, w=w, residual=r, eps=wl.eps)
+    y, h = out if r is not None else (out, None)
+    torch.cuda.synchronize()
+    row_bytes = hidden * 2
+    picks = {0, rows - 1}
+    for edge in (1 << 31, 1 << 32):
+        k = edge // row_bytes
+        picks.update({k - 1, k, k + 1})
+    idx = torch.as_tensor(sorted(i for i in picks if 0 <= i < rows), device=DEV)
+    check(y[idx], None if h is None else h[idx], x[idx], None if r is None else r[idx], w, wl.eps, "bf16",
+          what=f"{kind} {rows}x{hidden}")
+    del x, r, y, h, out
+    torch.cuda.empty_cache()
