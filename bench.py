@@ -566,6 +566,51 @@ def copy_floor_us(L, steps=8192):
     return e0.elapsed_time(e1) * 1e3 / (reps * G)
 
 
+def independent_chains_us(L, steps=8192):
+    """Mean time per launch when consecutive batches do not depend on each
+    other: the same C-ABI launches split into two chains on two streams (even
+    and odd buffer sets, disjoint), whose launches may then overlap.  Context
+    for the dependent-chain figure, not a replacement for it: in a model each
+    norm's input comes from the kernel before it."""
+    import torch
+    streams = [L.stream, torch.cuda.Stream(L.stream.device)]
+    G = max(2, min(steps // 2, 1024))
+    graphs = []
+    saved = L.stream
+    try:
+        for c, st in enumerate(streams):
+            L.stream = st
+            with torch.cuda.stream(st):
+                L.launch(c)   # library caches filled outside the capture
+            st.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=st):
+                for i in range(G):
+                    L.launch(2 * i + c)
+            graphs.append(g)
+    finally:
+        L.stream = saved
+    for g, st in zip(graphs, streams):
+        with torch.cuda.stream(st):
+            g.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    joined = torch.cuda.Event()
+    reps = max(1, steps // (2 * G))
+    e0.record(streams[0])
+    streams[1].wait_event(e0)
+    for _ in range(reps):
+        for g, st in zip(graphs, streams):
+            with torch.cuda.stream(st):
+                g.replay()
+    joined.record(streams[1])
+    streams[0].wait_event(joined)
+    e1.record(streams[0])
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / (reps * 2 * G)
+
+
 def single_launch_latency_us(L, reps=200):
     import torch
     ts = []
@@ -671,6 +716,7 @@ def run_ours(args):
     e2e_serial, _ = aggregate(world, launch_bytes, wl.rows, e2e_steps, reduce_max(s_ms, dist, device))
 
     floor_us = copy_floor_us(L)
+    indep_us = independent_chains_us(L)
     per_config = []
     if not args.no_per_config:
         del L
@@ -762,6 +808,10 @@ def run_ours(args):
                          "kernel_vs_copy": round(floor_us / (per_launch_s * 1e6), 3),
                          "what": "torch copy_ of the same x -> y bytes, same graphs and buffer rotation: "
                                  "the per-launch floor of a dependent chain of this size"},
+        "independent_batches": {"value": round(launch_bytes / (indep_us / 1e6) / 1e9, 1), "unit": "GB/s",
+                                "us_per_launch": round(indep_us, 3), "streams": 2,
+                                "what": "context, not the metric: the same launches as two chains of "
+                                        "independent batches on two streams, free to overlap"},
         "gpu_launches": args.steps,
         "clocks": clocks,
         "cpu_baseline": cpu,
