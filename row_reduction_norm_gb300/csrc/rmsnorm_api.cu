@@ -131,13 +131,15 @@ int vec_ok_of(const Op &o) {
            (o.x_stride * s) % 16 == 0 && (o.y_stride * s) % 16 == 0;
 }
 
-// The per-row schedule: everything but the grid.
-// odd_ch: chunk counts 3 and 6 may be chosen (a row of 3 * 2^k chunks then
-// fills every slot); measured to help LayerNorm rows, not RMSNorm rows.
+// The per-row schedule: everything but the grid (and, for contiguous
+// RMSNorm rows, the exact-fit chunk count that fit_chunks picks from the row
+// count).
+// odd_ch: chunk counts 3 and 6 are chosen where they fit the row exactly
+// (LayerNorm rows).
 // tma_ok: the op has a bulk-copy kernel (contiguous RMSNorm rows).  For
 // these ops, measured on GB300: rows of 16 to 32 KB run best as 256 threads
 // x 8 chunks (not 512 x 4), and longer rows on the bulk-copy kernel (not
-// 512 x 8 in registers) when they fit its rings.
+// 512 x 8 in registers); has_res matters only for rows past 80 KB (below).
 void schedule(int64_t hidden, int dtype, int vec_ok, int max_gt, rmsnorm_plan_t *p, bool odd_ch = false,
               bool tma_ok = false, bool has_res = false) {
     std::memset(p, 0, sizeof(*p));
