@@ -90,21 +90,28 @@ def load_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+# Host-side planning and argument checks: not device code, so not part of
+# the hash that says whether a profile still describes the kernels.
+HOST_ONLY_SOURCES = ("rmsnorm_api.cu",)
+
+
 def kernel_source_hash():
+    """Hash of the device code (kernels and their instantiations)."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "row_reduction_norm_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
+        if name.endswith((".cu", ".cuh", ".h")) and name not in HOST_ONLY_SOURCES:
             with open(os.path.join(csrc, name), "rb") as f:
                 h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload):
+def profiled_traffic(workload, plan=None):
     """DRAM bytes per launch from the committed ncu summary of this workload
     (profiles/ncu_*.md with a matching ``profile_workload:`` line), if it was
-    taken on the current kernel sources; else None."""
+    taken on the current device code and, when ``plan`` is given, with the
+    same launch plan; else None."""
     pdir = os.path.join(ROOT, "profiles")
     try:
         names = sorted(os.listdir(pdir))
@@ -119,6 +126,9 @@ def profiled_traffic(workload):
             continue
         m_hash = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", text)
         m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
+        m_plan = re.search(r"^Plan: `(\{.*\})`", text, re.M)
+        if plan is not None and (not m_plan or json.loads(m_plan.group(1)) != plan):
+            continue
         if m_hash and m_bytes and m_hash.group(1) == kernel_source_hash():
             return int(m_bytes.group(1))
     return None
@@ -767,7 +777,7 @@ def run_ours(args):
             dist.destroy_process_group()
         return
     clocks = sampler.summary(window[0], window[1]) if sampler and window else None
-    traffic = profiled_traffic(args.workload)
+    traffic = profiled_traffic(args.workload, plan_summary(L.plan))
     out = {
         "metric": METRIC,
         "value": round(value, 2),
