@@ -63,10 +63,10 @@ const void *reg_gt(int gt, int ch, int wm) {
 template <typename T, int GT, int CH, bool RES>
 const void *mx_wm(int wm) {
     switch (wm) {
-        case kNoWeight: return reinterpret_cast<const void *>(&rms_reg_kernel<T, GT, CH, RES, kNoWeight, false, kOutMxfp8>);
-        case kWeight: return reinterpret_cast<const void *>(&rms_reg_kernel<T, GT, CH, RES, kWeight, false, kOutMxfp8>);
+        case kNoWeight: return reinterpret_cast<const void *>(&rms_quant_kernel<T, GT, CH, RES, kNoWeight, kOutMxfp8>);
+        case kWeight: return reinterpret_cast<const void *>(&rms_quant_kernel<T, GT, CH, RES, kWeight, kOutMxfp8>);
         case kWeightBias:
-            return reinterpret_cast<const void *>(&rms_reg_kernel<T, GT, CH, RES, kWeightBias, false, kOutMxfp8>);
+            return reinterpret_cast<const void *>(&rms_quant_kernel<T, GT, CH, RES, kWeightBias, kOutMxfp8>);
         default: return nullptr;
     }
 }
@@ -105,10 +105,10 @@ const void *mx_gt(int gt, int ch, int wm) {
 template <typename T, int GT, int CH, bool RES>
 const void *nv_wm(int wm) {
     switch (wm) {
-        case kNoWeight: return reinterpret_cast<const void *>(&rms_reg_kernel<T, GT, CH, RES, kNoWeight, false, kOutNvfp4>);
-        case kWeight: return reinterpret_cast<const void *>(&rms_reg_kernel<T, GT, CH, RES, kWeight, false, kOutNvfp4>);
+        case kNoWeight: return reinterpret_cast<const void *>(&rms_quant_kernel<T, GT, CH, RES, kNoWeight, kOutNvfp4>);
+        case kWeight: return reinterpret_cast<const void *>(&rms_quant_kernel<T, GT, CH, RES, kWeight, kOutNvfp4>);
         case kWeightBias:
-            return reinterpret_cast<const void *>(&rms_reg_kernel<T, GT, CH, RES, kWeightBias, false, kOutNvfp4>);
+            return reinterpret_cast<const void *>(&rms_quant_kernel<T, GT, CH, RES, kWeightBias, kOutNvfp4>);
         default: return nullptr;
     }
 }

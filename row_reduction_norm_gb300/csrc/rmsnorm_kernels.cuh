@@ -337,19 +337,9 @@ __device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
     return (uint32_t)__nv_cvt_float2_to_fp4x2(make_float2(lo, hi), __NV_E2M1, cudaRoundNearest);
 }
 
-// Resident blocks the block-scaled epilogues are budgeted for: four 256-thread
-// blocks (64 registers a thread) up to 4 chunks, where they fit without
-// spilling more than a word; measured on GB300, four blocks beat the three
-// that the unbudgeted 76 registers allow (MXFP8 16384 x 2048 with residual
-// 0.940 -> 0.965 of peak, NVFP4 65536 x 8192 0.954 -> 1.004).  8 chunks would
-// spill, and the plain epilogue needs no budget.
-__host__ __device__ constexpr int reg_min_blocks(int gt, int ch, int out) {
-    return (out != kOutT && reg_block_threads(gt) == 256 && ch <= 4) ? 4 : 1;
-}
-
-template <typename T, int GT, int CH, bool RES, int WM, bool HEADS, int OUT = kOutT>
-__global__ void __launch_bounds__(reg_block_threads(GT), reg_min_blocks(GT, CH, OUT))
-rms_reg_kernel(const Params p) {
+// The register kernel's body: blocks stride over row groups of RPB rows.
+template <typename T, int GT, int CH, bool RES, int WM, bool HEADS, int OUT>
+__device__ __forceinline__ void rms_reg_rows(const Params &p) {
     constexpr bool W = WM != kNoWeight;
     static_assert(!(HEADS && RES), "head rows take no residual");
     static_assert(OUT == kOutT || (!HEADS && GT >= 32 / T::kVec), "block-scaled output: contiguous rows, "
@@ -577,6 +567,28 @@ rms_reg_kernel(const Params p) {
             }
         }
     }
+}
+
+// Plain output: the launch bound names the block size only.
+template <typename T, int GT, int CH, bool RES, int WM, bool HEADS>
+__global__ void __launch_bounds__(reg_block_threads(GT)) rms_reg_kernel(const Params p) {
+    rms_reg_rows<T, GT, CH, RES, WM, HEADS, kOutT>(p);
+}
+
+// Resident blocks the block-scaled epilogues are budgeted for: four 256-thread
+// blocks (64 registers a thread) up to 4 chunks, where they fit without
+// spilling more than a word; measured on GB300, four blocks beat the three
+// that the unbudgeted 76 registers allow (MXFP8 16384 x 2048 with residual
+// 0.940 -> 0.965 of peak, NVFP4 65536 x 8192 0.954 -> 1.004).  8 chunks would
+// spill.
+__host__ __device__ constexpr int quant_min_blocks(int gt, int ch) {
+    return (reg_block_threads(gt) == 256 && ch <= 4) ? 4 : 1;
+}
+
+// MXFP8 / NVFP4 output (contiguous rows).
+template <typename T, int GT, int CH, bool RES, int WM, int OUT>
+__global__ void __launch_bounds__(reg_block_threads(GT), quant_min_blocks(GT, CH)) rms_quant_kernel(const Params p) {
+    rms_reg_rows<T, GT, CH, RES, WM, false, OUT>(p);
 }
 
 // ------------------------------------------------------- two-pass kernel
