@@ -293,16 +293,20 @@ __device__ __forceinline__ float tree_sum(float (&v)[N]) {
 // nearest-even, saturated at 448.  A block holding NaN or Inf is all NaN
 // (scale 0xFF, codes 0x7F).  With the row's chunk c*GT + t owned by thread
 // t, the 32 elements of a block sit in LPB = 32 / V consecutive lanes, which
-// combine their maxima with xor shuffles.
+// combine their maxima with xor shuffles.  The maxima propagate NaN
+// (max.NaN), so a block's maximum is NaN or Inf exactly when one of its
+// elements is: that one value marks the special blocks.
+__device__ __forceinline__ float max_nan(float a, float b) {
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
+
 template <int LPB>
-__device__ __forceinline__ void mx_block_stats(float &amax, bool &special) {
-    unsigned sp = special ? 1u : 0u;
+__device__ __forceinline__ float block_amax(float amax) {
 #pragma unroll
-    for (int off = LPB / 2; off > 0; off >>= 1) {
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-        sp |= __shfl_xor_sync(0xffffffffu, sp, off);
-    }
-    special = sp != 0u;
+    for (int off = LPB / 2; off > 0; off >>= 1) amax = max_nan(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    return amax;
 }
 
 // E8M0 exponent of a block from its (finite, non-negative) amax.
@@ -464,16 +468,12 @@ __device__ __forceinline__ void rms_reg_rows(const Params &p) {
 #pragma unroll
                     for (int e = 0; e < V; ++e) wv[e] = 1.f;
                 }
-                float amax = 0.f;
-                bool special = false;
                 scale_out_pairs<WM>(a, r, wv, p.w_bias);
+                float amax = 0.f;
 #pragma unroll
-                for (int e = 0; e < V; ++e) {
-                    const float m = fabsf(a[e]);
-                    special |= !(m <= 3.402823466e38f);     // NaN or Inf
-                    amax = fmaxf(amax, m);
-                }
-                mx_block_stats<LPB>(amax, special);
+                for (int e = 0; e < V; ++e) amax = max_nan(amax, fabsf(a[e]));
+                amax = block_amax<LPB>(amax);
+                const bool special = !(amax <= 3.402823466e38f);     // NaN or Inf in the block
                 const int s = mx_scale_exponent(amax);
                 const float mult = __int_as_float((127 - s) << 23);   // 2^-s, a normal float
                 uint32_t q[V / 4];
@@ -516,14 +516,10 @@ __device__ __forceinline__ void rms_reg_rows(const Params &p) {
                 }
                 scale_out_pairs<WM>(a, r, wv, p.w_bias);
                 float amax = 0.f;
-                bool special = false;
 #pragma unroll
-                for (int e = 0; e < V; ++e) {
-                    const float m = fabsf(a[e]);
-                    special |= !(m <= 3.402823466e38f);     // NaN or Inf
-                    amax = fmaxf(amax, m);
-                }
-                mx_block_stats<LPB>(amax, special);
+                for (int e = 0; e < V; ++e) amax = max_nan(amax, fabsf(a[e]));
+                amax = block_amax<LPB>(amax);
+                const bool special = !(amax <= 3.402823466e38f);     // NaN or Inf in the block
                 const uint8_t sc = special ? (uint8_t)0x7F : e4m3_of(amax * p.q_inv6s);
                 const float sv = special ? 0.f : e4m3_value(sc);
                 uint32_t packed = 0u;

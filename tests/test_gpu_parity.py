@@ -212,8 +212,8 @@ def test_rows_zero_is_noop():
 # ------------------------------------------------------ alignment, aliasing
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
-def test_misaligned_base_pointer(dtype):
-    rows, hidden = 33, 2048
+@pytest.mark.parametrize("rows,hidden", [(33, 2048), (5, 65536), (9, 40960)])
+def test_misaligned_base_pointer(dtype, rows, hidden):
     tdt = W.TORCH_DTYPE[dtype]
     buf = W.random_rows(dtype, 1, rows * hidden + 1, seed=4, device=DEV).reshape(-1)
     x = buf[1:].view(rows, hidden)           # one element past a 16-byte boundary
