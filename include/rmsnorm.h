@@ -244,8 +244,11 @@ int rmsnorm_qk_plan_for(const void *x, const void *y, int64_t tokens, int64_t x_
  *   codes   [rows, hidden] bytes: E4M3 of v_i / 2^s, nearest-even, saturated at 448
  * A block holding NaN or Inf is a NaN block (scale 0xFF, every code 0x7F).
  * hidden must be a multiple of 32 and x, residual, w, codes and
- * residual_out 16-byte aligned (else RMSNORM_EINVAL); hidden up to 32768
- * (bf16) or 16384 (fp32), else RMSNORM_EUNSUPPORTED.  residual_out
+ * residual_out 16-byte aligned (else RMSNORM_EINVAL).  Rows past 32768 bf16
+ * or 16384 fp32 elements run on RMSNORM_KERNEL_TMA (16 KB pieces) while its
+ * rings hold them: every bf16 width, fp32 up to 40960 elements with a
+ * residual and a weight (49152 with one of them, 57344 with neither), else
+ * RMSNORM_EUNSUPPORTED.  residual_out
  * (required with a residual) receives h in the I/O type.  A code chosen by
  * the kernel may differ from the correctly rounded one only when the exact
  * value lies within the fp32 error of the op (about 1e-6 relative) of an
@@ -276,7 +279,8 @@ int rmsnorm_mxfp8_plan_for(const void *x, const void *residual, const void *w,
  * A block holding NaN or Inf gets the E4M3 NaN 0x7F as its scale and codes 0.
  * bf16 I/O only (fp32: RMSNORM_EUNSUPPORTED); hidden a multiple of 16;
  * tensor_scale > 0 and finite; x, residual, w, codes, residual_out 16-byte
- * aligned.  Codes and scales may differ from the correctly rounded ones only
+ * aligned.  Rows past 32768 elements run on RMSNORM_KERNEL_TMA (16 KB
+ * pieces).  Codes and scales may differ from the correctly rounded ones only
  * where the exact value lies within the op's fp32 error of a rounding
  * boundary, as for MXFP8.
  */

@@ -270,7 +270,11 @@ int mx_min_gt(int dtype) { return 32 / vec_elems_of(dtype); }
 const void *kernel_of(const rmsnorm_plan_t *p, const Op &o) {
     const bool res = o.res != nullptr;
     if (p->kernel == RMSNORM_KERNEL_TMA) {
-        if (o.mx || o.nv || o.ln || o.head_rows) return nullptr;
+        if (o.ln || o.head_rows) return nullptr;
+        if (o.mx || o.nv)
+            return p->chunks_per_thread == 2 ? rrn::tma_quant_kernel(o.dtype, res, o.wm, o.mx ? rrn::kOutMxfp8
+                                                                                              : rrn::kOutNvfp4)
+                                             : nullptr;
         return rrn::tma_kernel(o.dtype, p->chunks_per_thread, res, o.wm);
     }
     if (o.mx || o.nv) {
@@ -311,7 +315,8 @@ int validate_plan(const rmsnorm_plan_t *p, const Op &o, int vec_ok) {
         return RMSNORM_OK;
     }
     if (p->kernel == RMSNORM_KERNEL_TMA) {
-        if (o.mx || o.nv || o.ln || o.head_rows) return RMSNORM_EINVAL;   // contiguous RMSNorm rows only
+        if (o.ln || o.head_rows) return RMSNORM_EINVAL;   // contiguous RMSNorm rows only
+        if ((o.mx || o.nv) && p->chunks_per_thread != 2) return RMSNORM_EINVAL;   // compiled for 16 KB pieces
         if (!vec_ok || p->vec_elems != V) return RMSNORM_EINVAL;
         if (p->threads_per_row != rrn::kTmaGT || p->block_threads != rrn::kTmaBlock || p->rows_per_block != 1)
             return RMSNORM_EINVAL;
@@ -411,8 +416,22 @@ int blocks_per_sm_of(int dev, const void *fn, int block, size_t smem, int *out) 
 int plan_for_device(const Op &o, rmsnorm_plan_t *plan, int *dev_out) {
     schedule(o.row_elems, o.dtype, vec_ok_of(o), max_threads_per_row(o), plan, o.ln,
              !(o.ln || o.head_rows || o.mx || o.nv), o.res != nullptr);
-    if ((o.mx || o.nv) && plan->kernel != RMSNORM_KERNEL_REG) return RMSNORM_EUNSUPPORTED;
-    if (o.mx) {
+    if ((o.mx || o.nv) && plan->kernel != RMSNORM_KERNEL_REG) {
+        // rows too long for registers: the bulk-copy kernel with 16 KB pieces
+        // when its rings hold the row, else unsupported
+        if (!vec_ok_of(o) ||
+            !tma_rings(o.row_elems * elem_size(o.dtype), kTmaPlanPC, o.res != nullptr, o.w != nullptr, nullptr))
+            return RMSNORM_EUNSUPPORTED;
+        std::memset(plan, 0, sizeof(*plan));
+        plan->kernel = RMSNORM_KERNEL_TMA;
+        plan->regime = RMSNORM_REGIME_SMEM;
+        plan->threads_per_row = rrn::kTmaGT;
+        plan->chunks_per_thread = kTmaPlanPC;
+        plan->vec_elems = vec_elems_of(o.dtype);
+        plan->block_threads = rrn::kTmaBlock;
+        plan->rows_per_block = 1;
+    }
+    if (o.mx && plan->kernel == RMSNORM_KERNEL_REG) {
         const int V = vec_elems_of(o.dtype);
         while (plan->threads_per_row < mx_min_gt(o.dtype)) plan->threads_per_row <<= 1;
         int64_t need = ceil_div(o.row_elems / V, plan->threads_per_row);

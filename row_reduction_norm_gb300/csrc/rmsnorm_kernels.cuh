@@ -341,6 +341,68 @@ __device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
     return (uint32_t)__nv_cvt_float2_to_fp4x2(make_float2(lo, hi), __NV_E2M1, cudaRoundNearest);
 }
 
+// A7, block-scaled forms: the fp32 values a[] (h * r * w, not rounded) of
+// chunk u of `row`, quantised with the other lanes of their block and stored
+// (codes, and the block's scale from its first lane).  Every lane of a block
+// calls it together, with the same `valid`; t is the thread's index in the
+// row's group of threads.
+template <int V, int OUT>
+__device__ __forceinline__ void store_quantised(float (&a)[V], bool valid, const Params &p, int64_t row, int u,
+                                                int t) {
+    float amax = 0.f;
+#pragma unroll
+    for (int e = 0; e < V; ++e) amax = max_nan(amax, fabsf(a[e]));
+    if constexpr (OUT == kOutMxfp8) {
+        constexpr int LPB = 32 / V;
+        amax = block_amax<LPB>(amax);
+        const bool special = !(amax <= 3.402823466e38f);     // NaN or Inf in the block
+        const int s = mx_scale_exponent(amax);
+        const float mult = __int_as_float((127 - s) << 23);   // 2^-s, a normal float
+        uint32_t q[V / 4];
+#pragma unroll
+        for (int k = 0; k < V / 4; ++k) {
+            const uint32_t lo = e4m3x2(a[4 * k] * mult, a[4 * k + 1] * mult);
+            const uint32_t hi = e4m3x2(a[4 * k + 2] * mult, a[4 * k + 3] * mult);
+            q[k] = special ? 0x7F7F7F7Fu : (lo | (hi << 16));
+        }
+        if (valid) {
+            char *dst = static_cast<char *>(p.y) + row * p.row_elems + (int64_t)u * V;
+            if constexpr (V == 8) {
+                asm volatile("st.global.v2.u32 [%0], {%1, %2};" : : "l"(dst), "r"(q[0]), "r"(q[1]) : "memory");
+            } else {
+                asm volatile("st.global.u32 [%0], %1;" : : "l"(dst), "r"(q[0]) : "memory");
+            }
+            if (t % LPB == 0) {
+                const uint8_t sc = special ? (uint8_t)0xFF : (uint8_t)(s + 127);
+                static_cast<uint8_t *>(p.scales)[row * (p.row_elems / 32) + u / LPB] = sc;
+            }
+        }
+    } else {
+        constexpr int LPB = 16 / V;
+        amax = block_amax<LPB>(amax);
+        const bool special = !(amax <= 3.402823466e38f);     // NaN or Inf in the block
+        const uint8_t sc = special ? (uint8_t)0x7F : e4m3_of(amax * p.q_inv6s);
+        const float sv = special ? 0.f : e4m3_value(sc);
+        uint32_t packed = 0u;
+        if (sv > 0.f) {
+            // fast reciprocal (CUDA documents <= 2 ulp): the code decision
+            // tolerance covers it (a few 1e-7 against 2.5e-6)
+            const float rcp = __fdividef(1.f, sv * p.q_scale);
+#pragma unroll
+            for (int k = 0; k < V / 2; ++k) packed |= e2m1x2(a[2 * k] * rcp, a[2 * k + 1] * rcp) << (8 * k);
+        }
+        if (valid) {
+            char *dst = static_cast<char *>(p.y) + row * (p.row_elems / 2) + (int64_t)u * (V / 2);
+            if constexpr (V == 8) {
+                asm volatile("st.global.u32 [%0], %1;" : : "l"(dst), "r"(packed) : "memory");
+            } else {
+                asm volatile("st.global.u16 [%0], %1;" : : "l"(dst), "h"((unsigned short)packed) : "memory");
+            }
+            if (t % LPB == 0) static_cast<uint8_t *>(p.scales)[row * (p.row_elems / 16) + u / LPB] = sc;
+        }
+    }
+}
+
 // The register kernel's body: blocks stride over row groups of RPB rows.
 template <typename T, int GT, int CH, bool RES, int WM, bool HEADS, int OUT>
 __device__ __forceinline__ void rms_reg_rows(const Params &p) {
@@ -452,9 +514,8 @@ __device__ __forceinline__ void rms_reg_rows(const Params &p) {
         }
         // A6: the row's scale
         const float r = rsqrtf(sum / p.hidden_f + p.eps);
-        // A7 (MXFP8 form): values, block scale, E4M3 codes
-        if constexpr (OUT == kOutMxfp8) {
-            constexpr int LPB = 32 / V;
+        // A7, block-scaled forms: values, block scale, codes
+        if constexpr (OUT != kOutT) {
 #pragma unroll
             for (int c = 0; c < CH; ++c) {
                 const int u = c * GT + t;
@@ -469,78 +530,7 @@ __device__ __forceinline__ void rms_reg_rows(const Params &p) {
                     for (int e = 0; e < V; ++e) wv[e] = 1.f;
                 }
                 scale_out_pairs<WM>(a, r, wv, p.w_bias);
-                float amax = 0.f;
-#pragma unroll
-                for (int e = 0; e < V; ++e) amax = max_nan(amax, fabsf(a[e]));
-                amax = block_amax<LPB>(amax);
-                const bool special = !(amax <= 3.402823466e38f);     // NaN or Inf in the block
-                const int s = mx_scale_exponent(amax);
-                const float mult = __int_as_float((127 - s) << 23);   // 2^-s, a normal float
-                uint32_t q[V / 4];
-#pragma unroll
-                for (int k = 0; k < V / 4; ++k) {
-                    const uint32_t lo = e4m3x2(a[4 * k] * mult, a[4 * k + 1] * mult);
-                    const uint32_t hi = e4m3x2(a[4 * k + 2] * mult, a[4 * k + 3] * mult);
-                    q[k] = special ? 0x7F7F7F7Fu : (lo | (hi << 16));
-                }
-                if (valid) {
-                    char *dst = static_cast<char *>(p.y) + row * p.row_elems + (int64_t)u * V;
-                    if constexpr (V == 8) {
-                        asm volatile("st.global.v2.u32 [%0], {%1, %2};" : : "l"(dst), "r"(q[0]), "r"(q[1]) : "memory");
-                    } else {
-                        asm volatile("st.global.u32 [%0], %1;" : : "l"(dst), "r"(q[0]) : "memory");
-                    }
-                    if (t % LPB == 0) {
-                        const uint8_t sc = special ? (uint8_t)0xFF : (uint8_t)(s + 127);
-                        static_cast<uint8_t *>(p.scales)[row * (p.row_elems / 32) + u / LPB] = sc;
-                    }
-                }
-            }
-            continue;
-        }
-        // A7 (NVFP4 form): values, block scale, packed E2M1 codes
-        if constexpr (OUT == kOutNvfp4) {
-            constexpr int LPB = 16 / V;
-#pragma unroll
-            for (int c = 0; c < CH; ++c) {
-                const int u = c * GT + t;
-                const bool valid = row_ok && u < nch;     // uniform over a block's lanes
-                float a[V];
-                unpack(hc[c], a, T{});
-                float wv[V];
-                if constexpr (W) {
-                    unpack(w_smem[valid ? u : 0], wv, T{});
-                } else {
-#pragma unroll
-                    for (int e = 0; e < V; ++e) wv[e] = 1.f;
-                }
-                scale_out_pairs<WM>(a, r, wv, p.w_bias);
-                float amax = 0.f;
-#pragma unroll
-                for (int e = 0; e < V; ++e) amax = max_nan(amax, fabsf(a[e]));
-                amax = block_amax<LPB>(amax);
-                const bool special = !(amax <= 3.402823466e38f);     // NaN or Inf in the block
-                const uint8_t sc = special ? (uint8_t)0x7F : e4m3_of(amax * p.q_inv6s);
-                const float sv = special ? 0.f : e4m3_value(sc);
-                uint32_t packed = 0u;
-                if (sv > 0.f) {
-                    // fast reciprocal (CUDA documents <= 2 ulp): the code decision
-                    // tolerance covers it (a few 1e-7 against 2.5e-6)
-                    const float rcp = __fdividef(1.f, sv * p.q_scale);
-#pragma unroll
-                    for (int k = 0; k < V / 2; ++k)
-                        packed |= e2m1x2(a[2 * k] * rcp, a[2 * k + 1] * rcp) << (8 * k);
-                }
-                if (valid) {
-                    char *dst = static_cast<char *>(p.y) + row * (p.row_elems / 2) + (int64_t)u * (V / 2);
-                    if constexpr (V == 8) {
-                        asm volatile("st.global.u32 [%0], %1;" : : "l"(dst), "r"(packed) : "memory");
-                    } else {
-                        asm volatile("st.global.u16 [%0], %1;" : : "l"(dst), "h"((unsigned short)packed) : "memory");
-                    }
-                    if (t % LPB == 0)
-                        static_cast<uint8_t *>(p.scales)[row * (p.row_elems / 16) + u / LPB] = sc;
-                }
+                store_quantised<V, OUT>(a, valid, p, row, u, t);
             }
             continue;
         }

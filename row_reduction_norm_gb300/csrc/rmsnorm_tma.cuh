@@ -169,7 +169,10 @@ __device__ __forceinline__ void drain_ring(const Ring &R, unsigned issued) {
 // sx, sr, sw: slots of the x, residual and weight rings (sr = 0 without a
 // residual, sw = 0 without a weight).  sx >= pieces; sw >= pieces makes the
 // weight resident (copied once per block, never released).
-template <typename T, bool RES, int WM, int PC>
+// OUT: kOutT writes y in the I/O type; kOutMxfp8 / kOutNvfp4 write the
+// block-scaled codes and scales (the register kernel's epilogue, with the
+// same lane layout: a block's chunks sit in consecutive threads of a piece).
+template <typename T, bool RES, int WM, int PC, int OUT = kOutT>
 __global__ void __launch_bounds__(kTmaBlock, 1)
 rms_tma_kernel(const Params p, const int sx, const int sr, const int sw) {
     constexpr bool W = WM != kNoWeight;
@@ -304,19 +307,34 @@ rms_tma_kernel(const Params p, const int sx, const int sr, const int sw) {
 #pragma unroll
                 for (int j = 0; j < PC; ++j) {
                     const int u = (k * PC + j) * GT + t;
-                    if (u < nch) {
-                        const int so = (j * GT + t) * 16;
-                        float a[V];
-                        unpack(lds16(xp + so), a, T{});
-                        float wv[V];
-                        if constexpr (W) {
-                            unpack(lds16(wp + so), wv, T{});
-                        } else {
+                    const int so = (j * GT + t) * 16;
+                    if constexpr (OUT == kOutT) {
+                        if (u < nch) {
+                            float a[V];
+                            unpack(lds16(xp + so), a, T{});
+                            float wv[V];
+                            if constexpr (W) {
+                                unpack(lds16(wp + so), wv, T{});
+                            } else {
 #pragma unroll
-                            for (int e = 0; e < V; ++e) wv[e] = 1.f;
+                                for (int e = 0; e < V; ++e) wv[e] = 1.f;
+                            }
+                            scale_out_pairs<WM>(a, r, wv, p.w_bias);
+                            st16(static_cast<char *>(p.y) + roff + (int64_t)u * 16, pack(a, T{}));
+                        }
+                    } else {
+                        // every lane joins its block's shuffles; `valid` is
+                        // uniform over a block (rows are whole blocks)
+                        const bool valid = u < nch;
+                        float a[V], wv[V];
+#pragma unroll
+                        for (int e = 0; e < V; ++e) a[e] = 0.f, wv[e] = 1.f;
+                        if (valid) {
+                            unpack(lds16(xp + so), a, T{});
+                            if constexpr (W) unpack(lds16(wp + so), wv, T{});
                         }
                         scale_out_pairs<WM>(a, r, wv, p.w_bias);
-                        st16(static_cast<char *>(p.y) + roff + (int64_t)u * 16, pack(a, T{}));
+                        store_quantised<V, OUT>(a, valid, p, row, u, t);
                     }
                 }
                 // the slot's next copy comes through the async proxy: order

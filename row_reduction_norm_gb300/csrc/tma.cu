@@ -6,12 +6,12 @@
 namespace rrn {
 namespace {
 
-template <typename T, bool RES, int PC>
+template <typename T, bool RES, int PC, int OUT>
 const void *tma_wm(int wm) {
     switch (wm) {
-        case kNoWeight: return reinterpret_cast<const void *>(&rms_tma_kernel<T, RES, kNoWeight, PC>);
-        case kWeight: return reinterpret_cast<const void *>(&rms_tma_kernel<T, RES, kWeight, PC>);
-        case kWeightBias: return reinterpret_cast<const void *>(&rms_tma_kernel<T, RES, kWeightBias, PC>);
+        case kNoWeight: return reinterpret_cast<const void *>(&rms_tma_kernel<T, RES, kNoWeight, PC, OUT>);
+        case kWeight: return reinterpret_cast<const void *>(&rms_tma_kernel<T, RES, kWeight, PC, OUT>);
+        case kWeightBias: return reinterpret_cast<const void *>(&rms_tma_kernel<T, RES, kWeightBias, PC, OUT>);
         default: return nullptr;
     }
 }
@@ -19,9 +19,9 @@ const void *tma_wm(int wm) {
 template <typename T, bool RES>
 const void *tma_pc(int pc, int wm) {
     switch (pc) {
-        case 1: return tma_wm<T, RES, 1>(wm);
-        case 2: return tma_wm<T, RES, 2>(wm);
-        case 4: return tma_wm<T, RES, 4>(wm);
+        case 1: return tma_wm<T, RES, 1, kOutT>(wm);
+        case 2: return tma_wm<T, RES, 2, kOutT>(wm);
+        case 4: return tma_wm<T, RES, 4, kOutT>(wm);
         default: return nullptr;
     }
 }
@@ -31,6 +31,16 @@ const void *tma_pc(int pc, int wm) {
 const void *tma_kernel(int dtype, int pc, bool res, int wm) {
     if (dtype == 1) return res ? tma_pc<BF16, true>(pc, wm) : tma_pc<BF16, false>(pc, wm);
     return res ? tma_pc<F32, true>(pc, wm) : tma_pc<F32, false>(pc, wm);
+}
+
+const void *tma_quant_kernel(int dtype, bool res, int wm, int out) {
+    if (out == kOutMxfp8) {
+        if (dtype == 1) return res ? tma_wm<BF16, true, 2, kOutMxfp8>(wm) : tma_wm<BF16, false, 2, kOutMxfp8>(wm);
+        return res ? tma_wm<F32, true, 2, kOutMxfp8>(wm) : tma_wm<F32, false, 2, kOutMxfp8>(wm);
+    }
+    if (out == kOutNvfp4 && dtype == 1)
+        return res ? tma_wm<BF16, true, 2, kOutNvfp4>(wm) : tma_wm<BF16, false, 2, kOutNvfp4>(wm);
+    return nullptr;
 }
 
 int tma_timeouts_read(unsigned int *out) {

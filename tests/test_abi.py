@@ -192,7 +192,15 @@ def test_tma_plan_validation_without_cuda():
     assert st(q, x=P + 2) == N.RMSNORM_EINVAL
     # rows == 0 validates the plan and launches nothing
     assert N.rmsnorm_fwd_plan_status(P, None, None, P, None, 0, 40000, 1e-6, 1, good, 0) == N.RMSNORM_OK
-    # the other ops have no bulk-copy kernel
+    # block-scaled outputs run on it with 16 KB pieces only (rows = 0: validation only)
+    q = good.copy()
+    q.chunks_per_thread = 2
+    assert N.rmsnorm_fwd_mxfp8_status(P, None, None, P, P, None, 0, 40000, 1e-6, 0.0, 1, q) == N.RMSNORM_OK
+    assert N.rmsnorm_fwd_nvfp4_status(P, None, None, P, P, None, 0, 40000, 1e-6, 0.0, 1.0, 1, q) == N.RMSNORM_OK
+    q.chunks_per_thread = 4
+    assert N.rmsnorm_fwd_mxfp8_status(P, None, None, P, P, None, 0, 40000, 1e-6, 0.0, 1, q) == N.RMSNORM_EINVAL
+    assert N.rmsnorm_fwd_nvfp4_status(P, None, None, P, P, None, 0, 40000, 1e-6, 0.0, 1.0, 1, q) == N.RMSNORM_EINVAL
+    # LayerNorm and head rows have no bulk-copy kernel
     assert N.layernorm_fwd_status(P, None, None, None, P, None, 4, 40000, 1e-5, 1, good) == N.RMSNORM_EINVAL
     assert N.rmsnorm_qk_fwd_status(P, P, 4, 40000, 40000, 1, 0, 40000, None, None, 0.0, 1e-6, 1,
                                    good) == N.RMSNORM_EINVAL

@@ -90,8 +90,10 @@ def test_mx_argument_checks():
                                       0.0, 1) == N.RMSNORM_EINVAL     # codes not 16-byte aligned
     assert N.rmsnorm_fwd_mxfp8_status(x.data_ptr(), None, None, c.data_ptr(), None, None, 4, 64, 1e-6, 0.0, 1) \
         == N.RMSNORM_EINVAL                                           # no scales
+    # fp32 rows of 65536 (256 KB) fit neither registers nor the bulk-copy
+    # kernel's rings: refused at planning, before any launch
     big = N.rmsnorm_fwd_mxfp8_status(x.data_ptr(), None, None, c.data_ptr(), s.data_ptr(), None, 1, 65536, 1e-6,
-                                     0.0, 1)
+                                     0.0, 0)
     assert big == N.RMSNORM_EUNSUPPORTED
     torch.cuda.synchronize()
 
@@ -114,3 +116,25 @@ def test_mx_matches_plain_op_dequantised():
     in_range = np.abs(v64) <= 448.0 * scale_full          # saturated values (448..512 x scale) excluded
     assert np.all((np.abs(deq - v64) <= limit) | ~in_range)
     assert np.all(np.abs(deq[~in_range]) == 448.0 * scale_full[~in_range])
+
+
+@pytest.mark.parametrize("dtype,hidden,has_res,has_w", [("bf16", 40960, True, True), ("bf16", 65536, False, True),
+                                                        ("bf16", 65536, True, True), ("f32", 24576, True, True),
+                                                        ("f32", 40960, True, True)])
+def test_mx_long_rows_on_the_bulk_copy_kernel(dtype, hidden, has_res, has_w):
+    """Rows too long for registers take the bulk-copy kernel (16 KB pieces)
+    with the same block-scaled epilogue; a grid of 3 blocks over 11 rows also
+    checks that blocks walk several rows."""
+    wl = W.Workload("mx-long", dtype, 11, hidden, 1e-5, 1.0, 1.0 if has_res else None, 0.1 if has_w else None)
+    x, r, w = W.make_inputs(wl, seed=hidden + has_res, device=DEV)
+    p = R.rms_norm_mxfp8_plan_for(x, w=w, residual=r)
+    assert p.kernel == N.RMSNORM_KERNEL_TMA and p.chunks_per_thread == 2
+    out = R.rms_norm_mxfp8(x, w=w, residual=r, eps=wl.eps)
+    torch.cuda.synchronize()
+    mx_check(out, x, r, w, wl.eps, dtype, f"{dtype} {hidden} library plan")
+    q = p.copy()
+    q.grid = 3
+    out = R.rms_norm_mxfp8(x, w=w, residual=r, eps=wl.eps, weight_bias=1.0 if has_w else 0.0, plan=q)
+    torch.cuda.synchronize()
+    mx_check(out, x, r, w, wl.eps, dtype, f"{dtype} {hidden} grid 3", weight_bias=1.0 if has_w else 0.0)
+    assert N.rmsnorm_wait_timeouts() == 0

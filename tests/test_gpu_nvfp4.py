@@ -90,3 +90,23 @@ def test_nv_argument_checks():
     assert st(xf.data_ptr(), None, None, c.data_ptr(), s.data_ptr(), None, 4, 64, 1e-6, 0.0, 1.0, 0) \
         == N.RMSNORM_EUNSUPPORTED                                     # fp32 I/O
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("hidden,has_res", [(40960, True), (65536, False), (65536, True)])
+def test_nv_long_rows_on_the_bulk_copy_kernel(hidden, has_res):
+    """Rows past 32768 elements take the bulk-copy kernel (16 KB pieces) with
+    the same NVFP4 epilogue; a grid of 3 blocks over 11 rows as well."""
+    wl = W.Workload("nv-long", "bf16", 11, hidden, 1e-5, 1.0, 1.0 if has_res else None, 0.1)
+    x, r, w = W.make_inputs(wl, seed=hidden + has_res, device=DEV)
+    S = W.NV_TENSOR_SCALE
+    p = R.rms_norm_nvfp4_plan_for(x, w=w, residual=r)
+    assert p.kernel == N.RMSNORM_KERNEL_TMA and p.chunks_per_thread == 2
+    out = R.rms_norm_nvfp4(x, w=w, residual=r, eps=wl.eps, tensor_scale=S)
+    torch.cuda.synchronize()
+    nv_check(out, x, r, w, wl.eps, S, f"{hidden} library plan")
+    q = p.copy()
+    q.grid = 3
+    out = R.rms_norm_nvfp4(x, w=w, residual=r, eps=wl.eps, tensor_scale=S, plan=q)
+    torch.cuda.synchronize()
+    nv_check(out, x, r, w, wl.eps, S, f"{hidden} grid 3")
+    assert N.rmsnorm_wait_timeouts() == 0
