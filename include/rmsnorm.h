@@ -115,10 +115,11 @@ typedef struct {
                                    in one ring piece: 1, 2 or 4 (8, 16 or 32 KB
                                    pieces; 28, 14 or 7 slots of shared memory, of
                                    which avail / 7 (at least 1) go to a streamed
-                                   residual ring and as many to a streamed weight
-                                   ring -- one per piece when the weight stays
-                                   resident -- and the rest, which must hold a
-                                   whole row, to x)                                  */
+                                   residual ring; the weight ring gets one slot
+                                   per piece (resident) when that leaves x a row
+                                   and a spare slot, else every slot past one
+                                   spare x slot (at least avail / 7); the rest,
+                                   which must hold a whole row, goes to x)           */
     int32_t vec_elems;          /* elements per load: 16 / sizeof(T), or 1 (scalar)  */
     int32_t block_threads;      /* threads per block (TMA: 608)                       */
     int32_t rows_per_block;     /* rows one block handles per loop iteration          */

@@ -54,7 +54,7 @@ def tma_rings(row_bytes, pc, res, w):
     pieces = -(-row_bytes // piece)
     streamed = max(1, avail // 7)
     sr = streamed if res else 0
-    sw = (pieces if avail - sr - pieces >= pieces + 1 else streamed) if w else 0
+    sw = (pieces if avail - sr - pieces >= pieces + 1 else max(streamed, avail - sr - pieces - 1)) if w else 0
     sx = avail - sr - sw
     return (sx, sr, sw) if sx >= pieces else None
 
