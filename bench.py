@@ -43,7 +43,7 @@ HEADLINE = "bf16_4096x576"
 METRIC = "RMSNorm achieved HBM GB/s and % of GB300 peak; rows/s per config"
 PER_CONFIG = ["f32_64x256", "bf16_res_16384x2048", "bf16_qk_262144x128", "bf16_decode_1x4096",
               "bf16_decode_8x4096", "bf16_decode_64x4096", "bf16_res_65536x8192_w",
-              "bf16_res_65536x8192_nw", "bf16_4096x32768_w", "bf16_res_4096x40960_w", "bf16_res_2048x65536_w",
+              "bf16_res_65536x8192_nw", "bf16_4096x32768_w", "bf16_res_4096x40960_w", "bf16_2048x65536_w", "bf16_res_2048x65536_w",
               "f32_res_2048x65536_w"]
 FALLBACK_HBM_GBS = 6800.0
 

@@ -94,6 +94,8 @@ WORKLOADS = {
                  note="long rows, shared-memory regime, weight resident"),
         Workload("bf16_res_4096x40960_w", "bf16", 4096, 40960, 1e-6, 1.0, 1.0, 0.1,
                  note="longest rows of the shared-memory regime (80 KB), fused residual"),
+        Workload("bf16_2048x65536_w", "bf16", 2048, 65536, 1e-6, 1.0, None, 0.1,
+                 note="longest bf16 rows without a residual, shared-memory regime, weight streamed"),
         Workload("bf16_res_2048x65536_w", "bf16", 2048, 65536, 1e-6, 1.0, 1.0, 0.1,
                  note="longest bf16 rows, two-pass regime"),
         Workload("f32_res_2048x65536_w", "f32", 2048, 65536, 1e-6, 1.0, 1.0, 0.1,

@@ -73,7 +73,8 @@ def test_workload_full_size(name):
 
 
 @pytest.mark.parametrize("name", ["bf16_res_65536x8192_w", "bf16_res_65536x8192_nw", "bf16_4096x32768_w",
-                                  "bf16_res_4096x40960_w", "bf16_res_2048x65536_w", "f32_res_2048x65536_w"])
+                                  "bf16_res_4096x40960_w", "bf16_2048x65536_w", "bf16_res_2048x65536_w",
+                                  "f32_res_2048x65536_w"])
 def test_workload_large_sampled(name):
     wl = W.WORKLOADS[name]
     x, r, w = gpu_inputs(wl)
