@@ -95,15 +95,40 @@ def load_peaks():
 HOST_ONLY_SOURCES = ("rmsnorm_api.cu",)
 
 
+def code_tokens(text):
+    """C/C++ source with comments removed and whitespace collapsed (a comment
+    edit does not change the code a profile describes)."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":                       # string or character literal
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_hash():
-    """Hash of the device code (kernels and their instantiations)."""
+    """Hash of the device code (kernels and their instantiations), comments
+    and layout aside."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "row_reduction_norm_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
         if name.endswith((".cu", ".cuh", ".h")) and name not in HOST_ONLY_SOURCES:
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+            with open(os.path.join(csrc, name), encoding="utf-8") as f:
+                h.update(name.encode() + b"\0" + code_tokens(f.read()).encode())
     return h.hexdigest()[:16]
 
 

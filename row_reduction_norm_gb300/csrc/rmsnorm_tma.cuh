@@ -1,5 +1,10 @@
 // rmsnorm_tma.cuh -- RMSNorm with the row staged in shared memory by bulk
-// (TMA) copies: the kernel for rows too long to hold in registers.
+// (TMA) copies: the kernel for long rows (planned past 32 KB, where it beats
+// holding 512 x 8 chunks in registers) and for block-scaled outputs of rows
+// too long for registers.  "CuTeDSL at Perplexity", section "QK Norm": rows
+// of thousands of elements reduce through shared memory as well as
+// registers; "Building a GPU compiler from scratch ... (Emmy)", schedule
+// codec: TMA copies guarded by barriers, double buffered.
 //
 // The op and the per-thread arithmetic are those of the register kernel with
 // 512 threads a row (chunk u of a row belongs to thread u mod 512, the
