@@ -94,3 +94,14 @@ def test_warmup_floor():
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
                         "--steps", "5", "--warmup", "2"], capture_output=True, text=True, timeout=120)
     assert r.returncode != 0
+
+
+def test_device_code_tokens_ignore_comments_only():
+    """A profile stays valid across comment edits, not across code edits."""
+    a = "int f(int x) {  // doubles x\n  return 2 * x; /* twice */ }\n"
+    b = "/* header */\nint f(int x) {\n    return 2 * x;\n}\n"
+    c = "int f(int x) { return 3 * x; }"
+    s = 'const char *s = "a // not a comment"; char q = \'/\';'
+    assert bench.code_tokens(a) == bench.code_tokens(b)
+    assert bench.code_tokens(a) != bench.code_tokens(c)
+    assert "// not a comment" in bench.code_tokens(s)
