@@ -76,11 +76,13 @@ enum {
 enum {
     RMSNORM_KERNEL_REG = 0,   /* row held in registers, 128-bit I/O, one pass     */
     RMSNORM_KERNEL_LOOP = 1,  /* row streamed twice (second read from L2): any
-                                 alignment, and rows too long for the ring below  */
+                                 alignment; planned for unaligned rows, rows past
+                                 80 KB with a residual and rows past 192 KB     */
     RMSNORM_KERNEL_TMA = 2    /* row staged in shared memory by bulk (TMA) copies:
                                  rings for x, residual and weight fed by three
                                  producer warps, 512 threads a row; contiguous
-                                 RMSNorm rows too long for registers              */
+                                 RMSNorm rows past 32 KB (and block-scaled
+                                 outputs of rows too long for registers)        */
 };
 
 /* Regimes (rmsnorm_plan_t.regime), a summary of how rows map to threads. */
