@@ -936,12 +936,23 @@ def run_reference(args):
     threads = os.cpu_count() or 1
     x, r, w = W.make_inputs(wl, seed=0, device="cpu")
     xn, rn, wn = W.to_numpy_bits(x), W.to_numpy_bits(r), W.to_numpy_bits(w)
-    # size each step so that warmup + steps take about a minute of host time
-    t0 = time.perf_counter()
-    oracle.rmsnorm(xn, w=wn, residual=rn, eps=wl.eps, dtype=wl.dtype, threads=threads)
-    t_full = max(time.perf_counter() - t0, 1e-6)
+    # size each step so that warmup + steps take about a minute of host time.
+    # A step spread over a thread pool pays the pool's set-up: below 64 rows a
+    # thread it runs on one thread, sized from the single-thread row rate.
     budget = 60.0 / max(1, args.steps + args.warmup)
-    rows_per_step = int(max(1, min(wl.rows, wl.rows * budget / t_full)))
+    probe = min(wl.rows, 256)
+    t0 = time.perf_counter()
+    oracle.rmsnorm(xn[:probe], w=wn, residual=None if rn is None else rn[:probe], eps=wl.eps, dtype=wl.dtype,
+                   threads=1)
+    t_row1 = max(time.perf_counter() - t0, 1e-9) / probe
+    if budget / t_row1 >= 64 * threads:
+        t0 = time.perf_counter()
+        oracle.rmsnorm(xn, w=wn, residual=rn, eps=wl.eps, dtype=wl.dtype, threads=threads)
+        t_full = max(time.perf_counter() - t0, 1e-6)
+        rows_per_step = int(max(1, min(wl.rows, wl.rows * budget / t_full)))
+    else:
+        threads = 1
+        rows_per_step = int(max(1, min(wl.rows, budget / t_row1)))
 
     def step(i):
         lo = (i * rows_per_step) % wl.rows
@@ -961,7 +972,8 @@ def run_reference(args):
     wbytes = wl.hidden * wl.elem_bytes if wl.has_w else 0
     value = (rows_done * row_bytes + args.steps * wbytes) / dt / 1e9
     sample = (f"{rows_per_step} of {wl.rows} rows per step ({rows_per_step * wl.hidden} elements), "
-              f"fp64 C oracle, {threads} threads over row blocks")
+              f"fp64 C oracle, " + (f"{threads} threads over row blocks" if threads > 1 else
+                                    "one thread (steps too small for a thread pool to pay)"))
     out = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
