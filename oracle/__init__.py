@@ -64,6 +64,9 @@ def _load():
             lib.oracle_rmsnorm_rows.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64,
                                                 ctypes.c_float, ctypes.c_float, ctypes.c_int]
             lib.oracle_rmsnorm_rows.restype = ctypes.c_int
+            lib.oracle_rmsnorm_cast_rows.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64,
+                                                     ctypes.c_float, ctypes.c_int]
+            lib.oracle_rmsnorm_cast_rows.restype = ctypes.c_int
             lib.oracle_layernorm_rows.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64,
                                                   ctypes.c_float, ctypes.c_int]
             lib.oracle_layernorm_rows.restype = ctypes.c_int
@@ -146,6 +149,45 @@ def rmsnorm(x, w=None, residual=None, eps: float = 1e-6, dtype: str = "bf16",
         with ThreadPoolExecutor(max_workers=threads) as ex:
             list(ex.map(lambda i: run(int(bounds[i]), int(bounds[i + 1])), range(threads)))
     return y, res_out, y64
+
+
+def rmsnorm_cast(x, w=None, residual=None, eps: float = 1e-6, dtype: str = "bf16", threads: int = 1):
+    """Reference RMSNorm in the op-by-op cast order (see the C file): the
+    normalised value is rounded to the I/O type before the weight multiply.
+
+    Returns ``(y, residual_out, n_exact)``: ``y`` in the I/O type, the rounded
+    residual sum or None, and the fp64 normalised values h * r before their
+    rounding.
+    """
+    if dtype not in DTYPES:
+        raise ValueError(f"unknown dtype {dtype!r}")
+    x = np.ascontiguousarray(x)
+    if x.ndim != 2:
+        raise ValueError("x must be 2-D [rows, hidden]")
+    rows, hidden = x.shape
+    x = _check(x, "x", dtype, (rows, hidden))
+    residual = _check(residual, "residual", dtype, (rows, hidden))
+    w = _check(w, "w", dtype, (hidden,))
+    y = np.empty((rows, hidden), dtype=_NP_TYPE[dtype])
+    res_out = None if residual is None else np.empty((rows, hidden), dtype=_NP_TYPE[dtype])
+    n64 = np.empty((rows, hidden), dtype=np.float64)
+    if rows == 0 or hidden == 0:
+        return y, res_out, n64
+    lib = _load()
+    args = (_ptr(x), _ptr(residual), _ptr(w), _ptr(y), _ptr(n64), _ptr(res_out))
+
+    def run(lo, hi):
+        if lib.oracle_rmsnorm_cast_rows(*args, lo, hi, hidden, float(eps), DTYPES[dtype]) != 0:
+            raise ValueError("oracle rejected its arguments")
+
+    threads = max(1, min(int(threads), rows))
+    if threads == 1:
+        run(0, rows)
+    else:
+        bounds = np.linspace(0, rows, threads + 1).astype(np.int64)
+        with ThreadPoolExecutor(max_workers=threads) as ex:
+            list(ex.map(lambda i: run(int(bounds[i]), int(bounds[i + 1])), range(threads)))
+    return y, res_out, n64
 
 
 def layernorm(x, w=None, b=None, residual=None, eps: float = 1e-5, dtype: str = "bf16",

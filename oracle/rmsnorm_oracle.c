@@ -191,6 +191,48 @@ int oracle_rmsnorm_rows(const void *x, const void *residual, const void *w,
 }
 
 /*
+ * RMSNorm in the eager framework's op-by-op cast order, rows [row_begin,
+ * row_end).  "model-as-a-kernel" (sections "Method" and "Correctness") keeps
+ * the eager framework's bf16 semantics op for op and matches its fused
+ * rmsnorm bitwise; the pages give no cast order for the norm, and the reading
+ * taken is the one of a norm whose weight multiply is an op of its own: the
+ * normalised value is computed wide, rounded to the I/O type, then multiplied
+ * by the weight and rounded again.
+ *   v_i   = h_i * r                          (fp64, as oracle_rmsnorm_rows without w)
+ *   n_i   = RN_T(v_i)
+ *   y_i   = RN_T(n_i * w_i)                  (n_i without a weight)
+ * n_exact (optional) receives v.  Returns 0, or -1 on an invalid argument.
+ */
+int oracle_rmsnorm_cast_rows(const void *x, const void *residual, const void *w,
+                             void *y, double *n_exact, void *residual_out,
+                             int64_t row_begin, int64_t row_end, int64_t hidden,
+                             float eps, int dtype)
+{
+    if (x == NULL || y == NULL || hidden <= 0 || row_begin < 0 || row_end < row_begin)
+        return -1;
+    if (dtype != ORACLE_F32 && dtype != ORACLE_BF16)
+        return -1;
+    if ((residual == NULL) != (residual_out == NULL))
+        return -1;
+    double *v = (double *)malloc((size_t)hidden * sizeof(double));
+    if (v == NULL)
+        return -1;
+    for (int64_t row = row_begin; row < row_end; ++row) {
+        rms_row_values(x, residual, NULL, row, hidden, (double)eps, 0.0, dtype, v, residual_out);
+        for (int64_t i = 0; i < hidden; ++i) {
+            if (n_exact != NULL)
+                n_exact[row * hidden + i] = v[i];
+            double n = round_to_type(v[i], dtype);            /* the cast to the I/O type */
+            if (w != NULL)
+                n = n * load_elem(w, i, dtype);              /* exact in binary64 for bf16 and fp32 */
+            store_elem(y, row * hidden + i, dtype, n);       /* the weight op's rounding */
+        }
+    }
+    free(v);
+    return 0;
+}
+
+/*
  * LayerNorm, rows [row_begin, row_end) ("GPT-2 on the GPU", section "The
  * Whole Model as One Kernel": the traced block takes the mean and the
  * variance of the row, normalises as (x - mean) / sqrt(variance + eps) and

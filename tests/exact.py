@@ -142,6 +142,38 @@ def rmsnorm_row_exact(x, w, residual, eps_bits_value: Fraction, fmt: str, weight
     return y_bits, h_bits, qs, signs
 
 
+def rmsnorm_cast_row_exact(x, w, residual, eps_bits_value: Fraction, fmt: str):
+    """Exact RMSNorm of one row in the op-by-op cast order: the normalised
+    value is rounded to the format, then multiplied by the weight and rounded
+    again.  Returns (y_bits, residual_out_bits or None, n_bits, q_list, signs),
+    where n_bits are the rounded normalised values and sign_i * sqrt(q_i) their
+    exact values."""
+    n_bits, h_bits, qs, signs = rmsnorm_row_exact(x, None, residual, eps_bits_value, fmt)
+    if w is None:
+        return list(n_bits), h_bits, n_bits, qs, signs
+    return [cast_times_weight(nb, wb, fmt) for nb, wb in zip(n_bits, w)], h_bits, n_bits, qs, signs
+
+
+def cast_times_weight(n_bits: int, w_bits: int, fmt: str) -> int:
+    """Bits of RN(n * w) for two encodings (IEEE sign of an exact zero product)."""
+    sign_mask = 1 << (sum(FORMATS[fmt]))
+    p = decode(n_bits, fmt) * decode(w_bits, fmt)
+    if p == 0:
+        return sign_mask if ((n_bits & sign_mask) != 0) != ((w_bits & sign_mask) != 0) else 0
+    return round_value(p, fmt)
+
+
+def neighbours(bits: int, fmt: str):
+    """The encodings adjacent to a finite nonzero encoding of the same sign."""
+    sign_mask = 1 << (sum(FORMATS[fmt]))
+    mag = bits & (sign_mask - 1)
+    out = []
+    for m in (mag - 1, mag + 1):
+        if m >= 0:
+            out.append((bits & sign_mask) | m)
+    return out
+
+
 def _cmp_affine_sqrt(a: Fraction, d: Fraction, b: Fraction, v: Fraction) -> int:
     """Sign of (a / sqrt(d) + b) - v, exactly (d > 0)."""
     c = v - b                      # compare a / sqrt(d) with c

@@ -145,6 +145,37 @@ def reference_qk(x, q_heads, k_heads, head_dim, q_w, k_w, eps, dt, weight_bias=0
     return qy.reshape(tokens, q_heads, head_dim), ky.reshape(tokens, k_heads, head_dim)
 
 
+# Planted mistakes of the op-by-op cast order.
+CAST_MISTAKES = ["cast_single_rounding", "cast_to_f32", "cast_rsqrt_rounded", "cast_weight_before_norm",
+                 "cast_trunc", "cast_weight_dropped"]
+
+
+def reference_cast(x, w, residual, eps, dt, mistake=None):
+    """The cast order restated: n = RN(h * r), y = RN(n * w) (numpy fp64)."""
+    xv = _decode(x, dt)
+    e = float(np.float32(eps))
+    if residual is not None:
+        h = _round(xv + _decode(residual, dt), dt)
+        h_store = _encode(h, dt)
+    else:
+        h = xv
+        h_store = None
+    with np.errstate(invalid="ignore", divide="ignore", over="ignore"):
+        r = 1.0 / np.sqrt((h * h).sum(axis=1, keepdims=True) / h.shape[1] + e)
+        wv = None if (w is None or mistake == "cast_weight_dropped") else _decode(w, dt)
+        if mistake == "cast_rsqrt_rounded":
+            r = _round(r, dt)
+        v = h * r
+        if mistake == "cast_single_rounding":
+            y = v if wv is None else v * wv
+        elif mistake == "cast_weight_before_norm":
+            y = _round(h * wv, dt) * r if wv is not None else v
+        else:
+            n = _round(v, "f32" if mistake == "cast_to_f32" else dt, "trunc" if mistake == "cast_trunc" else "rne")
+            y = n if wv is None else n * wv
+    return _encode(_round(y, dt), dt), h_store, v
+
+
 LN_MISTAKES = ["bessel", "eps_outside_sqrt", "no_centering", "bias_inside_weight", "no_bias",
                "stats_from_x", "unrounded_residual", "mean_over_h_minus_1"]
 

@@ -751,6 +751,125 @@ def pin_nv_closed_forms(impl_nv):
 NV_PINS = [pin_nv_closed_forms, pin_nv_bruteforce]
 
 
+# ---------------------------------------------------------------- cast order
+
+CAST_GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "cast_order.txt")
+
+
+def parse_cast_golden(path=CAST_GOLDEN):
+    cases, cur = [], None
+    for raw in open(path):
+        line = raw.strip()
+        if not line or line.startswith("#"):
+            continue
+        key, *rest = line.split()
+        if key == "case":
+            cur = {"name": rest[0]}
+            cases.append(cur)
+        elif key == "dtype":
+            cur["dtype"] = rest[0]
+        elif key == "eps":
+            cur["eps"] = Fraction(rest[0])
+        elif key in ("x", "w", "residual", "y", "plain", "resout"):
+            cur[key] = None if rest == ["-"] else [Fraction(t) for t in _expand(rest)]
+        else:
+            raise ValueError(f"unknown key {key!r} in {path}")
+    return cases
+
+
+def pin_cast_golden(impl_cast):
+    """Hand-derived cases in tests/golden/cast_order.txt, chosen so that the
+    two-rounding order and the single rounding differ."""
+    fails = []
+    for c in parse_cast_golden():
+        dt = c["dtype"]
+        n = len(c["x"])
+        enc = lambda vals: to_array([encode_exact(v, dt) for v in vals], dt)
+        x = enc(c["x"]).reshape(1, n)
+        w = None if c["w"] is None else enc(c["w"])
+        res = None if c["residual"] is None else enc(c["residual"]).reshape(1, n)
+        y, rout, _ = impl_cast(x, w, res, float(c["eps"]), dt)
+        want = [encode_exact(v, dt) for v in c["y"]]
+        got = [int(b) for b in bits_of(y, dt).reshape(-1)]
+        if got != want:
+            fails.append(f"cast golden {c['name']}: y bits {got} != {want}")
+        if c.get("resout") is not None:
+            got_r = [int(b) for b in bits_of(rout, dt).reshape(-1)]
+            if got_r != [encode_exact(v, dt) for v in c["resout"]]:
+                fails.append(f"cast golden {c['name']}: residual_out {got_r}")
+    return fails
+
+
+def pin_cast_bruteforce(impl_cast, n_cases=60, seed=2468):
+    """Random tiny rows against the exact two-rounding answer.  The first
+    rounding may go to the other neighbour only where the exact normalised
+    value lies within 2^-44 (relative) of a rounding midpoint."""
+    rng = np.random.default_rng(seed)
+    fails = []
+    eps_choices = [0.0, 1e-6, 1e-5, 0.25, 3.0]
+    for k in range(n_cases):
+        dt = ("bf16", "f32")[k % 2]
+        has_w = (k // 2) % 4 != 0          # most cases with a weight: that is where the orders differ
+        has_res = bool((k // 8) % 2)
+        hidden = int(rng.integers(1, 9))
+        rows = 3
+        eps = eps_choices[k % len(eps_choices)]
+        xb = [random_bits(rng, dt, hidden) for _ in range(rows)]
+        rb = [random_bits(rng, dt, hidden) for _ in range(rows)] if has_res else None
+        wb = random_bits(rng, dt, hidden, -2, 2) if has_w else None
+        x = to_array(sum(xb, []), dt).reshape(rows, hidden)
+        res = to_array(sum(rb, []), dt).reshape(rows, hidden) if has_res else None
+        w = to_array(wb, dt) if has_w else None
+        y, rout, _ = impl_cast(x, w, res, eps, dt)
+        yb = bits_of(y, dt).reshape(rows, hidden)
+        for r in range(rows):
+            want, want_h, n_bits, qs, _ = exact.rmsnorm_cast_row_exact(
+                xb[r], wb, rb[r] if has_res else None, f32_exact(eps), dt)
+            for i in range(hidden):
+                if int(yb[r, i]) == want[i]:
+                    continue
+                d = exact.midpoint_distance(qs[i], dt)
+                alt = [exact.cast_times_weight(nb, wb[i], dt) if has_w else nb
+                       for nb in exact.neighbours(n_bits[i], dt)]
+                if d is None or d > Fraction(1, 2 ** 44) or int(yb[r, i]) not in alt:
+                    fails.append(f"cast bruteforce case {k} ({dt}, w={has_w}, res={has_res}, H={hidden}, "
+                                 f"eps={eps}) row {r} elem {i}: {int(yb[r, i]):#x} != {want[i]:#x}")
+            if has_res:
+                got_h = [int(b) for b in bits_of(rout, dt).reshape(rows, hidden)[r]]
+                if got_h != want_h:
+                    fails.append(f"cast bruteforce case {k}: residual_out row {r} {got_h} != {want_h}")
+    return fails
+
+
+def pin_cast_power_of_two_weight(impl_cast, seed=1357):
+    """With weights +-2^k the weight multiply is exact, so the output is the
+    unweighted output times the weight (both dtypes, rows of 300)."""
+    rng = np.random.default_rng(seed)
+    fails = []
+    for dt in ("bf16", "f32"):
+        rows, hidden = 4, 300
+        x = to_array(random_bits(rng, dt, rows * hidden), dt).reshape(rows, hidden)
+        wv = rng.choice([-4.0, -1.0, -0.5, 0.25, 1.0, 2.0, 8.0], hidden)
+        w = to_array([encode_exact(Fraction(v), dt) for v in wv], dt)
+        y0, _, _ = impl_cast(x, None, None, 1e-6, dt)
+        y1, _, _ = impl_cast(x, w, None, 1e-6, dt)
+        d0 = exact_values(y0, dt)
+        d1 = exact_values(y1, dt)
+        if not np.array_equal(d0 * wv[None, :], d1):
+            fails.append(f"cast power-of-two weight ({dt}): y(w) != y(no w) * w")
+    return fails
+
+
+def exact_values(a, dt):
+    """fp64 values of an I/O-type array (exact)."""
+    if dt == "bf16":
+        return (np.asarray(a, dtype=np.uint32) << 16).view(np.float32).astype(np.float64)
+    return np.asarray(a, dtype=np.float32).astype(np.float64)
+
+
+CAST_PINS = [pin_cast_golden, pin_cast_power_of_two_weight, pin_cast_bruteforce]
+
+
 ALL_PINS = [pin_golden, pin_bruteforce, pin_constant_row, pin_scale_invariance,
             pin_unit_rms, pin_special_values, pin_single_element, pin_row_independence,
             pin_eps_dominated, pin_near_ties]

@@ -274,3 +274,55 @@ def test_compare_nv_flags_planted_differences():
     s2 = so.copy()
     s2[4, 2] += 1
     assert not parity.compare_nv(co, s2, co, so, v, 1 / 64, oracle.e2m1_from_double)[0]
+
+
+# ---------------------------------------------------------------- cast order
+
+def oracle_impl_cast(x, w, residual, eps, dtype):
+    return oracle.rmsnorm_cast(x, w=w, residual=residual, eps=eps, dtype=dtype)
+
+
+@pytest.mark.parametrize("pin", pins.CAST_PINS, ids=lambda p: p.__name__)
+def test_oracle_cast_pin(pin):
+    assert pin(oracle_impl_cast) == []
+
+
+def test_cast_restatement_passes_pins():
+    for pin in pins.CAST_PINS:
+        assert pin(mutants.reference_cast) == [], pin.__name__
+
+
+@pytest.mark.parametrize("mistake", mutants.CAST_MISTAKES)
+def test_cast_pins_catch_planted_mistake(mistake):
+    impl = lambda x, w, r, e, d: mutants.reference_cast(x, w, r, e, d, mistake=mistake)
+    assert any(pin(impl) for pin in pins.CAST_PINS), f"no pin catches {mistake!r}"
+
+
+def test_cast_golden_cases_discriminate():
+    # the plain (single-rounding) oracle gives the "plain" column of every
+    # cast-order golden case, so each case separates the two orders
+    for c in pins.parse_cast_golden():
+        dt = c["dtype"]
+        n = len(c["x"])
+        enc = lambda vals: pins.to_array([pins.encode_exact(v, dt) for v in vals], dt)
+        res = None if c["residual"] is None else enc(c["residual"]).reshape(1, n)
+        y, _, _ = oracle.rmsnorm(enc(c["x"]).reshape(1, n), w=enc(c["w"]), residual=res,
+                                 eps=float(c["eps"]), dtype=dt)
+        assert [int(b) for b in pins.bits_of(y, dt).reshape(-1)] == [pins.encode_exact(v, dt) for v in c["plain"]]
+        assert c["plain"] != c["y"]
+
+
+@pytest.mark.parametrize("name", ["bf16_4096x576", "bf16_res_16384x2048", "f32_64x256"])
+def test_cast_oracle_matches_restatement_and_plain_without_weight(name):
+    wl = W.WORKLOADS[name]
+    x, r, w = W.make_inputs(wl, seed=11, rows=min(wl.rows, 64))
+    xn, rn, wn = W.to_numpy_bits(x), W.to_numpy_bits(r), W.to_numpy_bits(w)
+    y, h, n64 = oracle.rmsnorm_cast(xn, w=wn, residual=rn, eps=wl.eps, dtype=wl.dtype, threads=3)
+    y2, h2, v2 = mutants.reference_cast(xn, wn, rn, wl.eps, wl.dtype)
+    assert np.array_equal(pins.bits_of(y, wl.dtype), pins.bits_of(y2, wl.dtype))
+    if rn is not None:
+        assert np.array_equal(pins.bits_of(h, wl.dtype), pins.bits_of(h2, wl.dtype))
+    assert np.allclose(n64, v2, rtol=1e-13, atol=0)
+    y0, _, _ = oracle.rmsnorm_cast(xn, residual=rn, eps=wl.eps, dtype=wl.dtype)
+    yp, _, _ = oracle.rmsnorm(xn, residual=rn, eps=wl.eps, dtype=wl.dtype)
+    assert np.array_equal(pins.bits_of(y0, wl.dtype), pins.bits_of(yp, wl.dtype))
