@@ -310,6 +310,15 @@ class Launcher:
         return g
 
 
+class CastLauncher(Launcher):
+    """RMSNorm in the op-by-op cast order (rmsnorm_fwd_cast), same buffers."""
+
+    def launch(self, i):
+        x, r, y, h = self.ptrs[i % self.n_sets]
+        self.N.rmsnorm_fwd_cast(x, r, self.w_ptr, y, h, self.wl.rows, self.wl.hidden, self.wl.eps, self.code,
+                                None, self.stream.cuda_stream)
+
+
 class LNLauncher(Launcher):
     """LayerNorm workloads: the Launcher's buffer sets plus a bias."""
 
@@ -781,6 +790,8 @@ def run_ours(args):
                 entry.update({"op": "layernorm", "bias": cw.has_b})
             if mx:
                 entry.update({"op": "rmsnorm, MXFP8 output (E4M3 codes, E8M0 scale per 32)"})
+            if kind == "cast":
+                entry.update({"op": "rmsnorm, cast order (normalised value rounded to bf16 before the weight)"})
             if nv:
                 entry.update({"op": "rmsnorm, NVFP4 output (E2M1 codes, E4M3 scale per 16, tensor scale "
                                     f"{W.NV_TENSOR_SCALE})"})
@@ -863,6 +874,8 @@ def per_config_table(W):
     table = {}
     for name in PER_CONFIG:
         table[name] = (W.WORKLOADS[name], Launcher, lambda w: w.algorithmic_bytes(), "rms")
+    for name, wl in W.CAST_WORKLOADS.items():
+        table[name] = (wl, CastLauncher, lambda w: w.algorithmic_bytes(), "cast")
     for name, wl in W.QK_WORKLOADS.items():
         table[name] = (wl, QKLauncher, lambda w: w.algorithmic_bytes(), "qk")
     for name, wl in W.LN_WORKLOADS.items():

@@ -201,6 +201,24 @@ int rmsnorm_fwd_ex(const void *x, const void *residual, const void *w, void *y,
                    rmsnorm_stream_t stream);
 
 /*
+ * rmsnorm_fwd in the op-by-op cast order of an eager framework
+ * ("model-as-a-kernel", sections "Method" and "Correctness": eager bf16
+ * semantics op for op, its fused rmsnorm bitwise).  The card does not spell
+ * the order out; the reading taken is a norm whose weight multiply is an op of
+ * its own:
+ *   n_i = RN_T( h_i * rsqrt(mean(h^2) + eps) )      (statistics in fp32)
+ *   y_i = RN_T( n_i * w_i )                         (n_i without a weight)
+ * For bf16 this differs from rmsnorm_fwd, which rounds once; for fp32 I/O the
+ * two calls run the same arithmetic.  Without a weight it is rmsnorm_fwd.
+ * plan may be NULL (the library's plan) or a plan as for rmsnorm_fwd_plan;
+ * rmsnorm_plan_for returns the plan this call uses.  Other arguments, layout,
+ * ownership and status codes as rmsnorm_fwd.
+ */
+int rmsnorm_fwd_cast(const void *x, const void *residual, const void *w, void *y,
+                     void *residual_out, int64_t rows, int64_t hidden, float eps,
+                     int dtype, const rmsnorm_plan_t *plan, rmsnorm_stream_t stream);
+
+/*
  * Fused query + key per-head RMSNorm in one launch ("CuTeDSL at Perplexity",
  * section "QK Norm": per-head norm over 64..256 elements, the kernel picks
  * the query or key weight per head; the model-as-a-kernel card lists the

@@ -60,6 +60,7 @@ def tma_rings(row_bytes, pc, res, w):
 
 # Every symbol the header declares (checked by the CPU tests).
 EXPORTED = ["rmsnorm_fwd", "rmsnorm_plan", "rmsnorm_plan_for", "rmsnorm_fwd_plan", "rmsnorm_fwd_ex",
+            "rmsnorm_fwd_cast",
             "rmsnorm_qk_fwd", "rmsnorm_qk_plan_for", "rmsnorm_fwd_mxfp8", "rmsnorm_mxfp8_plan_for",
             "rmsnorm_fwd_nvfp4", "rmsnorm_nvfp4_plan_for",
             "layernorm_fwd", "layernorm_plan_for",
@@ -132,6 +133,8 @@ def load():
         lib.rmsnorm_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i64, i64, ctypes.c_float, ctypes.c_float, i32,
                                        ctypes.POINTER(Plan), vp]
         lib.rmsnorm_fwd_ex.restype = i32
+        lib.rmsnorm_fwd_cast.argtypes = fwd_args + [ctypes.POINTER(Plan), vp]
+        lib.rmsnorm_fwd_cast.restype = i32
         lib.rmsnorm_qk_fwd.argtypes = [vp, vp, i64, i64, i64, ctypes.c_int32, ctypes.c_int32, i64, vp, vp,
                                        ctypes.c_float, ctypes.c_float, i32, ctypes.POINTER(Plan), vp]
         lib.rmsnorm_qk_fwd.restype = i32
@@ -210,6 +213,16 @@ def rmsnorm_fwd_ex_status(x, residual, w, y, residual_out, rows, hidden, eps, we
                           stream=0) -> int:
     return load().rmsnorm_fwd_ex(x, residual, w, y, residual_out, rows, hidden, eps, weight_bias, dtype,
                                  _plan_ref(plan), stream)
+
+
+def rmsnorm_fwd_cast(x, residual, w, y, residual_out, rows, hidden, eps, dtype, plan=None, stream=0):
+    _check(load().rmsnorm_fwd_cast(x, residual, w, y, residual_out, rows, hidden, eps, dtype, _plan_ref(plan),
+                                   stream), "rmsnorm_fwd_cast")
+
+
+def rmsnorm_fwd_cast_status(x, residual, w, y, residual_out, rows, hidden, eps, dtype, plan=None, stream=0) -> int:
+    return load().rmsnorm_fwd_cast(x, residual, w, y, residual_out, rows, hidden, eps, dtype, _plan_ref(plan),
+                                   stream)
 
 
 def rmsnorm_qk_fwd(x, y, tokens, x_token_stride, y_token_stride, q_heads, k_heads, head_dim, q_w, k_w,

@@ -43,13 +43,15 @@ def _check_tensor(t, name, x):
 def rms_norm(x: torch.Tensor, w: Optional[torch.Tensor] = None, residual: Optional[torch.Tensor] = None,
              eps: float = 1e-6, out: Optional[torch.Tensor] = None,
              residual_out: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None,
-             plan: Optional[N.Plan] = None, weight_bias: float = 0.0):
+             plan: Optional[N.Plan] = None, weight_bias: float = 0.0, cast_before_weight: bool = False):
     """y = x * rsqrt(mean(x^2) + eps) * (w + weight_bias) over the last dimension.
 
     With ``residual``: h = x + residual (rounded to the I/O type) is written to
     ``residual_out`` and normalised; returns ``(y, residual_out)``.  Without:
     returns ``y``.  ``plan`` forces a launch plan (see ``rmsnorm_fwd_plan``).
-    ``weight_bias`` = 1 gives the (1 + w) weight form.
+    ``weight_bias`` = 1 gives the (1 + w) weight form.  ``cast_before_weight``
+    rounds the normalised value to the I/O type before the weight multiply
+    (``rmsnorm_fwd_cast``, the eager op-by-op order; no weight bias).
     """
     if x.dim() < 1:
         raise ValueError("x must have at least one dimension")
@@ -71,7 +73,11 @@ def rms_norm(x: torch.Tensor, w: Optional[torch.Tensor] = None, residual: Option
         s = stream if stream is not None else torch.cuda.current_stream(x.device)
         args = (_ptr(x), _ptr(residual), _ptr(w), _ptr(y), _ptr(residual_out), rows, hidden,
                 float(eps))
-        if weight_bias:
+        if cast_before_weight:
+            if weight_bias:
+                raise ValueError("cast_before_weight takes no weight_bias")
+            N.rmsnorm_fwd_cast(*args, code, plan, s.cuda_stream)
+        elif weight_bias:
             N.rmsnorm_fwd_ex(*args, float(weight_bias), code, plan, s.cuda_stream)
         elif plan is None:
             N.rmsnorm_fwd(*args, code, s.cuda_stream)

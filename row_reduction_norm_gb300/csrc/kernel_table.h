@@ -10,7 +10,8 @@ constexpr int kRegMaxCH = 8;
 // Block sizes compiled for the two-pass kernel.
 constexpr int kLoopBlocks[3] = {64, 256, 1024};
 
-// dtype: 0 = f32, 1 = bf16; wm: 0 no weight, 1 weight, 2 weight + bias.
+// dtype: 0 = f32, 1 = bf16; wm: 0 no weight, 1 weight, 2 weight + bias,
+// 3 weight after a bf16 cast of the normalised value.
 // Each returns the __global__ function as a launchable pointer, or nullptr
 // when that combination is not compiled.
 const void *reg_contig_f32_plain(int gt, int ch, int wm);
@@ -21,6 +22,10 @@ const void *reg_heads_f32(int gt, int ch, int wm);
 const void *reg_heads_bf16(int gt, int ch, int wm);
 const void *loop_contig(int dtype, int block, bool vec, bool res, int wm);
 const void *loop_heads(int dtype, int block, bool vec, int wm);
+// The cast-order weight mode (bf16 contiguous rows; the bulk-copy kernel's
+// instantiations are in tma_kernel).
+const void *reg_contig_bf16_cast(int gt, int ch, bool res);
+const void *loop_contig_bf16_cast(int block, bool vec, bool res);
 
 // RMSNorm with MXFP8 output (contiguous rows, register kernel only).
 const void *mx_reg_f32_plain(int gt, int ch, int wm);

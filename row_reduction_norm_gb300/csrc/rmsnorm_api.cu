@@ -295,6 +295,12 @@ const void *kernel_of(const rmsnorm_plan_t *p, const Op &o) {
                                            : rrn::ln_reg_f32(p->threads_per_row, p->chunks_per_thread, res, o.wm);
         return rrn::ln_loop(o.dtype, p->block_threads, p->vec_elems != 1, res, o.wm);
     }
+    if (o.wm == rrn::kWeightCast) {
+        if (o.dtype != RMSNORM_BF16 || o.head_rows) return nullptr;
+        if (p->kernel == RMSNORM_KERNEL_REG)
+            return rrn::reg_contig_bf16_cast(p->threads_per_row, p->chunks_per_thread, res);
+        return rrn::loop_contig_bf16_cast(p->block_threads, p->vec_elems != 1, res);
+    }
     if (p->kernel == RMSNORM_KERNEL_REG)
         return rrn::reg_kernel(o.dtype, p->threads_per_row, p->chunks_per_thread, res, o.wm, o.head_rows);
     return rrn::loop_kernel(o.dtype, p->block_threads, p->vec_elems != 1, res, o.wm, o.head_rows);
@@ -791,6 +797,17 @@ int rmsnorm_fwd_ex(const void *x, const void *residual, const void *w, void *y, 
     return run(o, plan, stream);
 }
 
+int rmsnorm_fwd_cast(const void *x, const void *residual, const void *w, void *y, void *residual_out,
+                     int64_t rows, int64_t hidden, float eps, int dtype, const rmsnorm_plan_t *plan,
+                     rmsnorm_stream_t stream) {
+    Op o;
+    int st = make_contig(x, residual, w, y, residual_out, rows, hidden, eps, 0.f, dtype, &o);
+    if (st != RMSNORM_OK) return st;
+    // fp32 I/O: the plain weight mode already rounds h * r to fp32 before the weight multiply.
+    if (w != nullptr && dtype == RMSNORM_BF16) o.wm = rrn::kWeightCast;
+    return run(o, plan, stream);
+}
+
 int rmsnorm_qk_fwd(const void *x, void *y, int64_t tokens, int64_t x_token_stride, int64_t y_token_stride,
                    int32_t q_heads, int32_t k_heads, int64_t head_dim, const void *q_w, const void *k_w,
                    float weight_bias, float eps, int dtype, const rmsnorm_plan_t *plan,
@@ -844,7 +861,7 @@ const char *rmsnorm_strerror(int status) {
 const char *rmsnorm_build_info(void) {
     return "row_reduction_norm_gb300 fused RMSNorm / LayerNorm 0.3; target sm_103a; kernels: register (warp/"
            "CTA/persistent), shared-memory ring fed by bulk copies, two/three-pass; contiguous rows and Q/K head "
-           "rows; weight, weight + bias, no weight; MXFP8 / NVFP4 outputs";
+           "rows; weight, weight + bias, weight after a bf16 cast, no weight; MXFP8 / NVFP4 outputs";
 }
 
 }  // extern "C"

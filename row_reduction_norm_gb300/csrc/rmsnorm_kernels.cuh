@@ -83,8 +83,12 @@ struct Params {
 // byte in y, one E4M3 scale per 16 elements in scales).
 enum OutputMode { kOutT = 0, kOutMxfp8 = 1, kOutNvfp4 = 2 };
 
-// How the weight enters y: none, w, or (w + w_bias).
-enum WeightMode { kNoWeight = 0, kWeight = 1, kWeightBias = 2 };
+// How the weight enters y: none, w, (w + w_bias), or w after the normalised
+// value has been rounded to bf16 (the op-by-op cast order of an eager
+// framework, "model-as-a-kernel", sections "Method" and "Correctness"; bf16
+// I/O only, since with fp32 I/O the kWeight product is already rounded to the
+// I/O type before the weight multiply).
+enum WeightMode { kNoWeight = 0, kWeight = 1, kWeightBias = 2, kWeightCast = 3 };
 
 template <int WM>
 __device__ __forceinline__ float scale_out(float h, float r, float w, float bias) {
@@ -92,6 +96,8 @@ __device__ __forceinline__ float scale_out(float h, float r, float w, float bias
         return h * r;
     } else if constexpr (WM == kWeight) {
         return (h * r) * w;
+    } else if constexpr (WM == kWeightCast) {
+        return __bfloat162float(__float2bfloat16_rn(h * r)) * w;
     } else {
         return (h * r) * (w + bias);
     }
@@ -252,6 +258,9 @@ __device__ __forceinline__ void scale_out_pairs(float (&a)[N], float r, const fl
     for (int k = 0; k < N / 2; ++k) {
         float2 v = __fmul2_rn(make_float2(a[2 * k], a[2 * k + 1]), r2);
         if constexpr (WM == kWeight) {
+            v = __fmul2_rn(v, make_float2(w[2 * k], w[2 * k + 1]));
+        } else if constexpr (WM == kWeightCast) {
+            v = __bfloat1622float2(__float22bfloat162_rn(v));   // exact product below: 8 x 8 bits
             v = __fmul2_rn(v, make_float2(w[2 * k], w[2 * k + 1]));
         } else if constexpr (WM == kWeightBias) {
             const float2 wb = __fadd2_rn(make_float2(w[2 * k], w[2 * k + 1]), make_float2(bias, bias));

@@ -1,5 +1,7 @@
 // tma.cu -- instantiations of the shared-memory (bulk copy) RMSNorm kernel,
 // and the device counter its bounded waits report to.
+#include <type_traits>
+
 #include "kernel_table.h"
 #include "rmsnorm_tma.cuh"
 
@@ -12,6 +14,11 @@ const void *tma_wm(int wm) {
         case kNoWeight: return reinterpret_cast<const void *>(&rms_tma_kernel<T, RES, kNoWeight, PC, OUT>);
         case kWeight: return reinterpret_cast<const void *>(&rms_tma_kernel<T, RES, kWeight, PC, OUT>);
         case kWeightBias: return reinterpret_cast<const void *>(&rms_tma_kernel<T, RES, kWeightBias, PC, OUT>);
+        case kWeightCast:
+            if constexpr (std::is_same<T, BF16>::value && OUT == kOutT)
+                return reinterpret_cast<const void *>(&rms_tma_kernel<T, RES, kWeightCast, PC, OUT>);
+            else
+                return nullptr;
         default: return nullptr;
     }
 }

@@ -257,6 +257,17 @@ def make_ln_inputs(wl: Workload, seed: int = 0, device="cpu", rows: Optional[int
     return x, r, w, b
 
 
+# RMSNorm in the op-by-op cast order (normalised value rounded to bf16 before
+# the weight multiply): the same data as three plain-order rows, one per
+# kernel family the library plans for them (CTA registers, CTA registers at
+# the bandwidth case, shared-memory rings).
+CAST_WORKLOADS = {
+    "cast_" + name: dataclasses.replace(WORKLOADS[name], name="cast_" + name,
+                                        note=WORKLOADS[name].note + ", cast order")
+    for name in ("bf16_res_16384x2048", "bf16_res_65536x8192_w", "bf16_res_4096x40960_w")
+}
+
+
 # RMSNorm with MXFP8 output (E4M3 codes + one E8M0 scale per 32 elements):
 # the Llama-3.2-1B-width residual case and the 65536 x 8192 bandwidth case.
 MX_WORKLOADS = {

@@ -64,6 +64,31 @@ def compare_y(got, ref, dtype):
                                       "n": int(r.size)}
 
 
+# RMSNorm in the op-by-op cast order, bf16: y = RN(RN(n) * w) with n = h * r.
+# The kernel's normalised value n' obeys the fp32 bound above,
+# |n' - n| <= CAST_REL_TOL |n|, so RN(n') = RN(n) except where n lies that
+# close to a bf16 rounding midpoint; there either neighbour is correct, and y
+# must be the weight product (rounded once, exactly as defined) of the one the
+# kernel took.  Everything else is bit-exact.
+CAST_REL_TOL = F32_RTOL
+
+
+def compare_cast_bf16(got, n64, w_bits, bf16_from_double):
+    """Return (ok, report) for bf16 cast-order outputs against the oracle's
+    fp64 normalised values ``n64`` and the weight bits (None: no weight)."""
+    got = np.asarray(got, dtype=np.uint16)
+    n64 = np.asarray(n64, dtype=np.float64)
+    if got.shape != n64.shape:
+        return False, {"error": f"shape {got.shape} != {n64.shape}"}
+    lo = bf16_from_double(n64 * (1.0 - CAST_REL_TOL)).reshape(n64.shape)
+    hi = bf16_from_double(n64 * (1.0 + CAST_REL_TOL)).reshape(n64.shape)
+    wv = 1.0 if w_bits is None else decode(w_bits, "bf16")[None, :]
+    y_lo = bf16_from_double(decode(lo, "bf16") * wv).reshape(n64.shape)
+    y_hi = bf16_from_double(decode(hi, "bf16") * wv).reshape(n64.shape)
+    ok = (got == y_lo) | (got == y_hi)
+    return bool(ok.all()), {"n_bad": int((~ok).sum()), "n_boundary": int((lo != hi).sum()), "n": int(got.size)}
+
+
 def bits_equal(a, b):
     a = np.ascontiguousarray(a)
     b = np.ascontiguousarray(b)

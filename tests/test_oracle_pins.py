@@ -326,3 +326,19 @@ def test_cast_oracle_matches_restatement_and_plain_without_weight(name):
     y0, _, _ = oracle.rmsnorm_cast(xn, residual=rn, eps=wl.eps, dtype=wl.dtype)
     yp, _, _ = oracle.rmsnorm(xn, residual=rn, eps=wl.eps, dtype=wl.dtype)
     assert np.array_equal(pins.bits_of(y0, wl.dtype), pins.bits_of(yp, wl.dtype))
+
+
+def test_compare_cast_flags_planted_differences():
+    import parity
+    wl = W.WORKLOADS["bf16_res_16384x2048"]
+    x, r, w = W.make_inputs(wl, seed=8, rows=64)
+    xn, rn, wn = W.to_numpy_bits(x), W.to_numpy_bits(r), W.to_numpy_bits(w)
+    y, _, n64 = oracle.rmsnorm_cast(xn, w=wn, residual=rn, eps=wl.eps, dtype="bf16")
+    ok, rep = parity.compare_cast_bf16(y, n64, wn, oracle.bf16_from_double)
+    assert ok and 0 < rep["n_boundary"] < rep["n"] // 100, rep
+    yp, _, _ = oracle.rmsnorm(xn, w=wn, residual=rn, eps=wl.eps, dtype="bf16")
+    ok, rep = parity.compare_cast_bf16(yp, n64, wn, oracle.bf16_from_double)
+    assert not ok and rep["n_bad"] > 0           # the single rounding is a different result
+    bad = y.copy()
+    bad[3, 5] ^= 1
+    assert not parity.compare_cast_bf16(bad, n64, wn, oracle.bf16_from_double)[0]
