@@ -143,3 +143,25 @@ def test_argument_checks():
                                      N.RMSNORM_BF16) == N.RMSNORM_EINVAL
     assert N.rmsnorm_fwd_cast_status(x.data_ptr(), None, w.data_ptr(), y.data_ptr(), None, 0, 64, 1e-6,
                                      N.RMSNORM_BF16) == N.RMSNORM_OK
+
+
+@pytest.mark.parametrize("hidden", [576, 4096, 40960])
+def test_misaligned_and_in_place(hidden):
+    # pointers one element off 16 bytes take the scalar two-pass kernel; y may be x
+    wl = W.Workload("cast_odd", "bf16", 7, hidden, 1e-6, 1.0, 1.0, 0.1)
+    x, r, w = W.make_inputs(wl, seed=hidden + 1, device=DEV)
+
+    def shifted(t):
+        buf = torch.empty(t.numel() + 1, dtype=t.dtype, device=DEV)
+        v = buf[1:].view(t.shape)
+        v.copy_(t)
+        return v
+
+    xs, rs, ws = shifted(x), shifted(r), shifted(w)
+    y, h = R.rms_norm(xs, w=ws, residual=rs, eps=wl.eps, cast_before_weight=True)
+    torch.cuda.synchronize()
+    check_cast(y, h, x, r, w, wl.eps, "bf16", what=f"misaligned H={hidden}")
+    xi = x.clone()
+    R.rms_norm(xi, w=w, eps=wl.eps, out=xi, cast_before_weight=True)
+    torch.cuda.synchronize()
+    check_cast(xi, None, x, None, w, wl.eps, "bf16", what=f"in place H={hidden}")
