@@ -210,6 +210,9 @@ int rmsnorm_fwd_ex(const void *x, const void *residual, const void *w, void *y,
  *   y_i = RN_T( n_i * w_i )                         (n_i without a weight)
  * For bf16 this differs from rmsnorm_fwd, which rounds once; for fp32 I/O the
  * two calls run the same arithmetic.  Without a weight it is rmsnorm_fwd.
+ * Accuracy (bf16): n_i is the correctly rounded normalised value except where
+ * the exact value lies within 2e-6 (relative) of a bf16 rounding midpoint,
+ * where it may be the other neighbour; y_i is then exactly RN_T(n_i * w_i).
  * plan may be NULL (the library's plan) or a plan as for rmsnorm_fwd_plan;
  * rmsnorm_plan_for returns the plan this call uses.  Other arguments, layout,
  * ownership and status codes as rmsnorm_fwd.
