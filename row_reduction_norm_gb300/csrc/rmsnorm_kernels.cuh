@@ -22,8 +22,10 @@
 //    adds a shared-memory combine across the row's warps (the "256 workers
 //    per row" schedule of the Emmy page, section "Tile IR").  Blocks stride
 //    over row groups, so a grid capped at the resident capacity is the
-//    persistent regime, and w (the same for every row) is staged once per
-//    block in shared memory.
+//    persistent regime.  w (the same for every row) is loaded by each lane
+//    next to its x chunks when a row is at most a warp (L1 serves the
+//    block's other rows), and staged once per block in shared memory when a
+//    row spans several warps or the output is block-scaled.
 //  * Both kernels also serve head rows (the fused Q+K norm of the Perplexity
 //    page's "QK Norm" section): rows are the heads of each token inside a
 //    packed projection, and query and key heads take different weights.
@@ -416,6 +418,7 @@ __device__ __forceinline__ void store_quantised(float (&a)[V], bool valid, const
 template <typename T, int GT, int CH, bool RES, int WM, bool HEADS, int OUT>
 __device__ __forceinline__ void rms_reg_rows(const Params &p) {
     constexpr bool W = WM != kNoWeight;
+    constexpr bool W_DIRECT = W && GT <= 32 && OUT == kOutT;   // per-lane weight loads (below)
     static_assert(!(HEADS && RES), "head rows take no residual");
     static_assert(OUT == kOutT || (!HEADS && GT >= 32 / T::kVec), "block-scaled output: contiguous rows, "
                                                                   "a block's lanes in one row group");
@@ -435,10 +438,14 @@ __device__ __forceinline__ void rms_reg_rows(const Params &p) {
     pdl_wait_for_inputs();
     pdl_allow_dependents();
 
-    // w (and w2 for head rows) is the same for every row: staged once per
-    // block in shared memory (dynamic, units * 16 bytes per weight) and read
-    // from there in every epilogue.  The staging happens after the first
-    // row's loads are issued, so the two memory round trips overlap.
+    // w (and w2 for head rows) is the same for every row.  Rows of a warp or
+    // less (W_DIRECT) load their weight chunks per lane right after their x
+    // chunks: no block barrier, and L1 serves the block's other rows
+    // (measured on GB300: bf16 4096 x 576 3.07 -> 3.01 us, Q+K heads of 8192
+    // tokens 26.5 -> 25.4 us).  Otherwise w is staged once per block in
+    // shared memory (dynamic, units * 16 bytes per weight; the host sizes it
+    // for every REG plan with a weight) after the first row's loads are
+    // issued, so the two memory round trips overlap.
     extern __shared__ Chunk w_smem[];
     bool w_staged = false;
 
@@ -471,7 +478,19 @@ __device__ __forceinline__ void rms_reg_rows(const Params &p) {
                     rc[c] = Chunk{{0u, 0u, 0u, 0u}};
             }
         }
-        if constexpr (W) {
+        Chunk wc[W_DIRECT ? CH : 1];
+        if constexpr (W_DIRECT) {
+            const char *wp = static_cast<const char *>(wsel ? p.w2 : p.w);
+#pragma unroll
+            for (int c = 0; c < CH; ++c) {
+                const int u = c * GT + t;
+                if (row_ok && u < nch)
+                    wc[c] = ld_readonly16(wp + (int64_t)u * 16);
+                else
+                    wc[c] = Chunk{{0u, 0u, 0u, 0u}};
+            }
+        }
+        if constexpr (W && !W_DIRECT) {
             if (!w_staged) {   // first iteration of the block (uniform across it)
                 for (int i = tid; i < nch; i += BLOCK)
                     w_smem[i] = ld_readonly16(static_cast<const char *>(p.w) + (int64_t)i * 16);
@@ -551,7 +570,9 @@ __device__ __forceinline__ void rms_reg_rows(const Params &p) {
                 float a[V];
                 unpack(hc[c], a, T{});
                 float wv[V];
-                if constexpr (W) {
+                if constexpr (W_DIRECT) {
+                    unpack(wc[c], wv, T{});
+                } else if constexpr (W) {
                     unpack(w_smem[wsel * nch + u], wv, T{});
                 } else {
 #pragma unroll
