@@ -340,12 +340,10 @@ __device__ __forceinline__ uint8_t e4m3_of(float v) {
     return (uint8_t)__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3);
 }
 
-// Value of a finite E4M3 code from its bit fields (4 exponent bits, bias 7;
-// 3 fraction bits; subnormals m * 2^-9).
+// Value of a finite E4M3 code: the hardware conversion to fp16 (every E4M3
+// value is exact in fp16), then to fp32.
 __device__ __forceinline__ float e4m3_value(uint8_t c) {
-    const int ef = (c >> 3) & 0xF, m = c & 0x7;
-    const float mag = ef == 0 ? (float)m * 0.001953125f : __int_as_float(((ef + 120) << 23) | (m << 20));
-    return (c & 0x80) ? -mag : mag;
+    return __half2float(__half(__nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)c, __NV_E4M3)));
 }
 
 __device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
