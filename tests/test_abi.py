@@ -305,3 +305,25 @@ def test_qk_and_ex_arguments_rejected_without_cuda():
     assert N.rmsnorm_qk_fwd_status(P, P, 4, 48 * 512, 48 * 512, 32, 8, 512, P, P, 0.0, 1e-6, 1,
                                    bad_plan) == N.RMSNORM_EINVAL
     del ok
+
+
+def test_cast_arguments_rejected_without_cuda():
+    P = 1 << 20
+    f = N.rmsnorm_fwd_cast_status
+    # x, residual, w, y, residual_out, rows, hidden, eps, dtype
+    bad = [
+        (P, None, P, P, None, 4, 64, -1.0, 1),            # negative eps
+        (P, None, P, P, None, 4, 64, float("nan"), 1),    # eps not finite
+        (P, None, P, P, None, 4, 64, 1e-6, 2),            # unknown dtype
+        (P, P, P, P, None, 4, 64, 1e-6, 1),               # residual without residual_out
+        (None, None, P, P, None, 4, 64, 1e-6, 1),         # null x
+        (P, None, P, P, None, 4, 0, 1e-6, 1),             # hidden 0
+        (P, None, P, P, None, -1, 64, 1e-6, 1),           # negative rows
+        (P + 1, None, P, P, None, 4, 64, 1e-6, 1),        # misaligned element
+    ]
+    for a in bad:
+        assert f(*a) == N.RMSNORM_EINVAL, a
+    assert f(P, None, P, P, None, 4, 1 << 40, 1e-6, 1) in (N.RMSNORM_EUNSUPPORTED, N.RMSNORM_EINVAL)
+    # zero rows: a successful no-op, pointers unused
+    assert f(None, None, None, None, None, 0, 64, 1e-6, 1) == N.RMSNORM_OK
+    assert f(P, P, P, P, P, 0, 64, 1e-6, 0) == N.RMSNORM_OK
