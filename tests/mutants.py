@@ -147,7 +147,7 @@ def reference_qk(x, q_heads, k_heads, head_dim, q_w, k_w, eps, dt, weight_bias=0
 
 # Planted mistakes of the op-by-op cast order.
 CAST_MISTAKES = ["cast_single_rounding", "cast_to_f32", "cast_rsqrt_rounded", "cast_weight_before_norm",
-                 "cast_trunc", "cast_weight_dropped"]
+                 "cast_trunc", "cast_weight_dropped", "cast_product_ties_away"]
 
 
 def reference_cast(x, w, residual, eps, dt, mistake=None):
@@ -173,7 +173,7 @@ def reference_cast(x, w, residual, eps, dt, mistake=None):
         else:
             n = _round(v, "f32" if mistake == "cast_to_f32" else dt, "trunc" if mistake == "cast_trunc" else "rne")
             y = n if wv is None else n * wv
-    return _encode(_round(y, dt), dt), h_store, v
+    return _encode(_round(y, dt, "away" if mistake == "cast_product_ties_away" else "rne"), dt), h_store, v
 
 
 LN_MISTAKES = ["bessel", "eps_outside_sqrt", "no_centering", "bias_inside_weight", "no_bias",

@@ -165,3 +165,36 @@ def test_misaligned_and_in_place(hidden):
     R.rms_norm(xi, w=w, eps=wl.eps, out=xi, cast_before_weight=True)
     torch.cuda.synchronize()
     check_cast(xi, None, x, None, w, wl.eps, "bf16", what=f"in place H={hidden}")
+
+
+def test_golden_cases_through_the_kernel():
+    # the hand-derived cases of tests/golden/cast_order.txt, through the C ABI;
+    # bf16 bit-exact (no case lies near a first-rounding midpoint), fp32 within
+    # the fp32 tolerance
+    import pins
+    for c in pins.parse_cast_golden():
+        dt = c["dtype"]
+        n = len(c["x"])
+        enc = lambda vals: pins.to_array([pins.encode_exact(v, dt) for v in vals], dt)
+        tdt = W.TORCH_DTYPE[dt]
+
+        def dev(a, shape):
+            t = torch.from_numpy(a.astype(a.dtype).reshape(shape).copy())
+            return (t.view(torch.bfloat16) if dt == "bf16" else t).to(DEV)
+
+        x = dev(enc(c["x"]), (1, n))
+        w = dev(enc(c["w"]), (n,))
+        r = None if c["residual"] is None else dev(enc(c["residual"]), (1, n))
+        out = R.rms_norm(x, w=w, residual=r, eps=float(c["eps"]), cast_before_weight=True)
+        y, h = out if r is not None else (out, None)
+        torch.cuda.synchronize()
+        assert y.dtype == tdt
+        want = enc(c["y"]).reshape(1, n)
+        got = W.to_numpy_bits(y)
+        if dt == "bf16":
+            assert np.array_equal(got, want), f"{c['name']}: {got} != {want}"
+        else:
+            ok, rep = parity.compare_y(got, want, dt)
+            assert ok, f"{c['name']}: {rep}"
+        if c.get("resout") is not None:
+            assert np.array_equal(W.to_numpy_bits(h), enc(c["resout"]).reshape(1, n)), c["name"]

@@ -302,6 +302,8 @@ def test_cast_golden_cases_discriminate():
     # the plain (single-rounding) oracle gives the "plain" column of every
     # cast-order golden case, so each case separates the two orders
     for c in pins.parse_cast_golden():
+        if c.get("plain") is None:
+            continue
         dt = c["dtype"]
         n = len(c["x"])
         enc = lambda vals: pins.to_array([pins.encode_exact(v, dt) for v in vals], dt)
