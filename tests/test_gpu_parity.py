@@ -402,3 +402,30 @@ def test_offsets_past_4gib(hidden, rows, has_res, kind):
           what=f"{kind} {rows}x{hidden}")
     del x, r, y, h, out
     torch.cuda.empty_cache()
+
+
+def test_golden_closed_forms_through_the_kernel():
+    # the hand-derived cases of tests/golden/closed_forms.txt through the C ABI,
+    # against their exactly rounded values (the usual tolerance; residual_out exact)
+    import exact
+    import pins
+    for c in pins.parse_golden():
+        dt = c["dtype"]
+        n = len(c["x"])
+        enc = lambda vals: pins.to_array([pins.encode_exact(v, dt) for v in vals], dt)
+
+        def dev(a, shape):
+            t = torch.from_numpy(a.reshape(shape).copy())
+            return (t.view(torch.bfloat16) if dt == "bf16" else t).to(DEV)
+
+        x = dev(enc(c["x"]), (1, n))
+        w = None if c["w"] is None else dev(enc(c["w"]), (n,))
+        r = None if c["residual"] is None else dev(enc(c["residual"]), (1, n))
+        out = R.rms_norm(x, w=w, residual=r, eps=float(c["eps"]))
+        y, h = out if r is not None else (out, None)
+        torch.cuda.synchronize()
+        want = pins.to_array([exact.round_sqrt(s, q, dt) for s, q in zip(c["sign"], c["y2"])], dt).reshape(1, n)
+        ok, rep = parity.compare_y(W.to_numpy_bits(y), want, dt)
+        assert ok, f"{c['name']}: {rep}"
+        if c.get("resout") is not None:
+            assert np.array_equal(W.to_numpy_bits(h), enc(c["resout"]).reshape(1, n)), c["name"]
