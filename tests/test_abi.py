@@ -327,3 +327,41 @@ def test_cast_arguments_rejected_without_cuda():
     # zero rows: a successful no-op, pointers unused
     assert f(None, None, None, None, None, 0, 64, 1e-6, 1) == N.RMSNORM_OK
     assert f(P, P, P, P, P, 0, 64, 1e-6, 0) == N.RMSNORM_OK
+
+
+def test_header_is_plain_c_and_links():
+    # the boundary as a C caller sees it: the header compiles as strict C99,
+    # the program links against the library and calls it (no CUDA work: a
+    # zero-row call and a call rejected for its eps)
+    import os
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("gcc not installed")
+    from row_reduction_norm_gb300 import build as B
+    lib = B.build()
+    out_dir = os.path.join(B.BUILD_DIR, "c_abi_check")
+    os.makedirs(out_dir, exist_ok=True)
+    src = os.path.join(out_dir, "abi_check.c")
+    exe = os.path.join(out_dir, "abi_check")
+    with open(src, "w") as f:
+        f.write(r'''
+#include "rmsnorm.h"
+#include <stdio.h>
+int main(void) {
+    const char *info = rmsnorm_build_info();
+    int zero = rmsnorm_fwd(NULL, NULL, NULL, NULL, NULL, 0, 64, 1e-6f, RMSNORM_BF16, NULL);
+    int bad = rmsnorm_fwd((const void *)1048576, NULL, NULL, (void *)1048576, NULL, 4, 64, -1.0f,
+                          RMSNORM_BF16, NULL);
+    int cast = rmsnorm_fwd_cast(NULL, NULL, NULL, NULL, NULL, 0, 64, 1e-6f, RMSNORM_BF16, NULL, NULL);
+    printf("%d %d %d %d\n", zero, bad, cast, info != NULL);
+    return 0;
+}
+''')
+    cmd = [gcc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I", B.INCLUDE, src,
+           "-L", os.path.dirname(lib), "-l:" + os.path.basename(lib), "-Wl,-rpath," + os.path.dirname(lib),
+           "-o", exe]
+    subprocess.run(cmd, check=True)
+    r = subprocess.run([exe], capture_output=True, text=True, check=True)
+    assert r.stdout.split() == [str(N.RMSNORM_OK), str(N.RMSNORM_EINVAL), str(N.RMSNORM_OK), "1"]
