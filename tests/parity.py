@@ -7,9 +7,9 @@ Tolerances (per element), against the oracle's result rounded to the I/O type:
 NaN must sit at the same positions on both sides.
 
 Derivation of the fp32 bound: the register and two-pass kernels sum squares
-in fp32 along a fixed
-tree at most 21 levels deep (<= 8 chunk steps, 3 levels over a chunk's
-lanes, 5 shuffle levels, 5 levels across warps), a relative error <= 21 u
+in fp32 along a fixed tree at most 21 levels deep (<= 8 chunk steps, 3 levels
+over a chunk's lanes, 5 shuffle levels, 5 levels across warps), a relative
+error <= 21 u
 (u = 2^-24) on the sum, i.e. <= 10.5 u on the scale after the square root;
 the mean and eps add 3 roundings (<= 1.5 u on the scale), rsqrtf <= 2 ulp
 (<= 4 u), and the two products 2 u: about 18 u = 1.1e-6 relative in the
