@@ -9,8 +9,8 @@ NaN must sit at the same positions on both sides.
 Derivation of the fp32 bound: the register and two-pass kernels sum squares
 in fp32 along a fixed tree at most 21 levels deep (<= 8 chunk steps, 3 levels
 over a chunk's lanes, 5 shuffle levels, 5 levels across warps), a relative
-error <= 21 u
-(u = 2^-24) on the sum, i.e. <= 10.5 u on the scale after the square root;
+error <= 21 u (u = 2^-24) on the sum, i.e. <= 10.5 u on the scale after the
+square root;
 the mean and eps add 3 roundings (<= 1.5 u on the scale), rsqrtf <= 2 ulp
 (<= 4 u), and the two products 2 u: about 18 u = 1.1e-6 relative in the
 worst case, inside 2e-6.  (The bulk-copy kernel's tree is at most 35 levels
