@@ -132,16 +132,23 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload, plan=None):
+def profiled_traffic(workload, plan=None, with_source=False):
     """DRAM bytes per launch from the committed ncu summary of this workload
     (profiles/ncu_*.md with a matching ``profile_workload:`` line), if it was
     taken on the current device code and, when ``plan`` is given, with the
-    same launch plan; else None."""
+    same launch plan; else None.  ``with_source`` also returns which summary
+    gave the figure, or why none did."""
+    value, source = _profiled_traffic(workload, plan)
+    return (value, source) if with_source else value
+
+
+def _profiled_traffic(workload, plan):
     pdir = os.path.join(ROOT, "profiles")
     try:
         names = sorted(os.listdir(pdir))
     except OSError:
-        return None
+        return None, "no profiles/ directory"
+    why = f"no ncu summary of {workload} in profiles/"
     for name in names:
         if not (name.startswith("ncu_") and name.endswith(".md")):
             continue
@@ -153,10 +160,12 @@ def profiled_traffic(workload, plan=None):
         m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
         m_plan = re.search(r"^Plan: `(\{.*\})`", text, re.M)
         if plan is not None and (not m_plan or json.loads(m_plan.group(1)) != plan):
+            why = f"profiles/{name} was taken with another launch plan"
             continue
         if m_hash and m_bytes and m_hash.group(1) == kernel_source_hash():
-            return int(m_bytes.group(1))
-    return None
+            return int(m_bytes.group(1)), f"profiles/{name} (device code hash {m_hash.group(1)}, same plan)"
+        why = f"profiles/{name} predates the current device code"
+    return None, why
 
 
 def aggregate(world, bytes_per_step, rows_per_step, steps, ms_max):
@@ -823,7 +832,7 @@ def run_ours(args):
             dist.destroy_process_group()
         return
     clocks = sampler.summary(window[0], window[1]) if sampler and window else None
-    traffic = profiled_traffic(args.workload, plan_summary(L.plan))
+    traffic, traffic_source = profiled_traffic(args.workload, plan_summary(L.plan), with_source=True)
     out = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -852,7 +861,7 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
                      else "fallback 6.8 TB/s", "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": traffic,
+                     "traffic": traffic, "traffic_source": traffic_source,
                      "kernel": f"rms_{plan_summary(L.plan)['kernel']}_kernel",
                      "algorithmic_bytes_per_launch": launch_bytes},
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,

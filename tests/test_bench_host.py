@@ -105,3 +105,12 @@ def test_device_code_tokens_ignore_comments_only():
     assert bench.code_tokens(a) == bench.code_tokens(b)
     assert bench.code_tokens(a) != bench.code_tokens(c)
     assert "// not a comment" in bench.code_tokens(s)
+
+
+def test_traffic_source_says_why():
+    import bench
+    v, why = bench.profiled_traffic("no_such_workload", None, with_source=True)
+    assert v is None and "no ncu summary" in why
+    v, why = bench.profiled_traffic("bf16_4096x576", {"kernel": "none"}, with_source=True)
+    assert v is None and "another launch plan" in why
+    assert bench.profiled_traffic("no_such_workload") is None
