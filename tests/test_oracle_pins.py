@@ -344,3 +344,7 @@ def test_compare_cast_flags_planted_differences():
     bad = y.copy()
     bad[3, 5] ^= 1
     assert not parity.compare_cast_bf16(bad, n64, wn, oracle.bf16_from_double)[0]
+
+
+def test_cast_oracle_bruteforce_many():
+    assert pins.pin_cast_bruteforce(oracle_impl_cast, n_cases=400, seed=4242) == []
