@@ -152,6 +152,22 @@ int rmsnorm_fwd(const void *x, const void *residual, const void *w, void *y,
                 int dtype, rmsnorm_stream_t stream);
 
 /*
+ * Regime dispatch ("CuTeDSL at Perplexity", section on prefill and decode
+ * specialisation: the grid and block shape of a row kernel follow the token
+ * count, the hidden size, the data type and the device's SM count).  The
+ * plan calls below expose that choice; rmsnorm_regime names the regime alone.
+ *
+ * rmsnorm_regime: the RMSNORM_REGIME_* that rmsnorm_fwd runs on the current
+ * device for `rows` rows of `hidden` elements of `dtype`, with 16-byte
+ * aligned tensors, a weight and no residual (rmsnorm_plan_for answers for
+ * any other pointers).  rows >= 0 and hidden, dtype as for rmsnorm_fwd.
+ * Queries the SM count and the kernel's occupancy once per device.  Returns
+ * the regime (>= 0) or a negative status: RMSNORM_EINVAL,
+ * RMSNORM_EUNSUPPORTED, or RMSNORM_ECUDA (no usable device).
+ */
+int rmsnorm_regime(int64_t rows, int64_t hidden, int dtype);
+
+/*
  * Pure host planning (no CUDA call): the plan rmsnorm_fwd would use without
  * a residual on a device with `sm_count` SMs where the chosen kernel keeps
  * `blocks_per_sm` blocks resident (with a residual, rows longer than 80 KB

@@ -59,7 +59,7 @@ def tma_rings(row_bytes, pc, res, w):
     return (sx, sr, sw) if sx >= pieces else None
 
 # Every symbol the header declares (checked by the CPU tests).
-EXPORTED = ["rmsnorm_fwd", "rmsnorm_plan", "rmsnorm_plan_for", "rmsnorm_fwd_plan", "rmsnorm_fwd_ex",
+EXPORTED = ["rmsnorm_fwd", "rmsnorm_regime", "rmsnorm_plan", "rmsnorm_plan_for", "rmsnorm_fwd_plan", "rmsnorm_fwd_ex",
             "rmsnorm_fwd_cast",
             "rmsnorm_qk_fwd", "rmsnorm_qk_plan_for", "rmsnorm_fwd_mxfp8", "rmsnorm_mxfp8_plan_for",
             "rmsnorm_fwd_nvfp4", "rmsnorm_nvfp4_plan_for",
@@ -160,6 +160,8 @@ def load():
         lib.rmsnorm_plan.restype = i32
         lib.rmsnorm_plan_for.argtypes = [vp, vp, vp, vp, vp, i64, i64, i32, ctypes.POINTER(Plan)]
         lib.rmsnorm_plan_for.restype = i32
+        lib.rmsnorm_regime.argtypes = [i64, i64, i32]
+        lib.rmsnorm_regime.restype = i32
         lib.rmsnorm_max_hidden.argtypes = [i32]
         lib.rmsnorm_max_hidden.restype = i64
         lib.rmsnorm_reg_max_chunks.argtypes = []
@@ -313,6 +315,20 @@ def rmsnorm_plan_for(x, residual, w, y, residual_out, rows, hidden, dtype) -> Pl
     _check(load().rmsnorm_plan_for(x, residual, w, y, residual_out, rows, hidden, dtype,
                                    ctypes.byref(p)), "rmsnorm_plan_for")
     return p
+
+
+def rmsnorm_regime(rows, hidden, dtype) -> int:
+    """The RMSNORM_REGIME_* rmsnorm_fwd runs on the current device for aligned
+    contiguous tensors with a weight and no residual."""
+    st = int(load().rmsnorm_regime(rows, hidden, dtype))
+    if st < 0:
+        raise RmsNormError(st, "rmsnorm_regime")
+    return st
+
+
+def rmsnorm_regime_status(rows, hidden, dtype) -> int:
+    """rmsnorm_regime's raw return value: a regime (>= 0) or a negative status."""
+    return int(load().rmsnorm_regime(rows, hidden, dtype))
 
 
 def rmsnorm_max_hidden(dtype) -> int:

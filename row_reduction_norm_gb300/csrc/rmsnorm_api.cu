@@ -758,6 +758,19 @@ int rmsnorm_plan(int64_t rows, int64_t hidden, int dtype, int vec_ok, int sm_cou
     return RMSNORM_OK;
 }
 
+int rmsnorm_regime(int64_t rows, int64_t hidden, int dtype) {
+    // A stand-in address for 16-byte aligned tensors: planning reads no
+    // pointer, it only looks at the alignment of each one.
+    alignas(16) static const unsigned char kAligned[16] = {0};
+    Op o;
+    int st = make_contig(kAligned, nullptr, kAligned, const_cast<unsigned char *>(kAligned), nullptr, rows, hidden,
+                         0.f, 0.f, dtype, &o);
+    if (st != RMSNORM_OK) return st;
+    rmsnorm_plan_t plan;
+    if ((st = plan_for_device(o, &plan, nullptr)) != RMSNORM_OK) return st;
+    return plan.regime;
+}
+
 int rmsnorm_plan_for(const void *x, const void *residual, const void *w, const void *y,
                      const void *residual_out, int64_t rows, int64_t hidden, int dtype,
                      rmsnorm_plan_t *plan) {

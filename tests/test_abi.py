@@ -232,6 +232,17 @@ def test_qk_norm_is_warp_regime_and_large_rows_cta():
     assert big.regime == N.RMSNORM_REGIME_CTA and big.threads_per_row > 32
 
 
+def test_regime_query_rejects_bad_input_without_cuda():
+    # argument checks come before any CUDA call; a valid query needs a device
+    assert N.rmsnorm_regime_status(-1, 576, N.RMSNORM_BF16) == N.RMSNORM_EINVAL
+    assert N.rmsnorm_regime_status(4, 0, N.RMSNORM_BF16) == N.RMSNORM_EINVAL
+    assert N.rmsnorm_regime_status(4, 576, 7) == N.RMSNORM_EINVAL
+    assert N.rmsnorm_regime_status(4, 65537, N.RMSNORM_BF16) == N.RMSNORM_EUNSUPPORTED
+    assert N.rmsnorm_regime_status(1 << 62, 576, N.RMSNORM_BF16) == N.RMSNORM_EINVAL
+    st = N.rmsnorm_regime_status(4096, 576, N.RMSNORM_BF16)
+    assert st in (N.RMSNORM_REGIME_WARP, N.RMSNORM_ECUDA)
+
+
 def test_plan_rejects_bad_input():
     with pytest.raises(N.RmsNormError):
         R.rmsnorm_plan(-1, 128, 1, True, 152, 1)
@@ -332,7 +343,8 @@ def test_cast_arguments_rejected_without_cuda():
 def test_header_is_plain_c_and_links():
     # the boundary as a C caller sees it: the header compiles as strict C99,
     # the program links against the library and calls it (no CUDA work: a
-    # zero-row call and a call rejected for its eps)
+    # zero-row call, a call rejected for its eps, and the regime query, which
+    # answers the warp regime on a GPU and a CUDA error without one)
     import os
     import shutil
     import subprocess
@@ -355,7 +367,10 @@ int main(void) {
     int bad = rmsnorm_fwd((const void *)1048576, NULL, NULL, (void *)1048576, NULL, 4, 64, -1.0f,
                           RMSNORM_BF16, NULL);
     int cast = rmsnorm_fwd_cast(NULL, NULL, NULL, NULL, NULL, 0, 64, 1e-6f, RMSNORM_BF16, NULL, NULL);
-    printf("%d %d %d %d\n", zero, bad, cast, info != NULL);
+    int regime_bad = rmsnorm_regime(-1, 576, RMSNORM_BF16);
+    int regime = rmsnorm_regime(4096, 576, RMSNORM_BF16);
+    printf("%d %d %d %d %d %d\n", zero, bad, cast, info != NULL, regime_bad,
+           regime == RMSNORM_REGIME_WARP || regime == RMSNORM_ECUDA);
     return 0;
 }
 ''')
@@ -364,4 +379,5 @@ int main(void) {
            "-o", exe]
     subprocess.run(cmd, check=True)
     r = subprocess.run([exe], capture_output=True, text=True, check=True)
-    assert r.stdout.split() == [str(N.RMSNORM_OK), str(N.RMSNORM_EINVAL), str(N.RMSNORM_OK), "1"]
+    assert r.stdout.split() == [str(N.RMSNORM_OK), str(N.RMSNORM_EINVAL), str(N.RMSNORM_OK), "1",
+                                str(N.RMSNORM_EINVAL), "1"]

@@ -204,6 +204,23 @@ def test_tail_sweep(hidden, dtype):
             check(y, h, x, r, w, wl.eps, dtype, what=f"H={hidden} rows={rows} res={has_res} w={has_w}")
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_regime_query_matches_the_plan(dtype):
+    """rmsnorm_regime names the regime of the plan rmsnorm_fwd uses (aligned
+    tensors, a weight, no residual) on every width of the tail sweep and on
+    row counts from one row to many waves."""
+    code = N.RMSNORM_BF16 if dtype == "bf16" else N.RMSNORM_F32
+    esz = 2 if dtype == "bf16" else 4
+    for hidden in HIDDENS:
+        if (hidden * esz) % 16:
+            continue
+        x = torch.empty((1, hidden), device=DEV, dtype=W.TORCH_DTYPE[dtype])
+        for rows in (0, 1, 3, 131, 65536, 1 << 22):
+            p = N.rmsnorm_plan_for(x.data_ptr(), None, x.data_ptr(), x.data_ptr(), None, rows, hidden, code)
+            assert R.rmsnorm_regime(rows, hidden, code) == p.regime, (hidden, rows, p.as_dict())
+    assert N.rmsnorm_regime_status(4, 1 << 17, code) == N.RMSNORM_EUNSUPPORTED
+
+
 def test_rows_zero_is_noop():
     x = torch.empty((0, 576), device=DEV, dtype=torch.bfloat16)
     y = R.rms_norm(x)
