@@ -5,19 +5,23 @@
 
 A step is one pass of the whole op (load, optional residual add, sum of
 squares, scale, weighted store) over one batch of the workload: one launch of
-the library through its C ABI.  The headline workload is bf16 4096 x 576 with
-a weight (SmolLM2-135M width).  The metric is achieved HBM bandwidth over the
-op's algorithmic bytes (read x [+ residual], write y [+ residual_out], read w
-once per launch), with rows/s beside it.
+the library through its C ABI.  The headline workload is the largest one that
+fits a GPU: bf16 65536 x 8192 with a fused residual add and a weight (x with
+0.1 % outliers; about 1 GiB a tensor), the bandwidth-roofline case.  The
+metric is achieved HBM bandwidth over the op's algorithmic bytes (read x
+[+ residual], write y [+ residual_out], read w once per launch), with rows/s
+beside it; every other workload is timed the same way in ``per_config``.
 
 Timing: inputs are resident on the device before the timed region; launches
 are recorded in CUDA graphs and rotate through enough distinct buffer sets
-that their footprint is at least 4x the L2 size, so each launch reads from
-HBM; CUDA events on the launching stream bracket exactly K steps, with a
-barrier and a device synchronise on both sides; nvidia-smi samples clocks
-during the timed region.  ``e2e`` repeats the measurement with the inputs
-copied from pinned host memory and the outputs read back every step.  The
-CPU baseline is the fp64 oracle on the host cores over a bounded sample.
+that their footprint is at least 4x the L2 size (the headline's one set of
+4 GiB already is), so each launch reads from HBM; CUDA events on the
+launching stream bracket exactly K steps, with a barrier and a device
+synchronise on both sides; nvidia-smi samples clocks during the timed region
+and the half second of identical launches just before it.  ``e2e`` repeats
+the measurement with the inputs copied from pinned host memory and the
+outputs read back every step.  The CPU baseline is the fp64 oracle on the
+host cores over a bounded sample of the headline's rows.
 
 Under torchrun each rank runs its own replica on its own GPU (the op has no
 exchange between rows, so there is no collective on the data path); the
@@ -39,20 +43,26 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-HEADLINE = "bf16_4096x576"
+HEADLINE = "bf16_res_65536x8192_w"
 METRIC = "RMSNorm achieved HBM GB/s and % of GB300 peak; rows/s per config"
-PER_CONFIG = ["f32_64x256", "bf16_res_16384x2048", "bf16_qk_262144x128", "bf16_decode_1x4096",
-              "bf16_decode_8x4096", "bf16_decode_64x4096", "bf16_res_65536x8192_w",
-              "bf16_res_65536x8192_nw", "bf16_4096x32768_w", "bf16_res_4096x40960_w", "bf16_2048x65536_w", "bf16_res_2048x65536_w",
-              "f32_res_2048x65536_w"]
+PER_CONFIG = ["bf16_4096x576", "f32_64x256", "bf16_res_16384x2048", "bf16_qk_262144x128", "bf16_decode_1x4096",
+              "bf16_decode_8x4096", "bf16_decode_64x4096", "bf16_res_65536x8192_nw", "bf16_4096x32768_w",
+              "bf16_res_4096x40960_w", "bf16_2048x65536_w", "bf16_res_2048x65536_w", "f32_res_2048x65536_w"]
+# Workloads whose per-config entry also carries the launch-overhead context
+# (copy floor, independent batches, hot L2, repeated runs).
+SMALL_CONTEXT = ("bf16_4096x576",)
+# Rows of the headline the CPU baseline's sample takes (64 MiB of each input),
+# and the rows the reference arm's steps are taken from.
+CPU_SAMPLE_ROWS = 4096
+REF_POOL_ROWS = 16384
 FALLBACK_HBM_GBS = 6800.0
 
 
 def parse_args(argv=None):
     ap = argparse.ArgumentParser(description="fused RMSNorm benchmark")
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200000)
-    ap.add_argument("--warmup", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=HEADLINE)
     ap.add_argument("--no-per-config", action="store_true", help="skip the per-config table")
@@ -132,37 +142,58 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload, plan=None, with_source=False):
+def profiled_traffic(workload, plan=None, with_source=False, rows=None):
     """DRAM bytes per launch from the committed ncu summary of this workload
     (profiles/ncu_*.md with a matching ``profile_workload:`` line), if it was
     taken on the current device code and, when ``plan`` is given, with the
-    same launch plan; else None.  ``with_source`` also returns which summary
-    gave the figure, or why none did."""
-    value, source = _profiled_traffic(workload, plan)
+    same launch plan; else None.  A summary of a row slice of the workload
+    (``profile_workload: <name>@--rows<n>``, taken where the full workload is
+    too large for a profiler capture) counts when ``rows`` is given: its
+    bytes are scaled by rows / n (every row of a launch moves the same bytes)
+    and its plan must match in everything but the grid.  ``with_source`` also
+    returns which summary gave the figure, or why none did."""
+    value, source = _profiled_traffic(workload, plan, rows)
     return (value, source) if with_source else value
 
 
-def _profiled_traffic(workload, plan):
+def _profiled_traffic(workload, plan, rows=None):
     pdir = os.path.join(ROOT, "profiles")
     try:
         names = sorted(os.listdir(pdir))
     except OSError:
         return None, "no profiles/ directory"
     why = f"no ncu summary of {workload} in profiles/"
+    found = []
     for name in names:
         if not (name.startswith("ncu_") and name.endswith(".md")):
             continue
         text = open(os.path.join(pdir, name)).read()
         m_wl = re.search(r"profile_workload:\s*(\S+)\s*$", text, re.M)
-        if not m_wl or m_wl.group(1) != workload:
+        if not m_wl:
             continue
+        base, _, slice_arg = m_wl.group(1).partition("@")
+        m_slice = re.fullmatch(r"--rows(\d+)", slice_arg)
+        if base != workload or (slice_arg and (not m_slice or not rows)):
+            continue
+        found.append((0 if not slice_arg else 1, name, text, int(m_slice.group(1)) if m_slice else None))
+    for _, name, text, slice_rows in sorted(found):
         m_hash = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", text)
         m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
         m_plan = re.search(r"^Plan: `(\{.*\})`", text, re.M)
-        if plan is not None and (not m_plan or json.loads(m_plan.group(1)) != plan):
-            why = f"profiles/{name} was taken with another launch plan"
-            continue
+        if plan is not None:
+            got = json.loads(m_plan.group(1)) if m_plan else None
+            if got is not None and slice_rows:
+                got, want = dict(got, grid=None), dict(plan, grid=None)
+            else:
+                want = plan
+            if got != want:
+                why = f"profiles/{name} was taken with another launch plan"
+                continue
         if m_hash and m_bytes and m_hash.group(1) == kernel_source_hash():
+            if slice_rows:
+                scaled = int(round(int(m_bytes.group(1)) * rows / slice_rows))
+                return scaled, (f"profiles/{name} (device code hash {m_hash.group(1)}, same plan but the grid): "
+                                f"a {slice_rows}-row slice, its DRAM bytes scaled by {rows}/{slice_rows}")
             return int(m_bytes.group(1)), f"profiles/{name} (device code hash {m_hash.group(1)}, same plan)"
         why = f"profiles/{name} predates the current device code"
     return None, why
@@ -272,7 +303,7 @@ def gpu_id_for(local_rank):
 class Launcher:
     """Buffer sets of one workload and a C-ABI launch over set i % n_sets."""
 
-    def __init__(self, wl, device, stream, min_footprint, seed=0):
+    def __init__(self, wl, device, stream, min_footprint, seed=0, n_sets=None):
         import torch
         from row_reduction_norm_gb300 import _native as N
         from row_reduction_norm_gb300 import api, workloads as W
@@ -280,7 +311,7 @@ class Launcher:
         self.wl = wl
         self.stream = stream
         per_set = wl.rows * wl.hidden * wl.elem_bytes * (4 if wl.has_res else 2)
-        self.n_sets = max(1, math.ceil(min_footprint / max(per_set, 1)))
+        self.n_sets = n_sets or max(1, math.ceil(min_footprint / max(per_set, 1)))
         self.sets = []
         w = None
         for s in range(self.n_sets):
@@ -459,8 +490,13 @@ class QKLauncher(Launcher):
                               self.stream.cuda_stream)
 
 
-def time_launches(L, steps, warmup, barrier=None, sampler_window=None, graph_len=1024):
-    """Exactly `steps` launches between two events on L.stream; returns ms."""
+def time_launches(L, steps, warmup, barrier=None, sampler_window=None, graph_len=1024, soak_s=0.0):
+    """Exactly `steps` launches between two events on L.stream; returns ms.
+    Before them: at least `warmup` launches, continued (untimed, same
+    launches) until `soak_s` seconds have passed, so that clock samples taken
+    from the start of that soak to the end of the timed region describe the
+    GPU under this load even when the timed region is shorter than the
+    sampling period."""
     import torch
     with torch.cuda.stream(L.stream):
         L.launch(0)   # fills the library's per-device caches outside any capture
@@ -474,6 +510,11 @@ def time_launches(L, steps, warmup, barrier=None, sampler_window=None, graph_len
         for _ in range(max(1, math.ceil(warmup / G))):
             g_main.replay()
     L.stream.synchronize()
+    t_soak = time.time()
+    while time.time() - t_soak < soak_s:
+        with torch.cuda.stream(L.stream):
+            g_main.replay()
+        L.stream.synchronize()
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
     if barrier:
@@ -493,7 +534,7 @@ def time_launches(L, steps, warmup, barrier=None, sampler_window=None, graph_len
     if barrier:
         barrier()
     if sampler_window is not None:
-        sampler_window.extend([t0, t1])
+        sampler_window.extend([t_soak if soak_s > 0 else t0, t1])
     return ev0.elapsed_time(ev1)
 
 
@@ -664,7 +705,32 @@ def independent_chains_us(L, steps=8192):
     return e0.elapsed_time(e1) * 1e3 / (reps * 2 * G)
 
 
+def graph_launch_latency_us(L, reps=1000):
+    """Device-side latency of one launch: CUDA events around the replay of a
+    CUDA graph holding that single launch, median of `reps` (no Python or
+    ctypes cost inside the events, unlike ``single_launch_latency_us``)."""
+    import torch
+    g = L.graph(0, 1)
+    with torch.cuda.stream(L.stream):
+        for _ in range(8):
+            g.replay()
+    L.stream.synchronize()
+    ts = []
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    for _ in range(reps):
+        with torch.cuda.stream(L.stream):
+            e0.record(L.stream)
+            g.replay()
+            e1.record(L.stream)
+        e1.synchronize()
+        ts.append(e0.elapsed_time(e1) * 1e3)
+    return statistics.median(ts)
+
+
 def single_launch_latency_us(L, reps=1000):
+    """One C-ABI launch issued from Python between two CUDA events, median of
+    `reps`: the device time plus the cost of issuing the call."""
     import torch
     ts = []
     for i in range(reps):
@@ -689,8 +755,8 @@ def plan_summary(p):
 # ------------------------------------------------------------ CPU oracle
 
 def oracle_rate(wl, seconds, threads, host_inputs=None):
-    """The oracle, as it stands, over whole batches of the workload (or row
-    blocks of it) until `seconds` of work; returns a dict."""
+    """The oracle, as it stands, over the given rows of the workload (all of
+    them by default), pass after pass until `seconds` of work; returns a dict."""
     import oracle
     from row_reduction_norm_gb300 import workloads as W
     if host_inputs is None:
@@ -708,10 +774,67 @@ def oracle_rate(wl, seconds, threads, host_inputs=None):
             break
     dt = time.perf_counter() - t0
     per_launch_bytes = wl.algorithmic_bytes(rows=xn.shape[0])
+    what = (f"the {wl.rows}x{wl.hidden} {wl.dtype} batch" if xn.shape[0] == wl.rows else
+            f"the first {xn.shape[0]} rows of the {wl.rows}x{wl.hidden} {wl.dtype} batch")
     return {"value": per_launch_bytes * passes / dt / 1e9, "unit": "GB/s", "cores": threads,
             "kind": "oracle", "rows_per_s": rows_done / dt,
-            "sample": f"{passes} full passes over the {xn.shape[0]}x{wl.hidden} {wl.dtype} batch "
-                      f"({dt:.1f} s, fp64 C oracle, {threads} threads over row blocks)"}
+            "sample": f"{passes} passes over {what} ({dt:.1f} s, fp64 C oracle, {threads} threads over row "
+                      f"blocks; GB/s counts the algorithmic bytes of the rows done, the weight once a pass)"}
+
+
+def bench_config(wl, world):
+    """The ``config`` object of the JSON line: the workload and how L2 is kept
+    out of the figure.  Both arms print exactly this object."""
+    per_launch = wl.algorithmic_bytes()
+    moved = wl.rows * wl.hidden * wl.elem_bytes
+    return {
+        "workload": wl.name, "rows": wl.rows, "hidden": wl.hidden, "dtype": wl.dtype, "eps": wl.eps,
+        "residual": wl.has_res, "weight": wl.has_w, "outliers": wl.outlier_frac,
+        "bytes_per_step": per_launch,
+        "l2": (f"inputs larger than L2: one step reads {moved * (2 if wl.has_res else 1) // 2 ** 20} MiB; "
+               "workloads whose launches fit in L2 rotate over buffer sets of at least 4x the L2 size"),
+        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+    }
+
+
+def small_context(L, wl, steps):
+    """Launch-overhead context for a workload whose launches move a few MB:
+    the copy floor, independent batches, repeated runs and a hot-L2 figure."""
+    import torch
+    b = wl.algorithmic_bytes()
+    floor_us = copy_floor_us(L)
+    indep_us = independent_chains_us(L)
+    rep_steps = 20000
+    reps_us = sorted(time_launches(L, rep_steps, 8) * 1e3 / rep_steps for _ in range(10))
+    LH = Launcher(wl, L.stream.device, L.stream, 0)
+    hot_us = time_launches(LH, rep_steps, max(3, rep_steps // 20)) * 1e3 / rep_steps
+    del LH
+    torch.cuda.empty_cache()
+    kernel_us = statistics.median(reps_us)
+    return {
+        "launch_floor": {"copy_us": round(floor_us, 3), "kernel_us": round(kernel_us, 3),
+                         "kernel_vs_copy": round(floor_us / kernel_us, 3),
+                         "what": "torch copy_ of the same x -> y bytes, same graphs and buffer rotation: the "
+                                 "per-launch floor of a dependent chain of this size"},
+        "independent_batches": {"gbs": round(b / (indep_us / 1e6) / 1e9, 1), "us_per_launch": round(indep_us, 3),
+                                "streams": 2,
+                                "what": "context, not the metric: the same launches as two chains of "
+                                        "independent batches on two streams, free to overlap"},
+        "repeats": {"n": len(reps_us), "steps_each": rep_steps, "median_us": round(kernel_us, 3),
+                    "min_us": round(reps_us[0], 3), "max_us": round(reps_us[-1], 3),
+                    "what": "the launches timed again as 10 separate runs of steps_each launches"},
+        "hot_l2": {"us_per_launch": round(hot_us, 3), "gbs": round(b / (hot_us / 1e6) / 1e9, 1),
+                   "what": "hot L2, not HBM: one buffer set reused by every launch, so the inputs stay in L2"},
+    }
+
+
+def e2e_steps_for(wl, requested):
+    """Steps of the end-to-end region: as asked, else about two seconds of
+    host-link traffic at 150 GB/s (8 to 4096 steps)."""
+    if requested:
+        return requested
+    link = wl.rows * wl.hidden * wl.elem_bytes * (4 if wl.has_res else 2)
+    return int(max(8, min(4096, 2.0 / max(link / 150e9, 1e-9))))
 
 
 # ------------------------------------------------------------------ arms
@@ -752,7 +875,7 @@ def run_ours(args):
         sampler.start()
         time.sleep(0.3)
     window = []
-    ms = time_launches(L, args.steps, args.warmup, barrier=barrier, sampler_window=window)
+    ms = time_launches(L, args.steps, args.warmup, barrier=barrier, sampler_window=window, soak_s=0.5)
     if sampler:
         time.sleep(0.15)
         sampler.stop()
@@ -761,26 +884,36 @@ def run_ours(args):
     per_launch_s = ms / 1e3 / args.steps
     achieved = launch_bytes / per_launch_s / 1e9
     value, rows_per_s = aggregate(world, launch_bytes, wl.rows, args.steps, ms_max)
+    plan = plan_summary(L.plan)
+    pdl = bool(L.plan.pdl)
+    rep_steps = max(1, min(args.steps, int(math.ceil(0.2 / max(per_launch_s, 1e-9)))))
+    reps_us = sorted(time_launches(L, rep_steps, 3) * 1e3 / rep_steps for _ in range(5))
 
-    e2e_steps = args.e2e_steps or max(64, min(args.steps, 4096))
-    e_ms, h2d, d2h = time_e2e(L, e2e_steps)
+    # end to end through the public call: a second buffer set lets uploads,
+    # launches and read-backs of consecutive steps overlap
+    e2e_steps = e2e_steps_for(wl, args.e2e_steps)
+    del L
+    torch.cuda.empty_cache()
+    LE = Launcher(wl, device, stream, 0, n_sets=2)
+    e_ms, h2d, d2h = time_e2e(LE, e2e_steps)
     e2e_value, _ = aggregate(world, launch_bytes, wl.rows, e2e_steps, reduce_max(e_ms, dist, device))
-    s_ms, _, _ = time_e2e(L, e2e_steps, pipelined=False)
+    s_ms, _, _ = time_e2e(LE, e2e_steps, pipelined=False)
     e2e_serial, _ = aggregate(world, launch_bytes, wl.rows, e2e_steps, reduce_max(s_ms, dist, device))
 
-    floor_us = copy_floor_us(L)
-    indep_us = independent_chains_us(L)
-    # the same launches as 10 separately timed runs (median per launch), and a
-    # labelled hot-L2 figure: one buffer set reused every launch
-    rep_steps = max(1, min(args.steps, 20000))
-    reps_us = sorted(time_launches(L, rep_steps, 8) * 1e3 / rep_steps for _ in range(10))
-    LH = Launcher(wl, device, stream, 0)
-    hot_us = time_launches(LH, rep_steps, max(3, rep_steps // 20)) * 1e3 / rep_steps
-    del LH
+    cpu = None
+    if rank == 0 and world == 1 and args.cpu_seconds > 0:
+        n = min(wl.rows, CPU_SAMPLE_ROWS)
+        x0, r0, _, _ = LE.sets[0]
+        host = (W.to_numpy_bits(x0[:n]), W.to_numpy_bits(None if r0 is None else r0[:n]), W.to_numpy_bits(LE.w))
+        cpu = oracle_rate(wl, args.cpu_seconds, os.cpu_count() or 1, host)
+        one = oracle_rate(wl, max(1.0, args.cpu_seconds / 4), 1, host)
+        cpu["single_thread"] = {"value": one["value"], "rows_per_s": one["rows_per_s"], "cores": 1,
+                                "sample": one["sample"]}
+    del LE
+    torch.cuda.empty_cache()
+
     per_config = []
     if not args.no_per_config:
-        del L
-        torch.cuda.empty_cache()
         for name, (cw, launcher_cls, bytes_of, kind) in per_config_table(W).items():
             qk, ln, mx, nv = kind == "qk", kind == "ln", kind == "mx", kind == "nv"
             CL = launcher_cls(cw, device, stream, min_footprint)
@@ -812,27 +945,22 @@ def run_ours(args):
                 entry.update({"op": "rmsnorm, NVFP4 output (E2M1 codes, E4M3 scale per 16, tensor scale "
                                     f"{W.NV_TENSOR_SCALE})"})
             if rows <= 64 or (qk and cw.tokens <= 64):
+                entry["graph_launch_latency_us"] = round(graph_launch_latency_us(CL), 3)
                 entry["single_launch_latency_us"] = round(single_launch_latency_us(CL), 2)
+            if name in SMALL_CONTEXT:
+                entry.update(small_context(CL, cw, k))
             per_config.append(entry)
             del CL
             torch.cuda.empty_cache()
-        L = Launcher(wl, device, stream, 0)
-
-    cpu = None
-    if rank == 0 and world == 1 and args.cpu_seconds > 0:
-        x0, r0, _, _ = L.sets[0]
-        host = (W.to_numpy_bits(x0), W.to_numpy_bits(r0), W.to_numpy_bits(L.w))
-        cpu = oracle_rate(wl, args.cpu_seconds, os.cpu_count() or 1, host)
-        one = oracle_rate(wl, max(1.0, args.cpu_seconds / 4), 1, host)
-        cpu["single_thread"] = {"value": one["value"], "rows_per_s": one["rows_per_s"], "cores": 1,
-                                "sample": one["sample"]}
 
     if rank != 0:
         if dist is not None:
             dist.destroy_process_group()
         return
     clocks = sampler.summary(window[0], window[1]) if sampler and window else None
-    traffic, traffic_source = profiled_traffic(args.workload, plan_summary(L.plan), with_source=True)
+    if clocks is not None and clocks.get("source") == "timed region":
+        clocks["source"] = "timed region and the 0.5 s of identical launches just before it"
+    traffic, traffic_source = profiled_traffic(args.workload, plan, with_source=True, rows=wl.rows)
     out = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -848,41 +976,27 @@ def run_ours(args):
         "data": "synthetic",
         "rows_per_s": round(rows_per_s, 1),
         "frac_of_peak": round(achieved / peak, 4),
-        "config": {
-            "workload": wl.name, "rows": wl.rows, "hidden": wl.hidden, "eps": wl.eps,
-            "residual": wl.has_res, "weight": wl.has_w, "bytes_per_step": launch_bytes,
-            "l2": f"inputs larger than L2 in aggregate: launches rotate over {headline_sets} "
-                  f"buffer sets (>= 4x the {l2 // 2**20} MiB L2)",
-            "timing": "CUDA graphs of C-ABI launches, CUDA events on the launching stream",
-            "plan": plan_summary(L.plan),
-            "pdl": bool(L.plan.pdl),
-            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-        },
+        "config": bench_config(wl, world),
+        "timing": f"CUDA graphs of C-ABI launches over {headline_sets} buffer set(s) (L2 {l2 // 2 ** 20} MiB), "
+                  "CUDA events on the launching stream, exactly `steps` launches between them",
+        "plan": plan,
+        "pdl": pdl,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
                      else "fallback 6.8 TB/s", "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": traffic, "traffic_source": traffic_source,
-                     "kernel": f"rms_{plan_summary(L.plan)['kernel']}_kernel",
+                     "kernel": f"rms_{plan['kernel']}_kernel",
                      "algorithmic_bytes_per_launch": launch_bytes},
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "serial_value": round(e2e_serial, 2),
-                "what": "every step: pinned host -> device copy of its inputs (x, w), the C-ABI launch, "
-                        "device -> pinned host copy of y; uploads, launches and read-backs pipelined on "
-                        "three streams over 4 device buffer slots (serial_value: one stream, no overlap)"},
-        "launch_floor": {"copy_us": round(floor_us, 3), "kernel_us": round(per_launch_s * 1e6, 3),
-                         "kernel_vs_copy": round(floor_us / (per_launch_s * 1e6), 3),
-                         "what": "torch copy_ of the same x -> y bytes, same graphs and buffer rotation: "
-                                 "the per-launch floor of a dependent chain of this size"},
-        "independent_batches": {"value": round(launch_bytes / (indep_us / 1e6) / 1e9, 1), "unit": "GB/s",
-                                "us_per_launch": round(indep_us, 3), "streams": 2,
-                                "what": "context, not the metric: the same launches as two chains of "
-                                        "independent batches on two streams, free to overlap"},
+                "what": "every step: pinned host -> device copy of its inputs (x, residual, w), the C-ABI launch, "
+                        "device -> pinned host copy of y and residual_out; uploads, launches and read-backs "
+                        "pipelined on three streams over 2 device buffer sets (serial_value: one stream, no "
+                        "overlap)"},
         "repeats": {"n": len(reps_us), "steps_each": rep_steps, "median_us": round(statistics.median(reps_us), 3),
                     "min_us": round(reps_us[0], 3), "max_us": round(reps_us[-1], 3),
-                    "what": "the headline launches timed again as 10 separate runs of steps_each launches"},
-        "hot_l2": {"us_per_launch": round(hot_us, 3), "gbs": round(launch_bytes / (hot_us / 1e6) / 1e9, 1),
-                   "what": "hot L2, not HBM: one buffer set reused by every launch, so the inputs stay in L2"},
+                    "what": "the headline launches timed again as separate runs of steps_each launches"},
         "gpu_launches": args.steps,
         "clocks": clocks,
         "cpu_baseline": cpu,
@@ -972,13 +1086,17 @@ def run_reference(args):
     from row_reduction_norm_gb300 import workloads as W
     wl = W.WORKLOADS[args.workload]
     threads = os.cpu_count() or 1
-    x, r, w = W.make_inputs(wl, seed=0, device="cpu")
+    # the rows a step may take: the first REF_POOL_ROWS rows of the workload
+    # as drawn on the host (the whole batch when it is smaller)
+    pool = min(wl.rows, REF_POOL_ROWS)
+    x, r, w = W.make_inputs(wl, seed=0, device="cpu", rows=pool)
     xn, rn, wn = W.to_numpy_bits(x), W.to_numpy_bits(r), W.to_numpy_bits(w)
+    del x, r, w
     # size each step so that warmup + steps take about a minute of host time.
     # A step spread over a thread pool pays the pool's set-up: below 64 rows a
     # thread it runs on one thread, sized from the single-thread row rate.
     budget = 60.0 / max(1, args.steps + args.warmup)
-    probe = min(wl.rows, 256)
+    probe = min(pool, 256)
     t0 = time.perf_counter()
     oracle.rmsnorm(xn[:probe], w=wn, residual=None if rn is None else rn[:probe], eps=wl.eps, dtype=wl.dtype,
                    threads=1)
@@ -987,14 +1105,14 @@ def run_reference(args):
         t0 = time.perf_counter()
         oracle.rmsnorm(xn, w=wn, residual=rn, eps=wl.eps, dtype=wl.dtype, threads=threads)
         t_full = max(time.perf_counter() - t0, 1e-6)
-        rows_per_step = int(max(1, min(wl.rows, wl.rows * budget / t_full)))
+        rows_per_step = int(max(1, min(pool, pool * budget / t_full)))
     else:
         threads = 1
-        rows_per_step = int(max(1, min(wl.rows, budget / t_row1)))
+        rows_per_step = int(max(1, min(pool, budget / t_row1)))
 
     def step(i):
-        lo = (i * rows_per_step) % wl.rows
-        hi = min(wl.rows, lo + rows_per_step)
+        lo = (i * rows_per_step) % pool
+        hi = min(pool, lo + rows_per_step)
         oracle.rmsnorm(xn[lo:hi], w=wn, residual=None if rn is None else rn[lo:hi], eps=wl.eps,
                        dtype=wl.dtype, threads=threads)
         return hi - lo
@@ -1009,18 +1127,21 @@ def run_reference(args):
     row_bytes = wl.algorithmic_bytes(rows=1) - (wl.hidden * wl.elem_bytes if wl.has_w else 0)
     wbytes = wl.hidden * wl.elem_bytes if wl.has_w else 0
     value = (rows_done * row_bytes + args.steps * wbytes) / dt / 1e9
-    sample = (f"{rows_per_step} of {wl.rows} rows per step ({rows_per_step * wl.hidden} elements), "
-              f"fp64 C oracle, " + (f"{threads} threads over row blocks" if threads > 1 else
-                                    "one thread (steps too small for a thread pool to pay)"))
+    sample = (f"{rows_per_step} of {wl.rows} rows per step ({rows_per_step * wl.hidden} elements, taken in "
+              f"turn from the first {pool} rows), fp64 C oracle, " +
+              (f"{threads} threads over row blocks" if threads > 1 else
+               "one thread (steps too small for a thread pool to pay)"))
     out = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
         "rows_per_s": round(rows_done / dt, 1),
-        "config": {"workload": wl.name, "rows": wl.rows, "hidden": wl.hidden, "eps": wl.eps,
-                   "residual": wl.has_res, "weight": wl.has_w, "rows_per_step": rows_per_step,
-                   "l2": "host run: no GPU L2 involved"},
+        "config": bench_config(wl, world),
+        "timing": "host wall clock around exactly `steps` steps of the fp64 C oracle on the host cores",
+        "plan": None,
+        "pdl": None,
+        "rows_per_step": rows_per_step,
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

@@ -80,7 +80,11 @@ def test_reference_arm_json_line():
         assert k in line, k
     assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["value"] > 0
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
-    assert line["config"]["workload"] == "bf16_4096x576"
+    assert line["config"]["workload"] == "bf16_res_65536x8192_w"
+    import bench as B
+    from row_reduction_norm_gb300 import workloads as W
+    # the same config object as the GPU arm prints
+    assert line["config"] == B.bench_config(W.WORKLOADS[B.HEADLINE], 1)
 
 
 def test_reference_arm_other_ranks_exit_quietly():
@@ -105,6 +109,28 @@ def test_device_code_tokens_ignore_comments_only():
     assert bench.code_tokens(a) == bench.code_tokens(b)
     assert bench.code_tokens(a) != bench.code_tokens(c)
     assert "// not a comment" in bench.code_tokens(s)
+
+
+def test_row_slice_profiles_scale_to_the_full_workload():
+    import bench
+    plan = {"kernel": "reg", "regime": "cta", "threads_per_row": 256, "chunks_per_thread": 4, "vec_elems": 8,
+            "block": 256, "grid": 65536}
+    v, why = bench.profiled_traffic("bf16_res_65536x8192_w", plan, with_source=True, rows=65536)
+    if v is None:   # the summary predates the device code or the plan
+        assert "predates" in why or "another launch plan" in why
+    else:
+        assert "scaled by 65536/8192" in why and v > 0
+    # a slice counts only when the caller says how many rows to scale to
+    v, why = bench.profiled_traffic("bf16_res_65536x8192_w", plan, with_source=True)
+    assert v is None
+
+
+def test_e2e_steps_are_bounded():
+    import bench
+    from row_reduction_norm_gb300 import workloads as W
+    assert bench.e2e_steps_for(W.WORKLOADS["bf16_res_65536x8192_w"], 0) < 200
+    assert bench.e2e_steps_for(W.WORKLOADS["bf16_4096x576"], 0) == 4096
+    assert bench.e2e_steps_for(W.WORKLOADS["bf16_4096x576"], 7) == 7
 
 
 def test_traffic_source_says_why():
