@@ -123,7 +123,9 @@ typedef struct {
                                    spare x slot (at least avail / 7); the rest,
                                    which must hold a whole row, goes to x)           */
     int32_t vec_elems;          /* elements per load: 16 / sizeof(T), or 1 (scalar)  */
-    int32_t block_threads;      /* threads per block (TMA: 608)                       */
+    int32_t block_threads;      /* threads per block: REG max(threads_per_row, 256),
+                                   or max(threads_per_row, 128) for LayerNorm;
+                                   LOOP: threads_per_row; TMA: 608                    */
     int32_t rows_per_block;     /* rows one block handles per loop iteration          */
     int32_t persistent;         /* 1 if grid < row blocks (blocks stride over rows)   */
     int32_t pdl;                /* 1: launch with programmatic stream serialisation

@@ -70,21 +70,28 @@ __device__ __forceinline__ float row_combine(float v, float (&red)[2][RPB][WPR],
     return v;
 }
 
-// Resident blocks per SM the register budget is sized for: four (64
-// registers a thread at 256 threads) for up to 4 chunks a thread, which keeps
-// enough loads in flight per SM; five (48 registers) for up to 3 chunks
-// without a residual, which fit them without spilling (measured on GB300:
-// bf16 16384 x 768 with weight and bias 11.47 -> 10.65 us; six spill and are
-// slower); two (128 registers) for 8 chunks.
-__host__ __device__ constexpr int ln_min_blocks(int ch, bool res) {
-    return (ch <= 3 && !res) ? 5 : (ch <= 4 ? 4 : 2);
+// Threads per block of the LayerNorm register kernel: at least four warps
+// (rows of a warp or less: 128 / threads_per_row rows a block).  Measured on
+// GB300 against the RMSNorm kernel's 256: bf16 16384 x 768 with weight and
+// bias 9.81 -> 9.52 us -- twice the blocks, so the last wave of each SM is
+// half as coarse, for the same warps resident.
+__host__ __device__ constexpr int ln_block_threads(int gt) { return gt >= 128 ? gt : 128; }
+
+// Resident 256-thread equivalents the register budget is sized for: four (64
+// registers a thread) for up to 4 chunks a thread, which keeps enough loads in
+// flight per SM; five (48 registers) for up to 3 chunks without a residual,
+// which fit them without spilling (measured on GB300: bf16 16384 x 768 with
+// weight and bias 11.47 -> 10.65 us; six spill and are slower); two (128
+// registers) for 8 chunks.  Blocks of 128 threads get twice as many.
+__host__ __device__ constexpr int ln_min_blocks(int gt, int ch, bool res) {
+    return (ln_block_threads(gt) == 128 ? 2 : 1) * ((ch <= 3 && !res) ? 5 : (ch <= 4 ? 4 : 2));
 }
 
 template <typename T, int GT, int CH, bool RES, int AFF>
-__global__ void __launch_bounds__(reg_block_threads(GT), ln_min_blocks(CH, RES))
+__global__ void __launch_bounds__(ln_block_threads(GT), ln_min_blocks(GT, CH, RES))
 ln_reg_kernel(const LnParams p) {
     constexpr int V = T::kVec;
-    constexpr int BLOCK = reg_block_threads(GT);
+    constexpr int BLOCK = ln_block_threads(GT);
     constexpr int RPB = BLOCK / GT;
     constexpr int LANES = GT < 32 ? GT : 32;
     constexpr int WPR = GT > 32 ? GT / 32 : 1;
@@ -98,6 +105,8 @@ ln_reg_kernel(const LnParams p) {
     const int t = tid % GT;
     const int nch = p.units;
 
+    // before the wait: the block's first row group into L2 (see prefetch_rows_l2)
+    if (tid == 0) prefetch_rows_l2<RES>(p.x, p.res, p.row_bytes, p.rows, (int64_t)blockIdx.x * RPB, RPB);
     pdl_wait_for_inputs();
     pdl_allow_dependents();
 
@@ -106,39 +115,32 @@ ln_reg_kernel(const LnParams p) {
     bool staged = false;
     int parity = 0;
 
-    // loads of row group rbi into (dx, dr); zeros past the row end
-    auto load_group = [&](int64_t rbi, Chunk (&dx)[CH], Chunk (&dr)[RES ? CH : 1]) {
-        const int64_t rw = rbi * RPB + slot;
-        const bool ok = rw < p.rows;
-        const int64_t o = ok ? rw * p.row_bytes : 0;
-#pragma unroll
-        for (int c = 0; c < CH; ++c) {
-            const int u = c * GT + t;
-            if (ok && u < nch)
-                dx[c] = ld_stream16(static_cast<const char *>(p.x) + o + (int64_t)u * 16);
-            else
-                dx[c] = Chunk{{0u, 0u, 0u, 0u}};
-        }
-        if constexpr (RES) {
-#pragma unroll
-            for (int c = 0; c < CH; ++c) {
-                const int u = c * GT + t;
-                if (ok && u < nch)
-                    dr[c] = ld_stream16(static_cast<const char *>(p.res) + o + (int64_t)u * 16);
-                else
-                    dr[c] = Chunk{{0u, 0u, 0u, 0u}};
-            }
-        }
-    };
-
     for (int64_t rb = blockIdx.x; rb * RPB < p.rows; rb += gridDim.x) {
         const int64_t row = rb * RPB + slot;
         const bool row_ok = row < p.rows;
         const int64_t off = row_ok ? row * p.row_bytes : 0;
 
+        // the row's chunks (zeros past the row end)
         Chunk hc[CH];
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+            const int u = c * GT + t;
+            if (row_ok && u < nch)
+                hc[c] = ld_stream16(static_cast<const char *>(p.x) + off + (int64_t)u * 16);
+            else
+                hc[c] = Chunk{{0u, 0u, 0u, 0u}};
+        }
         Chunk rc[RES ? CH : 1];
-        load_group(rb, hc, rc);
+        if constexpr (RES) {
+#pragma unroll
+            for (int c = 0; c < CH; ++c) {
+                const int u = c * GT + t;
+                if (row_ok && u < nch)
+                    rc[c] = ld_stream16(static_cast<const char *>(p.res) + off + (int64_t)u * 16);
+                else
+                    rc[c] = Chunk{{0u, 0u, 0u, 0u}};
+            }
+        }
         if constexpr (W) {
             if (!staged) {   // first iteration of the block (uniform across it)
                 for (int i = tid; i < nch; i += BLOCK)
@@ -179,6 +181,7 @@ ln_reg_kernel(const LnParams p) {
         // variance: centred squares of the valid elements (slots past the row end are skipped)
 #pragma unroll
         for (int e = 0; e < V; ++e) acc[e] = 0.f;
+        const float2 nmu2 = make_float2(-mu, -mu);
 #pragma unroll
         for (int c = 0; c < CH; ++c) {
             const int u = c * GT + t;
@@ -186,12 +189,17 @@ ln_reg_kernel(const LnParams p) {
                 float a[V];
                 unpack(hc[c], a, T{});
 #pragma unroll
-                for (int e = 0; e < V; ++e) a[e] = a[e] - mu;
-                sq_accumulate(a, acc);
+                for (int k = 0; k < V / 2; ++k) {
+                    const float2 d = __fadd2_rn(make_float2(a[2 * k], a[2 * k + 1]), nmu2);
+                    const float2 q = __ffma2_rn(d, d, make_float2(acc[2 * k], acc[2 * k + 1]));
+                    acc[2 * k] = q.x;
+                    acc[2 * k + 1] = q.y;
+                }
             }
         }
         const float var = row_combine<LANES, WPR, RPB>(tree_sum(acc), red, parity, slot, t, tid) / p.hidden_f;
         const float r = rsqrtf(var + p.eps);
+        const float2 r2 = make_float2(r, r);
 #pragma unroll
         for (int c = 0; c < CH; ++c) {
             const int u = c * GT + t;
@@ -200,11 +208,10 @@ ln_reg_kernel(const LnParams p) {
                 unpack(hc[c], a, T{});
                 if constexpr (W) unpack(wb_smem[u], wv, T{});
                 if constexpr (B) unpack(wb_smem[nch + u], bv, T{});
-                const float2 mu2 = make_float2(-mu, -mu), r2 = make_float2(r, r);
 #pragma unroll
                 for (int k = 0; k < V / 2; ++k) {
                     // n = (h - mu) * r, then n * w or fma(n, w, b): two lanes at a time
-                    float2 n = __fmul2_rn(__fadd2_rn(make_float2(a[2 * k], a[2 * k + 1]), mu2), r2);
+                    float2 n = __fmul2_rn(__fadd2_rn(make_float2(a[2 * k], a[2 * k + 1]), nmu2), r2);
                     if constexpr (AFF == kAffW) {
                         n = __fmul2_rn(n, make_float2(wv[2 * k], wv[2 * k + 1]));
                     } else if constexpr (AFF == kAffWB) {

@@ -119,6 +119,9 @@ struct Op {
     int dtype = RMSNORM_BF16;
 };
 
+// Threads per block of a register-kernel plan for this op.
+int reg_block_of(const Op &o, int gt) { return o.ln ? rrn::ln_block_threads(gt) : rrn::reg_block_threads(gt); }
+
 int max_threads_per_row(const Op &o) {
     return o.ln ? rrn::kLnMaxGT : (o.head_rows ? rrn::kRegMaxGTHeads : rrn::kRegMaxGT);
 }
@@ -323,7 +326,7 @@ int validate_plan(const rmsnorm_plan_t *p, const Op &o, int vec_ok) {
         if (ch < 1 || ch > rrn::kRegMaxCH || ((ch & (ch - 1)) != 0 && !odd_ch)) return RMSNORM_EINVAL;
         if (odd_ch && (o.head_rows || o.mx || o.nv)) return RMSNORM_EINVAL;
         if ((int64_t)gt * ch * V < o.row_elems) return RMSNORM_EINVAL;
-        if (p->block_threads != rrn::reg_block_threads(gt)) return RMSNORM_EINVAL;
+        if (p->block_threads != reg_block_of(o, gt)) return RMSNORM_EINVAL;
         if (p->rows_per_block != p->block_threads / gt) return RMSNORM_EINVAL;
         return RMSNORM_OK;
     }
@@ -443,6 +446,10 @@ int plan_for_device(const Op &o, rmsnorm_plan_t *plan, int *dev_out) {
         plan->vec_elems = vec_elems_of(o.dtype);
         plan->block_threads = rrn::kTmaBlock;
         plan->rows_per_block = 1;
+    }
+    if (o.ln && plan->kernel == RMSNORM_KERNEL_REG) {
+        plan->block_threads = reg_block_of(o, plan->threads_per_row);
+        plan->rows_per_block = plan->block_threads / plan->threads_per_row;
     }
     if (o.mx && plan->kernel == RMSNORM_KERNEL_REG) {
         const int V = vec_elems_of(o.dtype);

@@ -182,6 +182,38 @@ __device__ __forceinline__ void st16(void *p, const Chunk &c) {
 __device__ __forceinline__ void pdl_wait_for_inputs() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_allow_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
 
+// L2 prefetch of `bytes` bytes at `p` (16-byte aligned, a multiple of 16 bytes)
+// through the bulk-copy engine.  It returns no data to the thread and fills no
+// L1 line; it only warms L2, which is the device's point of coherence for
+// global memory.  So it may be issued before griddepcontrol.wait, even on
+// memory the kernel still running ahead of this one is writing: every load
+// of the kernel comes after the wait, reads the line in L2, and sees the
+// earlier kernel's stores there (a line prefetched before a store is updated
+// by that store).  A prefetch changes timing, never a value.
+__device__ __forceinline__ void prefetch_l2(const void *p, unsigned bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" : : "l"(p), "r"(bytes) : "memory");
+}
+
+// The first rows a block will read (rows r0 .. r0 + n - 1 of contiguous
+// [rows, row_bytes] tensors x and, with RES, the residual), prefetched into
+// L2 by the calling thread before the block waits on the kernel ahead of it.
+// Measured on GB300: a launch whose inputs were not written by the kernel
+// just before it (the residual stream of a transformer block, or any norm
+// after an unrelated kernel) saves one DRAM round trip of its critical path
+// -- bf16 4096 x 576 3.03 -> 2.24 us a launch, decode 1 x 4096 1.74 -> 1.47
+// us; when the kernel before it has just written x the lines are already in
+// L2 and the launch costs the same (2.158 -> 2.159 us).  A weight prefetched
+// the same way measured slower (it is read by every block and stays in L2).
+template <bool RES>
+__device__ __forceinline__ void prefetch_rows_l2(const void *x, const void *res, int64_t row_bytes, int64_t rows,
+                                                 int64_t r0, int n) {
+    if (r0 >= rows) return;
+    const int64_t nr = rows - r0 < n ? rows - r0 : n;
+    const unsigned bytes = (unsigned)(nr * row_bytes);
+    prefetch_l2(static_cast<const char *>(x) + r0 * row_bytes, bytes);
+    if constexpr (RES) prefetch_l2(static_cast<const char *>(res) + r0 * row_bytes, bytes);
+}
+
 // ------------------------------------------------------------- conversions
 // bf16 is the upper half of an fp32 encoding: widening is a 16-bit shift.
 // Narrowing rounds to nearest even with the CUDA intrinsic.
@@ -433,6 +465,11 @@ __device__ __forceinline__ void rms_reg_rows(const Params &p) {
     const int t = tid % GT;
     const int nch = p.units;
 
+    // before the wait: the block's first row group into L2 (contiguous rows,
+    // whose row group is one contiguous range)
+    if constexpr (!HEADS) {
+        if (tid == 0) prefetch_rows_l2<RES>(p.x, p.res, p.row_bytes, p.rows, (int64_t)blockIdx.x * RPB, RPB);
+    }
     pdl_wait_for_inputs();
     pdl_allow_dependents();
 

@@ -214,6 +214,8 @@ rms_tma_kernel(const Params p, const int sx, const int sr, const int sw) {
         s_issued[0] = s_issued[1] = s_issued[2] = 0;
     }
     __syncthreads();
+    // before the wait: the block's first row into L2 (see prefetch_rows_l2)
+    if (tid == 0) prefetch_rows_l2<RES>(p.x, p.res, row_bytes, p.rows, (int64_t)blockIdx.x, 1);
     pdl_wait_for_inputs();
     pdl_allow_dependents();
 
@@ -260,16 +262,27 @@ rms_tma_kernel(const Params p, const int sx, const int sr, const int sw) {
                     if (ok) ok = mbar_wait_bounded(&Rr.full[rs], (qr / Rr.n) & 1u);
                     rp = Rr.mem + (size_t)rs * PIECE;
                 }
+                // every shared-memory load of the piece is issued before the
+                // first is used, so a warp keeps PC (2 PC) of them in flight
+                Chunk xa[PC], ra[RES ? PC : 1];
+#pragma unroll
+                for (int j = 0; j < PC; ++j) {
+                    const int so = (j * GT + t) * 16;
+                    if ((k * PC + j) * GT + t < nch) {
+                        xa[j] = lds16(xp + so);
+                        if constexpr (RES) ra[j] = lds16(rp + so);
+                    }
+                }
 #pragma unroll
                 for (int j = 0; j < PC; ++j) {
                     const int u = (k * PC + j) * GT + t;
                     if (u < nch) {
                         const int so = (j * GT + t) * 16;
                         float a[V];
-                        unpack(lds16(xp + so), a, T{});
+                        unpack(xa[j], a, T{});
                         if constexpr (RES) {
                             float b[V];
-                            unpack(lds16(rp + so), b, T{});
+                            unpack(ra[j], b, T{});
 #pragma unroll
                             for (int e = 0; e < V; ++e) a[e] = add_round(a[e], b[e], T{});
                             const Chunk h = pack(a, T{});
@@ -309,6 +322,17 @@ rms_tma_kernel(const Params p, const int sx, const int sr, const int sw) {
                     if (ok) ok = mbar_wait_bounded(&Wr.full[ws], wpar);
                     wp = Wr.mem + (size_t)ws * PIECE;
                 }
+                Chunk xa[OUT == kOutT ? PC : 1], wa[OUT == kOutT && W ? PC : 1];
+                if constexpr (OUT == kOutT) {   // loads first, as in pass 1
+#pragma unroll
+                    for (int j = 0; j < PC; ++j) {
+                        const int so = (j * GT + t) * 16;
+                        if ((k * PC + j) * GT + t < nch) {
+                            xa[j] = lds16(xp + so);
+                            if constexpr (W) wa[j] = lds16(wp + so);
+                        }
+                    }
+                }
 #pragma unroll
                 for (int j = 0; j < PC; ++j) {
                     const int u = (k * PC + j) * GT + t;
@@ -316,10 +340,10 @@ rms_tma_kernel(const Params p, const int sx, const int sr, const int sw) {
                     if constexpr (OUT == kOutT) {
                         if (u < nch) {
                             float a[V];
-                            unpack(lds16(xp + so), a, T{});
+                            unpack(xa[j], a, T{});
                             float wv[V];
                             if constexpr (W) {
-                                unpack(lds16(wp + so), wv, T{});
+                                unpack(wa[j], wv, T{});
                             } else {
 #pragma unroll
                                 for (int e = 0; e < V; ++e) wv[e] = 1.f;

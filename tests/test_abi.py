@@ -225,6 +225,25 @@ def test_tma_ring_rule_matches_the_library(pc, res, w):
             assert got == want, (dtype, hidden)
 
 
+def test_layernorm_register_blocks_are_four_warps_or_the_row():
+    """LayerNorm register plans use blocks of max(threads_per_row, 128)
+    threads; a plan with the RMSNorm block size is refused (rows = 0:
+    validation only, no CUDA call)."""
+    P = 1 << 20
+    p = R.rmsnorm_plan(4, 768, N.RMSNORM_BF16, True, 152, 1)
+    p.threads_per_row, p.chunks_per_thread, p.block_threads, p.rows_per_block = 32, 3, 128, 4
+    assert N.layernorm_fwd_status(P, None, P, P, P, None, 0, 768, 1e-5, 1, p) == N.RMSNORM_OK
+    q = p.copy()
+    q.block_threads, q.rows_per_block = 256, 8
+    assert N.layernorm_fwd_status(P, None, P, P, P, None, 0, 768, 1e-5, 1, q) == N.RMSNORM_EINVAL
+    # RMSNorm keeps 256-thread blocks
+    assert N.rmsnorm_fwd_plan_status(P, None, P, P, None, 0, 768, 1e-5, 1, q, 0) == N.RMSNORM_OK
+    assert N.rmsnorm_fwd_plan_status(P, None, P, P, None, 0, 768, 1e-5, 1, p, 0) == N.RMSNORM_EINVAL
+    big = p.copy()
+    big.threads_per_row, big.chunks_per_thread, big.block_threads, big.rows_per_block = 128, 4, 128, 1
+    assert N.layernorm_fwd_status(P, None, P, P, P, None, 0, 4096, 1e-5, 1, big) == N.RMSNORM_OK
+
+
 def test_qk_norm_is_warp_regime_and_large_rows_cta():
     qk = R.rmsnorm_plan(1024, 128, N.RMSNORM_BF16, True, 152, 4)
     assert qk.regime == N.RMSNORM_REGIME_WARP and qk.threads_per_row <= 32

@@ -58,7 +58,7 @@ def test_ln_every_plan(rows, hidden, dtype):
     wl = W.Workload("ln-sweep", dtype, rows, hidden, 1e-5, 1.0, 1.0, 0.1, b_std=0.1, x_mean=0.25)
     x, r, w, b = W.make_ln_inputs(wl, seed=rows + hidden, device=DEV)
     code = R.dtype_code(x.dtype)
-    plans = [p for p in all_plans(rows, hidden, code, True, odd_ch=True)
+    plans = [p for p in all_plans(rows, hidden, code, True, odd_ch=True, min_block=128)
              if p.kernel == N.RMSNORM_KERNEL_LOOP or p.threads_per_row <= 256]
     for p in plans:
         for ww, bb, rr in ((w, b, r), (w, None, None), (None, None, r)):

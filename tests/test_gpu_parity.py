@@ -97,13 +97,14 @@ def test_workload_large_sampled(name):
 
 # ------------------------------------------------------------ forced plans
 
-def all_plans(rows, hidden, dtype_code, vec_ok, sm_count=152, odd_ch=False, tma=False):
+def all_plans(rows, hidden, dtype_code, vec_ok, sm_count=152, odd_ch=False, tma=False, min_block=256):
     """Every launch plan that is valid for the shape: all REG (threads, chunks)
     pairs that cover the row (chunks 3 and 6 too with ``odd_ch``, compiled for
     contiguous rows), the bulk-copy kernel with both piece sizes that fit
     (``tma``: contiguous RMSNorm rows), the two-pass kernel (vector / scalar,
     each block size that keeps the accuracy bound), each in a full grid and a
-    small (persistent) grid."""
+    small (persistent) grid.  ``min_block``: the register kernel's smallest
+    block (256 for RMSNorm, 128 for LayerNorm)."""
     V = 8 if dtype_code == N.RMSNORM_BF16 else 4
     plans = []
     if vec_ok:
@@ -117,7 +118,7 @@ def all_plans(rows, hidden, dtype_code, vec_ok, sm_count=152, odd_ch=False, tma=
                 p.threads_per_row = gt
                 p.chunks_per_thread = ch
                 p.vec_elems = V
-                p.block_threads = gt if gt >= 256 else 256
+                p.block_threads = gt if gt >= min_block else min_block
                 p.rows_per_block = p.block_threads // gt
                 plans.append(p)
     if vec_ok and tma:

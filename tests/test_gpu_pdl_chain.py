@@ -182,7 +182,7 @@ def test_layernorm_chain(rows, hidden, forced, graph):
     H = [r0.clone()] + [torch.empty_like(x0) for _ in range(STEPS)]
     plan = None
     if forced:
-        plan = [p for p in all_plans(rows, hidden, N.RMSNORM_BF16, True, odd_ch=True)
+        plan = [p for p in all_plans(rows, hidden, N.RMSNORM_BF16, True, odd_ch=True, min_block=128)
                 if p.kernel == N.RMSNORM_KERNEL_LOOP and p.grid == rows][0]
         plan.pdl = 1
 
