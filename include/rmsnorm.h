@@ -369,13 +369,38 @@ int rmsnorm_reg_max_chunks(void);
  * for a ring slot to be released) gives up after one second; the block then
  * finishes its rows without waiting (its outputs are not valid), waits, again
  * at most a second each, for its copies still in flight, and adds 1 to a
- * per-device counter.  This reads that counter for the current device (the
- * count since the library was loaded; 0 unless a launch went wrong).  It is a
- * blocking device-to-host read: call it after synchronising the streams that
- * ran the kernels, and not while a stream is being captured.
+ * per-device counter.  A consumer warp that gave up releases no ring slot from
+ * then on, so no copy is ever started into a slot whose previous copy may
+ * still be landing.  The launch itself returned RMSNORM_OK when it was
+ * issued; this counter is how the host learns that a block gave up.  This
+ * reads that counter for the current device (the count since the library was
+ * loaded; 0 unless a launch went wrong).  It is a blocking device-to-host
+ * read: call it after synchronising the streams that ran the kernels, and
+ * not while a stream is being captured.
  * Returns RMSNORM_OK, RMSNORM_EINVAL (count NULL) or RMSNORM_ECUDA.
  */
 int rmsnorm_wait_timeouts(uint32_t *count);
+
+/*
+ * Test hook of the bounded waits above (the pages describe no such hook):
+ * rmsnorm_fwd_plan with a RMSNORM_KERNEL_TMA plan (else RMSNORM_EINVAL),
+ * every wait of the kernel limited to wait_limit_ns nanoseconds (0: the
+ * one-second default; at most one second), and, with withhold_release = 1,
+ * one release of an x slot withheld by the first consumer warp of block 0.
+ * That block's x producer then waits for a slot that never frees: its wait
+ * runs out, so do the consumers' waits for the pieces it no longer copies,
+ * the block finishes with no valid output for its rows, waits for its copies
+ * in flight, and adds 1 to the count rmsnorm_wait_timeouts reads.  Blocks
+ * other than block 0 and every launch with withhold_release = 0 compute the
+ * op as rmsnorm_fwd_plan does.  Nothing faults and no wait is unbounded:
+ * a test uses it to see the failure path work and the next launch succeed.
+ * The launch is asynchronous like every other: its status says whether it
+ * was launched, the counter whether a block gave up.
+ */
+int rmsnorm_tma_wait_test(const void *x, const void *residual, const void *w, void *y,
+                          void *residual_out, int64_t rows, int64_t hidden, float eps, int dtype,
+                          const rmsnorm_plan_t *plan, uint64_t wait_limit_ns, int withhold_release,
+                          rmsnorm_stream_t stream);
 
 /* Static text for a status code. */
 const char *rmsnorm_strerror(int status);

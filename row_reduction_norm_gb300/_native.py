@@ -64,7 +64,8 @@ EXPORTED = ["rmsnorm_fwd", "rmsnorm_regime", "rmsnorm_plan", "rmsnorm_plan_for",
             "rmsnorm_qk_fwd", "rmsnorm_qk_plan_for", "rmsnorm_fwd_mxfp8", "rmsnorm_mxfp8_plan_for",
             "rmsnorm_fwd_nvfp4", "rmsnorm_nvfp4_plan_for",
             "layernorm_fwd", "layernorm_plan_for",
-            "rmsnorm_max_hidden", "rmsnorm_reg_max_chunks", "rmsnorm_wait_timeouts", "rmsnorm_strerror",
+            "rmsnorm_max_hidden", "rmsnorm_reg_max_chunks", "rmsnorm_wait_timeouts", "rmsnorm_tma_wait_test",
+            "rmsnorm_strerror",
             "rmsnorm_build_info"]
 
 
@@ -166,6 +167,8 @@ def load():
         lib.rmsnorm_max_hidden.restype = i64
         lib.rmsnorm_reg_max_chunks.argtypes = []
         lib.rmsnorm_reg_max_chunks.restype = i32
+        lib.rmsnorm_tma_wait_test.argtypes = fwd_args + [ctypes.POINTER(Plan), ctypes.c_uint64, i32, vp]
+        lib.rmsnorm_tma_wait_test.restype = i32
         lib.rmsnorm_wait_timeouts.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
         lib.rmsnorm_wait_timeouts.restype = i32
         lib.rmsnorm_strerror.argtypes = [i32]
@@ -345,6 +348,13 @@ def rmsnorm_strerror(status) -> str:
 
 def rmsnorm_build_info() -> str:
     return load().rmsnorm_build_info().decode()
+
+
+def rmsnorm_tma_wait_test_status(x, residual, w, y, residual_out, rows, hidden, eps, dtype, plan, wait_limit_ns,
+                                 withhold_release, stream=0) -> int:
+    """The bulk-copy kernel's bounded-wait test hook (see the header); returns the status."""
+    return load().rmsnorm_tma_wait_test(x, residual, w, y, residual_out, rows, hidden, eps, dtype, _plan_ref(plan),
+                                        wait_limit_ns, withhold_release, stream)
 
 
 def rmsnorm_wait_timeouts() -> int:

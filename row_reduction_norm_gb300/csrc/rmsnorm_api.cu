@@ -49,6 +49,8 @@ constexpr int kTmaLongPC = 4;
 // 16-byte units of a row past which contiguous RMSNorm rows leave the
 // register kernel for the bulk-copy kernel (2048 units: 32 KB).
 constexpr int64_t kRegWideUnits = 256 * rrn::kRegMaxCH;
+// Limit of every wait inside the bulk-copy kernel (ns).
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
 int elem_size(int dtype) { return dtype == RMSNORM_BF16 ? 2 : 4; }
 int vec_elems_of(int dtype) { return 16 / elem_size(dtype); }
@@ -117,6 +119,8 @@ struct Op {
     float eps = 0.f, w_bias = 0.f;
     int wm = 0;                // rrn::WeightMode (RMSNorm) or rrn::AffineMode (LayerNorm)
     int dtype = RMSNORM_BF16;
+    uint64_t wait_ns = kWaitLimitNs;   // bulk-copy kernel: limit of each wait
+    int withhold = 0;                  // bulk-copy kernel: test of its bounded waits
 };
 
 // Threads per block of a register-kernel plan for this op.
@@ -530,6 +534,8 @@ int launch(const Op &o, const rmsnorm_plan_t *plan, int dev, rmsnorm_stream_t st
     args.scales = o.scales;
     args.q_scale = o.q_scale;
     args.q_inv6s = (float)(1.0 / (6.0 * (double)o.q_scale));
+    args.wait_ns = o.wait_ns;
+    args.withhold = o.withhold;
     if (plan->kernel == RMSNORM_KERNEL_TMA) {
         if (!tma_rings(o.row_elems * s, plan->chunks_per_thread, o.res != nullptr, o.w != nullptr, &rings))
             return RMSNORM_EINVAL;
@@ -849,6 +855,19 @@ int rmsnorm_qk_plan_for(const void *x, const void *y, int64_t tokens, int64_t x_
     if (st != RMSNORM_OK) return st;
     if (!elem_aligned(o)) return RMSNORM_EINVAL;
     return plan_for_device(o, plan, nullptr);
+}
+
+int rmsnorm_tma_wait_test(const void *x, const void *residual, const void *w, void *y, void *residual_out,
+                          int64_t rows, int64_t hidden, float eps, int dtype, const rmsnorm_plan_t *plan,
+                          uint64_t wait_limit_ns, int withhold_release, rmsnorm_stream_t stream) {
+    if (plan == nullptr || plan->kernel != RMSNORM_KERNEL_TMA) return RMSNORM_EINVAL;
+    if (wait_limit_ns > kWaitLimitNs || (withhold_release != 0 && withhold_release != 1)) return RMSNORM_EINVAL;
+    Op o;
+    int st = make_contig(x, residual, w, y, residual_out, rows, hidden, eps, 0.f, dtype, &o);
+    if (st != RMSNORM_OK) return st;
+    o.wait_ns = wait_limit_ns == 0 ? kWaitLimitNs : wait_limit_ns;
+    o.withhold = withhold_release;
+    return run(o, plan, stream);
 }
 
 int64_t rmsnorm_max_hidden(int dtype) {

@@ -78,6 +78,10 @@ struct Params {
     void *scales;        // block-scaled outputs: the scales (y holds the codes)
     float q_scale;       // NVFP4: per-tensor scale S
     float q_inv6s;       // NVFP4: 1 / (6 S), rounded once to float
+    uint64_t wait_ns;    // bulk-copy kernel: limit of each of its waits, in ns
+    int32_t withhold;    // bulk-copy kernel, tests of its bounded waits only:
+                         // 1 = block 0's first consumer warp keeps its first
+                         // x slot (0 in every library launch)
 };
 
 // Output form of the register kernel: the I/O type; MXFP8 (E4M3 codes in y,

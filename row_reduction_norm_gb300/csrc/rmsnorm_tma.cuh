@@ -34,11 +34,17 @@
 // reduced, and the next rows stream in while this row is scaled.  Both passes
 // read shared memory only, so no warp waits on an L2 or HBM round trip.
 //
-// Every wait is bounded (kTmaWaitLimitNs on the globaltimer).  A wait that
-// runs out marks the thread failed; a failed thread skips its later waits but
-// keeps the same control flow (so every barrier is still reached), the block
-// counts itself in g_tma_timeouts, and before it exits one thread waits
-// (bounded again) for every copy still in flight into its shared memory.
+// Every wait is bounded (Params::wait_ns on the globaltimer, one second in
+// every library launch).  A wait that runs out marks the thread failed; a
+// failed thread skips its later waits but keeps the same control flow (so
+// every barrier is still reached), and a warp whose lane 0 has failed releases
+// no slot from then on.  A slot is released, that is, only by warps that saw
+// its copy land, so a producer never starts a copy into a slot whose previous
+// copy may still be in flight (which would arrive on the slot's "full"
+// barrier before its phase completed); a producer that waits for such a slot
+// gives up in turn.  The block counts itself in g_tma_timeouts, and before it
+// exits one thread waits (bounded again) for every copy still in flight into
+// its shared memory.
 //
 // This header defines the counter below, so one translation unit (tma.cu)
 // includes it.
@@ -50,7 +56,6 @@
 namespace rrn {
 
 constexpr int kTmaWarps = kTmaGT / 32;          // consumer warps
-constexpr unsigned long long kTmaWaitLimitNs = 1000000000ull;   // 1 s
 
 // Blocks that gave up on a wait since the library was loaded.
 __device__ unsigned int g_tma_timeouts = 0;
@@ -91,12 +96,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, unsigned parity) {
 }
 
 // Wait for the completion of the barrier phase of the given parity; false if
-// kTmaWaitLimitNs passed first.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, unsigned parity) {
+// limit_ns nanoseconds passed first.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, unsigned parity, unsigned long long limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer_ns();
     while (!mbar_try_wait(bar, parity)) {
-        if (globaltimer_ns() - t0 > kTmaWaitLimitNs) return false;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
     }
     return true;
 }
@@ -149,7 +154,7 @@ __device__ __forceinline__ bool feed_ring(const Ring &R, const char *src, int64_
         const char *base = src + (once ? 0 : row * row_stride);
         for (int k = 0; k < pieces; ++k) {
             const unsigned s = q % R.n, n = q / R.n;
-            if (n > 0 && !mbar_wait_bounded(&R.empty[s], (n - 1) & 1u)) {
+            if (n > 0 && !mbar_wait_bounded(&R.empty[s], (n - 1) & 1u, p.wait_ns)) {
                 issued = q;
                 return false;
             }
@@ -166,9 +171,9 @@ __device__ __forceinline__ bool feed_ring(const Ring &R, const char *src, int64_
 }
 
 // Waits (bounded) for the last copy issued into each slot of a ring.
-__device__ __forceinline__ void drain_ring(const Ring &R, unsigned issued) {
+__device__ __forceinline__ void drain_ring(const Ring &R, unsigned issued, unsigned long long limit_ns) {
     for (unsigned j = issued > R.n ? issued - R.n : 0u; j < issued; ++j)
-        (void)mbar_wait_bounded(&R.full[j % R.n], (j / R.n) & 1u);
+        (void)mbar_wait_bounded(&R.full[j % R.n], (j / R.n) & 1u, limit_ns);
 }
 
 // sx, sr, sw: slots of the x, residual and weight rings (sr = 0 without a
@@ -253,13 +258,13 @@ rms_tma_kernel(const Params p, const int sx, const int sr, const int sw) {
             // pass 1: A1-A3 over the pieces as they land
             for (int k = 0; k < pieces; ++k) {
                 const unsigned xs = (qx + (unsigned)k) % X.n;
-                if (ok) ok = mbar_wait_bounded(&X.full[xs], ((qx + (unsigned)k) / X.n) & 1u);
+                if (ok) ok = mbar_wait_bounded(&X.full[xs], ((qx + (unsigned)k) / X.n) & 1u, p.wait_ns);
                 unsigned char *xp = X.mem + (size_t)xs * PIECE;
                 unsigned rs = 0;
                 const unsigned char *rp = nullptr;
                 if constexpr (RES) {
                     rs = qr % Rr.n;
-                    if (ok) ok = mbar_wait_bounded(&Rr.full[rs], (qr / Rr.n) & 1u);
+                    if (ok) ok = mbar_wait_bounded(&Rr.full[rs], (qr / Rr.n) & 1u, p.wait_ns);
                     rp = Rr.mem + (size_t)rs * PIECE;
                 }
                 // every shared-memory load of the piece is issued before the
@@ -294,7 +299,7 @@ rms_tma_kernel(const Params p, const int sx, const int sr, const int sw) {
                 }
                 if constexpr (RES) {   // the residual piece is used up
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&Rr.empty[rs]);
+                    if (lane == 0 && ok) mbar_arrive(&Rr.empty[rs]);
                     ++qr;
                 }
             }
@@ -319,7 +324,7 @@ rms_tma_kernel(const Params p, const int sx, const int sr, const int sw) {
                 if constexpr (W) {
                     ws = w_resident ? (unsigned)k : qw % Wr.n;
                     const unsigned wpar = w_resident ? 0u : (qw / Wr.n) & 1u;
-                    if (ok) ok = mbar_wait_bounded(&Wr.full[ws], wpar);
+                    if (ok) ok = mbar_wait_bounded(&Wr.full[ws], wpar, p.wait_ns);
                     wp = Wr.mem + (size_t)ws * PIECE;
                 }
                 Chunk xa[OUT == kOutT ? PC : 1], wa[OUT == kOutT && W ? PC : 1];
@@ -370,8 +375,9 @@ rms_tma_kernel(const Params p, const int sx, const int sr, const int sw) {
                 // this thread's shared-memory writes before it
                 if constexpr (RES) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&X.empty[xs]);
+                if (lane == 0 && ok) {
+                    if (!(p.withhold && blockIdx.x == 0 && warp == 0 && qx + (unsigned)k == 0u))
+                        mbar_arrive(&X.empty[xs]);
                     if (W && !w_resident) mbar_arrive(&Wr.empty[ws]);
                 }
                 if (W && !w_resident) ++qw;
@@ -385,9 +391,9 @@ rms_tma_kernel(const Params p, const int sx, const int sr, const int sw) {
     if (s_failed && tid == 0) {
         atomicAdd(&g_tma_timeouts, 1u);
         // no copy may land after the block has left
-        drain_ring(X, s_issued[0]);
-        if (RES) drain_ring(Rr, s_issued[1]);
-        if (W) drain_ring(Wr, s_issued[2]);
+        drain_ring(X, s_issued[0], p.wait_ns);
+        if (RES) drain_ring(Rr, s_issued[1], p.wait_ns);
+        if (W) drain_ring(Wr, s_issued[2], p.wait_ns);
     }
 }
 

@@ -17,6 +17,17 @@ validation in test_abi.py) it checks:
   - a consumer reads a piece only after it landed, and it is the piece it
     expects (tensor, row, k);
   - every walk ends: no deadlock for any shape, grid or block tried.
+
+The failure path is modelled too: every wait has a budget of scheduler steps
+(the kernel's time limit); a consumer warp whose wait ran out skips its
+later waits and releases no slot from then on, a producer whose wait for an
+empty slot ran out stops, and the block's last act waits for the copies in
+flight.  With the test hook's withheld release, or with copies that land
+after the consumers gave up on them, the model checks that no copy is ever
+started into a slot whose previous copy has not landed (that would arrive
+twice on one phase of the slot's "full" barrier), that every walk still
+ends, and that nothing lands after the drain.  Releasing slots after a
+failure, the order the kernel had before, fails that check.
 """
 import random
 
@@ -47,6 +58,7 @@ class Bar:
         self._maybe_complete()
 
     def arrive_expect_tx(self, nbytes):
+        assert self.pending > 0, "arrival on a phase that already has all its arrivals"
         self.tx += nbytes
         self.pending -= 1
         self._maybe_complete()
@@ -60,7 +72,13 @@ class Bar:
         return (self.phase & 1) != parity
 
 
-def walk(rows, hidden, esz, pc, grid, block, res, w, seed):
+def walk(rows, hidden, esz, pc, grid, block, res, w, seed, budget=None, withhold=False, max_delay=8,
+         release_after_failure=False):
+    """One block's walk.  ``budget``: scheduler steps a wait may take before it
+    runs out (None: unbounded); ``withhold``: consumer warp 0 keeps its first x
+    slot (the kernel's test hook); ``release_after_failure``: the order the
+    kernel had before, where a warp that gave up still released its slots.
+    Returns the number of actors that gave up."""
     rnd = random.Random(seed)
     row_bytes = hidden * esz
     nch = row_bytes // 16
@@ -91,7 +109,12 @@ def walk(rows, hidden, esz, pc, grid, block, res, w, seed):
             for k in range(pieces):
                 s, ph = q % n, q // n
                 if ph > 0:
+                    waited = 0
                     while not empty[b + s].done((ph - 1) & 1):
+                        waited += 1
+                        if budget is not None and waited > budget:
+                            failed.append(tensor)
+                            return
                         yield
                 off = k * piece
                 nbytes = min(piece, row_bytes - off)
@@ -105,13 +128,33 @@ def walk(rows, hidden, esz, pc, grid, block, res, w, seed):
                 content[g] = (tensor, None if once else row, k)
                 landed[g] = False
                 readers[g] = set(range(WARPS))
-                inflight.append([rnd.randint(0, 8), g, nbytes])
+                inflight.append([rnd.randint(0, max_delay), g, nbytes])
                 q += 1
                 yield
             if once:
                 break
 
     arrived = {}
+    failed = []
+
+    def wait_full(g, parity, st):
+        """Consumer wait on a full barrier; st["ok"] turns False when it runs out."""
+        if not st["ok"]:
+            return
+        waited = 0
+        while not full[g].done(parity):
+            waited += 1
+            if budget is not None and waited > budget:
+                st["ok"] = False
+                failed.append("consumer")
+                return
+            yield
+
+    def release(g, wid, st, withheld=False):
+        if st["ok"] or release_after_failure:
+            readers[g].discard(wid)
+            if not withheld:
+                empty[g].arrive()
 
     def reads(g, k, wid):
         for t in range(wid * 32, wid * 32 + 32):
@@ -122,21 +165,21 @@ def walk(rows, hidden, esz, pc, grid, block, res, w, seed):
 
     def consumer(wid):
         qx = qr = qw = 0
+        st = {"ok": True}
         for ri, row in enumerate(my_rows):
             for k in range(pieces):                       # pass 1
                 g = (qx + k) % sx
-                while not full[g].done(((qx + k) // sx) & 1):
-                    yield
-                assert landed[g] and content[g] == ("x", row, k)
-                reads(g, k, wid)
+                yield from wait_full(g, ((qx + k) // sx) & 1, st)
+                if st["ok"]:
+                    assert landed[g] and content[g] == ("x", row, k)
+                    reads(g, k, wid)
                 if res:
                     gr = sx + qr % sr
-                    while not full[gr].done((qr // sr) & 1):
-                        yield
-                    assert landed[gr] and content[gr] == ("r", row, k)
-                    reads(gr, k, wid)
-                    readers[gr].discard(wid)
-                    empty[gr].arrive()
+                    yield from wait_full(gr, (qr // sr) & 1, st)
+                    if st["ok"]:
+                        assert landed[gr] and content[gr] == ("r", row, k)
+                        reads(gr, k, wid)
+                    release(gr, wid, st)
                     qr += 1
                 yield
             arrived[ri] = arrived.get(ri, 0) + 1          # barrier over the consumer warps
@@ -144,18 +187,18 @@ def walk(rows, hidden, esz, pc, grid, block, res, w, seed):
                 yield
             for k in range(pieces):                       # pass 2
                 g = (qx + k) % sx
-                assert content[g] == ("x", row, k)
+                if st["ok"]:
+                    assert content[g] == ("x", row, k)
+                gw = None
                 if w:
                     gw = sx + sr + (k if w_resident else qw % sw)
-                    while not full[gw].done(0 if w_resident else (qw // sw) & 1):
-                        yield
-                    assert landed[gw] and content[gw] == ("w", None if w_resident else row, k)
-                    reads(gw, k, wid)
-                readers[g].discard(wid)
-                empty[g].arrive()
+                    yield from wait_full(gw, 0 if w_resident else (qw // sw) & 1, st)
+                    if st["ok"]:
+                        assert landed[gw] and content[gw] == ("w", None if w_resident else row, k)
+                        reads(gw, k, wid)
+                release(g, wid, st, withheld=withhold and wid == 0 and qx + k == 0)
                 if w and not w_resident:
-                    readers[gw].discard(wid)
-                    empty[gw].arrive()
+                    release(gw, wid, st)
                     qw += 1
                 yield
             qx += pieces
@@ -186,7 +229,18 @@ def walk(rows, hidden, esz, pc, grid, block, res, w, seed):
                     next(actors[i])
                 except StopIteration:
                     alive[i] = False
+    if failed:
+        # the block's drain: its last thread waits for every copy in flight
+        while inflight:
+            for c in list(inflight):
+                if c[0] == 0:
+                    inflight.remove(c)
+                    landed[c[1]] = True
+                    full[c[1]].complete_tx(c[2])
+                else:
+                    c[0] -= 1
     assert not inflight, "copies still in flight when every actor finished"
+    return len(failed)
 
 
 SHAPES = [(2, 65536), (2, 40000), (4, 16388), (4, 40960), (2, 8), (2, 8200)]
@@ -222,3 +276,45 @@ def test_model_covers_every_ring_split():
     for pc in N.TMA_PIECE_CHUNKS:
         for res in (False, True):
             assert (pc, res, True) in seen and (pc, res, False) in seen, (pc, res)
+
+
+@pytest.mark.parametrize("esz,hidden", [(2, 40960), (2, 8200), (4, 16388)])
+@pytest.mark.parametrize("pc", N.TMA_PIECE_CHUNKS)
+def test_withheld_release_gives_up_safely(esz, hidden, pc):
+    """The test hook: warp 0 keeps its first x slot.  The x producer's wait
+    for that slot runs out, the consumers' waits for the pieces it no longer
+    copies run out, nothing is copied into a slot still in use, and every walk
+    ends (the kernel then counts the block in its timeout counter)."""
+    tried = 0
+    for res in (False, True):
+        for w in (False, True):
+            rings = N.tma_rings(hidden * esz, pc, res, w)
+            if rings is None:
+                continue
+            sx, pieces = rings[0], -(-hidden * esz // (GT * 16 * pc))
+            rows = 2 * -(-sx // pieces) + 1      # enough rows that slot 0 is needed again
+            for grid in (1, 2):
+                gave_up = walk(rows, hidden, esz, pc, grid, 0, res, w, seed=pc * 7 + grid, budget=60,
+                               withhold=True)
+                assert gave_up >= 1
+                tried += 1
+    if tried == 0:
+        pytest.skip("row larger than the rings at this piece size")
+
+
+def test_late_copies_with_failed_consumers_never_reuse_a_filling_slot():
+    """Copies that land after the consumers gave up on them: with failed warps
+    keeping their slots, no slot is refilled while its copy is in flight; the
+    order the kernel had before (a failed warp still releasing) is caught by
+    the model on at least one of the same walks."""
+    walks = [(2, 8200, 1, res, w, seed) for res in (False, True) for w in (False, True) for seed in range(12)]
+    old_order_caught = 0
+    for esz, hidden, pc, res, w, seed in walks:
+        if N.tma_rings(hidden * esz, pc, res, w) is None:
+            continue
+        walk(9, hidden, esz, pc, 1, 0, res, w, seed=seed, budget=6, max_delay=40)
+        try:
+            walk(9, hidden, esz, pc, 1, 0, res, w, seed=seed, budget=6, max_delay=40, release_after_failure=True)
+        except AssertionError:
+            old_order_caught += 1
+    assert old_order_caught > 0
