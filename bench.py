@@ -350,6 +350,26 @@ class Launcher:
         return g
 
 
+class ChainLauncher:
+    """A dependent chain of the workload's launches: two buffers, launch i
+    reads buffer i % 2 and writes the other, so every launch reads what the
+    one before it wrote (x only: workloads without a residual)."""
+
+    def __init__(self, L):
+        import torch
+        self.N, self.wl, self.stream, self.code, self.w_ptr = L.N, L.wl, L.stream, L.code, L.w_ptr
+        x0 = L.sets[0][0]
+        self.bufs = [x0.clone(), torch.empty_like(x0)]
+        self.n_sets = 2
+
+    def launch(self, i):
+        src, dst = self.bufs[i % 2], self.bufs[(i + 1) % 2]
+        self.N.rmsnorm_fwd(src.data_ptr(), None, self.w_ptr, dst.data_ptr(), None, self.wl.rows, self.wl.hidden,
+                           self.wl.eps, self.code, self.stream.cuda_stream)
+
+    graph = Launcher.graph
+
+
 class CastLauncher(Launcher):
     """RMSNorm in the op-by-op cast order (rmsnorm_fwd_cast), same buffers."""
 
@@ -809,6 +829,11 @@ def small_context(L, wl, steps):
     LH = Launcher(wl, L.stream.device, L.stream, 0)
     hot_us = time_launches(LH, rep_steps, max(3, rep_steps // 20)) * 1e3 / rep_steps
     del LH
+    chain_us = None
+    if not wl.has_res:
+        LC = ChainLauncher(L)
+        chain_us = time_launches(LC, rep_steps, max(3, rep_steps // 20)) * 1e3 / rep_steps
+        del LC
     torch.cuda.empty_cache()
     kernel_us = statistics.median(reps_us)
     return {
@@ -825,6 +850,10 @@ def small_context(L, wl, steps):
                     "what": "the launches timed again as 10 separate runs of steps_each launches"},
         "hot_l2": {"us_per_launch": round(hot_us, 3), "gbs": round(b / (hot_us / 1e6) / 1e9, 1),
                    "what": "hot L2, not HBM: one buffer set reused by every launch, so the inputs stay in L2"},
+        "dependent_chain": None if chain_us is None else {
+            "us_per_launch": round(chain_us, 3), "gbs": round(b / (chain_us / 1e6) / 1e9, 1),
+            "what": "each launch reads the y the launch before it wrote (two buffers; at this size they stay in "
+                    "L2): the norm as a model runs it, where its input is the previous kernel's output"},
     }
 
 
