@@ -767,9 +767,12 @@ def single_launch_latency_us(L, reps=1000):
 
 def plan_summary(p):
     d = p.as_dict()
-    return {"kernel": d["kernel_name"], "regime": d["regime_name"], "threads_per_row": d["threads_per_row"],
-            "chunks_per_thread": d["chunks_per_thread"], "vec_elems": d["vec_elems"],
-            "block": d["block_threads"], "grid": d["grid"]}
+    out = {"kernel": d["kernel_name"], "regime": d["regime_name"], "threads_per_row": d["threads_per_row"],
+           "chunks_per_thread": d["chunks_per_thread"], "vec_elems": d["vec_elems"],
+           "block": d["block_threads"], "grid": d["grid"]}
+    if d["rows_per_block"] != max(1, d["block_threads"] // max(1, d["threads_per_row"])):
+        out["rows_per_block"] = d["rows_per_block"]     # fewer rows a block than row slots
+    return out
 
 
 # ------------------------------------------------------------ CPU oracle

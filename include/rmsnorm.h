@@ -100,8 +100,10 @@ enum {
  * A launch plan.  The per-row schedule (kernel, threads_per_row, vec_elems,
  * block_threads) depends only on hidden, dtype and the alignment of the
  * pointers (and, for rows longer than 80 KB, on whether a residual is given);
- * rows sizes the grid and may pick a chunk count that fits the row exactly,
- * which never changes a result (chunks past the row end add exact zeros).
+ * rows sizes the grid, may pick a chunk count that fits the row exactly and
+ * may give each row a block of its own (rows_per_block 1), none of which ever
+ * changes a result (chunks past the row end add exact zeros; which block takes
+ * a row does not matter).
  */
 typedef struct {
     int32_t kernel;             /* RMSNORM_KERNEL_*                                   */
@@ -112,7 +114,8 @@ typedef struct {
                                    slots past the row end stay idle); 1, 2, 4 or 8,
                                    and 3 or 6 for contiguous RMSNorm / LayerNorm rows
                                    in the I/O type (planning takes them for LayerNorm,
-                                   and for RMSNorm launches of more than one wave of
+                                   for RMSNorm rows of a warp or less, and for wider
+                                   RMSNorm rows in launches of more than one wave of
                                    blocks); LOOP: 0; TMA: chunks per thread
                                    in one ring piece: 1, 2 or 4 (8, 16 or 32 KB
                                    pieces; 28, 14 or 7 slots of shared memory, of
@@ -126,7 +129,11 @@ typedef struct {
     int32_t block_threads;      /* threads per block: REG max(threads_per_row, 256),
                                    or max(threads_per_row, 128) for LayerNorm;
                                    LOOP: threads_per_row; TMA: 608                    */
-    int32_t rows_per_block;     /* rows one block handles per loop iteration          */
+    int32_t rows_per_block;     /* rows one block handles per loop iteration: REG
+                                   block_threads / threads_per_row, or (RMSNorm only)
+                                   fewer, down to 1; planning takes 1 when the launch
+                                   has no more rows than the device has SMs, so each
+                                   row has a block of its own; other kernels 1     */
     int32_t persistent;         /* 1 if grid < row blocks (blocks stride over rows)   */
     int32_t pdl;                /* 1: launch with programmatic stream serialisation
                                    (the kernel may start while the previous kernel on

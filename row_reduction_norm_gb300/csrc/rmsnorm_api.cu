@@ -256,14 +256,36 @@ int exact_ch(int64_t units, int gt, int ch) {
 }
 
 // Contiguous RMSNorm rows take the exact-fit chunk count when the launch has
-// more than one wave of blocks: measured on GB300 it is faster there (fewer
-// registers, more blocks resident: bf16 233016 x 576 without residual 0.874
-// -> 0.985 of peak, 26214 x 5120 0.855 -> 0.983) and slower for a single
-// wave (bf16 4096 x 576: 3.05 -> 3.17 us).
+// more than one wave of blocks, and always for rows of a warp or less:
+// measured on GB300 it is faster there (fewer registers, more blocks
+// resident: bf16 233016 x 576 without residual 0.874 -> 0.985 of peak,
+// 26214 x 5120 0.855 -> 0.983; with the first rows prefetched before the
+// dependency wait, a single wave of bf16 rows of 576 too: 4096 rows 2.31 ->
+// 2.18 us, 1024 rows 1.77 -> 1.70 us), but not for a single wave of wider
+// rows (bf16 600 x 5120: 2.85 us with 4 chunks against 3.01 with 3).
 void fit_chunks(int64_t rows, int64_t resident_blocks, bool contiguous_rms, int64_t units, rmsnorm_plan_t *p) {
     if (!contiguous_rms || p->kernel != RMSNORM_KERNEL_REG) return;
-    if (ceil_div(rows, p->rows_per_block) <= resident_blocks) return;
+    if (p->threads_per_row > 32 && ceil_div(rows, p->rows_per_block) <= resident_blocks) return;
     p->chunks_per_thread = exact_ch(units, p->threads_per_row, p->chunks_per_thread);
+}
+
+// Launches with no more rows than the device has SMs (decode batches) give
+// every row a block of its own, so the rows spread over as many SMs as they
+// can (the RMSNorm register kernel holds a run-time count of rows a block;
+// the idle row slots of a block load and store nothing).  Measured on GB300,
+// bf16 rows of 4096: 8 rows 1.66 -> 1.62 us, 64 rows 1.82 -> 1.71 us; rows of
+// 576: 8 rows 1.45 -> 1.34 us, 64 rows 1.53 -> 1.38 us; a single row is the
+// same.  The per-row schedule is unchanged, so no result changes.  Planned
+// for contiguous RMSNorm rows of at least a warp (what was measured); forced
+// plans may hold fewer rows a block on every RMSNorm register kernel.
+void spread_rows(int64_t rows, int sm_count, bool contiguous_rms, rmsnorm_plan_t *p) {
+    if (!contiguous_rms || p->kernel != RMSNORM_KERNEL_REG || p->threads_per_row < 32 || p->rows_per_block <= 1)
+        return;
+    if (rows < 1 || rows > (int64_t)(sm_count > 0 ? sm_count : 1)) return;
+    p->rows_per_block = 1;
+    p->grid = rows;
+    p->persistent = 0;
+    if (p->regime == RMSNORM_REGIME_PERSISTENT) p->regime = p->threads_per_row <= 32 ? RMSNORM_REGIME_WARP : RMSNORM_REGIME_CTA;
 }
 
 size_t dyn_smem_of(const rmsnorm_plan_t *p, const Op &o) {
@@ -331,7 +353,10 @@ int validate_plan(const rmsnorm_plan_t *p, const Op &o, int vec_ok) {
         if (odd_ch && (o.head_rows || o.mx || o.nv)) return RMSNORM_EINVAL;
         if ((int64_t)gt * ch * V < o.row_elems) return RMSNORM_EINVAL;
         if (p->block_threads != reg_block_of(o, gt)) return RMSNORM_EINVAL;
-        if (p->rows_per_block != p->block_threads / gt) return RMSNORM_EINVAL;
+        // LayerNorm blocks hold every row slot; the RMSNorm kernel may hold fewer
+        if (o.ln ? p->rows_per_block != p->block_threads / gt
+                 : (p->rows_per_block < 1 || p->rows_per_block > p->block_threads / gt))
+            return RMSNORM_EINVAL;
         return RMSNORM_OK;
     }
     if (p->kernel == RMSNORM_KERNEL_TMA) {
@@ -480,6 +505,7 @@ int plan_for_device(const Op &o, rmsnorm_plan_t *plan, int *dev_out) {
     size_grid(o.rows, sms, bps, plan);
     fit_chunks(o.rows, (int64_t)sms * bps, !(o.ln || o.head_rows || o.mx || o.nv), o.row_elems / vec_elems_of(o.dtype),
                plan);
+    spread_rows(o.rows, sms, !(o.ln || o.head_rows || o.mx || o.nv), plan);
     if (dev_out) *dev_out = dev;
     return RMSNORM_OK;
 }
@@ -534,6 +560,7 @@ int launch(const Op &o, const rmsnorm_plan_t *plan, int dev, rmsnorm_stream_t st
     args.scales = o.scales;
     args.q_scale = o.q_scale;
     args.q_inv6s = (float)(1.0 / (6.0 * (double)o.q_scale));
+    args.rpb = plan->rows_per_block;
     args.wait_ns = o.wait_ns;
     args.withhold = o.withhold;
     if (plan->kernel == RMSNORM_KERNEL_TMA) {
@@ -768,6 +795,7 @@ int rmsnorm_plan(int64_t rows, int64_t hidden, int dtype, int vec_ok, int sm_cou
     size_grid(rows, sm_count, blocks_per_sm, plan);
     fit_chunks(rows, (int64_t)(sm_count > 0 ? sm_count : 1) * (blocks_per_sm > 0 ? blocks_per_sm : 1), true,
                hidden / vec_elems_of(dtype), plan);
+    spread_rows(rows, sm_count, true, plan);
     return RMSNORM_OK;
 }
 

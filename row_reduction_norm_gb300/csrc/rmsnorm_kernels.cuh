@@ -78,6 +78,8 @@ struct Params {
     void *scales;        // block-scaled outputs: the scales (y holds the codes)
     float q_scale;       // NVFP4: per-tensor scale S
     float q_inv6s;       // NVFP4: 1 / (6 S), rounded once to float
+    int32_t rpb;         // register kernel: rows a block holds per iteration
+                         // (BLOCK / GT, or fewer for a launch of few rows)
     uint64_t wait_ns;    // bulk-copy kernel: limit of each of its waits, in ns
     int32_t withhold;    // bulk-copy kernel, tests of its bounded waits only:
                          // 1 = block 0's first consumer warp keeps its first
@@ -458,7 +460,7 @@ __device__ __forceinline__ void rms_reg_rows(const Params &p) {
                                                                   "a block's lanes in one row group");
     constexpr int V = T::kVec;
     constexpr int BLOCK = reg_block_threads(GT);
-    constexpr int RPB = BLOCK / GT;               // rows per block iteration
+    constexpr int RPB = BLOCK / GT;               // row groups a block can hold
     constexpr int LANES = GT < 32 ? GT : 32;      // butterfly width
     constexpr int WPR = GT > 32 ? GT / 32 : 1;    // warps per row
     static_assert((GT & (GT - 1)) == 0 && GT >= 4 && GT <= 1024, "GT: power of two in [4, 1024]");
@@ -472,7 +474,8 @@ __device__ __forceinline__ void rms_reg_rows(const Params &p) {
     // before the wait: the block's first row group into L2 (contiguous rows,
     // whose row group is one contiguous range)
     if constexpr (!HEADS) {
-        if (tid == 0) prefetch_rows_l2<RES>(p.x, p.res, p.row_bytes, p.rows, (int64_t)blockIdx.x * RPB, RPB);
+        const int n = p.rpb >= 1 && p.rpb <= RPB ? p.rpb : RPB;
+        if (tid == 0) prefetch_rows_l2<RES>(p.x, p.res, p.row_bytes, p.rows, (int64_t)blockIdx.x * n, n);
     }
     pdl_wait_for_inputs();
     pdl_allow_dependents();
@@ -489,9 +492,15 @@ __device__ __forceinline__ void rms_reg_rows(const Params &p) {
     bool w_staged = false;
 
     int parity = 0;
-    for (int64_t rb = blockIdx.x; rb * RPB < p.rows; rb += gridDim.x) {
-        const int64_t row = rb * RPB + slot;
-        const bool row_ok = row < p.rows;
+    // p.rpb (1 .. RPB) rows a block iteration: RPB, or one row a block when a
+    // launch has no more rows than the device has SMs (each row then gets an
+    // SM of its own; the idle row slots load and store nothing).  Which block
+    // takes a row changes no result.
+    const int rpb = p.rpb >= 1 && p.rpb <= RPB ? p.rpb : RPB;   // the host passes 1..RPB
+    const int64_t step = (int64_t)gridDim.x * rpb;
+    for (int64_t first = (int64_t)blockIdx.x * rpb; first < p.rows; first += step) {
+        const int64_t row = first + slot;
+        const bool row_ok = slot < rpb && row < p.rows;
         int64_t off = 0, yoff = 0;
         int wsel = 0;
         if (row_ok) row_offsets<HEADS>(p, row, off, yoff, wsel);

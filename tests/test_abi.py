@@ -92,11 +92,12 @@ def test_plan_properties(dtype, hidden):
         assert huge.persistent == 1 and huge.grid == (152 * 2 if tma else 152 * 2 * 4096)
         if huge.kernel == N.RMSNORM_KERNEL_REG:
             assert huge.regime == N.RMSNORM_REGIME_PERSISTENT
-        sched = {(p.kernel, p.threads_per_row, p.vec_elems, p.block_threads, p.rows_per_block) for p in plans}
+        sched = {(p.kernel, p.threads_per_row, p.vec_elems, p.block_threads) for p in plans}
         assert len(sched) == 1, "the per-row schedule must not depend on the row count"
         if plans[0].kernel == N.RMSNORM_KERNEL_REG:
             # only the chunk count may follow the row count: a power of two for
-            # a single wave of blocks, the exact fit (3 or 6) beyond
+            # a single wave of blocks of rows wider than a warp, the exact fit
+            # (3 or 6) beyond, and for rows of a warp or less in every launch
             gt = plans[0].threads_per_row
             need = -(-(hidden // V) // gt)
             pow2 = 1
@@ -104,8 +105,8 @@ def test_plan_properties(dtype, hidden):
                 pow2 *= 2
             exact = 3 if need == 3 else 6 if need in (5, 6) else pow2
             for rows, p in zip((1, 7, 1000, 10 ** 6), plans):
-                waves = -(-rows // p.rows_per_block) > 152 * 2
-                assert p.chunks_per_thread == (exact if waves else pow2), (rows, p)
+                waves = -(-rows // (p.block_threads // gt)) > 152 * 2
+                assert p.chunks_per_thread == (exact if waves or gt <= 32 else pow2), (rows, p)
         cap = 152 * 2 if tma else 152 * 2 * 4096
         for rows, p in zip((1, 7, 1000, 10 ** 6), plans):
             row_blocks = -(-rows // p.rows_per_block)
@@ -117,7 +118,10 @@ def test_plan_properties(dtype, hidden):
                 gt, ch = p.threads_per_row, p.chunks_per_thread
                 assert gt * ch * V >= hidden and gt & (gt - 1) == 0 and 4 <= gt <= 512
                 assert ch in (1, 2, 3, 4, 6, 8)
-                assert p.block_threads == max(gt, 256) and p.rows_per_block == p.block_threads // gt
+                assert p.block_threads == max(gt, 256)
+                # one row a block when the launch has no more rows than SMs (rows of a warp or more)
+                spread = rows <= 152 and gt >= 32
+                assert p.rows_per_block == (1 if spread else p.block_threads // gt), (rows, p)
                 want = (N.RMSNORM_REGIME_PERSISTENT if p.persistent else
                         N.RMSNORM_REGIME_WARP if gt <= 32 else N.RMSNORM_REGIME_CTA)
                 assert p.regime == want

@@ -60,6 +60,14 @@ def test_mx_every_plan(rows, hidden, dtype):
             torch.cuda.synchronize()
             mx_check(out, x, rr, ww, wl.eps, dtype, f"plan {p.as_dict()} w={ww is not None} res={rr is not None}",
                      weight_bias=b)
+        if p.rows_per_block > 1 and p.grid == -(-rows // p.rows_per_block):
+            # one row a block: the same codes and scales
+            q = p.copy()
+            q.rows_per_block, q.grid = 1, rows
+            a = R.rms_norm_mxfp8(x, w=w, residual=r, eps=wl.eps, plan=p)
+            c = R.rms_norm_mxfp8(x, w=w, residual=r, eps=wl.eps, plan=q)
+            torch.cuda.synchronize()
+            assert all(torch.equal(u, v) for u, v in zip(a, c)), q.as_dict()
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])

@@ -183,6 +183,61 @@ def test_every_plan_matches_oracle(rows, hidden, dtype):
         assert ok, f"plan {p.as_dict()} (no residual, no weight): {rep}"
 
 
+def _fewer_rows(p, rpb, rows, grid=None):
+    q = p.copy()
+    q.rows_per_block = rpb
+    q.grid = grid or -(-rows // rpb)
+    q.persistent = int(q.grid < -(-rows // rpb))
+    return q
+
+
+@pytest.mark.parametrize("rows,hidden,dtype", [(9, 4096, "bf16"), (131, 576, "bf16"), (37, 128, "f32"),
+                                               (300, 2048, "bf16"), (5, 64, "bf16")])
+def test_rows_per_block_changes_no_bit(rows, hidden, dtype):
+    """A register-kernel block may hold fewer rows than it has row slots (the
+    plan's rows_per_block; planning takes 1 for launches of no more rows than
+    SMs): every such plan, full grid or a grid of 3 blocks striding over the
+    rows, gives the bits of the plan that fills every slot, with and without
+    a residual and a weight."""
+    wl = W.Workload("rpb", dtype, rows, hidden, 1e-5, 1.0, 1.0, 0.1)
+    x, r, w = gpu_inputs(wl, seed=hidden + 3 * rows)
+    code = R.dtype_code(x.dtype)
+    yr, hr = oracle_run(x, r, w, wl.eps, dtype)
+    full = [p for p in all_plans(rows, hidden, code, True) if p.kernel == N.RMSNORM_KERNEL_REG
+            and p.rows_per_block > 1 and p.grid == -(-rows // p.rows_per_block)]
+    assert full
+    for p in full:
+        y0, h0 = R.rms_norm(x, w=w, residual=r, eps=wl.eps, plan=p)
+        n0 = R.rms_norm(x, eps=wl.eps, plan=p)
+        torch.cuda.synchronize()
+        ok, rep = parity.compare_y(W.to_numpy_bits(y0), yr, dtype)
+        assert ok, f"plan {p.as_dict()}: {rep}"
+        for rpb in sorted({1, p.rows_per_block // 2 + 1, p.rows_per_block - 1} - {0, p.rows_per_block}):
+            for grid in (None, 3):
+                q = _fewer_rows(p, rpb, rows, grid)
+                y1, h1 = R.rms_norm(x, w=w, residual=r, eps=wl.eps, plan=q)
+                n1 = R.rms_norm(x, eps=wl.eps, plan=q)
+                torch.cuda.synchronize()
+                assert parity.bits_equal(W.to_numpy_bits(y1), W.to_numpy_bits(y0)), q.as_dict()
+                assert parity.bits_equal(W.to_numpy_bits(h1), hr), q.as_dict()
+                assert parity.bits_equal(W.to_numpy_bits(n1), W.to_numpy_bits(n0)), q.as_dict()
+
+
+def test_decode_launches_spread_rows():
+    """Launches of no more rows than SMs plan one row a block for rows of at
+    least a warp; a longer batch fills every slot."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for hidden in (576, 4096):
+        x = torch.empty((1, hidden), device=DEV, dtype=torch.bfloat16)
+        for rows in (1, 8, 64, sms):
+            p = N.rmsnorm_plan_for(x.data_ptr(), None, x.data_ptr(), x.data_ptr(), None, rows, hidden,
+                                   N.RMSNORM_BF16)
+            assert p.rows_per_block == 1 and p.grid == rows, p.as_dict()
+        p = N.rmsnorm_plan_for(x.data_ptr(), None, x.data_ptr(), x.data_ptr(), None, 4 * sms, hidden,
+                               N.RMSNORM_BF16)
+        assert p.rows_per_block == p.block_threads // p.threads_per_row
+
+
 # ------------------------------------------------------------ shape sweep
 
 HIDDENS = [1, 7, 8, 31, 33, 64, 127, 128, 576, 1000, 1024, 1025, 2048, 4096, 8192, 12288,
@@ -317,14 +372,30 @@ def test_deterministic_and_batch_invariant(name):
 @pytest.mark.parametrize("hidden,has_res", [(576, False), (576, True), (5120, False), (12288, True)])
 def test_batch_invariant_across_chunk_fit(hidden, has_res):
     """A launch of many waves takes the chunk count that fits the row exactly
-    (3 or 6), a short one the power of two; a row's bits are the same in both."""
+    (3 or 6), a short one of rows wider than a warp the power of two (rows of
+    a warp or less take the exact fit in every launch); a row's bits are the
+    same in all of them."""
     rows = max(40000 * 576 // hidden, 2000)
     wl = W.Workload("fit", "bf16", rows, hidden, 1e-6, 1.0, 1.0 if has_res else None, 0.1)
     x, r, w = gpu_inputs(wl, seed=hidden + has_res)
     p_big = R.plan_for(x, w=w, residual=r)
     p_small = R.plan_for(x[:13], w=w, residual=None if r is None else r[:13])
     assert p_big.threads_per_row == p_small.threads_per_row
-    assert p_big.chunks_per_thread in (3, 6) and p_small.chunks_per_thread in (4, 8)
+    assert p_big.chunks_per_thread in (3, 6)
+    if p_small.threads_per_row > 32:
+        assert p_small.chunks_per_thread in (4, 8)
+    else:
+        # the power-of-two count, forced, gives the same bits as the exact fit
+        assert p_small.chunks_per_thread in (3, 6)
+        q = p_small.copy()
+        q.chunks_per_thread = 4 if p_small.chunks_per_thread == 3 else 8
+        forced = R.rms_norm(x[:13].contiguous(), w=w, residual=None if r is None else r[:13].contiguous(),
+                            eps=wl.eps, plan=q)
+        lib = R.rms_norm(x[:13].contiguous(), w=w, residual=None if r is None else r[:13].contiguous(), eps=wl.eps)
+        torch.cuda.synchronize()
+        yf = forced[0] if r is not None else forced
+        yl = lib[0] if r is not None else lib
+        assert parity.bits_equal(W.to_numpy_bits(yf), W.to_numpy_bits(yl))
     out = R.rms_norm(x, w=w, residual=r, eps=wl.eps)
     y = out[0] if r is not None else out
     part = R.rms_norm(x[:13].contiguous(), w=w, residual=None if r is None else r[:13].contiguous(), eps=wl.eps)

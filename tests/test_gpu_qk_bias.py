@@ -92,6 +92,14 @@ def test_qk_every_plan(dtype, head_dim, bias):
         ok1, rep1 = parity.compare_y(yb[:, :qc].reshape(qy.shape), qy, dtype)
         ok2, rep2 = parity.compare_y(yb[:, qc:qc + kc].reshape(ky.shape), ky, dtype)
         assert ok1 and ok2, f"plan {p.as_dict()}: {rep1} {rep2}"
+        if p.kernel == N.RMSNORM_KERNEL_REG and p.rows_per_block > 1 and head_dim == 128:
+            # a block holding one head row (of its rows_per_block slots): same bits
+            q = p.copy()
+            q.rows_per_block = 1
+            q.grid = wl.tokens * 6
+            y1 = R.qk_norm(qkv, wl.q_heads, wl.k_heads, head_dim, q_w, k_w, eps=wl.eps, weight_bias=bias, plan=q)
+            torch.cuda.synchronize()
+            assert parity.bits_equal(W.to_numpy_bits(y1), yb), q.as_dict()
     # the library's own plan
     y = R.qk_norm(qkv, wl.q_heads, wl.k_heads, head_dim, q_w, k_w, eps=wl.eps, weight_bias=bias)
     torch.cuda.synchronize()
