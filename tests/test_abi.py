@@ -266,6 +266,23 @@ def test_regime_query_rejects_bad_input_without_cuda():
     assert st in (N.RMSNORM_REGIME_WARP, N.RMSNORM_ECUDA)
 
 
+def test_rows_per_block_validation_without_cuda():
+    """A register plan may hold 1 .. block_threads / threads_per_row rows a
+    block (RMSNorm); 0 or more than its row slots is refused (rows = 0:
+    validation only)."""
+    P = 1 << 20
+    p = R.rmsnorm_plan(4096, 576, N.RMSNORM_BF16, True, 152, 4)
+    assert p.kernel == N.RMSNORM_KERNEL_REG and p.rows_per_block == 8
+    for rpb, want in ((1, N.RMSNORM_OK), (5, N.RMSNORM_OK), (8, N.RMSNORM_OK), (0, N.RMSNORM_EINVAL),
+                      (9, N.RMSNORM_EINVAL), (-1, N.RMSNORM_EINVAL)):
+        q = p.copy()
+        q.rows_per_block = rpb
+        assert N.rmsnorm_fwd_plan_status(P, None, P, P, None, 0, 576, 1e-6, 1, q, 0) == want, rpb
+        h = q.copy()
+        h.chunks_per_thread = 4   # head rows have no odd chunk counts
+        assert N.rmsnorm_qk_fwd_status(P, P, 0, 576, 576, 1, 0, 576, None, None, 0.0, 1e-6, 1, h) == want, rpb
+
+
 def test_plan_rejects_bad_input():
     with pytest.raises(N.RmsNormError):
         R.rmsnorm_plan(-1, 128, 1, True, 152, 1)
