@@ -474,7 +474,7 @@ __device__ __forceinline__ void rms_reg_rows(const Params &p) {
     // before the wait: the block's first row group into L2 (contiguous rows,
     // whose row group is one contiguous range)
     if constexpr (!HEADS) {
-        const int n = p.rpb >= 1 && p.rpb <= RPB ? p.rpb : RPB;
+        const int n = RPB == 1 ? 1 : (p.rpb >= 1 && p.rpb <= RPB ? p.rpb : RPB);
         if (tid == 0) prefetch_rows_l2<RES>(p.x, p.res, p.row_bytes, p.rows, (int64_t)blockIdx.x * n, n);
     }
     pdl_wait_for_inputs();
@@ -496,11 +496,12 @@ __device__ __forceinline__ void rms_reg_rows(const Params &p) {
     // launch has no more rows than the device has SMs (each row then gets an
     // SM of its own; the idle row slots load and store nothing).  Which block
     // takes a row changes no result.
-    const int rpb = p.rpb >= 1 && p.rpb <= RPB ? p.rpb : RPB;   // the host passes 1..RPB
+    // the host passes 1..RPB; a block of one row slot needs no run-time count
+    const int rpb = RPB == 1 ? 1 : (p.rpb >= 1 && p.rpb <= RPB ? p.rpb : RPB);
     const int64_t step = (int64_t)gridDim.x * rpb;
     for (int64_t first = (int64_t)blockIdx.x * rpb; first < p.rows; first += step) {
         const int64_t row = first + slot;
-        const bool row_ok = slot < rpb && row < p.rows;
+        const bool row_ok = (RPB == 1 || slot < rpb) && row < p.rows;
         int64_t off = 0, yoff = 0;
         int wsel = 0;
         if (row_ok) row_offsets<HEADS>(p, row, off, yoff, wsel);
