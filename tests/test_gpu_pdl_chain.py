@@ -52,6 +52,8 @@ def _plans(family, rows, hidden, dtype, x, w, r):
     if family in ("warp", "cta", "tma"):
         want = {"warp": N.RMSNORM_REGIME_WARP, "cta": N.RMSNORM_REGIME_CTA, "tma": N.RMSNORM_REGIME_SMEM}[family]
         assert lib.regime == want, lib.as_dict()
+        if rows <= torch.cuda.get_device_properties(0).multi_processor_count and family != "tma":
+            assert lib.rows_per_block == 1, lib.as_dict()   # the decode spread
         return [lib]
     forced = all_plans(rows, hidden, code, True, odd_ch=True, tma=True)
     full_grid = [p for p in forced if p.grid == -(-rows // p.rows_per_block)]
@@ -75,6 +77,8 @@ CASES = [
     ("warp", "bf16", 8192, 576),
     ("cta", "bf16", 2048, 4096),
     ("cta", "f32", 1024, 2048),
+    ("cta", "bf16", 64, 4096),      # a decode batch: one row a block
+    ("warp", "bf16", 100, 576),     # the same, rows of a warp
     ("tma", "bf16", 300, 40960),
     ("loop", "bf16", 1000, 4096),
     ("mixed", "bf16", 1000, 8192),
