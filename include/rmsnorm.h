@@ -120,11 +120,11 @@ typedef struct {
                                    in one ring piece: 1, 2 or 4 (8, 16 or 32 KB
                                    pieces; 28, 14 or 7 slots of shared memory, of
                                    which avail / 7 (at least 1) go to a streamed
-                                   residual ring; the weight ring gets one slot
-                                   per piece (resident) when that leaves x a row
-                                   and a spare slot, else every slot past one
-                                   spare x slot (at least avail / 7); the rest,
-                                   which must hold a whole row, goes to x)           */
+                                   residual ring; a weight ring gets one slot per
+                                   piece (the weight resident) when that leaves x
+                                   a row and two spare slots, else there is none
+                                   and the weight is read from global memory; the
+                                   rest, which must hold a whole row, goes to x)   */
     int32_t vec_elems;          /* elements per load: 16 / sizeof(T), or 1 (scalar)  */
     int32_t block_threads;      /* threads per block: REG max(threads_per_row, 256),
                                    or max(threads_per_row, 128) for LayerNorm;

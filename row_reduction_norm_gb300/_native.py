@@ -48,13 +48,14 @@ def tma_rings(row_bytes, pc, res, w):
     """(x, residual, weight) ring slots of the bulk-copy kernel for rows of
     ``row_bytes`` and pieces of ``pc`` chunks a thread, or None when the row
     does not fit -- the rule of ``rmsnorm_plan_t.chunks_per_thread``, restated
-    so tests can tell which forced plans are valid."""
+    so tests can tell which forced plans are valid.  A weight slot count of 0
+    with a weight means the kernel reads the weight from global memory."""
     piece = 512 * 16 * pc
     avail = min(32, (_TMA_SMEM_BUDGET - _TMA_BAR_BYTES) // piece)
     pieces = -(-row_bytes // piece)
     streamed = max(1, avail // 7)
     sr = streamed if res else 0
-    sw = (pieces if avail - sr - pieces >= pieces + 1 else max(streamed, avail - sr - pieces - 1)) if w else 0
+    sw = pieces if (w and avail - sr - pieces >= pieces + 2) else 0
     sx = avail - sr - sw
     return (sx, sr, sw) if sx >= pieces else None
 

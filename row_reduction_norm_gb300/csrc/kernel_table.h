@@ -58,10 +58,12 @@ constexpr int kTmaMaxSlots = 32;
 constexpr int kTmaBarBytes = 2 * kTmaMaxSlots * 8;
 constexpr int tma_piece_bytes(int pc) { return kTmaGT * 16 * pc; }
 constexpr int tma_smem_bytes(int pc, int slots) { return kTmaBarBytes + slots * tma_piece_bytes(pc); }
-const void *tma_kernel(int dtype, int pc, bool res, int wm);
+// wg: the weight is read from global memory (no weight ring) rather than
+// held resident in shared memory.
+const void *tma_kernel(int dtype, int pc, bool res, int wm, bool wg);
 // The same kernel with an MXFP8 (out 1: f32, bf16) or NVFP4 (out 2: bf16)
 // output, 16 KB pieces (pc 2).
-const void *tma_quant_kernel(int dtype, bool res, int wm, int out);
+const void *tma_quant_kernel(int dtype, bool res, int wm, int out, bool wg);
 // Reads the count of blocks whose bounded waits ran out (current device); 0 or -1.
 int tma_timeouts_read(unsigned int *out);
 

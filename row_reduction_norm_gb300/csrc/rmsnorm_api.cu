@@ -74,10 +74,13 @@ struct TmaRings {
 
 // Ring sizes for rows of row_bytes with pieces of pc chunks a thread: the
 // slots that fit the shared-memory budget are shared out as a streamed ring
-// of avail / 7 slots (at least 1) for the residual; for the weight, one slot
-// per piece (resident) when the x ring still gets a row and a spare slot,
-// else every slot past one spare x slot (at least avail / 7); the rest for x.
-// False when the x ring cannot hold a whole row.
+// of avail / 7 slots (at least 1) for the residual; a weight ring holding the
+// whole weight (one slot a piece) when the x ring still keeps a row and two
+// spare slots beside it, else no weight ring (the kernel reads the weight
+// from global memory: measured on GB300, bf16 2048 x 65536 without a residual
+// 0.92 -> 0.96 of peak against a weight streamed through a ring, 2730 x 49152
+// 0.93 -> 0.97 against a resident weight that left x one spare slot); the
+// rest for x.  False when the x ring cannot hold a whole row.
 bool tma_rings(int64_t row_bytes, int pc, bool res, bool w, TmaRings *out) {
     const int piece = rrn::tma_piece_bytes(pc);
     int avail = (kTmaSmemBudget - rrn::kTmaBarBytes) / piece;
@@ -86,14 +89,7 @@ bool tma_rings(int64_t row_bytes, int pc, bool res, bool w, TmaRings *out) {
     const int streamed = avail / 7 > 0 ? avail / 7 : 1;
     TmaRings R;
     R.sr = res ? streamed : 0;
-    if (w) {
-        // resident when a copy fits beside a row and a spare x slot; else
-        // streamed through every slot past that spare slot (at least
-        // `streamed`): measured on GB300, bf16 65536 without a residual 0.80
-        // -> 0.92 of peak against a weight ring of avail / 7 slots
-        const int64_t rest = avail - R.sr - pieces - 1;
-        R.sw = (avail - R.sr - pieces >= pieces + 1) ? (int)pieces : (int)(rest > streamed ? rest : streamed);
-    }
+    R.sw = (w && avail - R.sr - pieces >= pieces + 2) ? (int)pieces : 0;
     R.sx = avail - R.sr - R.sw;
     if (R.sx < pieces) return false;
     if (out) *out = R;
@@ -171,11 +167,11 @@ void schedule(int64_t hidden, int dtype, int vec_ok, int max_gt, rmsnorm_plan_t 
         TmaRings tr;
         int tma_pc = 0;
         if (tma_ok && nch > kRegWideUnits) {
-            if (tma_rings(row_bytes, kTmaPlanPC, true, true, &tr) &&
-                tr.sw >= ceil_div(row_bytes, rrn::tma_piece_bytes(kTmaPlanPC)))
+            if (tma_rings(row_bytes, kTmaPlanPC, true, true, &tr) && tr.sw > 0)
                 tma_pc = (!has_res && dtype == RMSNORM_BF16) ? kTmaLongPC : kTmaPlanPC;
-            else if (!has_res && tma_rings(row_bytes, kTmaLongPC, false, true, nullptr))
-                tma_pc = kTmaLongPC;
+            else if (!has_res && tma_rings(row_bytes, kTmaLongPC, false, true, &tr) &&
+                     tr.sx > ceil_div(row_bytes, rrn::tma_piece_bytes(kTmaLongPC)))
+                tma_pc = kTmaLongPC;   // planned while x keeps a spare slot (rows up to 192 KB)
         }
         if (tma_pc > 0) {
             p->kernel = RMSNORM_KERNEL_TMA;
@@ -307,11 +303,16 @@ const void *kernel_of(const rmsnorm_plan_t *p, const Op &o) {
     const bool res = o.res != nullptr;
     if (p->kernel == RMSNORM_KERNEL_TMA) {
         if (o.ln || o.head_rows) return nullptr;
+        // the weight from global memory when the rings give it no slots
+        TmaRings R;
+        if (!tma_rings(o.row_elems * elem_size(o.dtype), p->chunks_per_thread, res, o.w != nullptr, &R))
+            return nullptr;
+        const bool wg = o.w != nullptr && R.sw == 0;
         if (o.mx || o.nv)
             return p->chunks_per_thread == 2 ? rrn::tma_quant_kernel(o.dtype, res, o.wm, o.mx ? rrn::kOutMxfp8
-                                                                                              : rrn::kOutNvfp4)
+                                                                                              : rrn::kOutNvfp4, wg)
                                              : nullptr;
-        return rrn::tma_kernel(o.dtype, p->chunks_per_thread, res, o.wm);
+        return rrn::tma_kernel(o.dtype, p->chunks_per_thread, res, o.wm, wg);
     }
     if (o.mx || o.nv) {
         if (p->kernel != RMSNORM_KERNEL_REG) return nullptr;

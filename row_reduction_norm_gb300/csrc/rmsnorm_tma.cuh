@@ -16,8 +16,18 @@
 //
 // Block: 16 consumer warps (512 threads) and three producer warps.  A row is
 // cut into pieces of 512 x 16 x PC bytes (the last one shorter); piece k holds
-// the chunks c = k*PC .. k*PC + PC - 1 of every consumer thread.  Three rings
-// of pieces share the block's shared memory: x, the residual and the weight.
+// the chunks c = k*PC .. k*PC + PC - 1 of every consumer thread.  Up to three
+// rings of pieces share the block's shared memory: x, the residual and the
+// weight.  The weight ring, when there is one, holds the whole weight (one
+// slot a piece, copied once per block and never released); when the slots
+// are better spent on x (long rows: the x ring then keeps fewer than two
+// spare slots beside a resident weight), there is no weight ring and the
+// consumers read the weight's chunks straight from global memory, where
+// every block after the first finds them in L2 (measured on GB300, bf16
+// 2048 x 65536 without a residual 0.92 -> 0.96 of the measured peak against
+// a weight streamed through a ring, 2730 x 49152 0.93 -> 0.97 against a
+// resident weight with one spare x slot; with two or more spare slots the
+// resident weight is faster: 4096 x 32768 1.03 against 0.90).
 // Each slot has a "full" mbarrier (the producer's arrival plus the copy's
 // byte count) and an "empty" mbarrier (one arrival per consumer warp).  One
 // lane of each producer warp walks the block's rows (blockIdx.x, + gridDim.x,
@@ -27,12 +37,13 @@
 // pass 1 waits for each x piece (and residual piece), adds the residual (the
 // sum is written back into the x piece and out as residual_out), accumulates
 // the squares and releases the residual slot; after the row's reduction,
-// pass 2 waits for each weight piece, scales, writes y and releases the x and
-// weight slots.  When the weight ring has a slot per piece, the weight is
-// copied once per block and stays.  As long as the x ring has a slot for
+// pass 2 waits for each weight piece (when the weight has a ring), scales,
+// writes y and releases the x slot (and a streamed weight slot).  As long as
+// the x ring has a slot for
 // every piece of a row, no producer is ever blocked by the row being
 // reduced, and the next rows stream in while this row is scaled.  Both passes
-// read shared memory only, so no warp waits on an L2 or HBM round trip.
+// read x and the residual from shared memory only, so no warp waits on an HBM
+// round trip (the weight, when it is not resident, comes from L2).
 //
 // Every wait is bounded (Params::wait_ns on the globaltimer, one second in
 // every library launch).  A wait that runs out marks the thread failed; a
@@ -177,15 +188,19 @@ __device__ __forceinline__ void drain_ring(const Ring &R, unsigned issued, unsig
 }
 
 // sx, sr, sw: slots of the x, residual and weight rings (sr = 0 without a
-// residual, sw = 0 without a weight).  sx >= pieces; sw >= pieces makes the
-// weight resident (copied once per block, never released).
+// residual, sw = 0 without a weight ring).  sx >= pieces; sw >= pieces makes
+// the weight resident (copied once per block, never released); fewer weight
+// slots stream it.  WG: there is no weight ring, the consumers read the
+// weight from global memory (the library plans resident weights and WG; the
+// streaming form is kept for any other split a caller might pass).
 // OUT: kOutT writes y in the I/O type; kOutMxfp8 / kOutNvfp4 write the
 // block-scaled codes and scales (the register kernel's epilogue, with the
 // same lane layout: a block's chunks sit in consecutive threads of a piece).
-template <typename T, bool RES, int WM, int PC, int OUT = kOutT>
+template <typename T, bool RES, int WM, int PC, int OUT = kOutT, bool WG = false>
 __global__ void __launch_bounds__(kTmaBlock, 1)
 rms_tma_kernel(const Params p, const int sx, const int sr, const int sw) {
     constexpr bool W = WM != kNoWeight;
+    constexpr bool WR = W && !WG;   // the weight comes through a ring
     constexpr int V = T::kVec;
     constexpr int GT = kTmaGT;
     constexpr int PIECE = kTmaGT * 16 * PC;   // tma_piece_bytes(PC)
@@ -207,6 +222,14 @@ rms_tma_kernel(const Params p, const int sx, const int sr, const int sw) {
     const int64_t row_bytes = p.row_bytes;
     const int pieces = (int)((row_bytes + PIECE - 1) / PIECE);
     const bool w_resident = sw >= pieces;
+    if constexpr (WR) {
+        // a weight ring needs a slot: without one, count the launch as failed
+        // and touch nothing (every thread leaves here, before any barrier)
+        if (sw < 1) {
+            if (threadIdx.x == 0) atomicAdd(&g_tma_timeouts, 1u);
+            return;
+        }
+    }
 
     if (tid == 0) {
         for (int s = 0; s < sx + sr + sw; ++s) {
@@ -236,7 +259,7 @@ rms_tma_kernel(const Params p, const int sx, const int sr, const int sw) {
             else if (role == 1 && RES)
                 ok = feed_ring<PIECE>(Rr, static_cast<const char *>(p.res), row_bytes, p, pieces, row_bytes, false,
                                       issued);
-            else if (role == 2 && W)
+            else if (role == 2 && WR)
                 ok = feed_ring<PIECE>(Wr, static_cast<const char *>(p.w), 0, p, pieces, row_bytes, w_resident,
                                       issued);
             s_issued[role] = issued;
@@ -321,7 +344,7 @@ rms_tma_kernel(const Params p, const int sx, const int sr, const int sw) {
                 unsigned char *xp = X.mem + (size_t)xs * PIECE;
                 unsigned ws = 0;
                 const unsigned char *wp = nullptr;
-                if constexpr (W) {
+                if constexpr (WR) {
                     ws = w_resident ? (unsigned)k : qw % Wr.n;
                     const unsigned wpar = w_resident ? 0u : (qw / Wr.n) & 1u;
                     if (ok) ok = mbar_wait_bounded(&Wr.full[ws], wpar, p.wait_ns);
@@ -334,7 +357,10 @@ rms_tma_kernel(const Params p, const int sx, const int sr, const int sw) {
                         const int so = (j * GT + t) * 16;
                         if ((k * PC + j) * GT + t < nch) {
                             xa[j] = lds16(xp + so);
-                            if constexpr (W) wa[j] = lds16(wp + so);
+                            if constexpr (WR)
+                                wa[j] = lds16(wp + so);
+                            else if constexpr (W)   // the weight from global memory (L2)
+                                wa[j] = ld_readonly16(static_cast<const char *>(p.w) + (int64_t)((k * PC + j) * GT + t) * 16);
                         }
                     }
                 }
@@ -365,7 +391,10 @@ rms_tma_kernel(const Params p, const int sx, const int sr, const int sw) {
                         for (int e = 0; e < V; ++e) a[e] = 0.f, wv[e] = 1.f;
                         if (valid) {
                             unpack(lds16(xp + so), a, T{});
-                            if constexpr (W) unpack(lds16(wp + so), wv, T{});
+                            if constexpr (WR)
+                                unpack(lds16(wp + so), wv, T{});
+                            else if constexpr (W)
+                                unpack(ld_readonly16(static_cast<const char *>(p.w) + (int64_t)u * 16), wv, T{});
                         }
                         scale_out_pairs<WM>(a, r, wv, p.w_bias);
                         store_quantised<V, OUT>(a, valid, p, row, u, t);
@@ -378,9 +407,9 @@ rms_tma_kernel(const Params p, const int sx, const int sr, const int sw) {
                 if (lane == 0 && ok) {
                     if (!(p.withhold && blockIdx.x == 0 && warp == 0 && qx + (unsigned)k == 0u))
                         mbar_arrive(&X.empty[xs]);
-                    if (W && !w_resident) mbar_arrive(&Wr.empty[ws]);
+                    if (WR && !w_resident) mbar_arrive(&Wr.empty[ws]);
                 }
-                if (W && !w_resident) ++qw;
+                if (WR && !w_resident) ++qw;
             }
             qx += (unsigned)pieces;
         }
@@ -393,7 +422,7 @@ rms_tma_kernel(const Params p, const int sx, const int sr, const int sw) {
         // no copy may land after the block has left
         drain_ring(X, s_issued[0], p.wait_ns);
         if (RES) drain_ring(Rr, s_issued[1], p.wait_ns);
-        if (W) drain_ring(Wr, s_issued[2], p.wait_ns);
+        if (WR) drain_ring(Wr, s_issued[2], p.wait_ns);
     }
 }
 

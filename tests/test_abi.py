@@ -184,12 +184,18 @@ def test_tma_plan_validation_without_cuda():
         setattr(q, field, value)
         assert st(q) == N.RMSNORM_EINVAL, field
     # 65536 fp32 (256 KB) does not fit the x ring; 57344 fp32 (224 KB) fits it
-    # only without a residual and a weight
+    # only without a residual (a weight then takes no slot: it is read from
+    # global memory)
     q = good.copy()
     q.vec_elems = 4
     assert st(q, hidden=65536, dtype=N.RMSNORM_F32) == N.RMSNORM_EINVAL
-    for res, status in ((None, N.RMSNORM_OK), (P, N.RMSNORM_EINVAL)):   # rows = 0: validation only
-        assert N.rmsnorm_fwd_plan_status(P, res, None, P, res, 0, 57344, 1e-6, N.RMSNORM_F32, q, 0) == status
+    for res, w, status in ((None, None, N.RMSNORM_OK), (None, P, N.RMSNORM_OK), (P, None, N.RMSNORM_EINVAL),
+                           (P, P, N.RMSNORM_EINVAL)):   # rows = 0: validation only
+        assert N.rmsnorm_fwd_plan_status(P, res, w, P, res, 0, 57344, 1e-6, N.RMSNORM_F32, q, 0) == status
+    assert N.tma_rings(57344 * 4, 4, False, True) == (7, 0, 0)        # no weight ring
+    assert N.tma_rings(65536 * 2, 4, False, True) == (7, 0, 0)
+    assert N.tma_rings(32768 * 2, 4, False, True) == (5, 0, 2)        # resident: two spare x slots
+    assert N.tma_rings(40960 * 2, 2, True, True) == (7, 2, 5)
     # 32 KB pieces: 7 slots, 40000 bf16 (80 KB) fits, a misaligned x does not
     q = good.copy()
     q.chunks_per_thread = 4

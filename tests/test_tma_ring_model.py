@@ -1,11 +1,13 @@
 """A CPU model of the bulk-copy kernel's ring protocol (rmsnorm_tma.cuh).
 
-The model follows the kernel's walk: three producer lanes (x, residual,
-weight) each copy piece k of the block's rows, in order, into the next slot of
-their ring once that slot's "empty" barrier has completed the phase before;
-16 consumer warps wait on each piece's "full" barrier (arrival + byte count),
-release residual slots after pass 1 and x / weight slots after pass 2, with a
-barrier over the consumer warps between the passes.  Copies land after random
+The model follows the kernel's walk: producer lanes for x and the residual
+each copy piece k of the block's rows, in order, into the next slot of their
+ring once that slot's "empty" barrier has completed the phase before, and a
+third copies the weight once into its own slots when it is resident (else the
+consumers read it from global memory); 16 consumer warps wait on each
+piece's "full" barrier (arrival + byte count), release residual slots after
+pass 1 and x slots after pass 2, with a barrier over the consumer warps
+between the passes.  Copies land after random
 delays and actors run in random order.  For every ring split the library can
 choose (``_native.tma_rings``, itself checked against the library's plan
 validation in test_abi.py) it checks:
@@ -96,7 +98,8 @@ def walk(rows, hidden, esz, pc, grid, block, res, w, seed, budget=None, withhold
     readers = [set() for _ in range(total)]
     inflight = []
     my_rows = list(range(block, rows, grid))
-    w_resident = sw >= pieces
+    w_resident = w and sw >= pieces    # else the kernel reads the weight from global memory
+    assert sw in (0, pieces), "a weight ring holds the whole weight or there is none"
     base = {"x": 0, "r": sx, "w": sx + sr}
     size = {"x": sx, "r": max(sr, 1), "w": max(sw, 1)}
 
@@ -164,7 +167,7 @@ def walk(rows, hidden, esz, pc, grid, block, res, w, seed, budget=None, withhold
                     assert so + 16 <= min(piece, row_bytes - k * piece)
 
     def consumer(wid):
-        qx = qr = qw = 0
+        qx = qr = 0
         st = {"ok": True}
         for ri, row in enumerate(my_rows):
             for k in range(pieces):                       # pass 1
@@ -189,25 +192,27 @@ def walk(rows, hidden, esz, pc, grid, block, res, w, seed, budget=None, withhold
                 g = (qx + k) % sx
                 if st["ok"]:
                     assert content[g] == ("x", row, k)
-                gw = None
-                if w:
-                    gw = sx + sr + (k if w_resident else qw % sw)
-                    yield from wait_full(gw, 0 if w_resident else (qw // sw) & 1, st)
+                if w_resident:
+                    gw = sx + sr + k
+                    yield from wait_full(gw, 0, st)
                     if st["ok"]:
-                        assert landed[gw] and content[gw] == ("w", None if w_resident else row, k)
+                        assert landed[gw] and content[gw] == ("w", None, k)
                         reads(gw, k, wid)
+                elif w:
+                    for t in range(wid * 32, wid * 32 + 32):   # the weight's chunks, straight from global memory
+                        for j in range(pc):
+                            u = (k * pc + j) * GT + t
+                            if u < nch:
+                                assert (u + 1) * 16 <= row_bytes
                 release(g, wid, st, withheld=withhold and wid == 0 and qx + k == 0)
-                if w and not w_resident:
-                    release(gw, wid, st)
-                    qw += 1
                 yield
             qx += pieces
 
     actors = [producer("x", False)]
     if res:
         actors.append(producer("r", False))
-    if w:
-        actors.append(producer("w", w_resident))
+    if w_resident:
+        actors.append(producer("w", True))
     actors += [consumer(i) for i in range(WARPS)]
     alive = [True] * len(actors)
     steps = 0
@@ -263,8 +268,8 @@ def test_ring_protocol_model(esz, hidden, pc):
 
 
 def test_model_covers_every_ring_split():
-    """Both weight modes (resident, streamed), with and without a residual,
-    occur among the shapes above for every piece size."""
+    """Both weight modes (resident, read from global memory), with and without
+    a residual, occur among the shapes above for every piece size."""
     seen = set()
     for esz, hidden in SHAPES:
         for pc in N.TMA_PIECE_CHUNKS:
