@@ -49,6 +49,10 @@ def _plans(family, rows, hidden, dtype, x, w, r):
     code = N.RMSNORM_BF16 if dtype == "bf16" else N.RMSNORM_F32
     lib = R.plan_for(x, w=w, residual=r, out=torch.empty_like(x), residual_out=None if r is None else
                      torch.empty_like(x))
+    if family == "long":   # past 80 KB: the bulk-copy kernel (weight from L2), or two passes with a residual
+        want = N.RMSNORM_REGIME_LOOPED if r is not None else N.RMSNORM_REGIME_SMEM
+        assert lib.regime == want, lib.as_dict()
+        return [lib]
     if family in ("warp", "cta", "tma"):
         want = {"warp": N.RMSNORM_REGIME_WARP, "cta": N.RMSNORM_REGIME_CTA, "tma": N.RMSNORM_REGIME_SMEM}[family]
         assert lib.regime == want, lib.as_dict()
@@ -80,6 +84,7 @@ CASES = [
     ("cta", "bf16", 64, 4096),      # a decode batch: one row a block
     ("warp", "bf16", 100, 576),     # the same, rows of a warp
     ("tma", "bf16", 300, 40960),
+    ("long", "bf16", 200, 49152),
     ("loop", "bf16", 1000, 4096),
     ("mixed", "bf16", 1000, 8192),
 ]

@@ -46,10 +46,11 @@ def _hook(x, r, w, y, h, plan, withhold, eps, limit=LIMIT_NS):
                                           eps, N.RMSNORM_BF16, plan, limit, withhold, s.cuda_stream)
 
 
-@pytest.mark.parametrize("has_res", [False, True], ids=["plain", "residual"])
-def test_withheld_slot_times_out_and_the_next_launch_is_right(has_res):
+@pytest.mark.parametrize("has_res,hidden", [(False, 40960), (True, 40960), (False, 49152)],
+                         ids=["plain", "residual", "weight-from-L2"])
+def test_withheld_slot_times_out_and_the_next_launch_is_right(has_res, hidden):
     rows, grid = 12, 3
-    wl = W.Workload("wait", "bf16", rows, 40960, 1e-6, 1.0, 1.0 if has_res else None, 0.1)
+    wl = W.Workload("wait", "bf16", rows, hidden, 1e-6, 1.0, 1.0 if has_res else None, 0.1)
     x, r, w = W.make_inputs(wl, seed=21, device=DEV)
     y = torch.empty_like(x)
     h = torch.empty_like(x) if has_res else None
