@@ -131,9 +131,10 @@ typedef struct {
                                    LOOP: threads_per_row; TMA: 608                    */
     int32_t rows_per_block;     /* rows one block handles per loop iteration: REG
                                    block_threads / threads_per_row, or (RMSNorm only)
-                                   fewer, down to 1; planning takes 1 when the launch
-                                   has no more rows than the device has SMs, so each
-                                   row has a block of its own; other kernels 1     */
+                                   fewer, down to 1; planning takes one warp of rows
+                                   a block (1 for rows of 32 threads or more) when
+                                   that needs no more blocks than the device has
+                                   SMs (decode batches); other kernels 1           */
     int32_t persistent;         /* 1 if grid < row blocks (blocks stride over rows)   */
     int32_t pdl;                /* 1: launch with programmatic stream serialisation
                                    (the kernel may start while the previous kernel on

@@ -265,23 +265,30 @@ void fit_chunks(int64_t rows, int64_t resident_blocks, bool contiguous_rms, int6
     p->chunks_per_thread = exact_ch(units, p->threads_per_row, p->chunks_per_thread);
 }
 
-// Launches with no more rows than the device has SMs (decode batches) give
-// every row a block of its own, so the rows spread over as many SMs as they
-// can (the RMSNorm register kernel holds a run-time count of rows a block;
-// the idle row slots of a block load and store nothing).  Measured on GB300,
-// bf16 rows of 4096: 8 rows 1.66 -> 1.62 us, 64 rows 1.82 -> 1.71 us; rows of
-// 576: 8 rows 1.45 -> 1.34 us, 64 rows 1.53 -> 1.38 us; a single row is the
-// same.  The per-row schedule is unchanged, so no result changes.  Planned
-// for contiguous RMSNorm rows of at least a warp (what was measured); forced
-// plans may hold fewer rows a block on every RMSNorm register kernel.
+// Decode batches -- launches whose rows fit in one warp of row slots a block
+// without needing more blocks than the device has SMs -- hold one warp of
+// rows a block (one row for rows of a warp or more, 32 / threads_per_row
+// rows below), so the rows spread over as many SMs as they can (the register
+// kernel takes a run-time count of rows a block; the idle row slots load and
+// store nothing).  The page's decode variant is one warp a block while fewer
+// warps than SMs are needed; measured on GB300: bf16 rows of 4096, 8 rows
+// 1.66 -> 1.62 us, 64 rows 1.82 -> 1.71 us; rows of 576, 8 rows 1.45 -> 1.34
+// us, 64 rows 1.53 -> 1.38 us; fp32 64 x 256 (16 threads a row) 1.40 -> 1.26
+// us; bf16 64 x 128 (4 threads a row) 1.48 -> 1.27 us; a single row the same.
+// The per-row schedule is unchanged, so no result changes.  Planned for
+// contiguous RMSNorm rows (what was measured); forced plans may hold fewer
+// rows a block on every RMSNorm register kernel.
 void spread_rows(int64_t rows, int sm_count, bool contiguous_rms, rmsnorm_plan_t *p) {
-    if (!contiguous_rms || p->kernel != RMSNORM_KERNEL_REG || p->threads_per_row < 32 || p->rows_per_block <= 1)
-        return;
-    if (rows < 1 || rows > (int64_t)(sm_count > 0 ? sm_count : 1)) return;
-    p->rows_per_block = 1;
-    p->grid = rows;
+    if (!contiguous_rms || p->kernel != RMSNORM_KERNEL_REG) return;
+    const int gt = p->threads_per_row;
+    const int want = gt >= 32 ? 1 : 32 / gt;   // one warp of rows a block
+    if (want >= p->rows_per_block || rows < 1) return;
+    const int64_t blocks = ceil_div(rows, want);
+    if (blocks > (int64_t)(sm_count > 0 ? sm_count : 1)) return;
+    p->rows_per_block = want;
+    p->grid = blocks;
     p->persistent = 0;
-    if (p->regime == RMSNORM_REGIME_PERSISTENT) p->regime = p->threads_per_row <= 32 ? RMSNORM_REGIME_WARP : RMSNORM_REGIME_CTA;
+    if (p->regime == RMSNORM_REGIME_PERSISTENT) p->regime = gt <= 32 ? RMSNORM_REGIME_WARP : RMSNORM_REGIME_CTA;
 }
 
 size_t dyn_smem_of(const rmsnorm_plan_t *p, const Op &o) {

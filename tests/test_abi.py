@@ -119,9 +119,10 @@ def test_plan_properties(dtype, hidden):
                 assert gt * ch * V >= hidden and gt & (gt - 1) == 0 and 4 <= gt <= 512
                 assert ch in (1, 2, 3, 4, 6, 8)
                 assert p.block_threads == max(gt, 256)
-                # one row a block when the launch has no more rows than SMs (rows of a warp or more)
-                spread = rows <= 152 and gt >= 32
-                assert p.rows_per_block == (1 if spread else p.block_threads // gt), (rows, p)
+                # decode batches: one warp of rows a block while that needs no more blocks than SMs
+                want = 1 if gt >= 32 else 32 // gt
+                spread = -(-rows // want) <= 152 and want < p.block_threads // gt
+                assert p.rows_per_block == (want if spread else p.block_threads // gt), (rows, p)
                 want = (N.RMSNORM_REGIME_PERSISTENT if p.persistent else
                         N.RMSNORM_REGIME_WARP if gt <= 32 else N.RMSNORM_REGIME_CTA)
                 assert p.regime == want

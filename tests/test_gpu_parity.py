@@ -224,16 +224,18 @@ def test_rows_per_block_changes_no_bit(rows, hidden, dtype):
 
 
 def test_decode_launches_spread_rows():
-    """Launches of no more rows than SMs plan one row a block for rows of at
-    least a warp; a longer batch fills every slot."""
+    """Decode batches hold one warp of rows a block (one row for rows of a
+    warp or more, 32 / threads_per_row below) while that needs no more blocks
+    than SMs; a longer batch fills every slot."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    for hidden in (576, 4096):
+    for hidden, per_warp in ((576, 1), (4096, 1), (128, 8), (256, 4)):
         x = torch.empty((1, hidden), device=DEV, dtype=torch.bfloat16)
         for rows in (1, 8, 64, sms):
             p = N.rmsnorm_plan_for(x.data_ptr(), None, x.data_ptr(), x.data_ptr(), None, rows, hidden,
                                    N.RMSNORM_BF16)
-            assert p.rows_per_block == 1 and p.grid == rows, p.as_dict()
-        p = N.rmsnorm_plan_for(x.data_ptr(), None, x.data_ptr(), x.data_ptr(), None, 4 * sms, hidden,
+            assert p.rows_per_block == min(per_warp, p.block_threads // p.threads_per_row), p.as_dict()
+            assert p.grid == -(-rows // p.rows_per_block), p.as_dict()
+        p = N.rmsnorm_plan_for(x.data_ptr(), None, x.data_ptr(), x.data_ptr(), None, 40 * sms, hidden,
                                N.RMSNORM_BF16)
         assert p.rows_per_block == p.block_threads // p.threads_per_row
 
