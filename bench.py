@@ -20,8 +20,10 @@ launching stream bracket exactly K steps, with a barrier and a device
 synchronise on both sides; nvidia-smi samples clocks during the timed region
 and the half second of identical launches just before it.  ``e2e`` repeats
 the measurement with the inputs copied from pinned host memory and the
-outputs read back every step.  The CPU baseline is the fp64 oracle on the
-host cores over a bounded sample of the headline's rows.
+outputs read back every step, beside the host link's own rate for the same
+copies with no launch (``link_gbs``), which bounds it.  The CPU baseline is
+the fp64 oracle on the host cores over a bounded sample of the headline's
+rows.
 
 Under torchrun each rank runs its own replica on its own GPU (the op has no
 exchange between rows, so there is no collective on the data path); the
@@ -78,6 +80,8 @@ def parse_args(argv=None):
                     help="profiling mode: force this grid (blocks stride over row groups)")
     ap.add_argument("--misalign", action="store_true",
                     help="profiling mode: offset every tensor by one element (scalar path)")
+    ap.add_argument("--plan", default="",
+                    help="profiling mode: JSON object of plan fields set over the library's plan")
     return ap.parse_args(argv)
 
 
@@ -558,6 +562,56 @@ def time_launches(L, steps, warmup, barrier=None, sampler_window=None, graph_len
     return ev0.elapsed_time(ev1)
 
 
+def host_buffers(L):
+    """Pinned host copies of buffer set 0's inputs (x, residual, w) and pinned
+    host outputs (y, residual_out), with the bytes each step moves each way."""
+    import torch
+    x, r, y, h = L.sets[0]
+    hx = x.cpu().pin_memory()
+    hr = None if r is None else r.cpu().pin_memory()
+    hw = None if L.w is None else L.w.cpu().pin_memory()
+    hy = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+    hh = None if h is None else torch.empty(h.shape, dtype=h.dtype).pin_memory()
+    nbytes = lambda t: 0 if t is None else t.numel() * t.element_size()
+    return hx, hr, hw, hy, hh, nbytes(hx) + nbytes(hr) + nbytes(hw), nbytes(hy) + nbytes(hh)
+
+
+def host_link_gbs(L, reps=5):
+    """The host link's rate for one step's copies alone: the uploads of x,
+    residual and w into buffer set 0 on one stream while the read-backs of y
+    and residual_out from buffer set 1 run on another, no launch between;
+    (h2d + d2h bytes) / median time, GB/s.  It bounds the end-to-end rate,
+    which moves the same bytes each step."""
+    import torch
+    hx, hr, hw, hy, hh, h2d, d2h = host_buffers(L)
+    xd, rd, _, _ = L.sets[0]
+    _, _, yd, hd = L.sets[min(1, L.n_sets - 1)]
+    wd = None if L.w is None else torch.empty_like(L.w)
+    s_k = L.stream
+    s_up, s_dn = torch.cuda.Stream(s_k.device), torch.cuda.Stream(s_k.device)
+    times = []
+    for _ in range(reps + 1):
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s_k)
+        s_up.wait_stream(s_k)
+        s_dn.wait_stream(s_k)
+        with torch.cuda.stream(s_up):
+            for dst, src in ((xd, hx), (rd, hr), (wd, hw)):
+                if dst is not None:
+                    dst.copy_(src, non_blocking=True)
+        with torch.cuda.stream(s_dn):
+            for dst, src in ((hy, yd), (hh, hd)):
+                if dst is not None:
+                    dst.copy_(src, non_blocking=True)
+        s_k.wait_stream(s_up)
+        s_k.wait_stream(s_dn)
+        e1.record(s_k)
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    return (h2d + d2h) / statistics.median(times[1:]) / 1e6
+
+
 def time_e2e(L, steps, pipelined=True):
     """End-to-end steps through the public call: every step copies its inputs
     (x, residual, w) from pinned host memory to the device, launches, and reads
@@ -567,15 +621,7 @@ def time_e2e(L, steps, pipelined=True):
     slots are reused only after their previous read-back finished).  Returns
     (ms for `steps` steps, h2d bytes per step, d2h bytes per step)."""
     import torch
-    x, r, y, h = L.sets[0]
-    hx = x.cpu().pin_memory()
-    hr = None if r is None else r.cpu().pin_memory()
-    hw = None if L.w is None else L.w.cpu().pin_memory()
-    hy = torch.empty(y.shape, dtype=y.dtype).pin_memory()
-    hh = None if h is None else torch.empty(h.shape, dtype=h.dtype).pin_memory()
-    h2d = hx.numel() * hx.element_size() + (0 if hr is None else hr.numel() * hr.element_size()) + \
-        (0 if hw is None else hw.numel() * hw.element_size())
-    d2h = hy.numel() * hy.element_size() + (0 if hh is None else hh.numel() * hh.element_size())
+    hx, hr, hw, hy, hh, h2d, d2h = host_buffers(L)
     nbuf = min(L.n_sets, 4) if pipelined else 1
     s_k = L.stream
     s_up = torch.cuda.Stream(s_k.device) if nbuf > 1 else s_k
@@ -772,6 +818,8 @@ def plan_summary(p):
            "block": d["block_threads"], "grid": d["grid"]}
     if d["rows_per_block"] != max(1, d["block_threads"] // max(1, d["threads_per_row"])):
         out["rows_per_block"] = d["rows_per_block"]     # fewer rows a block than row slots
+    if d["cluster_ctas"]:
+        out["cluster_ctas"] = d["cluster_ctas"]         # blocks of a cluster that share a row
     return out
 
 
@@ -931,6 +979,7 @@ def run_ours(args):
     e2e_value, _ = aggregate(world, launch_bytes, wl.rows, e2e_steps, reduce_max(e_ms, dist, device))
     s_ms, _, _ = time_e2e(LE, e2e_steps, pipelined=False)
     e2e_serial, _ = aggregate(world, launch_bytes, wl.rows, e2e_steps, reduce_max(s_ms, dist, device))
+    link = host_link_gbs(LE)
 
     cpu = None
     if rank == 0 and world == 1 and args.cpu_seconds > 0:
@@ -1022,6 +1071,9 @@ def run_ours(args):
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "serial_value": round(e2e_serial, 2),
+                "link_gbs": round(link, 2), "frac_of_link": round(e2e_value / world / link, 4),
+                "link_what": "one step's uploads and read-backs alone, the two directions concurrent on two "
+                             "streams, no launch (median of 5, same process, just after the e2e region)",
                 "what": "every step: pinned host -> device copy of its inputs (x, residual, w), the C-ABI launch, "
                         "device -> pinned host copy of y and residual_out; uploads, launches and read-backs "
                         "pipelined on three streams over 2 device buffer sets (serial_value: one stream, no "
@@ -1098,6 +1150,11 @@ def run_profile_case(args, device, stream):
     y = shifted(torch.empty_like(x))
     h = None if r is None else shifted(torch.empty_like(x))
     plan = api.plan_for(x, w=w, residual=r, out=y, residual_out=h)
+    if args.plan:
+        # fields of another kernel family's plan over the library's (that
+        # family on this workload; the library validates the result)
+        for k, v in json.loads(args.plan).items():
+            setattr(plan, k, v)
     if args.grid:
         plan.grid = args.grid
         plan.persistent = 1

@@ -76,13 +76,19 @@ enum {
 enum {
     RMSNORM_KERNEL_REG = 0,   /* row held in registers, 128-bit I/O, one pass     */
     RMSNORM_KERNEL_LOOP = 1,  /* row streamed twice (second read from L2): any
-                                 alignment; planned for unaligned rows, rows past
-                                 80 KB with a residual and rows past 192 KB     */
-    RMSNORM_KERNEL_TMA = 2    /* row staged in shared memory by bulk (TMA) copies:
+                                 alignment; planned for unaligned rows and for
+                                 rows past 192 KB without a residual           */
+    RMSNORM_KERNEL_TMA = 2,   /* row staged in shared memory by bulk (TMA) copies:
                                  rings for x, residual and weight fed by three
                                  producer warps, 512 threads a row; contiguous
-                                 RMSNorm rows past 32 KB (and block-scaled
-                                 outputs of rows too long for registers)        */
+                                 RMSNorm rows past 32 KB without a residual
+                                 (and block-scaled outputs of rows too long for
+                                 registers)                                     */
+    RMSNORM_KERNEL_CLUSTER = 3 /* row split over the 2..8 blocks of a thread-block
+                                 cluster, each holding a slice in registers; the
+                                 blocks' partial sums meet in distributed shared
+                                 memory behind one cluster barrier; contiguous
+                                 RMSNorm rows past 32 KB with a residual       */
 };
 
 /* Regimes (rmsnorm_plan_t.regime), a summary of how rows map to threads. */
@@ -92,14 +98,16 @@ enum {
     RMSNORM_REGIME_PERSISTENT = 2,  /* grid capped at the resident capacity; blocks
                                        stride over the rows                          */
     RMSNORM_REGIME_LOOPED = 3,      /* RMSNORM_KERNEL_LOOP                           */
-    RMSNORM_REGIME_SMEM = 4         /* RMSNORM_KERNEL_TMA: one block per SM, blocks
+    RMSNORM_REGIME_SMEM = 4,        /* RMSNORM_KERNEL_TMA: one block per SM, blocks
                                        stride over the rows                          */
+    RMSNORM_REGIME_CLUSTER = 5      /* RMSNORM_KERNEL_CLUSTER: one cluster a row     */
 };
 
 /*
  * A launch plan.  The per-row schedule (kernel, threads_per_row, vec_elems,
- * block_threads) depends only on hidden, dtype and the alignment of the
- * pointers (and, for rows longer than 80 KB, on whether a residual is given);
+ * block_threads, cluster_ctas) depends only on hidden, dtype and the
+ * alignment of the pointers (and, for rows longer than 32 KB, on whether a
+ * residual is given);
  * rows sizes the grid, may pick a chunk count that fits the row exactly and
  * may give each row a block of its own (rows_per_block 1), none of which ever
  * changes a result (chunks past the row end add exact zeros; which block takes
@@ -109,7 +117,8 @@ typedef struct {
     int32_t kernel;             /* RMSNORM_KERNEL_*                                   */
     int32_t regime;             /* RMSNORM_REGIME_*                                   */
     int32_t threads_per_row;    /* REG: 4..512 (4..32 for head rows), power of two;
-                                   LOOP: block_threads; TMA: 512                      */
+                                   LOOP: block_threads; TMA: 512; CLUSTER: 256 *
+                                   cluster_ctas                                       */
     int32_t chunks_per_thread;  /* REG: vector chunks per thread (an upper bound:
                                    slots past the row end stay idle); 1, 2, 4 or 8,
                                    and 3 or 6 for contiguous RMSNorm / LayerNorm rows
@@ -124,11 +133,15 @@ typedef struct {
                                    piece (the weight resident) when that leaves x
                                    a row and two spare slots, else there is none
                                    and the weight is read from global memory; the
-                                   rest, which must hold a whole row, goes to x)   */
+                                   rest, which must hold a whole row, goes to x);
+                                   CLUSTER: chunks per thread of a block's slice of
+                                   256 * chunks_per_thread chunks: 4 (16 KB), or 8
+                                   (32 KB, fp32 only; planned for rows past 128 KB),
+                                   a result depending on it (not on cluster_ctas)  */
     int32_t vec_elems;          /* elements per load: 16 / sizeof(T), or 1 (scalar)  */
     int32_t block_threads;      /* threads per block: REG max(threads_per_row, 256),
                                    or max(threads_per_row, 128) for LayerNorm;
-                                   LOOP: threads_per_row; TMA: 608                    */
+                                   LOOP: threads_per_row; TMA: 608; CLUSTER: 256      */
     int32_t rows_per_block;     /* rows one block handles per loop iteration: REG
                                    block_threads / threads_per_row, or (RMSNorm only)
                                    fewer, down to 1; planning takes one warp of rows
@@ -140,8 +153,12 @@ typedef struct {
                                    (the kernel may start while the previous kernel on
                                    the stream drains; it reads no input before that
                                    kernel has completed).  Planning sets 1.          */
-    int32_t reserved;           /* must be 0                                          */
-    int64_t grid;               /* blocks launched (0 when rows == 0)                 */
+    int32_t cluster_ctas;       /* CLUSTER: blocks of a cluster, which share a row,
+                                   2..8, covering the row (the fewest that do, in
+                                   planning); 0 for the other kernels              */
+    int64_t grid;               /* blocks launched (0 when rows == 0); CLUSTER: a
+                                   multiple of cluster_ctas (rows * cluster_ctas
+                                   in planning; fewer clusters stride over rows)   */
 } rmsnorm_plan_t;
 
 /*
@@ -180,13 +197,22 @@ int rmsnorm_regime(int64_t rows, int64_t hidden, int dtype);
 /*
  * Pure host planning (no CUDA call): the plan rmsnorm_fwd would use without
  * a residual on a device with `sm_count` SMs where the chosen kernel keeps
- * `blocks_per_sm` blocks resident (with a residual, rows longer than 80 KB
- * take RMSNORM_KERNEL_LOOP instead of RMSNORM_KERNEL_TMA).  vec_ok: 1 if
- * every pointer is 16-byte aligned and hidden * sizeof(T) is a multiple of
- * 16.  Returns a status.
+ * `blocks_per_sm` blocks resident (with a residual, rows longer than 32 KB
+ * take RMSNORM_KERNEL_CLUSTER instead: 16 KB slices up to 128 KB rows, 32 KB
+ * slices beyond).  vec_ok: 1 if every pointer is 16-byte aligned and
+ * hidden * sizeof(T) is a multiple of 16.  Returns a status.
  */
 int rmsnorm_plan(int64_t rows, int64_t hidden, int dtype, int vec_ok, int sm_count,
                  int blocks_per_sm, rmsnorm_plan_t *plan);
+
+/*
+ * rmsnorm_plan with the residual stated: has_residual 1 gives the plan
+ * rmsnorm_fwd uses when a residual (and residual_out) is passed, 0 is
+ * rmsnorm_plan.  Pure host planning, no CUDA call.  Returns a status
+ * (RMSNORM_EINVAL for has_residual other than 0 or 1).
+ */
+int rmsnorm_plan_ex(int64_t rows, int64_t hidden, int dtype, int vec_ok, int has_residual,
+                    int sm_count, int blocks_per_sm, rmsnorm_plan_t *plan);
 
 /*
  * The plan rmsnorm_fwd would use for these pointers on the current device
@@ -202,9 +228,11 @@ int rmsnorm_plan_for(const void *x, const void *residual, const void *w, const v
  * row (threads_per_row * chunks_per_thread * vec_elems >= hidden, with a
  * compiled chunks_per_thread, see rmsnorm_plan_t), block_threads and
  * rows_per_block must match threads_per_row, a TMA plan must fit the row in
- * its ring (see rmsnorm_plan_t), a vector plan (REG, TMA) needs aligned
- * pointers, grid >= 1, pdl 0 or 1 and reserved 0.  Returns RMSNORM_EINVAL for
- * a plan that does not fit.
+ * its ring (see rmsnorm_plan_t), a CLUSTER plan needs a residual, a compiled
+ * chunks_per_thread, 2..8 cluster_ctas that cover the row and a grid that is
+ * a multiple of cluster_ctas, a vector plan (REG, TMA, CLUSTER) needs aligned
+ * pointers, grid >= 1, pdl 0 or 1 and cluster_ctas 0 for the other kernels.
+ * Returns RMSNORM_EINVAL for a plan that does not fit.
  */
 int rmsnorm_fwd_plan(const void *x, const void *residual, const void *w, void *y,
                      void *residual_out, int64_t rows, int64_t hidden, float eps,

@@ -26,15 +26,17 @@ RMSNORM_ECUDA = -3
 RMSNORM_KERNEL_REG = 0
 RMSNORM_KERNEL_LOOP = 1
 RMSNORM_KERNEL_TMA = 2
+RMSNORM_KERNEL_CLUSTER = 3
 
 RMSNORM_REGIME_WARP = 0
 RMSNORM_REGIME_CTA = 1
 RMSNORM_REGIME_PERSISTENT = 2
 RMSNORM_REGIME_LOOPED = 3
 RMSNORM_REGIME_SMEM = 4
+RMSNORM_REGIME_CLUSTER = 5
 
-REGIME_NAMES = {0: "warp", 1: "cta", 2: "persistent", 3: "looped", 4: "smem"}
-KERNEL_NAMES = {0: "reg", 1: "loop", 2: "tma"}
+REGIME_NAMES = {0: "warp", 1: "cta", 2: "persistent", 3: "looped", 4: "smem", 5: "cluster"}
+KERNEL_NAMES = {0: "reg", 1: "loop", 2: "tma", 3: "cluster"}
 
 # Shape of the bulk-copy (TMA) kernel's block and rings (include/rmsnorm.h).
 TMA_THREADS_PER_ROW = 512
@@ -60,7 +62,7 @@ def tma_rings(row_bytes, pc, res, w):
     return (sx, sr, sw) if sx >= pieces else None
 
 # Every symbol the header declares (checked by the CPU tests).
-EXPORTED = ["rmsnorm_fwd", "rmsnorm_regime", "rmsnorm_plan", "rmsnorm_plan_for", "rmsnorm_fwd_plan", "rmsnorm_fwd_ex",
+EXPORTED = ["rmsnorm_fwd", "rmsnorm_regime", "rmsnorm_plan", "rmsnorm_plan_ex", "rmsnorm_plan_for", "rmsnorm_fwd_plan", "rmsnorm_fwd_ex",
             "rmsnorm_fwd_cast",
             "rmsnorm_qk_fwd", "rmsnorm_qk_plan_for", "rmsnorm_fwd_mxfp8", "rmsnorm_mxfp8_plan_for",
             "rmsnorm_fwd_nvfp4", "rmsnorm_nvfp4_plan_for",
@@ -88,7 +90,7 @@ class Plan(ctypes.Structure):
         ("rows_per_block", ctypes.c_int32),
         ("persistent", ctypes.c_int32),
         ("pdl", ctypes.c_int32),
-        ("reserved", ctypes.c_int32),
+        ("cluster_ctas", ctypes.c_int32),
         ("grid", ctypes.c_int64),
     ]
 
@@ -160,6 +162,8 @@ def load():
         lib.layernorm_plan_for.restype = i32
         lib.rmsnorm_plan.argtypes = [i64, i64, i32, i32, i32, i32, ctypes.POINTER(Plan)]
         lib.rmsnorm_plan.restype = i32
+        lib.rmsnorm_plan_ex.argtypes = [i64, i64, i32, i32, i32, i32, i32, ctypes.POINTER(Plan)]
+        lib.rmsnorm_plan_ex.restype = i32
         lib.rmsnorm_plan_for.argtypes = [vp, vp, vp, vp, vp, i64, i64, i32, ctypes.POINTER(Plan)]
         lib.rmsnorm_plan_for.restype = i32
         lib.rmsnorm_regime.argtypes = [i64, i64, i32]
@@ -311,6 +315,13 @@ def rmsnorm_plan(rows, hidden, dtype, vec_ok, sm_count, blocks_per_sm) -> Plan:
     p = Plan()
     _check(load().rmsnorm_plan(rows, hidden, dtype, int(vec_ok), sm_count, blocks_per_sm,
                                ctypes.byref(p)), "rmsnorm_plan")
+    return p
+
+
+def rmsnorm_plan_ex(rows, hidden, dtype, vec_ok, has_residual, sm_count, blocks_per_sm) -> Plan:
+    p = Plan()
+    _check(load().rmsnorm_plan_ex(rows, hidden, dtype, int(vec_ok), int(has_residual), sm_count, blocks_per_sm,
+                                  ctypes.byref(p)), "rmsnorm_plan_ex")
     return p
 
 

@@ -67,6 +67,14 @@ const void *tma_quant_kernel(int dtype, bool res, int wm, int out, bool wg);
 // Reads the count of blocks whose bounded waits ran out (current device); 0 or -1.
 int tma_timeouts_read(unsigned int *out);
 
+// RMSNorm of contiguous rows with a residual, a row split over the blocks of
+// a thread-block cluster: kClusterGT threads a block, each block a slice of
+// kClusterGT * ch 16-byte units, up to kClusterMaxCtas blocks a cluster.
+// Compiled for ch 4 (bf16, fp32) and 8 (fp32), with a residual only.
+constexpr int kClusterGT = 256;
+constexpr int kClusterMaxCtas = 8;
+const void *cluster_kernel(int dtype, int ch, bool res, int wm);
+
 // LayerNorm (contiguous rows); aff: 0 none, 1 weight, 2 weight and bias.
 constexpr int kLnMaxGT = 256;
 const void *ln_reg_f32(int gt, int ch, bool res, int aff);

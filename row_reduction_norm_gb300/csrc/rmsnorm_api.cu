@@ -42,12 +42,14 @@ constexpr int kRegMaxWeightSmem = rrn::kRegMaxGT * rrn::kRegMaxCH * 16;
 // Dynamic shared memory the bulk-copy kernel's ring may take: the 227 KB a
 // block may opt in to on sm_103a, less 1 KB for the kernel's static arrays.
 constexpr int kTmaSmemBudget = 227 * 1024 - 1024;
-// Chunks per consumer thread per ring piece chosen by planning: 16 KB pieces,
-// and 32 KB pieces without a residual for bf16 rows and rows past 80 KB.
+// Chunks per consumer thread per ring piece chosen by planning: 16 KB pieces
+// (block-scaled outputs, fp32 rows up to 80 KB), and 32 KB pieces for bf16
+// rows and rows past 80 KB (rows without a residual).
 constexpr int kTmaPlanPC = 2;
 constexpr int kTmaLongPC = 4;
 // 16-byte units of a row past which contiguous RMSNorm rows leave the
-// register kernel for the bulk-copy kernel (2048 units: 32 KB).
+// register kernel for the cluster kernel (with a residual) or the bulk-copy
+// kernel (without one): 2048 units, 32 KB.
 constexpr int64_t kRegWideUnits = 256 * rrn::kRegMaxCH;
 // Limit of every wait inside the bulk-copy kernel (ns).
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
@@ -146,30 +148,54 @@ int vec_ok_of(const Op &o) {
 // count).
 // odd_ch: chunk counts 3 and 6 are chosen where they fit the row exactly
 // (LayerNorm rows).
-// tma_ok: the op has a bulk-copy kernel (contiguous RMSNorm rows).  For
-// these ops, measured on GB300: rows of 16 to 32 KB run best as 256 threads
-// x 8 chunks (not 512 x 4), and longer rows on the bulk-copy kernel (not
-// 512 x 8 in registers); has_res matters only for rows past 80 KB (below).
+// tma_ok: the op has bulk-copy and cluster kernels (contiguous RMSNorm rows
+// in the I/O type).  For these ops, measured on GB300: rows of 16 to 32 KB
+// run best as 256 threads x 8 chunks (not 512 x 4), and longer rows on the
+// cluster kernel with a residual and on the bulk-copy kernel without one
+// (not 512 x 8 in registers); has_res matters only for rows past 32 KB.
 void schedule(int64_t hidden, int dtype, int vec_ok, int max_gt, rmsnorm_plan_t *p, bool odd_ch = false,
               bool tma_ok = false, bool has_res = false) {
     std::memset(p, 0, sizeof(*p));
     const int V = vec_elems_of(dtype);
     if (vec_ok) {
         const int64_t nch = hidden / V;
-        // Rows past 32 KB: the bulk-copy kernel when, with a residual and a
-        // weight, the weight stays resident beside the row (rows up to 80 KB);
-        // longer rows without a residual also take it (the weight streamed),
-        // and longer rows with a residual the two-pass kernel.  Pieces of
-        // 16 KB, or 32 KB without a residual for bf16 rows and for rows past
-        // 80 KB -- each the faster choice measured on GB300.  The piece size
-        // changes no result; the kernel does.
         const int64_t row_bytes = hidden * elem_size(dtype);
+        // Rows past 32 KB with a residual: the cluster kernel, a row over the
+        // fewest blocks of 16 KB slices (32 KB slices for fp32 rows past 128
+        // KB) -- measured on GB300 faster than the bulk-copy kernel (rows up
+        // to 80 KB) and the two-pass kernel (longer rows) for every such row;
+        // without a residual the bulk-copy kernel stays (below).
+        if (tma_ok && has_res && nch > kRegWideUnits) {
+            int ch = 4;
+            int64_t ctas = ceil_div(nch, (int64_t)rrn::kClusterGT * ch);
+            if (ctas > rrn::kClusterMaxCtas && dtype == RMSNORM_F32) {
+                ch = 8;
+                ctas = ceil_div(nch, (int64_t)rrn::kClusterGT * ch);
+            }
+            if (ctas <= rrn::kClusterMaxCtas) {
+                p->kernel = RMSNORM_KERNEL_CLUSTER;
+                p->regime = RMSNORM_REGIME_CLUSTER;
+                p->threads_per_row = rrn::kClusterGT * (int32_t)ctas;
+                p->chunks_per_thread = ch;
+                p->vec_elems = V;
+                p->block_threads = rrn::kClusterGT;
+                p->rows_per_block = 1;
+                p->cluster_ctas = (int32_t)ctas;
+                return;
+            }
+        }
+        // Rows past 32 KB without a residual: the bulk-copy kernel, the
+        // weight resident beside the row where that leaves x two spare slots
+        // (rows up to 80 KB), else read from global memory while x keeps one
+        // spare slot (rows up to 192 KB).  Pieces of 32 KB for bf16 rows and
+        // rows past 80 KB, else 16 KB -- each the faster choice measured on
+        // GB300.  The piece size changes no result; the kernel does.
         TmaRings tr;
         int tma_pc = 0;
-        if (tma_ok && nch > kRegWideUnits) {
+        if (tma_ok && !has_res && nch > kRegWideUnits) {
             if (tma_rings(row_bytes, kTmaPlanPC, true, true, &tr) && tr.sw > 0)
-                tma_pc = (!has_res && dtype == RMSNORM_BF16) ? kTmaLongPC : kTmaPlanPC;
-            else if (!has_res && tma_rings(row_bytes, kTmaLongPC, false, true, &tr) &&
+                tma_pc = dtype == RMSNORM_BF16 ? kTmaLongPC : kTmaPlanPC;
+            else if (tma_rings(row_bytes, kTmaLongPC, false, true, &tr) &&
                      tr.sx > ceil_div(row_bytes, rrn::tma_piece_bytes(kTmaLongPC)))
                 tma_pc = kTmaLongPC;   // planned while x keeps a spare slot (rows up to 192 KB)
         }
@@ -228,6 +254,13 @@ void size_grid(int64_t rows, int sm_count, int blocks_per_sm, rmsnorm_plan_t *p)
     const int64_t row_blocks = ceil_div(rows, p->rows_per_block);
     const int64_t resident = (int64_t)(sm_count > 0 ? sm_count : 1) * (blocks_per_sm > 0 ? blocks_per_sm : 1);
     p->pdl = 1;
+    if (p->kernel == RMSNORM_KERNEL_CLUSTER) {   // one cluster a row
+        const int64_t cap = INT_MAX / (p->cluster_ctas > 0 ? p->cluster_ctas : 1);
+        const int64_t clusters = rows < cap ? rows : cap;
+        p->grid = clusters * p->cluster_ctas;
+        p->persistent = rows > clusters;
+        return;
+    }
     if (p->kernel == RMSNORM_KERNEL_TMA) {   // one wave; blocks stride over the rows
         p->grid = row_blocks < resident ? row_blocks : resident;
         p->persistent = row_blocks > p->grid;
@@ -308,6 +341,10 @@ int mx_min_gt(int dtype) { return 32 / vec_elems_of(dtype); }
 
 const void *kernel_of(const rmsnorm_plan_t *p, const Op &o) {
     const bool res = o.res != nullptr;
+    if (p->kernel == RMSNORM_KERNEL_CLUSTER) {
+        if (o.ln || o.head_rows || o.mx || o.nv) return nullptr;
+        return rrn::cluster_kernel(o.dtype, p->chunks_per_thread, res, o.wm);
+    }
     if (p->kernel == RMSNORM_KERNEL_TMA) {
         if (o.ln || o.head_rows) return nullptr;
         // the weight from global memory when the rings give it no slots
@@ -349,7 +386,7 @@ int validate_plan(const rmsnorm_plan_t *p, const Op &o, int vec_ok) {
     const int V = vec_elems_of(o.dtype);
     if (o.rows > 0 && (p->grid < 1 || p->grid > INT_MAX)) return RMSNORM_EINVAL;
     if (p->pdl != 0 && p->pdl != 1) return RMSNORM_EINVAL;
-    if (p->reserved != 0) return RMSNORM_EINVAL;
+    if (p->kernel != RMSNORM_KERNEL_CLUSTER && p->cluster_ctas != 0) return RMSNORM_EINVAL;
     if (p->kernel == RMSNORM_KERNEL_REG) {
         const int gt = p->threads_per_row, ch = p->chunks_per_thread;
         const int max_gt = max_threads_per_row(o);
@@ -365,6 +402,20 @@ int validate_plan(const rmsnorm_plan_t *p, const Op &o, int vec_ok) {
         if (o.ln ? p->rows_per_block != p->block_threads / gt
                  : (p->rows_per_block < 1 || p->rows_per_block > p->block_threads / gt))
             return RMSNORM_EINVAL;
+        return RMSNORM_OK;
+    }
+    if (p->kernel == RMSNORM_KERNEL_CLUSTER) {
+        // contiguous RMSNorm rows with a residual, in the I/O type
+        if (o.ln || o.head_rows || o.mx || o.nv || o.res == nullptr) return RMSNORM_EINVAL;
+        if (!vec_ok || p->vec_elems != V) return RMSNORM_EINVAL;
+        const int ch = p->chunks_per_thread, c = p->cluster_ctas;
+        if (rrn::cluster_kernel(o.dtype, ch, true, o.wm) == nullptr) return RMSNORM_EINVAL;   // not compiled
+        if (c < 2 || c > rrn::kClusterMaxCtas) return RMSNORM_EINVAL;
+        if (p->block_threads != rrn::kClusterGT || p->threads_per_row != rrn::kClusterGT * c ||
+            p->rows_per_block != 1)
+            return RMSNORM_EINVAL;
+        if ((int64_t)c * rrn::kClusterGT * ch * V < o.row_elems) return RMSNORM_EINVAL;
+        if (o.rows > 0 && p->grid % c != 0) return RMSNORM_EINVAL;
         return RMSNORM_OK;
     }
     if (p->kernel == RMSNORM_KERNEL_TMA) {
@@ -578,16 +629,27 @@ int launch(const Op &o, const rmsnorm_plan_t *plan, int dev, rmsnorm_stream_t st
         argv[2] = &rings.sr;
         argv[3] = &rings.sw;
     }
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    unsigned nattr = 0;
+    if (plan->pdl) {
+        attr[nattr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[nattr].val.programmaticStreamSerializationAllowed = 1;
+        ++nattr;
+    }
+    if (plan->kernel == RMSNORM_KERNEL_CLUSTER) {   // blocks q*C .. q*C + C - 1 form cluster q
+        attr[nattr].id = cudaLaunchAttributeClusterDimension;
+        attr[nattr].val.clusterDim.x = (unsigned)plan->cluster_ctas;
+        attr[nattr].val.clusterDim.y = 1;
+        attr[nattr].val.clusterDim.z = 1;
+        ++nattr;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)plan->grid);
     cfg.blockDim = dim3((unsigned)plan->block_threads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = reinterpret_cast<cudaStream_t>(stream);
     cfg.attrs = attr;
-    cfg.numAttrs = plan->pdl ? 1 : 0;
+    cfg.numAttrs = nattr;
     cudaError_t e = cudaLaunchKernelExC(&cfg, fn, argv);
     if (e != cudaSuccess) {
         (void)cudaGetLastError();   // clear the non-sticky launch error
@@ -795,11 +857,17 @@ int layernorm_plan_for(const void *x, const void *residual, const void *w, const
 
 int rmsnorm_plan(int64_t rows, int64_t hidden, int dtype, int vec_ok, int sm_count, int blocks_per_sm,
                  rmsnorm_plan_t *plan) {
+    return rmsnorm_plan_ex(rows, hidden, dtype, vec_ok, 0, sm_count, blocks_per_sm, plan);
+}
+
+int rmsnorm_plan_ex(int64_t rows, int64_t hidden, int dtype, int vec_ok, int has_residual, int sm_count,
+                    int blocks_per_sm, rmsnorm_plan_t *plan) {
     if (plan == nullptr || dtype < RMSNORM_F32 || dtype > RMSNORM_BF16 || rows < 0 || hidden <= 0)
         return RMSNORM_EINVAL;
+    if (has_residual != 0 && has_residual != 1) return RMSNORM_EINVAL;
     if (hidden > kMaxHidden) return RMSNORM_EUNSUPPORTED;
     if (vec_ok && (hidden * elem_size(dtype)) % 16 != 0) return RMSNORM_EINVAL;
-    schedule(hidden, dtype, vec_ok ? 1 : 0, rrn::kRegMaxGT, plan, false, true);
+    schedule(hidden, dtype, vec_ok ? 1 : 0, rrn::kRegMaxGT, plan, false, true, has_residual == 1);
     size_grid(rows, sm_count, blocks_per_sm, plan);
     fit_chunks(rows, (int64_t)(sm_count > 0 ? sm_count : 1) * (blocks_per_sm > 0 ? blocks_per_sm : 1), true,
                hidden / vec_elems_of(dtype), plan);

@@ -236,6 +236,104 @@ def test_tma_ring_rule_matches_the_library(pc, res, w):
             assert got == want, (dtype, hidden)
 
 
+def _cluster_expected(hidden, dtype):
+    """(chunks_per_thread, cluster_ctas) of the cluster rule: 256-thread
+    blocks of 16 KB slices, as few as cover the row, or 32 KB slices for fp32
+    rows the eight-block cap of 16 KB slices cannot cover."""
+    V = 8 if dtype == N.RMSNORM_BF16 else 4
+    units = hidden // V
+    ch = 4 if units <= 8 * 256 * 4 else 8
+    return ch, -(-units // (256 * ch))
+
+
+@pytest.mark.parametrize("dtype", [N.RMSNORM_BF16, N.RMSNORM_F32])
+def test_residual_rows_past_32kb_take_the_cluster_kernel(dtype):
+    """With a residual, aligned rows past 32 KB run on the cluster kernel,
+    one cluster a row; shorter rows, unaligned rows and rows without a
+    residual keep rmsnorm_plan's plan."""
+    esz = 2 if dtype == N.RMSNORM_BF16 else 4
+    V = 16 // esz
+    edge = [32768 // esz, 32768 // esz + V, 131072 // esz, 131072 // esz + V, 65536]
+    hiddens = sorted(set(list(range(V, 65537, 1000 - 1000 % V)) + [h for h in edge if h <= 65536]))
+    for hidden in hiddens:
+        for rows in (0, 1, 1000, 10 ** 6):
+            p = R.rmsnorm_plan_ex(rows, hidden, dtype, True, True, 152, 4)
+            q = R.rmsnorm_plan(rows, hidden, dtype, True, 152, 4)
+            assert R.rmsnorm_plan_ex(rows, hidden, dtype, True, False, 152, 4).as_dict() == q.as_dict()
+            assert R.rmsnorm_plan_ex(rows, hidden, dtype, False, True, 152, 4).as_dict() == \
+                R.rmsnorm_plan(rows, hidden, dtype, False, 152, 4).as_dict()
+            if hidden * esz <= 32768:
+                assert p.as_dict() == q.as_dict(), hidden
+                assert q.cluster_ctas == 0
+                continue
+            ch, ctas = _cluster_expected(hidden, dtype)
+            assert 2 <= ctas <= 8 and (ctas - 1) * 256 * ch * V < hidden <= ctas * 256 * ch * V
+            assert dtype == N.RMSNORM_F32 or ch == 4
+            assert (p.kernel, p.regime) == (N.RMSNORM_KERNEL_CLUSTER, N.RMSNORM_REGIME_CLUSTER)
+            assert (p.chunks_per_thread, p.cluster_ctas, p.threads_per_row) == (ch, ctas, 256 * ctas)
+            assert (p.vec_elems, p.block_threads, p.rows_per_block) == (V, 256, 1)
+            assert (p.grid, p.persistent, p.pdl) == (rows * ctas, 0, 1)
+            assert q.kernel in (N.RMSNORM_KERNEL_TMA, N.RMSNORM_KERNEL_LOOP) and q.cluster_ctas == 0
+    with pytest.raises(N.RmsNormError):
+        R.rmsnorm_plan_ex(4, 40960, dtype, True, 2, 152, 4)
+
+
+def test_cluster_plan_validation_without_cuda():
+    """A forced cluster plan is checked before any CUDA call (rows = 0
+    validates and launches nothing; a bad plan is refused whatever rows is)."""
+    P = 1 << 20
+    OK, EINVAL = N.RMSNORM_OK, N.RMSNORM_EINVAL
+    good = R.rmsnorm_plan_ex(4, 40960, N.RMSNORM_BF16, True, True, 152, 4)
+    assert (good.kernel, good.cluster_ctas, good.chunks_per_thread, good.grid) == (N.RMSNORM_KERNEL_CLUSTER, 5, 4, 20)
+
+    def st(plan, hidden=40960, dtype=N.RMSNORM_BF16, res=P, rows=0, w=None):
+        return N.rmsnorm_fwd_plan_status(P, res, w, P, res, rows, hidden, 1e-6, dtype, plan, 0)
+
+    assert st(good) == OK and st(good, w=P) == OK
+    # more blocks than the row needs: the extra slices are past the row end
+    for c in (6, 7, 8):
+        q = good.copy()
+        q.cluster_ctas, q.threads_per_row, q.grid = c, 256 * c, 4 * c
+        assert st(q) == OK, c
+    bad = []
+    for field, value in (("chunks_per_thread", 8), ("chunks_per_thread", 2), ("block_threads", 512),
+                         ("rows_per_block", 2), ("vec_elems", 4), ("threads_per_row", 256 * 6),
+                         ("cluster_ctas", 0), ("cluster_ctas", 1), ("cluster_ctas", 9)):
+        q = good.copy()
+        setattr(q, field, value)
+        bad.append(q)
+    q = good.copy()
+    q.cluster_ctas, q.threads_per_row = 4, 1024          # 4 x 16 KB slices do not cover 80 KB
+    bad.append(q)
+    for q in bad:
+        assert st(q) == EINVAL, q.as_dict()
+    assert st(good, res=None) == EINVAL                  # compiled for rows with a residual
+    q = good.copy()
+    q.grid = 21                                          # not a whole number of clusters
+    assert st(q, rows=4) == EINVAL
+    # fp32: 32 KB slices, 8 blocks for 65536 elements; 16 KB slices do not cover them
+    f = R.rmsnorm_plan_ex(4, 65536, N.RMSNORM_F32, True, True, 152, 4)
+    assert (f.chunks_per_thread, f.cluster_ctas) == (8, 8)
+    assert st(f, hidden=65536, dtype=N.RMSNORM_F32) == OK
+    q = f.copy()
+    q.chunks_per_thread = 4
+    assert st(q, hidden=65536, dtype=N.RMSNORM_F32) == EINVAL
+    assert st(q, hidden=32768, dtype=N.RMSNORM_F32) == OK
+    # weight forms: bias and the cast order (bf16) run on it
+    assert N.rmsnorm_fwd_ex_status(P, P, P, P, P, 0, 40960, 1e-6, 1.0, N.RMSNORM_BF16, good) == OK
+    assert N.rmsnorm_fwd_cast_status(P, P, P, P, P, 0, 40960, 1e-6, N.RMSNORM_BF16, good) == OK
+    # no block-scaled, LayerNorm or head-row form of it
+    assert N.rmsnorm_fwd_mxfp8_status(P, P, None, P, P, P, 0, 40960, 1e-6, 0.0, 1, good) == EINVAL
+    assert N.rmsnorm_fwd_nvfp4_status(P, P, None, P, P, P, 0, 40960, 1e-6, 0.0, 1.0, 1, good) == EINVAL
+    assert N.layernorm_fwd_status(P, P, None, None, P, P, 0, 40960, 1e-5, 1, good) == EINVAL
+    assert N.rmsnorm_qk_fwd_status(P, P, 4, 40960, 40960, 1, 0, 40960, None, None, 0.0, 1e-6, 1,
+                                   good) == EINVAL
+    # cluster_ctas belongs to cluster plans only
+    reg = R.rmsnorm_plan(4, 576, N.RMSNORM_BF16, True, 152, 4)
+    reg.cluster_ctas = 2
+    assert st(reg, hidden=576, res=None) == EINVAL
+
+
 def test_layernorm_register_blocks_are_four_warps_or_the_row():
     """LayerNorm register plans use blocks of max(threads_per_row, 128)
     threads; a plan with the RMSNorm block size is refused (rows = 0:
@@ -390,8 +488,9 @@ def test_cast_arguments_rejected_without_cuda():
 def test_header_is_plain_c_and_links():
     # the boundary as a C caller sees it: the header compiles as strict C99,
     # the program links against the library and calls it (no CUDA work: a
-    # zero-row call, a call rejected for its eps, and the regime query, which
-    # answers the warp regime on a GPU and a CUDA error without one)
+    # zero-row call, a call rejected for its eps, the regime query, which
+    # answers the warp regime on a GPU and a CUDA error without one, and the
+    # host planner's cluster plan for rows of 80 KB with a residual)
     import os
     import shutil
     import subprocess
@@ -416,8 +515,12 @@ int main(void) {
     int cast = rmsnorm_fwd_cast(NULL, NULL, NULL, NULL, NULL, 0, 64, 1e-6f, RMSNORM_BF16, NULL, NULL);
     int regime_bad = rmsnorm_regime(-1, 576, RMSNORM_BF16);
     int regime = rmsnorm_regime(4096, 576, RMSNORM_BF16);
-    printf("%d %d %d %d %d %d\n", zero, bad, cast, info != NULL, regime_bad,
-           regime == RMSNORM_REGIME_WARP || regime == RMSNORM_ECUDA);
+    rmsnorm_plan_t plan;
+    int planned = rmsnorm_plan_ex(100, 40960, RMSNORM_BF16, 1, 1, 152, 4, &plan);
+    int cluster = planned == RMSNORM_OK && plan.kernel == RMSNORM_KERNEL_CLUSTER &&
+                  plan.regime == RMSNORM_REGIME_CLUSTER && plan.cluster_ctas == 5 && plan.grid == 500;
+    printf("%d %d %d %d %d %d %d\n", zero, bad, cast, info != NULL, regime_bad,
+           regime == RMSNORM_REGIME_WARP || regime == RMSNORM_ECUDA, cluster);
     return 0;
 }
 ''')
@@ -427,4 +530,4 @@ int main(void) {
     subprocess.run(cmd, check=True)
     r = subprocess.run([exe], capture_output=True, text=True, check=True)
     assert r.stdout.split() == [str(N.RMSNORM_OK), str(N.RMSNORM_EINVAL), str(N.RMSNORM_OK), "1",
-                                str(N.RMSNORM_EINVAL), "1"]
+                                str(N.RMSNORM_EINVAL), "1", "1"]

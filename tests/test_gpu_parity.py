@@ -470,7 +470,8 @@ def test_status_codes_on_device():
 @pytest.mark.parametrize("hidden,rows,has_res,kind", [
     (8192, 288000, False, "reg"),      # x 4.4 GiB: register kernel
     (40960, 57600, False, "tma"),      # x 4.4 GiB: bulk-copy kernel
-    (65536, 36000, True, "loop"),      # x and residual 4.4 GiB each: two-pass kernel
+    (65536, 36000, True, "cluster"),   # x and residual 4.4 GiB each: a cluster of blocks a row
+    (65536, 36000, True, "loop"),      # the same, the two-pass kernel forced
 ])
 def test_offsets_past_4gib(hidden, rows, has_res, kind):
     """Tensors larger than 4 GiB: rows near the end sit at byte offsets past
@@ -479,8 +480,12 @@ def test_offsets_past_4gib(hidden, rows, has_res, kind):
     wl = W.Workload("big", "bf16", rows, hidden, 1e-6, 1.0, 1.0 if has_res else None, 0.1)
     x, r, w = gpu_inputs(wl, seed=hidden)
     p = R.plan_for(x, w=w, residual=r)
+    if kind == "loop":
+        p.kernel, p.regime, p.threads_per_row, p.chunks_per_thread = (N.RMSNORM_KERNEL_LOOP,
+                                                                      N.RMSNORM_REGIME_LOOPED, 1024, 0)
+        p.block_threads, p.rows_per_block, p.grid, p.persistent, p.cluster_ctas = 1024, 1, rows, 0, 0
     assert p.as_dict()["kernel_name"] == kind
-    out = R.rms_norm(x, w=w, residual=r, eps=wl.eps)
+    out = R.rms_norm(x, w=w, residual=r, eps=wl.eps, plan=p)
     y, h = out if r is not None else (out, None)
     torch.cuda.synchronize()
     row_bytes = hidden * 2

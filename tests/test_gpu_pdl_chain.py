@@ -6,9 +6,10 @@ so launch k+1 may start while launch k drains; its blocks execute
 k+1 read what launch k wrote -- y becomes the next x, residual_out the next
 residual -- in place and out of place, eagerly and inside a captured CUDA
 graph, on every kernel family (register warp / CTA, two-pass vector and
-scalar, shared-memory rings fed by bulk copies, and a chain that switches
-family every launch), and compare every step with the oracle applied to the
-previous step's output as the GPU wrote it.
+scalar, shared-memory rings fed by bulk copies, a row split over the blocks
+of a thread-block cluster, and a chain that switches family every launch),
+and compare every step with the oracle applied to the previous step's output
+as the GPU wrote it.
 
 In-place chains keep a snapshot per step: launch "snap" normalises buffer A
 into B[k] (out of place), then launch "in place" normalises A over itself
@@ -49,14 +50,16 @@ def _plans(family, rows, hidden, dtype, x, w, r):
     code = N.RMSNORM_BF16 if dtype == "bf16" else N.RMSNORM_F32
     lib = R.plan_for(x, w=w, residual=r, out=torch.empty_like(x), residual_out=None if r is None else
                      torch.empty_like(x))
-    if family == "long":   # past 80 KB: the bulk-copy kernel (weight from L2), or two passes with a residual
-        want = N.RMSNORM_REGIME_LOOPED if r is not None else N.RMSNORM_REGIME_SMEM
+    if family in ("tma", "long"):
+        # past 32 KB: a cluster of blocks a row with a residual; the bulk-copy
+        # kernel without one (past 80 KB with the weight read from L2)
+        want = N.RMSNORM_REGIME_CLUSTER if r is not None else N.RMSNORM_REGIME_SMEM
         assert lib.regime == want, lib.as_dict()
         return [lib]
-    if family in ("warp", "cta", "tma"):
-        want = {"warp": N.RMSNORM_REGIME_WARP, "cta": N.RMSNORM_REGIME_CTA, "tma": N.RMSNORM_REGIME_SMEM}[family]
+    if family in ("warp", "cta"):
+        want = {"warp": N.RMSNORM_REGIME_WARP, "cta": N.RMSNORM_REGIME_CTA}[family]
         assert lib.regime == want, lib.as_dict()
-        if rows <= torch.cuda.get_device_properties(0).multi_processor_count and family != "tma":
+        if rows <= torch.cuda.get_device_properties(0).multi_processor_count:
             assert lib.rows_per_block == 1, lib.as_dict()   # the decode spread
         return [lib]
     forced = all_plans(rows, hidden, code, True, odd_ch=True, tma=True)
@@ -73,7 +76,22 @@ def _plans(family, rows, hidden, dtype, x, w, r):
     persistent = lib.copy()
     persistent.grid = min(persistent.grid, 5)   # blocks stride over the rows
     persistent.persistent = 1
-    return [lib, tma[0], loop_vec[-1], reg[0], loop_scalar[0], persistent, tma[-1]]
+    chain = [lib, tma[0], loop_vec[-1], reg[0], loop_scalar[0], persistent, tma[-1]]
+    if r is not None:
+        # the cluster kernel on a row one 16 KB slice covers: two blocks a
+        # cluster (the second past the row end), then three clusters striding
+        # over the rows
+        V = 8 if dtype == "bf16" else 4
+        cl = R.rmsnorm_plan_ex(rows, 40960, code, True, True, 152, 4)
+        cl.cluster_ctas, cl.threads_per_row = 2, 512
+        cl.chunks_per_thread = 4
+        assert 2 * 256 * 4 * V >= hidden
+        cl.grid = rows * 2
+        few = cl.copy()
+        few.grid, few.persistent = 6, 1
+        chain[2:2] = [cl]
+        chain.append(few)
+    return chain
 
 
 CASES = [

@@ -69,8 +69,9 @@ def oracle_ref(x, r, w, eps, dtype, weight_bias=0.0):
     return y, h
 
 
-# rows the library plans on the bulk-copy kernel (32 to 80 KB), and longer
-# rows it can run when forced (up to 160 KB with a residual and a weight)
+# rows the library plans on the bulk-copy kernel without a residual (32 to 80
+# KB; with a residual it plans the cluster kernel), and longer rows it can run
+# when forced (up to 160 KB with a residual and a weight)
 PLANNED = [("bf16", 32776), ("bf16", 40000), ("bf16", 40960), ("f32", 16388), ("f32", 20480)]
 LONG = PLANNED + [("bf16", 65536), ("f32", 24576), ("f32", 40960)]
 
@@ -83,10 +84,14 @@ def test_long_rows_library_plan(dtype, hidden):
                         0.1 if has_w else None)
         x, r, w = W.make_inputs(wl, seed=hidden + rows, device=DEV)
         p = R.plan_for(x, w=w, residual=r)
+        if has_res:
+            assert p.kernel == N.RMSNORM_KERNEL_CLUSTER and p.regime == N.RMSNORM_REGIME_CLUSTER
+            p = R.plan_for(x, w=w)          # the bulk-copy plan, forced with the residual
+            p.chunks_per_thread = 2
         assert p.kernel == N.RMSNORM_KERNEL_TMA and p.regime == N.RMSNORM_REGIME_SMEM
         assert p.chunks_per_thread == (4 if dtype == "bf16" and not has_res else 2)
         assert fits(hidden, esz, p.chunks_per_thread, has_res, has_w)
-        out = R.rms_norm(x, w=w, residual=r, eps=wl.eps)
+        out = R.rms_norm(x, w=w, residual=r, eps=wl.eps, plan=p)
         y, h = out if r is not None else (out, None)
         torch.cuda.synchronize()
         yr, hr = oracle_ref(x, r, w, wl.eps, dtype)
@@ -99,14 +104,15 @@ def test_long_rows_library_plan(dtype, hidden):
 @pytest.mark.parametrize("dtype,hidden", [("bf16", 65536), ("f32", 24576), ("f32", 49152)])
 def test_rows_past_80kb_plan_by_residual(dtype, hidden):
     """Past 80 KB the weight cannot stay resident beside the row: without a
-    residual the library plans the bulk-copy kernel with 32 KB pieces, with a
-    residual the two-pass kernel; both match the oracle."""
+    residual the library plans the bulk-copy kernel with 32 KB pieces (the
+    weight read from L2), with a residual the cluster kernel; both match the
+    oracle."""
     for has_res in (False, True):
         wl = W.Workload("past80", dtype, 9, hidden, 1e-6, 1.0, 1.0 if has_res else None, 0.1)
         x, r, w = W.make_inputs(wl, seed=hidden + has_res, device=DEV)
         p = R.plan_for(x, w=w, residual=r)
         if has_res:
-            assert p.kernel == N.RMSNORM_KERNEL_LOOP
+            assert p.kernel == N.RMSNORM_KERNEL_CLUSTER
         else:
             assert p.kernel == N.RMSNORM_KERNEL_TMA and p.chunks_per_thread == 4
         out = R.rms_norm(x, w=w, residual=r, eps=wl.eps)
