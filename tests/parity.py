@@ -15,8 +15,11 @@ the mean and eps add 3 roundings (<= 1.5 u on the scale), rsqrtf <= 2 ulp
 (<= 4 u), and the two products 2 u: about 18 u = 1.1e-6 relative in the
 worst case, inside 2e-6.  (The bulk-copy kernel's tree is at most 35 levels
 deep, 24 chunk steps for fp32 rows of 49152: about 25 u = 1.5e-6, still
-inside.)  A bf16 result computed that accurately is within one bf16 ulp of
-the correctly rounded value.
+inside.  The cluster kernel's tree is at most 21 levels deep too: 8 chunk
+steps, 2 lane levels, 5 shuffle levels, 3 warp levels and 3 levels over the
+cluster's partial sums for fp32 rows in 32 KB slices.)  A bf16 result
+computed that accurately is within one bf16 ulp of the correctly rounded
+value.
 """
 from __future__ import annotations
 
