@@ -19,9 +19,10 @@ that their footprint is at least 4x the L2 size (the headline's one set of
 launching stream bracket exactly K steps, with a barrier and a device
 synchronise on both sides; nvidia-smi samples clocks during the timed region
 and the half second of identical launches just before it.  ``e2e`` repeats
-the measurement with the inputs copied from pinned host memory and the
-outputs read back every step, beside the host link's own rate for the same
-copies with no launch (``link_gbs``), which bounds it.  The CPU baseline is
+the measurement through the C ABI's host-buffer call (``rmsnorm_fwd_host``:
+inputs in pinned host memory, outputs read back, every step), beside the
+host link's own rate for the same copies with no launch (``link_gbs``),
+which bounds it.  The CPU baseline is
 the fp64 oracle on the host cores over a bounded sample of the headline's
 rows.
 
@@ -106,7 +107,7 @@ def load_peaks():
 
 # Host-side planning and argument checks: not device code, so not part of
 # the hash that says whether a profile still describes the kernels.
-HOST_ONLY_SOURCES = ("rmsnorm_api.cu",)
+HOST_ONLY_SOURCES = ("rmsnorm_api.cu", "rmsnorm_host.cu")
 
 
 def code_tokens(text):
@@ -612,88 +613,43 @@ def host_link_gbs(L, reps=5):
     return (h2d + d2h) / statistics.median(times[1:]) / 1e6
 
 
-def time_e2e(L, steps, pipelined=True):
-    """End-to-end steps through the public call: every step copies its inputs
-    (x, residual, w) from pinned host memory to the device, launches, and reads
-    y (and residual_out) back into pinned host memory.  Pipelined: uploads,
-    launches and read-backs run on three streams with per-buffer events, so
-    step i's read-back overlaps step i+1's upload and launch (device buffer
-    slots are reused only after their previous read-back finished).  Returns
-    (ms for `steps` steps, h2d bytes per step, d2h bytes per step)."""
+E2E_CHUNK_BYTES = 64 << 20   # rows a chunk of the host call: about 64 MiB of each tensor
+
+
+def e2e_chunk_rows(wl):
+    return max(1, min(wl.rows, E2E_CHUNK_BYTES // (wl.hidden * wl.elem_bytes)))
+
+
+def time_e2e_host(L, steps, chunk_rows):
+    """End to end through the C ABI's host-buffer call: every step is one
+    ``rmsnorm_fwd_host`` call on pinned host x, residual and w, writing pinned
+    host y and residual_out; the library streams the rows through the device
+    in chunks of ``chunk_rows`` rows (uploads, launches and read-backs on
+    three streams over two halves of a device workspace).  Returns (ms for
+    `steps` calls, h2d bytes per step, d2h bytes per step)."""
     import torch
+    from row_reduction_norm_gb300 import _native as N
     hx, hr, hw, hy, hh, h2d, d2h = host_buffers(L)
-    nbuf = min(L.n_sets, 4) if pipelined else 1
-    s_k = L.stream
-    s_up = torch.cuda.Stream(s_k.device) if nbuf > 1 else s_k
-    s_dn = torch.cuda.Stream(s_k.device) if nbuf > 1 else s_k
-    # one device weight copy per slot, so an upload never races a running launch
-    w_slots = [None if L.w is None else torch.empty_like(L.w) for _ in range(nbuf)]
+    wl = L.wl
+    nbytes = N.rmsnorm_host_workspace_bytes(chunk_rows, wl.hidden, L.code, hr is not None)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=L.stream.device)
+    ptr = lambda t: None if t is None else t.data_ptr()
 
-    def step(i, ev):
-        slot = i % nbuf
-        xd, rd, yd, hd = L.sets[slot]
-        wd = w_slots[slot]
-        up, kd, dn = ev[i]
-        with torch.cuda.stream(s_up):
-            if i >= nbuf:
-                s_up.wait_event(ev[i - nbuf][1])    # the launch that read this slot is done
-            xd.copy_(hx, non_blocking=True)
-            if rd is not None:
-                rd.copy_(hr, non_blocking=True)
-            if wd is not None:
-                wd.copy_(hw, non_blocking=True)
-            up.record(s_up)
-        with torch.cuda.stream(s_k):
-            s_k.wait_event(up)
-            if i >= nbuf:
-                s_k.wait_event(ev[i - nbuf][2])     # the read-back of this slot is done
-            L.launch_with(i, slot, None if wd is None else wd.data_ptr())
-            kd.record(s_k)
-        with torch.cuda.stream(s_dn):
-            s_dn.wait_event(kd)
-            hy.copy_(yd, non_blocking=True)
-            if hh is not None:
-                hh.copy_(hd, non_blocking=True)
-            dn.record(s_dn)
+    def step():
+        N.rmsnorm_fwd_host(ptr(hx), ptr(hr), ptr(hw), ptr(hy), ptr(hh), wl.rows, wl.hidden, wl.eps, L.code,
+                           ws.data_ptr(), nbytes, chunk_rows, L.stream.cuda_stream)
 
-    def capture(count):
-        ev = [(torch.cuda.Event(), torch.cuda.Event(), torch.cuda.Event()) for _ in range(count)]
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=s_k):
-            s_up.wait_stream(s_k)
-            s_dn.wait_stream(s_k)
-            for i in range(count):
-                step(i, ev)
-            s_k.wait_stream(s_up)
-            s_k.wait_stream(s_dn)
-        return g
-
-    # eager warm-up of the three-stream schedule, then capture
-    ev = [(torch.cuda.Event(), torch.cuda.Event(), torch.cuda.Event()) for _ in range(3)]
-    s_up.wait_stream(s_k)
-    s_dn.wait_stream(s_k)
-    for i in range(3):
-        step(i, ev)
-    s_k.wait_stream(s_up)
-    s_k.wait_stream(s_dn)
-    torch.cuda.synchronize()
-    G = max(1, min(steps, 64))
-    g = capture(G)
-    rem = steps % G
-    g2 = capture(rem) if rem else None
-    with torch.cuda.stream(s_k):
-        g.replay()
+    for _ in range(2):
+        step()
     torch.cuda.synchronize()
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(s_k):
-        ev0.record(s_k)
-        for _ in range(steps // G):
-            g.replay()
-        if g2 is not None:
-            g2.replay()
-        ev1.record(s_k)
+    ev0.record(L.stream)
+    for _ in range(steps):
+        step()
+    ev1.record(L.stream)
     torch.cuda.synchronize()
+    del ws
     return ev0.elapsed_time(ev1), h2d, d2h
 
 
@@ -975,10 +931,12 @@ def run_ours(args):
     del L
     torch.cuda.empty_cache()
     LE = Launcher(wl, device, stream, 0, n_sets=2)
-    e_ms, h2d, d2h = time_e2e(LE, e2e_steps)
+    chunk = e2e_chunk_rows(wl)
+    e_ms, h2d, d2h = time_e2e_host(LE, e2e_steps, chunk)
     e2e_value, _ = aggregate(world, launch_bytes, wl.rows, e2e_steps, reduce_max(e_ms, dist, device))
-    s_ms, _, _ = time_e2e(LE, e2e_steps, pipelined=False)
-    e2e_serial, _ = aggregate(world, launch_bytes, wl.rows, e2e_steps, reduce_max(s_ms, dist, device))
+    serial_steps = max(2, e2e_steps // 4)
+    s_ms, _, _ = time_e2e_host(LE, serial_steps, wl.rows)
+    e2e_serial, _ = aggregate(world, launch_bytes, wl.rows, serial_steps, reduce_max(s_ms, dist, device))
     link = host_link_gbs(LE)
 
     cpu = None
@@ -1070,14 +1028,15 @@ def run_ours(args):
                      "algorithmic_bytes_per_launch": launch_bytes},
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                "serial_value": round(e2e_serial, 2),
+                "serial_value": round(e2e_serial, 2), "chunk_rows": chunk,
                 "link_gbs": round(link, 2), "frac_of_link": round(e2e_value / world / link, 4),
                 "link_what": "one step's uploads and read-backs alone, the two directions concurrent on two "
                              "streams, no launch (median of 5, same process, just after the e2e region)",
-                "what": "every step: pinned host -> device copy of its inputs (x, residual, w), the C-ABI launch, "
-                        "device -> pinned host copy of y and residual_out; uploads, launches and read-backs "
-                        "pipelined on three streams over 2 device buffer sets (serial_value: one stream, no "
-                        "overlap)"},
+                "what": "every step one rmsnorm_fwd_host call (the C ABI's host-buffer entry point) on pinned "
+                        "host x, residual and w, writing pinned host y and residual_out: the library copies "
+                        "chunks of chunk_rows rows into a device workspace, launches on them and copies the "
+                        "outputs back, uploads, launches and read-backs overlapping on three streams "
+                        "(serial_value: the same call with the whole batch as one chunk, nothing overlapping)"},
         "repeats": {"n": len(reps_us), "steps_each": rep_steps, "median_us": round(statistics.median(reps_us), 3),
                     "min_us": round(reps_us[0], 3), "max_us": round(reps_us[-1], 3),
                     "what": "the headline launches timed again as separate runs of steps_each launches"},

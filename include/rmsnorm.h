@@ -21,7 +21,7 @@
  *
  * Arithmetic: inputs are widened to fp32; the sum of squares is formed in
  * fp32 in a fixed order that depends only on (hidden, dtype, alignment, and,
- * for rows longer than 80 KB, whether a residual is given), so every call
+ * for rows longer than 32 KB, whether a residual is given), so every call
  * gives bit-identical results for a row, whatever the row count, grid or
  * stream ("batch invariant").  Accuracy: y is within 1 ulp of the
  * correctly rounded result for bf16 and within 2e-6 relative for fp32;
@@ -30,6 +30,8 @@
  * Conventions common to every entry point:
  *  - All tensor pointers are DEVICE pointers owned by the caller, on the
  *    caller's current CUDA device; the library allocates and frees nothing.
+ *    (rmsnorm_fwd_host takes HOST tensors and a caller-owned device
+ *    workspace; it allocates no memory either.)
  *  - Every tensor shares one I/O type (dtype).  x, residual, y and
  *    residual_out are contiguous row-major [rows, hidden]; w is [hidden].
  *  - Calls are asynchronous on `stream` (0 = the legacy default stream) and
@@ -43,8 +45,9 @@
  *    is a multiple of 16, rows move with 128-bit loads and stores; otherwise a
  *    scalar path runs (same results up to the stated tolerance).
  *  - Thread safety: entry points may be called from several host threads.
- *    The only library state is a per-device cache of the SM count and of
- *    kernel occupancy.
+ *    The library's state is a per-device cache of the SM count and of
+ *    kernel occupancy, and the three streams and seven events per device
+ *    that rmsnorm_fwd_host creates at its first call there.
  */
 #ifndef ROW_REDUCTION_NORM_GB300_RMSNORM_H
 #define ROW_REDUCTION_NORM_GB300_RMSNORM_H
@@ -393,6 +396,56 @@ int layernorm_fwd(const void *x, const void *residual, const void *w, const void
 int layernorm_plan_for(const void *x, const void *residual, const void *w, const void *b,
                        const void *y, const void *residual_out, int64_t rows, int64_t hidden,
                        int dtype, rmsnorm_plan_t *plan);
+
+/*
+ * The op of rmsnorm_fwd (Emmy page, running example and section "Tensor
+ * IR") on rows that live in HOST memory: x, residual, w, y and residual_out
+ * are host pointers, with rmsnorm_fwd's layout and argument rules.  The rows
+ * go through the current device in chunks of chunk_rows rows (the last may
+ * be shorter): a chunk's inputs are copied into one of the two halves of
+ * `workspace`, one rmsnorm_fwd launch normalises them there, and its outputs
+ * are copied back; uploads, launches and read-backs run on three streams of
+ * the library's, so a chunk's uploads overlap the previous chunk's launch
+ * and read-backs and both copy directions run at once.  The pages describe
+ * no such call: it is the op end to end from host memory, the form a caller
+ * holding activations in host memory uses (and the benchmark's end-to-end
+ * figure).
+ *   workspace        DEVICE memory owned by the caller, 256-byte aligned,
+ *                    workspace_bytes >= rmsnorm_host_workspace_bytes(
+ *                    chunk_rows, hidden, dtype, residual != NULL); used by
+ *                    no one else until the call's work on `stream` is done
+ *   chunk_rows       >= 1
+ *   stream           the call's copies start after the work issued on
+ *                    `stream` before the call, and work issued on `stream`
+ *                    after it starts after the call's last read-back:
+ *                    synchronise `stream` before reading y on the host
+ * Overlap needs page-locked host memory (cudaHostAlloc, cudaHostRegister);
+ * with pageable memory the results are the same and the CUDA runtime
+ * serialises the copies.  Each chunk is one rmsnorm_fwd launch on 256-byte
+ * aligned device copies, so the results are those of rmsnorm_fwd on such
+ * copies of the same rows, bit for bit (the schedule does not depend on the
+ * row count).  Calls on one device are queued one at a time (a per-device
+ * lock held while the copies and launches are issued, not while they run);
+ * not for use while a stream is being captured.  Returns RMSNORM_OK or a
+ * negative status: RMSNORM_EINVAL for a NULL x or y with rows > 0, a
+ * residual without residual_out or the reverse, chunk_rows < 1, a NULL,
+ * misaligned or too small workspace, or rmsnorm_fwd's own argument errors;
+ * RMSNORM_EUNSUPPORTED; RMSNORM_ECUDA.  rows == 0 does nothing.
+ */
+int rmsnorm_fwd_host(const void *x, const void *residual, const void *w, void *y,
+                     void *residual_out, int64_t rows, int64_t hidden, float eps, int dtype,
+                     void *workspace, uint64_t workspace_bytes, int64_t chunk_rows,
+                     rmsnorm_stream_t stream);
+
+/*
+ * Device workspace bytes rmsnorm_fwd_host needs: the weight, then two halves
+ * of chunk_rows rows of x and y (and of residual and residual_out with
+ * has_residual = 1), each part starting on a 256-byte boundary.  Returns the
+ * byte count (> 0) or a negative status (RMSNORM_EINVAL: chunk_rows < 1,
+ * hidden < 1, unknown dtype, has_residual not 0 or 1, a size that overflows;
+ * RMSNORM_EUNSUPPORTED: hidden above rmsnorm_max_hidden).
+ */
+int64_t rmsnorm_host_workspace_bytes(int64_t chunk_rows, int64_t hidden, int dtype, int has_residual);
 
 /* Largest supported hidden size for a dtype (0 for an unknown dtype). */
 int64_t rmsnorm_max_hidden(int dtype);

@@ -1,7 +1,8 @@
 """ctypes binding of the C ABI in ``include/rmsnorm.h`` (argument marshalling only).
 
 The functions keep the C names and argument order; pointers are plain
-integers (device addresses), streams are ``cudaStream_t`` values as integers.
+integers (device addresses; host addresses for the tensors of
+``rmsnorm_fwd_host``), streams are ``cudaStream_t`` values as integers.
 A non-zero status raises ``RmsNormError``.  Nothing here computes any part of
 the op: every step runs in the CUDA kernels of ``librmsnorm_gb300.so``, and a
 missing library is an error, never a fallback.
@@ -62,11 +63,12 @@ def tma_rings(row_bytes, pc, res, w):
     return (sx, sr, sw) if sx >= pieces else None
 
 # Every symbol the header declares (checked by the CPU tests).
-EXPORTED = ["rmsnorm_fwd", "rmsnorm_regime", "rmsnorm_plan", "rmsnorm_plan_ex", "rmsnorm_plan_for", "rmsnorm_fwd_plan", "rmsnorm_fwd_ex",
-            "rmsnorm_fwd_cast",
+EXPORTED = ["rmsnorm_fwd", "rmsnorm_regime", "rmsnorm_plan", "rmsnorm_plan_ex", "rmsnorm_plan_for",
+            "rmsnorm_fwd_plan", "rmsnorm_fwd_ex", "rmsnorm_fwd_cast",
             "rmsnorm_qk_fwd", "rmsnorm_qk_plan_for", "rmsnorm_fwd_mxfp8", "rmsnorm_mxfp8_plan_for",
             "rmsnorm_fwd_nvfp4", "rmsnorm_nvfp4_plan_for",
             "layernorm_fwd", "layernorm_plan_for",
+            "rmsnorm_fwd_host", "rmsnorm_host_workspace_bytes",
             "rmsnorm_max_hidden", "rmsnorm_reg_max_chunks", "rmsnorm_wait_timeouts", "rmsnorm_tma_wait_test",
             "rmsnorm_strerror",
             "rmsnorm_build_info"]
@@ -176,6 +178,10 @@ def load():
         lib.rmsnorm_tma_wait_test.restype = i32
         lib.rmsnorm_wait_timeouts.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
         lib.rmsnorm_wait_timeouts.restype = i32
+        lib.rmsnorm_fwd_host.argtypes = fwd_args + [vp, ctypes.c_uint64, i64, vp]
+        lib.rmsnorm_fwd_host.restype = i32
+        lib.rmsnorm_host_workspace_bytes.argtypes = [i64, i64, i32, i32]
+        lib.rmsnorm_host_workspace_bytes.restype = i64
         lib.rmsnorm_strerror.argtypes = [i32]
         lib.rmsnorm_strerror.restype = ctypes.c_char_p
         lib.rmsnorm_build_info.argtypes = []
@@ -344,6 +350,27 @@ def rmsnorm_regime(rows, hidden, dtype) -> int:
 def rmsnorm_regime_status(rows, hidden, dtype) -> int:
     """rmsnorm_regime's raw return value: a regime (>= 0) or a negative status."""
     return int(load().rmsnorm_regime(rows, hidden, dtype))
+
+
+def rmsnorm_fwd_host(x, residual, w, y, residual_out, rows, hidden, eps, dtype, workspace, workspace_bytes,
+                     chunk_rows, stream=0):
+    """The op on HOST pointers, streamed through the device in chunks (see
+    the header); asynchronous on ``stream``."""
+    _check(load().rmsnorm_fwd_host(x, residual, w, y, residual_out, rows, hidden, eps, dtype, workspace,
+                                   workspace_bytes, chunk_rows, stream), "rmsnorm_fwd_host")
+
+
+def rmsnorm_fwd_host_status(x, residual, w, y, residual_out, rows, hidden, eps, dtype, workspace,
+                            workspace_bytes, chunk_rows, stream=0) -> int:
+    return load().rmsnorm_fwd_host(x, residual, w, y, residual_out, rows, hidden, eps, dtype, workspace,
+                                   workspace_bytes, chunk_rows, stream)
+
+
+def rmsnorm_host_workspace_bytes(chunk_rows, hidden, dtype, has_residual) -> int:
+    n = int(load().rmsnorm_host_workspace_bytes(chunk_rows, hidden, dtype, int(has_residual)))
+    if n < 0:
+        raise RmsNormError(n, "rmsnorm_host_workspace_bytes")
+    return n
 
 
 def rmsnorm_max_hidden(dtype) -> int:

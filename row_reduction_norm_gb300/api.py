@@ -86,6 +86,50 @@ def rms_norm(x: torch.Tensor, w: Optional[torch.Tensor] = None, residual: Option
     return (y, residual_out) if residual is not None else y
 
 
+def rms_norm_host(x: torch.Tensor, w: Optional[torch.Tensor] = None, residual: Optional[torch.Tensor] = None,
+                  eps: float = 1e-6, out: Optional[torch.Tensor] = None, residual_out: Optional[torch.Tensor] = None,
+                  chunk_rows: int = 4096, workspace: Optional[torch.Tensor] = None,
+                  device: Optional[torch.device] = None, stream: Optional[torch.cuda.Stream] = None):
+    """``rms_norm`` on CPU tensors, streamed through a GPU in chunks of
+    ``chunk_rows`` rows (``rmsnorm_fwd_host``): uploads, launches and
+    read-backs overlap when the tensors are in pinned memory.  ``workspace``
+    is a CUDA uint8 tensor of at least ``rmsnorm_host_workspace_bytes(...)``
+    bytes
+    (allocated on ``device`` when not given).  Returns after the work is
+    queued on ``stream``: synchronise it before reading the outputs."""
+    if x.dim() < 1:
+        raise ValueError("x must have at least one dimension")
+    code = dtype_code(x.dtype)
+    hidden = x.shape[-1]
+    rows = x.numel() // hidden if hidden else 0
+    y = torch.empty_like(x) if out is None else out
+    if residual is not None and residual_out is None:
+        residual_out = torch.empty_like(x)
+    for name, t in (("x", x), ("w", w), ("residual", residual), ("out", y), ("residual_out", residual_out)):
+        if t is None:
+            continue
+        if t.is_cuda:
+            raise ValueError(f"{name} must be a CPU tensor (use rms_norm for device tensors)")
+        if t.dtype != x.dtype or not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous with dtype {x.dtype}")
+        if name != "w" and t.shape != x.shape:
+            raise ValueError(f"{name} has shape {tuple(t.shape)}, x has {tuple(x.shape)}")
+    if w is not None and tuple(w.shape) != (hidden,):
+        raise ValueError(f"w must have shape ({hidden},), got {tuple(w.shape)}")
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    need = N.rmsnorm_host_workspace_bytes(chunk_rows, hidden, code, residual is not None)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    if not workspace.is_cuda or workspace.numel() * workspace.element_size() < need:
+        raise ValueError(f"workspace must be a CUDA tensor of at least {need} bytes")
+    with torch.cuda.device(workspace.device):
+        s = stream if stream is not None else torch.cuda.current_stream(workspace.device)
+        N.rmsnorm_fwd_host(_ptr(x), _ptr(residual), _ptr(w), _ptr(y), _ptr(residual_out), rows, hidden,
+                           float(eps), code, workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                           chunk_rows, s.cuda_stream)
+    return (y, residual_out) if residual is not None else y
+
+
 def _token_view(t: torch.Tensor, name: str):
     """(tokens, token_stride) of a [tokens, width] tensor with a contiguous last dimension."""
     if t.dim() != 2:

@@ -334,6 +334,44 @@ def test_cluster_plan_validation_without_cuda():
     assert st(reg, hidden=576, res=None) == EINVAL
 
 
+def test_host_call_workspace_and_validation_without_cuda():
+    """rmsnorm_fwd_host's workspace size (the weight, then two halves of
+    chunk_rows rows of x and y, and of residual and residual_out with one,
+    every part on a 256-byte boundary) and its argument checks, which all
+    return before any CUDA call."""
+    up = lambda v: -(-v // 256) * 256
+    for dtype, esz in ((N.RMSNORM_BF16, 2), (N.RMSNORM_F32, 4)):
+        for chunk, hidden, res in ((1, 1, False), (7, 576, True), (4096, 8192, True), (3, 65536, False)):
+            rb = hidden * esz
+            want = up(rb) + 2 * (4 if res else 2) * up(chunk * rb)
+            assert R.rmsnorm_host_workspace_bytes(chunk, hidden, dtype, res) == want
+    W = N.load().rmsnorm_host_workspace_bytes
+    assert W(0, 64, 1, 0) == N.RMSNORM_EINVAL and W(4, 0, 1, 0) == N.RMSNORM_EINVAL
+    assert W(4, 64, 7, 0) == N.RMSNORM_EINVAL and W(4, 64, 1, 2) == N.RMSNORM_EINVAL
+    assert W(4, 65537, 1, 0) == N.RMSNORM_EUNSUPPORTED
+    assert W(1 << 60, 65536, 0, 1) == N.RMSNORM_EINVAL      # overflows
+
+    P, H = 1 << 20, 1 << 21                                  # stand-in addresses (never touched)
+    need = R.rmsnorm_host_workspace_bytes(16, 1024, N.RMSNORM_BF16, True)
+
+    def st(x=H, r=H, w=H, y=H, h=H, rows=100, hidden=1024, eps=1e-6, dtype=N.RMSNORM_BF16, ws=P, nbytes=need,
+           chunk=16):
+        return N.rmsnorm_fwd_host_status(x, r, w, y, h, rows, hidden, eps, dtype, ws, nbytes, chunk, 0)
+
+    assert st(rows=0, x=None, r=None, w=None, y=None, h=None, ws=None, nbytes=0) == N.RMSNORM_OK
+    EINVAL = N.RMSNORM_EINVAL
+    assert st(chunk=0) == EINVAL
+    assert st(ws=None) == EINVAL and st(ws=P + 16) == EINVAL and st(nbytes=need - 1) == EINVAL
+    assert st(x=None) == EINVAL and st(y=None) == EINVAL
+    assert st(h=None) == EINVAL and st(r=None) == EINVAL     # residual and residual_out go together
+    assert st(eps=-1.0) == EINVAL and st(dtype=5) == EINVAL and st(rows=-1) == EINVAL
+    assert st(hidden=65537) == N.RMSNORM_EUNSUPPORTED
+    # without a residual the smaller workspace is enough
+    small = R.rmsnorm_host_workspace_bytes(16, 1024, N.RMSNORM_BF16, False)
+    assert small < need
+    assert st(r=None, h=None, nbytes=small - 1) == EINVAL
+
+
 def test_layernorm_register_blocks_are_four_warps_or_the_row():
     """LayerNorm register plans use blocks of max(threads_per_row, 128)
     threads; a plan with the RMSNorm block size is refused (rows = 0:
