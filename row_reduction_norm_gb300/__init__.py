@@ -11,7 +11,7 @@ from ._native import (  # noqa: F401  (the C ABI, same names)
     Plan, RmsNormError, rmsnorm_build_info, rmsnorm_fwd, rmsnorm_fwd_ex, rmsnorm_fwd_plan, rmsnorm_fwd_cast,
     rmsnorm_max_hidden, rmsnorm_plan, rmsnorm_plan_ex, rmsnorm_plan_for, rmsnorm_regime, rmsnorm_qk_fwd, rmsnorm_qk_plan_for,
     layernorm_fwd, layernorm_plan_for, rmsnorm_fwd_mxfp8, rmsnorm_mxfp8_plan_for, rmsnorm_fwd_nvfp4,
-    rmsnorm_nvfp4_plan_for, rmsnorm_fwd_host, rmsnorm_host_workspace_bytes,
+    rmsnorm_nvfp4_plan_for, rmsnorm_fwd_host, rmsnorm_host_workspace_bytes, rmsnorm_fwd_host_static,
     rmsnorm_reg_max_chunks, rmsnorm_wait_timeouts, rmsnorm_strerror,
     RMSNORM_BF16, RMSNORM_F32, RMSNORM_OK, RMSNORM_EINVAL, RMSNORM_EUNSUPPORTED, RMSNORM_ECUDA,
 )

@@ -68,7 +68,7 @@ EXPORTED = ["rmsnorm_fwd", "rmsnorm_regime", "rmsnorm_plan", "rmsnorm_plan_ex", 
             "rmsnorm_qk_fwd", "rmsnorm_qk_plan_for", "rmsnorm_fwd_mxfp8", "rmsnorm_mxfp8_plan_for",
             "rmsnorm_fwd_nvfp4", "rmsnorm_nvfp4_plan_for",
             "layernorm_fwd", "layernorm_plan_for",
-            "rmsnorm_fwd_host", "rmsnorm_host_workspace_bytes",
+            "rmsnorm_fwd_host", "rmsnorm_host_workspace_bytes", "rmsnorm_fwd_host_static",
             "rmsnorm_max_hidden", "rmsnorm_reg_max_chunks", "rmsnorm_wait_timeouts", "rmsnorm_tma_wait_test",
             "rmsnorm_strerror",
             "rmsnorm_build_info"]
@@ -182,6 +182,8 @@ def load():
         lib.rmsnorm_fwd_host.restype = i32
         lib.rmsnorm_host_workspace_bytes.argtypes = [i64, i64, i32, i32]
         lib.rmsnorm_host_workspace_bytes.restype = i64
+        lib.rmsnorm_fwd_host_static.argtypes = fwd_args + [vp]
+        lib.rmsnorm_fwd_host_static.restype = i32
         lib.rmsnorm_strerror.argtypes = [i32]
         lib.rmsnorm_strerror.restype = ctypes.c_char_p
         lib.rmsnorm_build_info.argtypes = []
@@ -364,6 +366,12 @@ def rmsnorm_fwd_host_status(x, residual, w, y, residual_out, rows, hidden, eps, 
                             workspace_bytes, chunk_rows, stream=0) -> int:
     return load().rmsnorm_fwd_host(x, residual, w, y, residual_out, rows, hidden, eps, dtype, workspace,
                                    workspace_bytes, chunk_rows, stream)
+
+
+def rmsnorm_fwd_host_static(x, residual, w, y, residual_out, rows, hidden, eps, dtype, stream=0):
+    """rmsnorm_fwd_host with the library's own device scratch (no workspace)."""
+    _check(load().rmsnorm_fwd_host_static(x, residual, w, y, residual_out, rows, hidden, eps, dtype, stream),
+           "rmsnorm_fwd_host_static")
 
 
 def rmsnorm_host_workspace_bytes(chunk_rows, hidden, dtype, has_residual) -> int:
