@@ -157,7 +157,7 @@ int rmsnorm_fwd_host(const void *x, const void *residual, const void *w, void *y
         if (!ok) break;
         st = rmsnorm_fwd(dx, dr, w != nullptr ? ws + L.w : nullptr, dy, dh, n, hidden, eps, dtype,
                          reinterpret_cast<rmsnorm_stream_t>(P.run));
-        if (st != RMSNORM_OK) return st;
+        if (st != RMSNORM_OK) break;
         cu(cudaEventRecord(P.done[h], P.run));
         // read-backs
         cu(cudaStreamWaitEvent(P.down, P.done[h], 0));
@@ -166,8 +166,14 @@ int rmsnorm_fwd_host(const void *x, const void *residual, const void *w, void *y
         cu(cudaEventRecord(P.out[h], P.down));
     }
     // work issued on the caller's stream after this call follows the read-backs
+    // (on an error too: whatever was queued still uses the workspace)
+    cu(cudaEventRecord(P.in[0], P.up));
+    cu(cudaStreamWaitEvent(caller, P.in[0], 0));
+    cu(cudaEventRecord(P.done[0], P.run));
+    cu(cudaStreamWaitEvent(caller, P.done[0], 0));
     cu(cudaStreamWaitEvent(caller, P.out[0], 0));
     cu(cudaStreamWaitEvent(caller, P.out[1], 0));
+    if (st != RMSNORM_OK) return st;
     if (!ok) {
         (void)cudaGetLastError();
         return RMSNORM_ECUDA;
