@@ -180,3 +180,35 @@ def test_zero_rows_and_device_plan_is_the_host_plan():
         y, h = R.rms_norm(x, w=None, residual=torch.empty_like(x), eps=1e-6)
         torch.cuda.synchronize()
         assert y.shape == x.shape and h.shape == x.shape
+
+
+@pytest.mark.parametrize("dtype,hidden", [("bf16", 40960), ("f32", 65536)])
+def test_special_values(dtype, hidden):
+    """NaN, +-Inf, zero and tiny rows in a cluster's slices (the NaN and Inf
+    fall in other blocks than the first): the partial sums carry them across
+    the cluster as the oracle's sum does.  A zero residual keeps h = x."""
+    tdt = W.TORCH_DTYPE[dtype]
+    x = W.random_rows(dtype, 6, hidden, seed=13, device=DEV)
+    x[0, hidden // 3] = float("nan")
+    x[1, hidden // 2] = float("inf")
+    x[2] = 0.0
+    x[3, 0] = float("-inf")
+    x[3, hidden - 1] = float("inf")
+    x[4] = x[4] * 1e-12
+    r = torch.zeros_like(x)
+    w = torch.ones(hidden, device=DEV, dtype=tdt)
+    assert R.plan_for(x, w=w, residual=r).kernel == N.RMSNORM_KERNEL_CLUSTER
+    for eps in (1e-5, 0.0):
+        y, h = R.rms_norm(x, w=w, residual=r, eps=eps)
+        torch.cuda.synchronize()
+        yr, hr, _, _ = _oracle(x, r, w, eps, dtype)
+        ok, rep = parity.compare_y(W.to_numpy_bits(y), yr, dtype)
+        assert ok, f"eps={eps}: {rep}"
+        # residual_out: NaN where the oracle has NaN (the payload is not part
+        # of the op), every other element bit-exact
+        hg = h.float().cpu().numpy()
+        nan_g = np.isnan(hg)
+        nan_o = np.isnan(W.from_numpy_bits(hr, dtype).float().numpy())
+        assert (nan_g == nan_o).all()
+        keep = ~nan_g
+        assert parity.bits_equal(W.to_numpy_bits(h)[keep], hr[keep])
