@@ -372,6 +372,49 @@ def test_host_call_workspace_and_validation_without_cuda():
     assert st(r=None, h=None, nbytes=small - 1) == EINVAL
 
 
+def _sum_depth(plan, hidden, dtype):
+    """Rounding steps a square passes through on its way into the row's sum,
+    for the planned kernel (the count the fp32 tolerance in parity.py is
+    derived from): sequential per-accumulator steps, then the fixed trees."""
+    V = 8 if dtype == N.RMSNORM_BF16 else 4
+    lg = lambda n: max(0, (n - 1).bit_length())
+    k, gt, ch = plan.kernel, plan.threads_per_row, plan.chunks_per_thread
+    if k == N.RMSNORM_KERNEL_REG:
+        return ch + lg(V) + lg(min(gt, 32)) + lg(max(1, gt // 32))
+    if k == N.RMSNORM_KERNEL_CLUSTER:
+        return ch + lg(V) + 5 + lg(256 // 32) + lg(8)
+    if k == N.RMSNORM_KERNEL_TMA:
+        return -(-(hidden // V) // 512) + lg(V) + 5 + lg(512 // 32)
+    assert k == N.RMSNORM_KERNEL_LOOP
+    ve = plan.vec_elems
+    units = hidden // ve
+    terms = -(-units // plan.block_threads) * ve       # a thread's elements
+    return -(-terms // 8) + 3 + 5 + lg(plan.block_threads // 32)
+
+
+@pytest.mark.parametrize("dtype", [N.RMSNORM_BF16, N.RMSNORM_F32])
+def test_planned_sum_trees_stay_within_the_tolerance_derivation(dtype):
+    """Every plan the planner makes keeps the fp32 sum of squares within the
+    depth the tolerance is derived from: 21 levels for the register, cluster
+    and two-pass kernels, 35 for the bulk-copy kernel (see tests/parity.py)."""
+    esz = 2 if dtype == N.RMSNORM_BF16 else 4
+    worst = {}
+    edges = [16 // esz * k for k in (1, 512, 2048, 2049, 8192, 16384)]
+    for hidden in list(range(1, 65537, 61)) + [h for h in edges if h <= 65536]:
+        for vec_ok in (True, False):
+            if vec_ok and (hidden * esz) % 16:
+                continue
+            for res in (False, True):
+                for rows in (1, 4096):
+                    p = R.rmsnorm_plan_ex(rows, hidden, dtype, vec_ok, res, 152, 4)
+                    d = _sum_depth(p, hidden, dtype)
+                    limit = 35 if p.kernel == N.RMSNORM_KERNEL_TMA else 21
+                    assert d <= limit, (hidden, vec_ok, res, rows, p.as_dict(), d)
+                    worst[p.kernel] = max(worst.get(p.kernel, 0), d)
+    assert set(worst) == {N.RMSNORM_KERNEL_REG, N.RMSNORM_KERNEL_CLUSTER, N.RMSNORM_KERNEL_TMA,
+                          N.RMSNORM_KERNEL_LOOP}
+
+
 def test_layernorm_register_blocks_are_four_warps_or_the_row():
     """LayerNorm register plans use blocks of max(threads_per_row, 128)
     threads; a plan with the RMSNorm block size is refused (rows = 0:
