@@ -138,7 +138,8 @@ typedef struct {
                                    and the weight is read from global memory; the
                                    rest, which must hold a whole row, goes to x);
                                    CLUSTER: chunks per thread of a block's slice of
-                                   256 * chunks_per_thread chunks: 4 (16 KB), or 8
+                                   256 * chunks_per_thread chunks: 4 (16 KB), 5
+                                   (20 KB; planned for rows of 64 to 80 KB), or 8
                                    (32 KB, fp32 only; planned for rows past 128 KB),
                                    a result depending on it (not on cluster_ctas)  */
     int32_t vec_elems;          /* elements per load: 16 / sizeof(T), or 1 (scalar)  */
@@ -201,8 +202,8 @@ int rmsnorm_regime(int64_t rows, int64_t hidden, int dtype);
  * Pure host planning (no CUDA call): the plan rmsnorm_fwd would use without
  * a residual on a device with `sm_count` SMs where the chosen kernel keeps
  * `blocks_per_sm` blocks resident (with a residual, rows longer than 32 KB
- * take RMSNORM_KERNEL_CLUSTER instead: 16 KB slices up to 128 KB rows, 32 KB
- * slices beyond).  vec_ok: 1 if every pointer is 16-byte aligned and
+ * take RMSNORM_KERNEL_CLUSTER instead: 16 KB slices up to 128 KB rows, but
+ * 20 KB for rows of 64 to 80 KB, and 32 KB slices past 128 KB).  vec_ok: 1 if every pointer is 16-byte aligned and
  * hidden * sizeof(T) is a multiple of 16.  Returns a status.
  */
 int rmsnorm_plan(int64_t rows, int64_t hidden, int dtype, int vec_ok, int sm_count,

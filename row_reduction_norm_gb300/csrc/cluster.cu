@@ -27,8 +27,13 @@ const void *cluster_wm(int wm) {
 
 const void *cluster_kernel(int dtype, int ch, bool res, int wm) {
     if (!res) return nullptr;
-    if (dtype == 1) return ch == 4 ? cluster_wm<BF16, 4>(wm) : nullptr;
+    if (dtype == 1) {
+        if (ch == 4) return cluster_wm<BF16, 4>(wm);
+        if (ch == 5) return cluster_wm<BF16, 5>(wm);
+        return nullptr;
+    }
     if (ch == 4) return cluster_wm<F32, 4>(wm);
+    if (ch == 5) return cluster_wm<F32, 5>(wm);
     if (ch == 8) return cluster_wm<F32, 8>(wm);
     return nullptr;
 }

@@ -70,7 +70,7 @@ int tma_timeouts_read(unsigned int *out);
 // RMSNorm of contiguous rows with a residual, a row split over the blocks of
 // a thread-block cluster: kClusterGT threads a block, each block a slice of
 // kClusterGT * ch 16-byte units, up to kClusterMaxCtas blocks a cluster.
-// Compiled for ch 4 (bf16, fp32) and 8 (fp32), with a residual only.
+// Compiled for ch 4 and 5 (bf16, fp32) and 8 (fp32), with a residual only.
 constexpr int kClusterGT = 256;
 constexpr int kClusterMaxCtas = 8;
 const void *cluster_kernel(int dtype, int ch, bool res, int wm);

@@ -10,7 +10,8 @@
 //
 //  * A cluster of C blocks (2..8, the portable cluster size) owns a row; block
 //    q of the cluster owns the slice of units [q*S, (q+1)*S), S = 256 * CH
-//    16-byte units (16 KB with CH = 4, 32 KB with CH = 8), thread t the units
+//    16-byte units (16 KB with CH = 4, 20 KB with CH = 5, 32 KB with CH = 8),
+//    thread t the units
 //    q*S + c*256 + t, so a warp's loads of one chunk slot are 512 contiguous
 //    bytes.  The slice lives in registers from its load to its store.
 //  * Each block reduces its slice exactly as the register kernel's CTA regime
@@ -33,8 +34,9 @@
 //
 // Measured on GB300 (bf16 rows with a residual and a weight, against the
 // kernels these rows ran on before): 48 KB rows 0.936 -> 0.982 of the
-// measured HBM peak, 64 KB 0.946 -> 0.986, 80 KB 0.949 -> 0.964 (all against
-// the bulk-copy kernel), 128 KB 0.915 -> 0.959 (against the two-pass
+// measured HBM peak, 64 KB 0.946 -> 0.986, 80 KB 0.949 -> 0.964 with five
+// 16 KB slices, 0.976 with four 20 KB slices (all against the bulk-copy
+// kernel), 128 KB 0.915 -> 0.959 (against the two-pass
 // kernel); fp32 rows of 160 KB 0.969 -> 1.025 and of 256 KB 0.934 -> 1.006
 // with 32 KB slices.  Without a residual a block moves half the bytes per
 // barrier and the bulk-copy kernel stays faster (64 KB rows 0.709 against
@@ -47,10 +49,11 @@
 namespace rrn {
 
 // Resident blocks each slice size is compiled for: four (64 registers a
-// thread) for 16 KB slices, three (85) for 32 KB slices; measured on GB300,
-// fp32 rows of 256 KB with 32 KB slices 1.006 of peak at three blocks, 0.907
-// at two.
-__host__ __device__ constexpr int cluster_min_blocks(int ch) { return ch <= 4 ? 4 : 3; }
+// thread) for 16 and 20 KB slices, three (85) for 32 KB slices; measured on
+// GB300, fp32 rows of 256 KB with 32 KB slices 1.006 of peak at three
+// blocks, 0.907 at two; bf16 rows of 80 KB with 20 KB slices 0.976 at four
+// blocks, 0.956 at three.
+__host__ __device__ constexpr int cluster_min_blocks(int ch) { return ch <= 5 ? 4 : 3; }
 
 __device__ __forceinline__ uint32_t cluster_rank() {
     uint32_t r;

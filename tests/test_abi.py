@@ -238,11 +238,14 @@ def test_tma_ring_rule_matches_the_library(pc, res, w):
 
 def _cluster_expected(hidden, dtype):
     """(chunks_per_thread, cluster_ctas) of the cluster rule: 256-thread
-    blocks of 16 KB slices, as few as cover the row, or 32 KB slices for fp32
-    rows the eight-block cap of 16 KB slices cannot cover."""
+    blocks of 16 KB slices, as few as cover the row; four 20 KB slices where
+    that takes five (rows of 64 to 80 KB); 32 KB slices for fp32 rows the
+    eight-block cap of 16 KB slices cannot cover."""
     V = 8 if dtype == N.RMSNORM_BF16 else 4
     units = hidden // V
     ch = 4 if units <= 8 * 256 * 4 else 8
+    if ch == 4 and -(-units // 1024) == 5:
+        ch = 5
     return ch, -(-units // (256 * ch))
 
 
@@ -268,7 +271,8 @@ def test_residual_rows_past_32kb_take_the_cluster_kernel(dtype):
                 continue
             ch, ctas = _cluster_expected(hidden, dtype)
             assert 2 <= ctas <= 8 and (ctas - 1) * 256 * ch * V < hidden <= ctas * 256 * ch * V
-            assert dtype == N.RMSNORM_F32 or ch == 4
+            assert dtype == N.RMSNORM_F32 or ch in (4, 5)
+            assert ch != 5 or (ctas == 4 and 64 * 1024 < hidden * esz <= 80 * 1024)
             assert (p.kernel, p.regime) == (N.RMSNORM_KERNEL_CLUSTER, N.RMSNORM_REGIME_CLUSTER)
             assert (p.chunks_per_thread, p.cluster_ctas, p.threads_per_row) == (ch, ctas, 256 * ctas)
             assert (p.vec_elems, p.block_threads, p.rows_per_block) == (V, 256, 1)
@@ -284,26 +288,29 @@ def test_cluster_plan_validation_without_cuda():
     P = 1 << 20
     OK, EINVAL = N.RMSNORM_OK, N.RMSNORM_EINVAL
     good = R.rmsnorm_plan_ex(4, 40960, N.RMSNORM_BF16, True, True, 152, 4)
-    assert (good.kernel, good.cluster_ctas, good.chunks_per_thread, good.grid) == (N.RMSNORM_KERNEL_CLUSTER, 5, 4, 20)
+    assert (good.kernel, good.cluster_ctas, good.chunks_per_thread, good.grid) == (N.RMSNORM_KERNEL_CLUSTER, 4, 5, 16)
 
     def st(plan, hidden=40960, dtype=N.RMSNORM_BF16, res=P, rows=0, w=None):
         return N.rmsnorm_fwd_plan_status(P, res, w, P, res, rows, hidden, 1e-6, dtype, plan, 0)
 
     assert st(good) == OK and st(good, w=P) == OK
     # more blocks than the row needs: the extra slices are past the row end
-    for c in (6, 7, 8):
+    for c in (5, 6, 7, 8):
         q = good.copy()
         q.cluster_ctas, q.threads_per_row, q.grid = c, 256 * c, 4 * c
         assert st(q) == OK, c
     bad = []
     for field, value in (("chunks_per_thread", 8), ("chunks_per_thread", 2), ("block_threads", 512),
                          ("rows_per_block", 2), ("vec_elems", 4), ("threads_per_row", 256 * 6),
-                         ("cluster_ctas", 0), ("cluster_ctas", 1), ("cluster_ctas", 9)):
+                         ("cluster_ctas", 0), ("cluster_ctas", 1), ("cluster_ctas", 9), ("chunks_per_thread", 3)):
         q = good.copy()
         setattr(q, field, value)
         bad.append(q)
     q = good.copy()
-    q.cluster_ctas, q.threads_per_row = 4, 1024          # 4 x 16 KB slices do not cover 80 KB
+    q.chunks_per_thread = 4                              # 4 x 16 KB slices do not cover 80 KB
+    bad.append(q)
+    q = good.copy()
+    q.cluster_ctas, q.threads_per_row = 3, 768           # nor do 3 x 20 KB
     bad.append(q)
     for q in bad:
         assert st(q) == EINVAL, q.as_dict()
@@ -599,7 +606,8 @@ int main(void) {
     rmsnorm_plan_t plan;
     int planned = rmsnorm_plan_ex(100, 40960, RMSNORM_BF16, 1, 1, 152, 4, &plan);
     int cluster = planned == RMSNORM_OK && plan.kernel == RMSNORM_KERNEL_CLUSTER &&
-                  plan.regime == RMSNORM_REGIME_CLUSTER && plan.cluster_ctas == 5 && plan.grid == 500;
+                  plan.regime == RMSNORM_REGIME_CLUSTER && plan.cluster_ctas == 4 &&
+                  plan.chunks_per_thread == 5 && plan.grid == 400;
     printf("%d %d %d %d %d %d %d\n", zero, bad, cast, info != NULL, regime_bad,
            regime == RMSNORM_REGIME_WARP || regime == RMSNORM_ECUDA, cluster);
     return 0;

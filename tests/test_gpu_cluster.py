@@ -33,8 +33,9 @@ THREADS = os.cpu_count() or 1
 DEV = "cuda"
 
 # (dtype, hidden): the planner's cluster sizes 3..8, ragged and exact last
-# slices, 16 KB and (fp32 past 128 KB) 32 KB slices
-SHAPES = [("bf16", 16392), ("bf16", 24576), ("bf16", 32768), ("bf16", 40960), ("bf16", 40968),
+# slices, 16 KB, 20 KB (rows of 64 to 80 KB) and (fp32 past 128 KB) 32 KB
+# slices
+SHAPES = [("bf16", 16392), ("bf16", 24576), ("bf16", 32768), ("bf16", 32776), ("bf16", 40960), ("bf16", 40968),
           ("bf16", 57344), ("bf16", 65536),
           ("f32", 8196), ("f32", 20480), ("f32", 32768), ("f32", 32772), ("f32", 40960), ("f32", 65536)]
 
@@ -43,6 +44,8 @@ def _expected(dtype, hidden):
     V = 8 if dtype == "bf16" else 4
     units = hidden // V
     ch = 4 if units <= 8 * 1024 else 8
+    if ch == 4 and -(-units // 1024) == 5:   # rows of 64 to 80 KB: four 20 KB slices
+        ch = 5
     return ch, -(-units // (256 * ch))
 
 
