@@ -449,10 +449,12 @@ int rmsnorm_fwd_host(const void *x, const void *residual, const void *w, void *y
 int64_t rmsnorm_host_workspace_bytes(int64_t chunk_rows, int64_t hidden, int dtype, int has_residual);
 
 /*
- * rmsnorm_fwd_host without a workspace argument: the library's own 64 MiB of
- * device scratch (a file-scope __device__ array, one per device, its address
- * taken with cudaGetSymbolAddress at the first call) serves as the
- * workspace, with chunks of as many rows as fit it.  The call allocates
+ * The op of rmsnorm_fwd (Emmy page, running example and section "Tensor
+ * IR") on host rows, as rmsnorm_fwd_host computes it, without a workspace
+ * argument: the library's own 64 MiB of device scratch (a file-scope
+ * __device__ array, one per device, its address taken with
+ * cudaGetSymbolAddress at the first call) serves as the workspace, with
+ * chunks of as many rows as fit it.  The call allocates
  * nothing; the scratch belongs to the library's device image (with lazy
  * module loading, claimed on the device at the first call).  Arguments,
  * ordering on `stream`, results (bit for bit) and statuses as
