@@ -133,6 +133,29 @@ def test_e2e_steps_are_bounded():
     assert bench.e2e_steps_for(W.WORKLOADS["bf16_4096x576"], 7) == 7
 
 
+def test_e2e_chunks_are_about_64_mib_of_rows():
+    import bench
+    from row_reduction_norm_gb300 import workloads as W
+    head = W.WORKLOADS["bf16_res_65536x8192_w"]
+    assert bench.e2e_chunk_rows(head) == 4096                # 4096 x 16 KiB = 64 MiB
+    small = W.WORKLOADS["bf16_4096x576"]
+    assert bench.e2e_chunk_rows(small) == small.rows         # the whole batch fits one chunk
+    for wl in W.WORKLOADS.values():
+        c = bench.e2e_chunk_rows(wl)
+        assert 1 <= c <= wl.rows and c * wl.hidden * wl.elem_bytes <= max(64 << 20, wl.hidden * wl.elem_bytes)
+
+
+def test_plan_summary_names_the_cluster_size():
+    import bench
+    from row_reduction_norm_gb300 import _native as N
+    import row_reduction_norm_gb300 as R
+    p = R.rmsnorm_plan_ex(100, 65536, N.RMSNORM_BF16, True, True, 152, 4)
+    d = bench.plan_summary(p)
+    assert d["kernel"] == "cluster" and d["cluster_ctas"] == 8 and "rows_per_block" not in d
+    q = R.rmsnorm_plan(100, 8192, N.RMSNORM_BF16, True, 152, 4)
+    assert "cluster_ctas" not in bench.plan_summary(q)
+
+
 def test_traffic_source_says_why():
     import bench
     v, why = bench.profiled_traffic("no_such_workload", None, with_source=True)
